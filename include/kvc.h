@@ -1,0 +1,297 @@
+/*
+ * kvc.h — C ABI of the query-conditioned KV compression event (sm_103a).
+ *
+ * One compression event runs once per agent step, after prefill and before
+ * decode (KVMem: Virtualizing Million-Token Agent Workspaces on a Consumer
+ * GPU, "Step-level scheduling").  It follows the three primitives of
+ * ActKV: Efficient LLM Agents through Action-Guided KV Cache Management,
+ * §3.3 ("unified workflow": attention calculation → entry eviction with a
+ * Boolean keep mask → cache compaction):
+ *
+ *   score   kvc_score        Mean-K block scoring (KVMem, "Query-conditioned
+ *                            retrieval"), or
+ *           kvc_score_qmem   QueryMemory rule score (IntentKV: Cross-Turn
+ *                            Intent-Aware KV Cache Pruning for Agent
+ *                            Inference, §4 "Rule score")
+ *   select  kvc_select       budgeted top-k with a forced set, chronological
+ *                            output + keep mask (IntentKV §4 "Top-k
+ *                            selection"; KVMem "Query-conditioned retrieval")
+ *   layout  kvc_pack_rerope  execution view: gather + re-RoPE K, copy V
+ *                            (KVMem, "Tiered movement"), or
+ *           kvc_redirect_free slot-map redirection to a dead slot with
+ *                            alias/refcount-aware freeing (IntentKV §4
+ *                            "Redirect", §4 check 6, §7)
+ *
+ * Conventions (all entry points):
+ *  - Every pointer named "device" is CUDA device memory owned by the caller.
+ *    The library never allocates or frees memory and keeps no state between
+ *    calls.  Scratch space ("ws") is passed in; its size comes from the
+ *    matching *_workspace_size() query.
+ *  - bf16 tensors are passed as kvc_bf16 (the raw 16-bit bf16 bit pattern).
+ *  - All work is enqueued asynchronously on `stream`.  The return value
+ *    reports host-side validation only; it is returned before any launch.
+ *    Errors found on the device (an out-of-range index, a NaN score) are
+ *    recorded in the caller's `dev_status` word (first error wins, written
+ *    with an atomic compare-and-swap; a NULL dev_status disables the record
+ *    but not the bounds checks: a bad index is skipped, never dereferenced).
+ *    Read it with kvc_device_status() after the stream has been synchronised.
+ *    No kernel traps, asserts or spins without a bound.
+ *  - Sizes are element counts unless a name ends in _bytes.  Layouts are
+ *    row-major with the last dimension contiguous.
+ *  - KV blocks are KVC_BLOCK_TOKENS = 32 tokens (KVMem's default block
+ *    size).  Histories are multiples of 32 tokens; head_dim D ∈ {64, 128}.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_BLOCK_TOKENS 32
+/* bf16 of -1e4 rounded to nearest even = -9984.0 (bit pattern 0xC61C):
+ * the dead-slot key (IntentKV §2 "Layout": K set to -10^4, V set to 0). */
+#define KVC_SENTINEL_K_BITS 0xC61Cu
+/* Longest segment kvc_select accepts (its keys are staged in shared memory). */
+#define KVC_SELECT_MAX_SEG 49152
+/* Widest query-row set (W * G) kvc_score accepts for one KV head. */
+#define KVC_SCORE_MAX_ROWS 256
+
+typedef uint16_t kvc_bf16;
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_ERR_INVALID_ARG = 1, /* NULL pointer, negative or zero size            */
+  KVC_ERR_SHAPE = 2,       /* unsupported D, history not a multiple of 32 …  */
+  KVC_ERR_BUDGET = 3,      /* budget < 1 or sink + recent > budget           */
+  KVC_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned               */
+  KVC_ERR_WORKSPACE = 5,   /* ws_bytes smaller than the size query returned  */
+  KVC_ERR_CUDA = 6,        /* a CUDA launch or query failed                  */
+  KVC_ERR_BOUNDS = 7,      /* device: an index or offset was out of range    */
+  KVC_ERR_NAN = 8,         /* device: a NaN score reached kvc_select         */
+  KVC_ERR_TIMEOUT = 9,     /* device: a bounded wait gave up                 */
+  KVC_ERR_CAPACITY = 10    /* device: the freed-slot list overflowed         */
+} kvc_status;
+
+/* Static, never-NULL description of a status code. */
+const char *kvc_status_string(kvc_status s);
+
+/* Copies *dev_status (device int32) to *host_out, synchronously (this call
+ * blocks until all prior work on the device is done).  Returns KVC_ERR_CUDA
+ * if the copy fails. */
+kvc_status kvc_device_status(const int32_t *dev_status, int32_t *host_out);
+
+/* Library version, "major.minor.patch". */
+const char *kvc_version(void);
+
+/* ------------------------------------------------------------------------
+ * Index maintenance (not part of the timed event).
+ *
+ * kvc_build_meank — KVMem, "Query-conditioned retrieval": one RoPE-stripped
+ * mean key per (layer, KV head, 32-token block).
+ *   kraw   device bf16 [L][H][n_tok][D]   raw (pre-RoPE) keys
+ *   meank  device bf16 [L][H][n_tok/32][D] out: block means
+ * Each output element is the exact mean of the 32 inputs rounded once to
+ * bf16 (round-to-nearest-even); the sum is taken in fp64, which is exact
+ * whenever the 32 magnitudes span less than 2^40.
+ * Errors: KVC_ERR_INVALID_ARG (NULL, sizes < 1), KVC_ERR_SHAPE (n_tok % 32,
+ * D ∉ {64,128}), KVC_ERR_ALIGN (pointers not 16-byte aligned).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
+                           int32_t H, int32_t D, int64_t n_tok,
+                           int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 1 (score), Mean-K mode.
+ * KVMem, "Query-conditioned retrieval" (score blocks in the model's own
+ * attention space against RoPE-stripped Mean-K), with the GQA aggregation of
+ * ActKV §7.1 (Algorithm 3: max over the query heads of a group, mean over
+ * the query tokens):
+ *   z[w,g,b]   = q[l, h*G+g, w] · meank[l,h,b] / sqrt(D)
+ *   LSE[w,g]   = log Σ_b exp z[w,g,b]          (over the session's blocks)
+ *   score[l,h,b] = (1/W) Σ_w max_g exp(z[w,g,b] − LSE[w,g])
+ *   q        device bf16 [n_sess][L][Hq][W][D]  pre-RoPE query window
+ *   meank    device bf16 [L][H][nb_total][D]
+ *   blk_off  device int64 [n_sess+1]  session r owns blocks
+ *            [blk_off[r], blk_off[r+1]) of every (l, h) row; blk_off[0] = 0,
+ *            blk_off[n_sess] = nb_total, each session non-empty and at most
+ *            nb_max blocks (violations: KVC_ERR_BOUNDS in dev_status, the
+ *            session is skipped)
+ *   scores   device fp32 [L][H][nb_total]  out
+ *   ws       device scratch of kvc_score_workspace_size() bytes
+ * G = Hq/H; W*G ≤ KVC_SCORE_MAX_ROWS.
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (Hq % H, D, W*G too wide),
+ * KVC_ERR_ALIGN, KVC_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+size_t kvc_score_workspace_size(int32_t L, int32_t H, int32_t Hq, int32_t W,
+                                int32_t n_sess, int32_t nb_max);
+kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
+                     int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                     const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
+                     int32_t nb_max, void *ws, size_t ws_bytes,
+                     int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * QueryMemory update (IntentKV §4 "Memory recurrence", §7 item 1):
+ *   M ← decay·M + gain·mean_t q_turn[t];  then, if renorm, M ← M/‖M‖₂ along D
+ *   (a zero vector stays zero).
+ *   M       device fp32 [n_sess][L][Hq][D]  in/out (start from zeros)
+ *   q_turn  device bf16 [n_sess][L][Hq][T][D]  the turn's pre-RoPE queries
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D), KVC_ERR_ALIGN.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_qmem_update(float *M, const kvc_bf16 *q_turn, int32_t n_sess,
+                           int32_t L, int32_t Hq, int32_t D, int32_t T,
+                           float decay, float gain, int32_t renorm,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 1 (score), QueryMemory mode (IntentKV §4 "Rule score", §4 check 1:
+ * GQA KV heads expanded to the Hq query heads):
+ *   z[l,hq,j]  = M[r,l,hq] · kpool[l, slot_map[r,j], hq/G] / sqrt(D)
+ *   rule[r,j]  = Σ_{l,hq} exp(z[l,hq,j] − LSE[l,hq]),  LSE over the live j
+ * A position whose slot is `sentinel` (redirected by an earlier event) is
+ * dead: it is left out of every softmax and gets rule = -1, below any live
+ * score.
+ *   M        device fp32 [n_sess][L][Hq][D]
+ *   kpool    device bf16 [L][n_slots][H][D]   paged K pool, one row per slot
+ *   slot_map device int32 [n_sess][N]         logical position → slot
+ *   rule     device fp32 [n_sess][N]          out
+ *   ws       device scratch of kvc_score_qmem_workspace_size() bytes
+ * A slot outside [0, n_slots) is recorded as KVC_ERR_BOUNDS and treated as
+ * dead.  Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE, KVC_ERR_ALIGN,
+ * KVC_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+size_t kvc_score_qmem_workspace_size(int32_t n_sess, int32_t L, int32_t Hq,
+                                     int32_t N);
+kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
+                          const int32_t *slot_map, int32_t sentinel,
+                          float *rule, int32_t n_sess, int32_t L, int32_t H,
+                          int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
+                          void *ws, size_t ws_bytes, int32_t *dev_status,
+                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 2 (select): budgeted top-k with a forced set (IntentKV §4 "Top-k
+ * selection": K* = F ∪ argtop_{C*} s), sink and recent always kept and the
+ * result restored in chronological order (KVMem, "Query-conditioned
+ * retrieval"), plus the Boolean keep mask (ActKV §3.3).
+ * Per segment s of length n = seg_off[s+1] − seg_off[s]:
+ *   F = {0 … n_sink−1} ∪ {n−n_recent … n−1}  (clipped to the segment)
+ *   if n ≤ budget: keep all n; otherwise keep F plus the budget − |F|
+ *   non-forced items ranked by (score descending, index ascending);
+ *   −0.0 ranks equal to +0.0.
+ *   scores     device fp32, segment s at [seg_off[s], seg_off[s+1])
+ *   seg_off    device int64 [n_seg+1], non-decreasing, each n ≤ max_seg_len
+ *   kept       device int32 [n_seg][budget] out: ascending segment-local
+ *              indices; entries past kept_count[s] are set to -1
+ *   kept_count device int32 [n_seg] out: min(budget, n)
+ *   keepmask   device uint32 [n_seg][ceil(max_seg_len/32)] out, may be NULL:
+ *              bit (i%32) of word i/32 is 1 iff item i is kept; bits at or
+ *              past n are 0
+ * A NaN score is recorded as KVC_ERR_NAN and ranks below every number.
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_BUDGET (budget < 1, n_sink < 0,
+ * n_recent < 0, n_sink + n_recent > budget), KVC_ERR_SHAPE (max_seg_len >
+ * KVC_SELECT_MAX_SEG), KVC_ERR_ALIGN.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_select(const float *scores, const int64_t *seg_off,
+                      int32_t n_seg, int32_t max_seg_len, int32_t budget,
+                      int32_t n_sink, int32_t n_recent, int32_t *kept,
+                      int32_t *kept_count, uint32_t *keepmask,
+                      int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * RoPE table for the execution view (NeoX rotate-half convention):
+ *   tab[i][j] = (cos a, sin a),  a = (pos0 + i) · theta^(−2j/D),  j < D/2
+ * computed in fp64 and rounded to fp32.
+ *   tab  device fp32 [n_pos][D/2][2]
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D), KVC_ERR_ALIGN.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_rope_table(float *tab, int32_t n_pos, int32_t pos0, int32_t D,
+                          double theta, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 3a (layout): execution-view pack (KVMem, "Tiered movement": selected
+ * blocks packed into contiguous logical positions, raw K re-RoPEd at the
+ * new positions, V copied as-is).  For view token i of segment (l,h,r)
+ * with i < 32·kept_count:
+ *   src         = tok_off[r] + 32·kept[(l,h,r)][i/32] + i%32
+ *   kview[i]    = RoPE(kraw[l,h,src], position of table row i)
+ *   vview[i]    = vraw[l,h,src]   (bit copy)
+ * View tokens at or past 32·kept_count are written as zeros.
+ *   kraw, vraw  device bf16 [L][H][n_tok][D]   (pre-RoPE K, V)
+ *   kept, kept_count  as written by kvc_select over segments ordered
+ *               (l, h, r) with r fastest: [L][H][n_sess][budget], [L][H][n_sess]
+ *   tok_off     device int64 [n_sess+1], multiples of 32, tok_off[n_sess] = n_tok
+ *   rope_tab    device fp32 [32·budget][D/2][2] from kvc_rope_table
+ *   kview, vview device bf16 [L][H][n_sess][32·budget][D] out
+ * RoPE pairs element j with j + D/2:
+ *   (x_j, x_{j+D/2}) → (x_j·c − x_{j+D/2}·s, x_{j+D/2}·c + x_j·s),
+ * computed in fp32 and rounded to bf16 (nearest even).
+ * A kept index outside the session's blocks is recorded as KVC_ERR_BOUNDS;
+ * its view block is zero-filled.
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE, KVC_ERR_BUDGET, KVC_ERR_ALIGN.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_pack_rerope(const kvc_bf16 *kraw, const kvc_bf16 *vraw,
+                           const int32_t *kept, const int32_t *kept_count,
+                           int32_t L, int32_t H, int32_t D,
+                           const int64_t *tok_off, int32_t n_sess,
+                           int64_t n_tok, int32_t budget,
+                           const float *rope_tab, kvc_bf16 *kview,
+                           kvc_bf16 *vview, int32_t *dev_status,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dead slot (IntentKV §2 "Layout", §4 check 3): writes K = bf16(−1e4) =
+ * −9984 (0xC61C) into every element and V = +0.0 into slot `sentinel` of
+ * every layer and head.
+ *   kpool, vpool  device bf16 [L][n_slots][H][D]; vpool may be NULL
+ * Errors: KVC_ERR_INVALID_ARG (sentinel outside [0, n_slots)), KVC_ERR_SHAPE.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_init_sentinel(kvc_bf16 *kpool, kvc_bf16 *vpool, int32_t L,
+                             int32_t H, int32_t D, int64_t n_slots,
+                             int32_t sentinel, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step 3b (layout): slot-map redirection and alias-aware free (IntentKV §4
+ * "Redirect": S_r[j] ← s† for every dropped j; §4 check 6 and §7 "alias-
+ * aware deallocation": a dropped slot u is freed only if j is outside the
+ * protected prefix, u ≠ s†, and no remaining reference holds u).
+ * Every slot-map entry holds one count in refcnt (the sentinel's count is
+ * never touched).  Semantics are those of visiting (r, j) in row-major
+ * order: for each position with keep bit 0 and u = slot_map[r,j] ≠ sentinel,
+ *   slot_map[r,j] ← sentinel;  refcnt[u] −= 1;
+ *   if refcnt[u] reaches 0 and j ≥ prefix_len: append u to `freed`.
+ * The freed list is therefore ordered by the (r, j) of each slot's last
+ * dropping reference.  Kept positions and the K/V pools are not touched.
+ *   slot_map  device int32 [n_sess][N]   in/out
+ *   keepmask  device uint32 [n_sess][ceil(N/32)]  from kvc_select
+ *   refcnt    device int32 [n_slots]     in/out
+ *   freed     device int32 [freed_cap]   out
+ *   n_freed   device int32 [1]           out: list length
+ *   ws        device scratch of kvc_redirect_free_workspace_size() bytes
+ * A slot outside [0, n_slots) or a count that would go below zero is
+ * recorded as KVC_ERR_BOUNDS and that position is left as it was; a list
+ * longer than freed_cap is recorded as KVC_ERR_CAPACITY (the first
+ * freed_cap entries are written).
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE, KVC_ERR_ALIGN,
+ * KVC_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+size_t kvc_redirect_free_workspace_size(int32_t n_sess, int32_t N,
+                                        int64_t n_slots);
+kvc_status kvc_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
+                             int32_t n_sess, int32_t N, int32_t *refcnt,
+                             int64_t n_slots, int32_t prefix_len,
+                             int32_t sentinel, int32_t *freed,
+                             int32_t freed_cap, int32_t *n_freed, void *ws,
+                             size_t ws_bytes, int32_t *dev_status,
+                             cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H_ */
