@@ -1,0 +1,415 @@
+"""Benchmark of the query-conditioned KV compression event on GB300.
+
+Workload: the 8B-class single-session event — 36 layers, 8 KV / 32 query
+heads, head dim 128, a 131072-token history (4096 blocks of 32), a 32-query
+window, 256 kept blocks per (layer, KV head) with 1 sink and 4 recent
+blocks, re-RoPE pack to positions 0..8191.  Inputs are seeded synthetic
+bf16 tensors resident in HBM (see workloads/).
+
+One step = one event: score (Mean-K) → select → pack.  The metric is KV
+history tokens compressed per second; the roofline is algorithmic bytes over
+measured kernel time against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (the plain fp64 definition) on a
+bounded sample of the same workload on the host cores.  Under torchrun
+(N > 1) every rank runs its own event (independent sessions, weak scaling,
+no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens compressed/s per event (score+select+pack); % of HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "8b_128k: 36 layers, 8 KV / 32 query heads, d 128, 131072-token history, " \
+           "W 32, budget 256 blocks (1 sink, 4 recent), view 8192 tokens"
+L2_NOTE = "L2 flushed between steps (256 MiB write outside the event's timed span); " \
+          "the event also touches 2.7 GB > 129 MB L2"
+
+
+def algorithmic_bytes(cfg):
+    """Bytes the method must move per event (HBM), by stage."""
+    D = cfg.D
+    meank = cfg.L * cfg.H * cfg.nb_total * D * 2
+    q = cfg.n_sess * cfg.L * cfg.Hq * cfg.W * D * 2
+    view_elems = cfg.lp * cfg.H * cfg.n_sess * cfg.view_tokens * D
+    pack_rw = 2 * 2 * view_elems * 2          # K and V, read and write
+    kept = cfg.L * cfg.H * cfg.n_sess * cfg.budget * 4
+    return {"score": meank + q, "select": 0, "pack": pack_rw + kept,
+            "event": meank + q + pack_rw + kept}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if its source
+    fingerprint still matches the kernel source; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rows = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or "=" not in line:
+                continue
+            k, v = line.strip().split("=", 1)
+            rows[k.strip()] = v.strip()
+    src = rows.get(f"{kernel}.source")
+    if not src:
+        return None
+    with open(os.path.join(ROOT, src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    if sha != rows.get(f"{kernel}.sha"):
+        return None
+    scale = float(rows.get(f"{kernel}.scale", "1"))
+    return float(rows[f"{kernel}.bytes_per_launch"]) * scale
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed span."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def reduce_max_ms(ms: float, world: int, device) -> float:
+    """Max over ranks of a per-rank time (the job is as slow as its slowest
+    rank); identity at world size 1."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank's history tokens over the slowest
+    rank's event time."""
+    return tokens_per_rank * world / (ms_max * 1e-3)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import MeanKEvent
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = W.config_8b()
+    # inputs resident in HBM before the timed region
+    q = cfg.q(dev)
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = torch.empty(cfg.L, cfg.H, cfg.nb_total, cfg.D, dtype=torch.bfloat16, device=dev)
+    kvc.kvc_build_meank(kraw, meank, cfg.L, cfg.H, cfg.D, cfg.n_tok)
+    ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                    cfg.n_recent, theta=cfg.theta, pos0=cfg.pos0, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def step(evts=None):
+        if evts:
+            evts[0].record(stream)
+        ev.score(q, meank)
+        if evts:
+            evts[1].record(stream)
+        ev.select()
+        if evts:
+            evts[2].record(stream)
+        ev.pack(kraw, vraw)
+        if evts:
+            evts[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    if kvc.kvc_device_status(ev.dev_status) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    evts = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)  # L2 flush, outside the event span
+        step(evts[k])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    stage_ms = {"score": [], "select": [], "pack": [], "event": []}
+    for e in evts:
+        stage_ms["score"].append(e[0].elapsed_time(e[1]))
+        stage_ms["select"].append(e[1].elapsed_time(e[2]))
+        stage_ms["pack"].append(e[2].elapsed_time(e[3]))
+        stage_ms["event"].append(e[0].elapsed_time(e[3]))
+    mean = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+    ms_event = mean["event"]
+    ms_event = reduce_max_ms(ms_event, world, dev)
+    value = whole_job_value(cfg.n_tok, world, ms_event)
+
+    # e2e through the public API with host buffers (pinned), copies timed
+    e2e = None
+    if args.e2e_steps > 0:
+        h_q = q.cpu().pin_memory()
+        h_mk = meank.cpu().pin_memory()
+        h_k = kraw.cpu().pin_memory()
+        h_v = vraw.cpu().pin_memory()
+        o_k = torch.empty(ev.kview.shape, dtype=torch.bfloat16).pin_memory()
+        o_v = torch.empty(ev.vview.shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_mk, h_k, h_v))
+        d2h = 2 * ev.kview.numel() * 2
+        for i in range(args.e2e_steps + 1):
+            if i == 1:
+                torch.cuda.synchronize(dev)
+                te = time.perf_counter()
+            q.copy_(h_q, non_blocking=True)
+            meank.copy_(h_mk, non_blocking=True)
+            kraw.copy_(h_k, non_blocking=True)
+            vraw.copy_(h_v, non_blocking=True)
+            ev.run(q, meank, kraw, vraw)
+            o_k.copy_(ev.kview, non_blocking=True)
+            o_v.copy_(ev.vview, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - te) / args.e2e_steps
+        e2e = {"value": cfg.n_tok / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+               "note": "C-ABI calls on pinned host buffers: H2D of q, Mean-K, raw K/V; "
+                       "D2H of the K/V execution view"}
+
+    ab = algorithmic_bytes(cfg)
+    peak, peak_src = peaks()
+    dom = max(("score", "select", "pack"), key=lambda s: mean[s])
+    kern = {"score": "k_score_pass1+k_score_pass2", "select": "k_select",
+            "pack": "k_pack_rerope"}[dom]
+    achieved = ab[dom] / (mean[dom] * 1e-3) / 1e9 if ab[dom] else 0.0
+    pack_gbs = ab["pack"] / (mean["pack"] * 1e-3) / 1e9
+    event_gbs = ab["event"] / (ms_event * 1e-3) / 1e9
+    traffic = ncu_traffic(dom)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_event,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded, workloads/)",
+        "config": {"workload": WORKLOAD, "sessions": 1, "history_tokens": cfg.n_tok,
+                   "layers": cfg.L, "kv_heads": cfg.H, "q_heads": cfg.Hq, "head_dim": cfg.D,
+                   "window": cfg.W, "budget_blocks": cfg.budget, "parallelism": f"replicas{world}",
+                   "l2": L2_NOTE},
+        "hbm_roofline_event": {"achieved_gbs": event_gbs, "peak_gbs": peak,
+                               "frac": event_gbs / peak,
+                               "algorithmic_bytes": ab["event"]},
+        "stages_ms": {k: round(v, 4) for k, v in mean.items()},
+        "roofline": {"bound": "hbm", "kernel": kern, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab[dom], "peak_source": peak_src},
+        "pack_roofline": {"achieved": pack_gbs, "frac": pack_gbs / peak},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, dev)
+    return line
+
+
+# ------------------------------------------------------------ oracle arm
+
+def _oracle_sample(n_units, dev):
+    """Oracle inputs of the first n_units (layer, KV head) units of the
+    workload: (q rows, raw K, raw V) per unit, as numpy bit patterns."""
+    import numpy as np
+    import torch
+    import workloads as W
+    cfg = W.config_8b()
+    units = []
+    for u in range(n_units):
+        l, h = divmod(u * 37 % (cfg.L * cfg.H), cfg.H)
+        k = W.bf16_bits(cfg.kraw_unit(l, h, 0, dev))
+        v = W.bf16_bits(cfg.vraw_unit(l, h, 0, dev))
+        qg = [W.bf16_bits(cfg.q_unit(0, l, h * cfg.G + g, dev)) for g in range(cfg.G)]
+        units.append((l, h, np.stack(qg), k, v))
+    if dev is not None and getattr(dev, "type", "cpu") == "cuda":
+        torch.cuda.synchronize(dev)
+    return cfg, units
+
+
+def _oracle_event(cfg, units, threads):
+    """score → select → pack of the sampled units with the oracle; returns
+    (seconds, units done).  Mean-K (index maintenance) is built first and is
+    not part of the timed event."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    mks = [oracle.meank(u[3][None])[0] for u in units]
+
+    def one(i):
+        l, h, qg, k, v = units[i]
+        s = oracle.score_unit(qg, mks[i])
+        kept, cnt, _ = oracle.select(s, cfg.budget, cfg.n_sink, cfg.n_recent)
+        oracle.pack_unit(k, v, kept, cnt, cfg.budget, cfg.pos0, cfg.theta)
+        return cnt
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, range(len(units))))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(args, dev=None):
+    cores = os.cpu_count() or 1
+    n_units = args.cpu_units
+    cfg, units = _oracle_sample(n_units, dev)
+    secs = _oracle_event(cfg, units, cores)
+    frac = n_units / (cfg.L * cfg.H)
+    value = cfg.n_tok * frac / secs
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_units} of {cfg.L * cfg.H} (layer, KV head) units of the event "
+                      f"(score+select+pack, fp64 C oracle, thread pool of {cores}); "
+                      f"{secs:.2f} s wall, tokens scaled by {frac:.4f}"}
+
+
+def run_reference(args, rank, world):
+    import torch
+    dev = None
+    if torch.cuda.is_available():
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+    cores = os.cpu_count() or 1
+    cfg, units = _oracle_sample(args.cpu_units, dev)
+    for _ in range(args.warmup_ref):
+        _oracle_event(cfg, units[:1], 1)
+    times = [_oracle_event(cfg, units, cores) for _ in range(args.steps_ref)]
+    secs = sum(times) / len(times)
+    frac = args.cpu_units / (cfg.L * cfg.H)
+    value = cfg.n_tok * frac / secs
+    sample = (f"{args.cpu_units} of {cfg.L * cfg.H} (layer, KV head) units per step, "
+              f"{args.steps_ref} steps; tokens scaled by {frac:.4f}")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps_ref, "warmup": args.warmup_ref,
+            "ms_per_step": secs * 1e3 / frac, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, workloads/)",
+            "config": {"workload": WORKLOAD, "parallelism": "host thread pool"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-units", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.steps_ref = max(1, min(args.steps, 2))
+    args.warmup_ref = 1
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+"""query_conditioned_kv_gb300 — Python binding of libkvc (sm_103a).
+
+A thin ctypes layer over the C ABI declared in ``include/kvc.h``: every
+function here has the name of the C entry point it calls and only marshals
+arguments (tensor → device pointer, current torch stream → cudaStream_t).
+Every step of the compression event runs in the library's CUDA kernels;
+there is no Python or CPU fallback.  PyTorch is used for device memory and
+streams only.
+
+Importing this package loads ``libkvc.so`` and fails loudly if it has not
+been built (``python -c "import __graft_entry__ as g; g.build()"``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG",
+    "kvc_status_string", "kvc_version", "kvc_device_status",
+    "kvc_build_meank", "kvc_score_workspace_size", "kvc_score",
+    "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
+    "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_init_sentinel",
+    "kvc_redirect_free_workspace_size", "kvc_redirect_free",
+]
+
+BLOCK_TOKENS = 32
+SENTINEL_K_BITS = 0xC61C
+SELECT_MAX_SEG = 49152
+SCORE_MAX_ROWS = 256
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: the CUDA library must be built first "
+        "(python -c 'import __graft_entry__ as g; g.build()'); there is no "
+        "fallback path")
+
+_c = ctypes
+_P = _c.c_void_p
+_I32 = _c.c_int32
+_I64 = _c.c_int64
+_SZ = _c.c_size_t
+
+lib = _c.CDLL(LIB_PATH)
+
+_SIGS = {
+    "kvc_status_string": (_c.c_char_p, [_c.c_int]),
+    "kvc_version": (_c.c_char_p, []),
+    "kvc_device_status": (_c.c_int, [_P, _P]),
+    "kvc_build_meank": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _P, _P]),
+    "kvc_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "kvc_score": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
+                             _I32, _I64, _I32, _P, _SZ, _P, _P]),
+    "kvc_qmem_update": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32,
+                                   _c.c_float, _c.c_float, _I32, _P]),
+    "kvc_score_qmem_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "kvc_score_qmem": (_c.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                  _I32, _I32, _I32, _I64, _P, _SZ, _P, _P]),
+    "kvc_select": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P,
+                              _P, _P, _P]),
+    "kvc_rope_table": (_c.c_int, [_P, _I32, _I32, _I32, _c.c_double, _P]),
+    "kvc_pack_rerope": (_c.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _I32,
+                                   _I64, _I32, _P, _P, _P, _P, _P]),
+    "kvc_init_sentinel": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _I32,
+                                     _P]),
+    "kvc_redirect_free_workspace_size": (_SZ, [_I32, _I32, _I64]),
+    "kvc_redirect_free": (_c.c_int, [_P, _P, _I32, _I32, _P, _I64, _I32, _I32,
+                                     _P, _I32, _P, _P, _SZ, _P, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class KvcError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {kvc_status_string(code)} (status {code})")
+
+
+def kvc_status_string(code: int) -> str:
+    return lib.kvc_status_string(int(code)).decode()
+
+
+def kvc_version() -> str:
+    return lib.kvc_version().decode()
+
+
+def _ptr(t):
+    """Device pointer of a CUDA tensor (None → NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libkvc takes device tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ok(code: int, where: str) -> None:
+    if code != 0:
+        raise KvcError(code, where)
+
+
+def kvc_device_status(dev_status) -> int:
+    """Synchronously reads the device status word (0 = no device error)."""
+    out = _c.c_int32(0)
+    _ok(lib.kvc_device_status(_ptr(dev_status), _c.addressof(out)),
+        "kvc_device_status")
+    return int(out.value)
+
+
+def kvc_build_meank(kraw, meank, L, H, D, n_tok, dev_status=None, stream=None):
+    _ok(lib.kvc_build_meank(_ptr(kraw), _ptr(meank), L, H, D, n_tok,
+                            _ptr(dev_status), _stream(stream)), "kvc_build_meank")
+
+
+def kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max) -> int:
+    return int(lib.kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max))
+
+
+def kvc_score(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,
+              nb_max, ws, dev_status=None, stream=None):
+    _ok(lib.kvc_score(_ptr(q), _ptr(meank), _ptr(scores), L, H, Hq, D, W,
+                      _ptr(blk_off), n_sess, nb_total, nb_max, _ptr(ws),
+                      ws.numel() * ws.element_size(), _ptr(dev_status),
+                      _stream(stream)), "kvc_score")
+
+
+def kvc_qmem_update(M, q_turn, n_sess, L, Hq, D, T, decay=0.9, gain=0.1,
+                    renorm=1, stream=None):
+    _ok(lib.kvc_qmem_update(_ptr(M), _ptr(q_turn), n_sess, L, Hq, D, T,
+                            float(decay), float(gain), int(renorm),
+                            _stream(stream)), "kvc_qmem_update")
+
+
+def kvc_score_qmem_workspace_size(n_sess, L, Hq, N) -> int:
+    return int(lib.kvc_score_qmem_workspace_size(n_sess, L, Hq, N))
+
+
+def kvc_score_qmem(M, kpool, slot_map, sentinel, rule, n_sess, L, H, Hq, D, N,
+                   n_slots, ws, dev_status=None, stream=None):
+    _ok(lib.kvc_score_qmem(_ptr(M), _ptr(kpool), _ptr(slot_map), sentinel,
+                           _ptr(rule), n_sess, L, H, Hq, D, N, n_slots,
+                           _ptr(ws), ws.numel() * ws.element_size(),
+                           _ptr(dev_status), _stream(stream)), "kvc_score_qmem")
+
+
+def kvc_select(scores, seg_off, n_seg, max_seg_len, budget, n_sink, n_recent,
+               kept, kept_count, keepmask=None, dev_status=None, stream=None):
+    _ok(lib.kvc_select(_ptr(scores), _ptr(seg_off), n_seg, max_seg_len, budget,
+                       n_sink, n_recent, _ptr(kept), _ptr(kept_count),
+                       _ptr(keepmask), _ptr(dev_status), _stream(stream)),
+        "kvc_select")
+
+
+def kvc_rope_table(tab, n_pos, pos0, D, theta, stream=None):
+    _ok(lib.kvc_rope_table(_ptr(tab), n_pos, pos0, D, float(theta),
+                           _stream(stream)), "kvc_rope_table")
+
+
+def kvc_pack_rerope(kraw, vraw, kept, kept_count, L, H, D, tok_off, n_sess,
+                    n_tok, budget, rope_tab, kview, vview, dev_status=None,
+                    stream=None):
+    _ok(lib.kvc_pack_rerope(_ptr(kraw), _ptr(vraw), _ptr(kept),
+                            _ptr(kept_count), L, H, D, _ptr(tok_off), n_sess,
+                            n_tok, budget, _ptr(rope_tab), _ptr(kview),
+                            _ptr(vview), _ptr(dev_status), _stream(stream)),
+        "kvc_pack_rerope")
+
+
+def kvc_init_sentinel(kpool, vpool, L, H, D, n_slots, sentinel, stream=None):
+    _ok(lib.kvc_init_sentinel(_ptr(kpool), _ptr(vpool), L, H, D, n_slots,
+                              sentinel, _stream(stream)), "kvc_init_sentinel")
+
+
+def kvc_redirect_free_workspace_size(n_sess, N, n_slots) -> int:
+    return int(lib.kvc_redirect_free_workspace_size(n_sess, N, n_slots))
+
+
+def kvc_redirect_free(slot_map, keepmask, n_sess, N, refcnt, n_slots,
+                      prefix_len, sentinel, freed, freed_cap, n_freed, ws,
+                      dev_status=None, stream=None):
+    _ok(lib.kvc_redirect_free(_ptr(slot_map), _ptr(keepmask), n_sess, N,
+                              _ptr(refcnt), n_slots, prefix_len, sentinel,
+                              _ptr(freed), freed_cap, _ptr(n_freed), _ptr(ws),
+                              ws.numel() * ws.element_size(), _ptr(dev_status),
+                              _stream(stream)), "kvc_redirect_free")

@@ -1,0 +1,209 @@
+// kvc_abi.cu — the extern "C" boundary of libkvc: host-side validation of
+// every call (before any launch), then the launch of the kernels in this
+// directory on the caller's stream.  No allocation, no state.
+#include <math.h>
+
+#include "kvc_internal.cuh"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool head_dim_ok(int D) { return D == 64 || D == 128; }
+
+kvc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
+
+__global__ void k_init_sentinel(uint16_t *kpool, uint16_t *vpool, int L, int H,
+                                int D, int64_t n_slots, int32_t sentinel) {
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t per_layer = (int64_t)H * D;
+  if (t >= (int64_t)L * per_layer) return;
+  int64_t l = t / per_layer, e = t - l * per_layer;
+  int64_t idx = (l * n_slots + sentinel) * per_layer + e;
+  kpool[idx] = (uint16_t)KVC_SENTINEL_K_BITS;
+  if (vpool) vpool[idx] = 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvc_status_string(kvc_status s) {
+  switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument (NULL pointer or size out of range)";
+    case KVC_ERR_SHAPE: return "unsupported shape";
+    case KVC_ERR_BUDGET: return "invalid budget (budget < 1 or sink + recent > budget)";
+    case KVC_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case KVC_ERR_WORKSPACE: return "workspace too small";
+    case KVC_ERR_CUDA: return "CUDA launch or copy failed";
+    case KVC_ERR_BOUNDS: return "device: index or offset out of range";
+    case KVC_ERR_NAN: return "device: NaN score";
+    case KVC_ERR_TIMEOUT: return "device: bounded wait timed out";
+    case KVC_ERR_CAPACITY: return "device: freed-slot list overflowed its capacity";
+  }
+  return "unknown status";
+}
+
+const char *kvc_version(void) { return "0.1.0"; }
+
+kvc_status kvc_device_status(const int32_t *dev_status, int32_t *host_out) {
+  if (!dev_status || !host_out) return KVC_ERR_INVALID_ARG;
+  return from_cuda(cudaMemcpy(host_out, dev_status, sizeof(int32_t),
+                              cudaMemcpyDeviceToHost));
+}
+
+kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
+                           int32_t H, int32_t D, int64_t n_tok,
+                           int32_t *dev_status, cudaStream_t stream) {
+  (void)dev_status;
+  if (!kraw || !meank || L < 1 || H < 1 || n_tok < 1) return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D) || n_tok % KVC_BLOCK_TOKENS) return KVC_ERR_SHAPE;
+  if (!aligned16(kraw) || !aligned16(meank)) return KVC_ERR_ALIGN;
+  return from_cuda(kvc::launch_build_meank(kraw, meank, (int64_t)L * H, n_tok, D, stream));
+}
+
+size_t kvc_score_workspace_size(int32_t L, int32_t H, int32_t Hq, int32_t W,
+                                int32_t n_sess, int32_t nb_max) {
+  if (L < 1 || H < 1 || Hq < H || Hq % H || W < 1 || n_sess < 1 || nb_max < 1) return 0;
+  return kvc::score_meank_ws_bytes(L, H, Hq, W, n_sess, nb_max);
+}
+
+kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
+                     int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                     const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
+                     int32_t nb_max, void *ws, size_t ws_bytes,
+                     int32_t *dev_status, cudaStream_t stream) {
+  if (!q || !meank || !scores || !blk_off || !ws) return KVC_ERR_INVALID_ARG;
+  if (L < 1 || H < 1 || Hq < 1 || W < 1 || n_sess < 1 || nb_total < 1 || nb_max < 1 ||
+      nb_max > nb_total)
+    return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D) || Hq % H || (int64_t)(Hq / H) * W > KVC_SCORE_MAX_ROWS ||
+      (int64_t)L * H * n_sess > 65535)
+    return KVC_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(meank) || !aligned16(scores) || !aligned16(ws))
+    return KVC_ERR_ALIGN;
+  if (ws_bytes < kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max))
+    return KVC_ERR_WORKSPACE;
+  return from_cuda(kvc::launch_score_meank(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
+                                           nb_total, nb_max, ws, dev_status, stream));
+}
+
+kvc_status kvc_qmem_update(float *M, const kvc_bf16 *q_turn, int32_t n_sess,
+                           int32_t L, int32_t Hq, int32_t D, int32_t T,
+                           float decay, float gain, int32_t renorm,
+                           cudaStream_t stream) {
+  if (!M || !q_turn || n_sess < 1 || L < 1 || Hq < 1 || T < 1) return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return KVC_ERR_SHAPE;
+  if (!aligned16(M) || !aligned16(q_turn)) return KVC_ERR_ALIGN;
+  return from_cuda(kvc::launch_qmem_update(M, q_turn, (int64_t)n_sess * L * Hq, D, T, decay,
+                                           gain, renorm, stream));
+}
+
+size_t kvc_score_qmem_workspace_size(int32_t n_sess, int32_t L, int32_t Hq,
+                                     int32_t N) {
+  if (n_sess < 1 || L < 1 || Hq < 1 || N < 1) return 0;
+  return kvc::score_qmem_ws_bytes(n_sess, L, Hq, N);
+}
+
+kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
+                          const int32_t *slot_map, int32_t sentinel,
+                          float *rule, int32_t n_sess, int32_t L, int32_t H,
+                          int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
+                          void *ws, size_t ws_bytes, int32_t *dev_status,
+                          cudaStream_t stream) {
+  if (!M || !kpool || !slot_map || !rule || !ws) return KVC_ERR_INVALID_ARG;
+  if (n_sess < 1 || L < 1 || H < 1 || Hq < 1 || N < 1 || n_slots < 1 || n_slots > INT32_MAX)
+    return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D) || Hq % H || H > 32 || 32 % H || (H * D) % 256 || (H * D) / 32 > 64 ||
+      n_sess > 65535 || (N + 127) / 128 > 65535 || L > 65535)
+    return KVC_ERR_SHAPE;
+  if (!aligned16(M) || !aligned16(kpool) || !aligned16(ws)) return KVC_ERR_ALIGN;
+  if (ws_bytes < kvc_score_qmem_workspace_size(n_sess, L, Hq, N)) return KVC_ERR_WORKSPACE;
+  return from_cuda(kvc::launch_score_qmem(M, kpool, slot_map, sentinel, rule, n_sess, L, H, Hq,
+                                          D, N, n_slots, ws, dev_status, stream));
+}
+
+kvc_status kvc_select(const float *scores, const int64_t *seg_off,
+                      int32_t n_seg, int32_t max_seg_len, int32_t budget,
+                      int32_t n_sink, int32_t n_recent, int32_t *kept,
+                      int32_t *kept_count, uint32_t *keepmask,
+                      int32_t *dev_status, cudaStream_t stream) {
+  if (!scores || !seg_off || !kept || !kept_count || n_seg < 1 || max_seg_len < 1)
+    return KVC_ERR_INVALID_ARG;
+  if (budget < 1 || n_sink < 0 || n_recent < 0 || (int64_t)n_sink + n_recent > budget)
+    return KVC_ERR_BUDGET;
+  if (max_seg_len > KVC_SELECT_MAX_SEG) return KVC_ERR_SHAPE;
+  return from_cuda(kvc::launch_select(scores, seg_off, n_seg, max_seg_len, budget, n_sink,
+                                      n_recent, kept, kept_count, keepmask, dev_status, stream));
+}
+
+kvc_status kvc_rope_table(float *tab, int32_t n_pos, int32_t pos0, int32_t D,
+                          double theta, cudaStream_t stream) {
+  if (!tab || n_pos < 1 || pos0 < 0 || !(theta > 1.0) || !isfinite(theta))
+    return KVC_ERR_INVALID_ARG;
+  if ((int64_t)pos0 + n_pos > INT32_MAX) return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return KVC_ERR_SHAPE;
+  if (!aligned16(tab)) return KVC_ERR_ALIGN;
+  return from_cuda(kvc::launch_rope_table(tab, n_pos, pos0, D, theta, stream));
+}
+
+kvc_status kvc_pack_rerope(const kvc_bf16 *kraw, const kvc_bf16 *vraw,
+                           const int32_t *kept, const int32_t *kept_count,
+                           int32_t L, int32_t H, int32_t D,
+                           const int64_t *tok_off, int32_t n_sess,
+                           int64_t n_tok, int32_t budget,
+                           const float *rope_tab, kvc_bf16 *kview,
+                           kvc_bf16 *vview, int32_t *dev_status,
+                           cudaStream_t stream) {
+  if (!kraw || !vraw || !kept || !kept_count || !tok_off || !rope_tab || !kview || !vview)
+    return KVC_ERR_INVALID_ARG;
+  if (L < 1 || H < 1 || n_sess < 1 || n_tok < 1) return KVC_ERR_INVALID_ARG;
+  if (budget < 1 || budget > 65535) return KVC_ERR_BUDGET;
+  if (!head_dim_ok(D) || n_tok % KVC_BLOCK_TOKENS) return KVC_ERR_SHAPE;
+  if (!aligned16(kraw) || !aligned16(vraw) || !aligned16(rope_tab) || !aligned16(kview) ||
+      !aligned16(vview))
+    return KVC_ERR_ALIGN;
+  if ((int64_t)L * n_sess > 65535) return KVC_ERR_SHAPE;
+  return from_cuda(kvc::launch_pack_rerope(kraw, vraw, kept, kept_count, L, H, D, tok_off,
+                                           n_sess, n_tok, budget, rope_tab, kview, vview,
+                                           dev_status, stream));
+}
+
+kvc_status kvc_init_sentinel(kvc_bf16 *kpool, kvc_bf16 *vpool, int32_t L,
+                             int32_t H, int32_t D, int64_t n_slots,
+                             int32_t sentinel, cudaStream_t stream) {
+  if (!kpool || L < 1 || H < 1 || n_slots < 1 || sentinel < 0 || sentinel >= n_slots)
+    return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D)) return KVC_ERR_SHAPE;
+  int64_t n = (int64_t)L * H * D;
+  k_init_sentinel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(kpool, vpool, L, H, D,
+                                                                    n_slots, sentinel);
+  return from_cuda(cudaGetLastError());
+}
+
+size_t kvc_redirect_free_workspace_size(int32_t n_sess, int32_t N,
+                                        int64_t n_slots) {
+  if (n_sess < 1 || N < 1 || n_slots < 1) return 0;
+  return kvc::redirect_free_ws_bytes(n_sess, N, n_slots);
+}
+
+kvc_status kvc_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
+                             int32_t n_sess, int32_t N, int32_t *refcnt,
+                             int64_t n_slots, int32_t prefix_len,
+                             int32_t sentinel, int32_t *freed,
+                             int32_t freed_cap, int32_t *n_freed, void *ws,
+                             size_t ws_bytes, int32_t *dev_status,
+                             cudaStream_t stream) {
+  if (!slot_map || !keepmask || !refcnt || !n_freed || !ws || (!freed && freed_cap > 0))
+    return KVC_ERR_INVALID_ARG;
+  if (n_sess < 1 || N < 1 || n_slots < 1 || n_slots > INT32_MAX || freed_cap < 0 ||
+      prefix_len < 0 || (int64_t)n_sess * N > INT32_MAX)
+    return KVC_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return KVC_ERR_ALIGN;
+  if (ws_bytes < kvc_redirect_free_workspace_size(n_sess, N, n_slots)) return KVC_ERR_WORKSPACE;
+  return from_cuda(kvc::launch_redirect_free(slot_map, keepmask, n_sess, N, refcnt, n_slots,
+                                             prefix_len, sentinel, freed, freed_cap, n_freed,
+                                             ws, dev_status, stream));
+}
+
+}  // extern "C"

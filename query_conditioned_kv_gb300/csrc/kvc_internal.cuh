@@ -1,0 +1,95 @@
+// kvc_internal.cuh — shared device helpers and the internal launch API of
+// libkvc (sm_103a).  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+constexpr int kBlock = KVC_BLOCK_TOKENS;
+
+// First device-side error wins; a NULL status word disables the record.
+__device__ __forceinline__ void record_error(int32_t *status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) {
+  return __uint_as_float(w << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t w) {
+  return __uint_as_float(w & 0xFFFF0000u);
+}
+// Two fp32 → packed bf16x2 (round to nearest even); `a` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Streaming 16-byte global accesses (data touched once per event).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, uint4 v) {
+  __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+// ------------------------------------------------------------ launches
+// Each returns cudaGetLastError() of its launch(es).
+
+cudaError_t launch_build_meank(const uint16_t *kraw, uint16_t *meank,
+                               int64_t rows, int64_t n_tok, int D,
+                               cudaStream_t s);
+
+cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
+                               float *scores, int L, int H, int Hq, int D,
+                               int W, const int64_t *blk_off, int n_sess,
+                               int64_t nb_total, int nb_max, void *ws,
+                               int32_t *status, cudaStream_t s);
+size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
+                            int nb_max);
+
+cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
+                               int D, int T, float decay, float gain,
+                               int renorm, cudaStream_t s);
+
+cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
+                              const int32_t *slot_map, int32_t sentinel,
+                              float *rule, int n_sess, int L, int H, int Hq,
+                              int D, int N, int64_t n_slots, void *ws,
+                              int32_t *status, cudaStream_t s);
+size_t score_qmem_ws_bytes(int n_sess, int L, int Hq, int N);
+
+cudaError_t launch_select(const float *scores, const int64_t *seg_off,
+                          int n_seg, int max_seg_len, int budget, int n_sink,
+                          int n_recent, int32_t *kept, int32_t *kept_count,
+                          uint32_t *keepmask, int32_t *status,
+                          cudaStream_t s);
+
+cudaError_t launch_rope_table(float *tab, int n_pos, int pos0, int D,
+                              double theta, cudaStream_t s);
+
+cudaError_t launch_pack_rerope(const uint16_t *kraw, const uint16_t *vraw,
+                               const int32_t *kept, const int32_t *kept_count,
+                               int L, int H, int D, const int64_t *tok_off,
+                               int n_sess, int64_t n_tok, int budget,
+                               const float *rope_tab, uint16_t *kview,
+                               uint16_t *vview, int32_t *status,
+                               cudaStream_t s);
+
+cudaError_t launch_init_sentinel(uint16_t *kpool, uint16_t *vpool, int L,
+                                 int H, int D, int64_t n_slots,
+                                 int32_t sentinel, cudaStream_t s);
+
+cudaError_t launch_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
+                                 int n_sess, int N, int32_t *refcnt,
+                                 int64_t n_slots, int prefix_len,
+                                 int32_t sentinel, int32_t *freed,
+                                 int freed_cap, int32_t *n_freed, void *ws,
+                                 int32_t *status, cudaStream_t s);
+size_t redirect_free_ws_bytes(int n_sess, int N, int64_t n_slots);
+
+}  // namespace kvc

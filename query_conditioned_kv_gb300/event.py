@@ -1,0 +1,171 @@
+"""One compression event as a user runs it: buffers plus the C-ABI calls.
+
+``MeanKEvent``   score (Mean-K) → select → pack + re-RoPE
+``SlotMapEvent`` score (QueryMemory) → select → redirect + free
+
+Both only allocate caller-side buffers with torch and call the library's
+entry points in order on one stream; an event can be captured in a CUDA
+graph (``capture()``) so that its launches replay without host overhead.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_redirect_free,
+               kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
+               kvc_score_qmem, kvc_score_qmem_workspace_size,
+               kvc_score_workspace_size, kvc_select)
+
+
+def _dev_i64(x, device) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(x, dtype=np.int64), device=device)
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class MeanKEvent:
+    """Buffers and calls of a Mean-K-mode event over ragged sessions.
+
+    Layouts (see include/kvc.h): q [n_sess][L][Hq][W][D], meank
+    [L][H][nb_total][D], kraw/vraw [L_pack][H][n_tok][D]; outputs scores
+    [L][H][nb_total], kept [L][H][n_sess][budget], kview/vview
+    [L_pack][H][n_sess][32·budget][D].  Pack runs on the first L_pack layers.
+    """
+
+    def __init__(self, L: int, H: int, Hq: int, D: int, W: int,
+                 hist: Sequence[int], budget: int, n_sink: int, n_recent: int,
+                 L_pack: Optional[int] = None, theta: float = 1e6,
+                 pos0: int = 0, keepmask: bool = False, device="cuda"):
+        self.L, self.H, self.Hq, self.D, self.W = L, H, Hq, D, W
+        self.hist = [int(n) for n in hist]
+        if any(n % BLOCK_TOKENS for n in self.hist):
+            raise ValueError("history lengths must be multiples of 32 tokens")
+        self.n_sess = len(self.hist)
+        self.budget, self.n_sink, self.n_recent = budget, n_sink, n_recent
+        self.L_pack = L if L_pack is None else L_pack
+        self.device = torch.device(device)
+        tok_off = np.concatenate([[0], np.cumsum(self.hist)]).astype(np.int64)
+        blk_off = tok_off // BLOCK_TOKENS
+        self.n_tok = int(tok_off[-1])
+        self.nb_total = int(blk_off[-1])
+        self.nb_max = max(n // BLOCK_TOKENS for n in self.hist)
+        seg = [0]
+        for l in range(L):
+            for h in range(H):
+                base = (l * H + h) * self.nb_total
+                for r in range(self.n_sess):
+                    seg.append(base + int(blk_off[r + 1]))
+        self.n_seg = L * H * self.n_sess
+        dev = self.device
+        self.tok_off = _dev_i64(tok_off, dev)
+        self.blk_off = _dev_i64(blk_off, dev)
+        self.seg_off = _dev_i64(seg, dev)
+        self.scores = torch.empty(L, H, self.nb_total, dtype=torch.float32, device=dev)
+        self.kept = torch.empty(L, H, self.n_sess, budget, dtype=torch.int32, device=dev)
+        self.kept_count = torch.empty(L, H, self.n_sess, dtype=torch.int32, device=dev)
+        words = (self.nb_max + 31) // 32
+        self.keepmask = (torch.empty(self.n_seg, words, dtype=torch.int32, device=dev)
+                         if keepmask else None)
+        self.ws = _ws(kvc_score_workspace_size(L, H, Hq, W, self.n_sess, self.nb_max), dev)
+        self.view_tokens = BLOCK_TOKENS * budget
+        self.rope_tab = torch.empty(self.view_tokens, D // 2, 2, dtype=torch.float32,
+                                    device=dev)
+        kvc_rope_table(self.rope_tab, self.view_tokens, pos0, D, theta)
+        shape = (self.L_pack, H, self.n_sess, self.view_tokens, D)
+        self.kview = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        self.vview = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    # -- the three steps -------------------------------------------------
+    def score(self, q, meank, stream=None):
+        kvc_score(q, meank, self.scores, self.L, self.H, self.Hq, self.D, self.W,
+                  self.blk_off, self.n_sess, self.nb_total, self.nb_max, self.ws,
+                  self.dev_status, stream)
+
+    def select(self, scores=None, stream=None):
+        kvc_select(self.scores if scores is None else scores, self.seg_off,
+                   self.n_seg, self.nb_max, self.budget, self.n_sink,
+                   self.n_recent, self.kept, self.kept_count, self.keepmask,
+                   self.dev_status, stream)
+
+    def pack(self, kraw, vraw, kept=None, kept_count=None, stream=None):
+        kvc_pack_rerope(kraw, vraw, self.kept if kept is None else kept,
+                        self.kept_count if kept_count is None else kept_count,
+                        self.L_pack, self.H, self.D, self.tok_off, self.n_sess,
+                        self.n_tok, self.budget, self.rope_tab, self.kview,
+                        self.vview, self.dev_status, stream)
+
+    def run(self, q, meank, kraw, vraw, stream=None):
+        """score → select → pack on one stream (asynchronous)."""
+        self.score(q, meank, stream)
+        self.select(stream=stream)
+        self.pack(kraw, vraw, stream=stream)
+
+    # -- CUDA graph ----------------------------------------------------
+    def capture(self, q, meank, kraw, vraw):
+        """Capture run() on these input tensors; replay() re-runs it."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self.run(q, meank, kraw, vraw)  # warm-up (sets kernel attributes)
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(q, meank, kraw, vraw)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+
+class SlotMapEvent:
+    """Buffers and calls of a QueryMemory-mode event: rule score over the
+    paged K pool, token-level select (no forced set), redirect + free."""
+
+    def __init__(self, n_sess: int, N: int, L: int, H: int, Hq: int, D: int,
+                 n_slots: int, budget: int, prefix_len: int, sentinel: int = 0,
+                 freed_cap: Optional[int] = None, device="cuda"):
+        self.n_sess, self.N, self.L, self.H, self.Hq, self.D = n_sess, N, L, H, Hq, D
+        self.n_slots, self.budget = n_slots, budget
+        self.prefix_len, self.sentinel = prefix_len, sentinel
+        dev = self.device = torch.device(device)
+        self.rule = torch.empty(n_sess, N, dtype=torch.float32, device=dev)
+        self.seg_off = _dev_i64(np.arange(n_sess + 1) * N, dev)
+        self.kept = torch.empty(n_sess, budget, dtype=torch.int32, device=dev)
+        self.kept_count = torch.empty(n_sess, dtype=torch.int32, device=dev)
+        self.words = (N + 31) // 32
+        self.keepmask = torch.empty(n_sess, self.words, dtype=torch.int32, device=dev)
+        self.ws_score = _ws(kvc_score_qmem_workspace_size(n_sess, L, Hq, N), dev)
+        self.ws_free = _ws(kvc_redirect_free_workspace_size(n_sess, N, n_slots), dev)
+        self.freed_cap = n_slots if freed_cap is None else freed_cap
+        self.freed = torch.empty(max(self.freed_cap, 1), dtype=torch.int32, device=dev)
+        self.n_freed = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def score(self, M, kpool, slot_map, stream=None):
+        kvc_score_qmem(M, kpool, slot_map, self.sentinel, self.rule, self.n_sess,
+                       self.L, self.H, self.Hq, self.D, self.N, self.n_slots,
+                       self.ws_score, self.dev_status, stream)
+
+    def select(self, rule=None, stream=None):
+        kvc_select(self.rule if rule is None else rule, self.seg_off, self.n_sess,
+                   self.N, self.budget, 0, 0, self.kept, self.kept_count,
+                   self.keepmask, self.dev_status, stream)
+
+    def redirect(self, slot_map, refcnt, keepmask=None, stream=None):
+        kvc_redirect_free(slot_map, self.keepmask if keepmask is None else keepmask,
+                          self.n_sess, self.N, refcnt, self.n_slots, self.prefix_len,
+                          self.sentinel, self.freed, self.freed_cap, self.n_freed,
+                          self.ws_free, self.dev_status, stream)
+
+    def run(self, M, kpool, slot_map, refcnt, stream=None):
+        self.score(M, kpool, slot_map, stream)
+        self.select(stream=stream)
+        self.redirect(slot_map, refcnt, stream=stream)

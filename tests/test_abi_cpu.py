@@ -1,0 +1,110 @@
+"""The C-ABI library loads and exports every entry point of include/kvc.h;
+host-side validation rejects bad arguments before any launch.  CPU only:
+no call here reaches a kernel (every call below fails validation first)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    with open(os.path.join(ROOT, "include", "kvc.h")) as f:
+        src = f.read()
+    for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(kvc_\w+)\s*\(", src, re.M):
+        names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import query_conditioned_kv_gb300.build as b
+    b.build()
+    import query_conditioned_kv_gb300 as k
+    return k
+
+
+def test_header_declares_the_event_calls():
+    names = _declared()
+    for n in ("kvc_build_meank", "kvc_score", "kvc_select", "kvc_pack_rerope",
+              "kvc_redirect_free", "kvc_qmem_update", "kvc_score_qmem",
+              "kvc_rope_table", "kvc_init_sentinel", "kvc_status_string",
+              "kvc_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvc):
+    lib = ctypes.CDLL(kvc.LIB_PATH)
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(kvc):
+    for code in range(0, 11):
+        s = kvc.kvc_status_string(code)
+        assert s and s != "unknown status"
+    assert kvc.kvc_status_string(99) == "unknown status"
+
+
+def test_workspace_queries(kvc):
+    assert kvc.kvc_score_workspace_size(36, 8, 32, 32, 1, 4096) > 0
+    assert kvc.kvc_score_workspace_size(1, 3, 4, 1, 1, 1) == 0  # Hq % H
+    assert kvc.kvc_score_qmem_workspace_size(64, 36, 32, 32768) >= 64 * 36 * 32 * 32768 * 4
+    assert kvc.kvc_redirect_free_workspace_size(64, 32768, 1839120) >= 1839120 * 4
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-NULL address; never dereferenced
+
+
+def _call(kvc, name, *args):
+    return getattr(kvc.lib, name)(*args)
+
+
+def test_validation_rejects_before_launch(kvc):
+    P, U = FAKE, FAKE + 2  # U: misaligned
+    # build_meank: shape (n_tok % 32), head dim, alignment, NULL
+    assert _call(kvc, "kvc_build_meank", P, P, 1, 1, 128, 33, None, None) == 2
+    assert _call(kvc, "kvc_build_meank", P, P, 1, 1, 96, 64, None, None) == 2
+    assert _call(kvc, "kvc_build_meank", U, P, 1, 1, 128, 64, None, None) == 4
+    assert _call(kvc, "kvc_build_meank", None, P, 1, 1, 128, 64, None, None) == 1
+    # score: Hq % H, too many rows, workspace too small
+    assert _call(kvc, "kvc_score", P, P, P, 1, 3, 4, 128, 16, P, 1, 128, 128, P,
+                 1 << 20, None, None) == 2
+    assert _call(kvc, "kvc_score", P, P, P, 1, 1, 16, 128, 32, P, 1, 128, 128, P,
+                 1 << 20, None, None) == 2
+    assert _call(kvc, "kvc_score", P, P, P, 1, 2, 4, 64, 16, P, 1, 128, 128, P,
+                 8, None, None) == 5
+    # select: budget rules and the segment cap
+    assert _call(kvc, "kvc_select", P, P, 1, 100, 0, 0, 0, P, P, None, None, None) == 3
+    assert _call(kvc, "kvc_select", P, P, 1, 100, 4, 3, 2, P, P, None, None, None) == 3
+    assert _call(kvc, "kvc_select", P, P, 1, 100, 4, -1, 0, P, P, None, None, None) == 3
+    assert _call(kvc, "kvc_select", P, P, 1, 49153, 4, 1, 1, P, P, None, None, None) == 2
+    # pack: shape, alignment, budget
+    assert _call(kvc, "kvc_pack_rerope", P, P, P, P, 1, 1, 128, P, 1, 100, 4, P, P, P,
+                 None, None) == 2
+    assert _call(kvc, "kvc_pack_rerope", P, U, P, P, 1, 1, 128, P, 1, 128, 4, P, P, P,
+                 None, None) == 4
+    assert _call(kvc, "kvc_pack_rerope", P, P, P, P, 1, 1, 128, P, 1, 128, 0, P, P, P,
+                 None, None) == 3
+    # rope table: theta must be > 1
+    assert _call(kvc, "kvc_rope_table", P, 16, 0, 128, 0.5, None) == 1
+    # sentinel outside the pool
+    assert _call(kvc, "kvc_init_sentinel", P, None, 1, 8, 128, 10, 10, None) == 1
+    # score_qmem: H·D not a multiple of 256
+    assert _call(kvc, "kvc_score_qmem", P, P, P, 0, P, 1, 1, 1, 2, 64, 16, 10, P, 1 << 30,
+                 None, None) == 2
+    # redirect: workspace too small
+    assert _call(kvc, "kvc_redirect_free", P, P, 1, 64, P, 100, 0, 0, P, 100, P, P, 16,
+                 None, None) == 5
+    assert _call(kvc, "kvc_device_status", None, None) == 1
+
+
+def test_binding_raises_on_error(kvc):
+    with pytest.raises(kvc.KvcError) as ei:
+        kvc._ok(3, "kvc_select")
+    assert ei.value.code == 3 and "budget" in str(ei.value)

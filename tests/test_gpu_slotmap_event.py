@@ -1,0 +1,225 @@
+"""GPU ↔ oracle parity of the QueryMemory event: memory update, rule score,
+token select, redirect + alias-aware free (bit-exact slot maps, refcounts
+and free lists), plus the dead-slot sentinel."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import workloads as W  # noqa: E402
+from helpers import NEAR_TIE_REL, assert_scores_close, kth_gap  # noqa: E402
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import query_conditioned_kv_gb300 as k
+    return k
+
+
+def small_cfg(H=8, D=128, **kw):
+    base = dict(name="sm", n_sess=3, N=1008, prefix=256, page=16, L=2, H=H,
+                Hq=4 * H, D=D, T=32, turns=4, budget=300, seed=31)
+    base.update(kw)
+    return W.SlotMapConfig(**base)
+
+
+def kpool_of(cfg, device):
+    return torch.stack([cfg.kpool_layer(l, device) for l in range(cfg.L)])
+
+
+def memory_chain(orc, cfg):
+    """Oracle QueryMemory after cfg.turns turns (an input of the score)."""
+    M = np.zeros((cfg.n_sess, cfg.L, cfg.Hq, cfg.D), np.float32)
+    for t in range(cfg.turns):
+        M = orc.qmem_update(M, W.bf16_bits(cfg.q_turn(t)), cfg.decay, cfg.gain)
+    return M
+
+
+def with_prior_redirects(cfg, sm, rng, frac=0.05):
+    """Positions already redirected by an earlier event (private part only)."""
+    sm = sm.copy()
+    dead = rng.random(sm.shape) < frac
+    dead[:, :cfg.prefix] = False
+    sm[dead] = cfg.sentinel
+    return sm
+
+
+def test_qmem_update_parity(kvc, orc):
+    cfg = small_cfg()
+    M = torch.zeros(cfg.n_sess, cfg.L, cfg.Hq, cfg.D, dtype=torch.float32, device=DEV)
+    Mo = np.zeros(tuple(M.shape), np.float32)
+    for t in range(cfg.turns):
+        q = cfg.q_turn(t, DEV)
+        kvc.kvc_qmem_update(M, q, cfg.n_sess, cfg.L, cfg.Hq, cfg.D, cfg.T,
+                            cfg.decay, cfg.gain, 1)
+        Mo = orc.qmem_update(Mo, W.bf16_bits(q), cfg.decay, cfg.gain)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(M.cpu().numpy(), Mo, rtol=2e-5, atol=2e-7)
+    n = np.linalg.norm(M.cpu().numpy().astype(np.float64), axis=-1)
+    np.testing.assert_allclose(n, 1.0, rtol=1e-5)
+    # renorm off follows the plain EMA
+    M2 = torch.zeros_like(M)
+    q = cfg.q_turn(0, DEV)
+    kvc.kvc_qmem_update(M2, q, cfg.n_sess, cfg.L, cfg.Hq, cfg.D, cfg.T, 0.9, 0.1, 0)
+    ref = orc.qmem_update(np.zeros(tuple(M.shape), np.float32), W.bf16_bits(q),
+                          renorm=False)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(M2.cpu().numpy(), ref, rtol=2e-5, atol=1e-8)
+
+
+@pytest.mark.parametrize("H,D", [(8, 128), (2, 128), (4, 64)])
+def test_rule_score_parity(kvc, orc, H, D):
+    cfg = small_cfg(H=H, D=D)
+    rng = np.random.default_rng(H * 1000 + D)
+    sm = with_prior_redirects(cfg, cfg.slot_maps(), rng)
+    kp = kpool_of(cfg, DEV)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    M = memory_chain(orc, cfg)
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                      cfg.budget, cfg.prefix, cfg.sentinel, device=DEV)
+    ev.score(torch.from_numpy(M).to(DEV), kp, torch.from_numpy(sm).to(DEV))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(ev.dev_status) == 0
+    got = ev.rule.cpu().numpy()
+    kpb = W.bf16_bits(kp)
+    for r in range(cfg.n_sess):
+        ref = orc.rule_session(M[r], kpb, sm[r], cfg.H, cfg.sentinel)
+        dead = sm[r] == cfg.sentinel
+        assert np.all(got[r][dead] == -1.0) and np.all(ref[dead] == -1.0)
+        assert_scores_close(got[r][~dead], ref[~dead], "rule")
+        live_sum = float(got[r][~dead].astype(np.float64).sum())
+        assert abs(live_sum - cfg.L * cfg.Hq) < 1e-3 * cfg.L * cfg.Hq
+
+
+def _redirect_case(orc, cfg, rng):
+    sm = with_prior_redirects(cfg, cfg.slot_maps(), rng)
+    rc = cfg.refcounts(sm)
+    rule = rng.random(sm.shape).astype(np.float32)
+    rule[sm == cfg.sentinel] = -1.0
+    off = (np.arange(cfg.n_sess + 1) * cfg.N).astype(np.int64)
+    _, _, mask = orc.select_segments(rule.reshape(-1), off, cfg.budget, 0, 0)
+    return sm, rc, mask
+
+
+def test_redirect_free_bit_exact(kvc, orc):
+    cfg = small_cfg()
+    rng = np.random.default_rng(5)
+    sm, rc, mask = _redirect_case(orc, cfg, rng)
+    # the shared prefix is dropped by every session in places: counts reach
+    # zero there, yet nothing in the prefix may be freed
+    mask[:, :2] = 0
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                      cfg.budget, cfg.prefix, cfg.sentinel, device=DEV)
+    sm_d = torch.from_numpy(sm).to(DEV)
+    rc_d = torch.from_numpy(rc).to(DEV)
+    ev.redirect(sm_d, rc_d, keepmask=torch.from_numpy(mask.view(np.int32)).to(DEV))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(ev.dev_status) == 0
+    sm_ref, rc_ref, freed_ref, code, nf = orc.redirect_free(sm, mask, rc, cfg.prefix,
+                                                            cfg.sentinel)
+    assert code == 0
+    assert np.array_equal(sm_d.cpu().numpy(), sm_ref)
+    assert np.array_equal(rc_d.cpu().numpy(), rc_ref)
+    n = int(ev.n_freed.item())
+    assert n == nf
+    assert np.array_equal(ev.freed[:n].cpu().numpy(), freed_ref)
+    # every freed slot is unreferenced, not the dead slot, not in the prefix
+    live = set(sm_ref.reshape(-1).tolist())
+    pref = set(sm[:, :cfg.prefix].reshape(-1).tolist())
+    for u in freed_ref.tolist():
+        assert u not in live and u != cfg.sentinel and u not in pref
+
+
+def test_redirect_capacity_and_bounds(kvc, orc):
+    cfg = small_cfg()
+    rng = np.random.default_rng(6)
+    sm, rc, mask = _redirect_case(orc, cfg, rng)
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+    cap = 7
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                      cfg.budget, cfg.prefix, cfg.sentinel, freed_cap=cap, device=DEV)
+    ev.redirect(torch.from_numpy(sm).to(DEV), torch.from_numpy(rc).to(DEV),
+                keepmask=torch.from_numpy(mask.view(np.int32)).to(DEV))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(ev.dev_status) == 10  # KVC_ERR_CAPACITY
+    _, _, freed_ref, _, nf = orc.redirect_free(sm, mask, rc, cfg.prefix, cfg.sentinel)
+    assert int(ev.n_freed.item()) == nf > cap
+    assert np.array_equal(ev.freed[:cap].cpu().numpy(), freed_ref[:cap])
+    # a slot outside the pool: recorded, left in place, nothing dereferenced
+    sm2 = sm.copy()
+    j = int(np.nonzero(~np.asarray([(mask[0, i // 32] >> (i % 32)) & 1
+                                    for i in range(cfg.N)], bool))[0][-1])
+    sm2[0, j] = cfg.n_slots + 5
+    ev2 = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                       cfg.budget, cfg.prefix, cfg.sentinel, device=DEV)
+    sm2_d = torch.from_numpy(sm2).to(DEV)
+    ev2.redirect(sm2_d, torch.from_numpy(rc).to(DEV),
+                 keepmask=torch.from_numpy(mask.view(np.int32)).to(DEV))
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(ev2.dev_status) == 7  # KVC_ERR_BOUNDS
+    assert int(sm2_d[0, j].item()) == cfg.n_slots + 5
+
+
+def test_sentinel_rows(kvc):
+    L, H, D, n_slots = 3, 8, 128, 40
+    kp = torch.randn(L, n_slots, H, D, device=DEV).to(torch.bfloat16)
+    vp = torch.randn(L, n_slots, H, D, device=DEV).to(torch.bfloat16)
+    before_k, before_v = kp.clone(), vp.clone()
+    kvc.kvc_init_sentinel(kp, vp, L, H, D, n_slots, 0)
+    torch.cuda.synchronize()
+    kb = kp.view(torch.int16).cpu().numpy().view(np.uint16)
+    vb = vp.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.all(kb[:, 0] == 0xC61C) and np.all(vb[:, 0] == 0)
+    assert float(kp[0, 0, 0, 0].float()) == -9984.0
+    assert torch.equal(kp[:, 1:], before_k[:, 1:]) and torch.equal(vp[:, 1:], before_v[:, 1:])
+
+
+def test_slotmap_event_end_to_end(kvc, orc):
+    cfg = small_cfg(n_sess=4, N=2048 + 16 * 5, prefix=512, budget=700)
+    rng = np.random.default_rng(8)
+    sm = with_prior_redirects(cfg, cfg.slot_maps(), rng, frac=0.03)
+    rc = cfg.refcounts(sm)
+    kp = kpool_of(cfg, DEV)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    M = memory_chain(orc, cfg)
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                      cfg.budget, cfg.prefix, cfg.sentinel, device=DEV)
+    sm_d = torch.from_numpy(sm).to(DEV)
+    rc_d = torch.from_numpy(rc).to(DEV)
+    ev.run(torch.from_numpy(M).to(DEV), kp, sm_d, rc_d)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(ev.dev_status) == 0
+    kpb = W.bf16_bits(kp)
+    rule_ref = np.stack([orc.rule_session(M[r], kpb, sm[r], cfg.H, cfg.sentinel)
+                         for r in range(cfg.n_sess)])
+    off = (np.arange(cfg.n_sess + 1) * cfg.N).astype(np.int64)
+    kept_ref, cnt_ref, mask_ref = orc.select_segments(rule_ref.reshape(-1), off,
+                                                      cfg.budget, 0, 0)
+    kept = ev.kept.cpu().numpy()
+    assert np.array_equal(ev.kept_count.cpu().numpy(), cnt_ref)
+    near = 0
+    for r in range(cfg.n_sess):
+        if not np.array_equal(kept[r], kept_ref[r]):
+            gap = kth_gap(rule_ref[r], cfg.budget, 0, 0)
+            assert gap is not None and gap < NEAR_TIE_REL, (r, gap)
+            near += 1
+    # redirect/free of the GPU's own keep mask equals the oracle's on it
+    mask = ev.keepmask.cpu().numpy().view(np.uint32)
+    sm_ref, rc_ref, freed_ref, code, nf = orc.redirect_free(sm, mask, rc, cfg.prefix,
+                                                            cfg.sentinel)
+    assert code == 0
+    assert np.array_equal(sm_d.cpu().numpy(), sm_ref)
+    assert np.array_equal(rc_d.cpu().numpy(), rc_ref)
+    assert int(ev.n_freed.item()) == nf
+    assert np.array_equal(ev.freed[:nf].cpu().numpy(), freed_ref)
+    print(f"slot-map event: near-tie sessions {near} of {cfg.n_sess}")
