@@ -23,8 +23,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def kvc():
-    import query_conditioned_kv_gb300.build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import query_conditioned_kv_gb300 as k
     return k
 
