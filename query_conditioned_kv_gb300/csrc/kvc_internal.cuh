@@ -52,6 +52,15 @@ cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
 size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
                             int nb_max);
 
+// tcgen05 scorer (score_tc.cu); cudaErrorNotSupported if the shape is not
+// covered (the caller then uses the CUDA-core scorer).
+bool score_tc_supported(int R, int W, int D);
+size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max);
+cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *scores, int L,
+                            int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
+                            int64_t nb_total, int nb_max, void *ws, int32_t *status,
+                            cudaStream_t s);
+
 cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
                                int D, int T, float decay, float gain,
                                int renorm, cudaStream_t s);

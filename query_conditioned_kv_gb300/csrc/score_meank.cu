@@ -22,6 +22,8 @@
 //           w into the block scores.
 // The logit tile is an R×64×D fp32 product from shared memory (q and Mean-K
 // staged transposed so that both operand reads are bank-conflict free).
+#include <stdlib.h>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -271,7 +273,16 @@ size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
   int n_units = L * H * n_sess;
   int R = (Hq / H) * W;
   int split = pick_split(n_units, nb_max);
-  return (size_t)n_units * split * R * sizeof(float2);
+  size_t cc = (size_t)n_units * split * R * sizeof(float2);
+  size_t tc = score_tc_ws_bytes(L, H, Hq, W, n_sess, nb_max);
+  return cc > tc ? cc : tc;
+}
+
+// Which scorer runs: the tensor-core one whenever it covers the shape;
+// KVC_SCORE_PATH=cc selects the CUDA-core one (both are tested).
+static bool prefer_cuda_cores() {
+  const char *e = getenv("KVC_SCORE_PATH");
+  return e && e[0] == 'c' && e[1] == 'c';
 }
 
 cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
@@ -279,6 +290,11 @@ cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
                                int W, const int64_t *blk_off, int n_sess,
                                int64_t nb_total, int nb_max, void *ws,
                                int32_t *status, cudaStream_t s) {
+  if (!prefer_cuda_cores() && score_tc_supported((Hq / H) * W, W, D)) {
+    cudaError_t e = launch_score_tc(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
+                                    nb_total, nb_max, ws, status, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   ScoreArgs a;
   a.q = q;
   a.meank = meank;

@@ -45,6 +45,10 @@ CONFIGS = {
     "gqa6_rows192": W.MeanKConfig(name="g6", L=1, H=2, Hq=12, D=128, W=32,
                                   hist=[32 * 700], budget=64, n_sink=1,
                                   n_recent=8, gamma=W.GAMMA_PLANTED, seed=12),
+    # longer than one 8-CTA cluster covers: two-launch split scoring
+    "split_long": W.MeanKConfig(name="split", L=1, H=2, Hq=8, D=128, W=32,
+                                hist=[32 * 4500, 32 * 700], budget=96, n_sink=1,
+                                n_recent=4, gamma=W.GAMMA_PLANTED, L_pack=1, seed=13),
 }
 
 
@@ -125,6 +129,21 @@ def test_score_parity(kvc, orc, name):
     c = case(kvc, orc, name)
     got = c.ev.scores.cpu().numpy()
     assert_scores_close(got.reshape(-1), c.scores_ref.reshape(-1))
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b_scaled", "gqa6_rows192", "split_long"])
+def test_score_parity_cuda_core_scorer(kvc, orc, name, monkeypatch):
+    """The CUDA-core scorer (used for shapes the tensor-core one does not
+    cover) against the oracle on the same inputs."""
+    c = case(kvc, orc, name)
+    monkeypatch.setenv("KVC_SCORE_PATH", "cc")
+    out = torch.full_like(c.ev.scores, -1.0)
+    kvc.kvc_score(c.q, c.meank, out, c.cfg.L, c.cfg.H, c.cfg.Hq, c.cfg.D, c.cfg.W,
+                  c.ev.blk_off, c.cfg.n_sess, c.cfg.nb_total, c.ev.nb_max, c.ev.ws,
+                  c.ev.dev_status)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(c.ev.dev_status) == 0
+    assert_scores_close(out.cpu().numpy().reshape(-1), c.scores_ref.reshape(-1))
 
 
 @pytest.mark.parametrize("name", list(CONFIGS))
