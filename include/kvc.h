@@ -114,7 +114,7 @@ kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
  *   z[w,g,b]   = q[l, h*G+g, w] · meank[l,h,b] / sqrt(D)
  *   LSE[w,g]   = log Σ_b exp z[w,g,b]          (over the session's blocks)
  *   score[l,h,b] = (1/W) Σ_w max_g exp(z[w,g,b] − LSE[w,g])
- *   q        device bf16 [n_sess][L][Hq][W][D]  pre-RoPE query window
+ *   q        device bf16 [L][n_sess][Hq][W][D]  pre-RoPE query window
  *   meank    device bf16 [L][H][nb_total][D]
  *   blk_off  device int64 [n_sess+1]  session r owns blocks
  *            [blk_off[r], blk_off[r+1]) of every (l, h) row; blk_off[0] = 0,
@@ -134,6 +134,12 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                      const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
                      int32_t nb_max, void *ws, size_t ws_bytes,
                      int32_t *dev_status, cudaStream_t stream);
+
+/* Number of kernels one kvc_score call with these sizes launches on this
+ * device (1: tensor-core scorer with a thread-block-cluster LSE exchange;
+ * 2: two-launch scoring), 0 for invalid sizes.  Host-only query. */
+int32_t kvc_score_launches(int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                           int32_t n_sess, int32_t nb_max);
 
 /* ------------------------------------------------------------------------
  * QueryMemory update (IntentKV §4 "Memory recurrence", §7 item 1):

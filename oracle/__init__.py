@@ -127,10 +127,10 @@ def score_meank(q: np.ndarray, meank_all: np.ndarray, H: int,
                 blk_off) -> np.ndarray:
     """Mean-K score of every unit.
 
-    q [n_sess][L][Hq][W][D], meank_all [L][H][nb_total][D] → fp32
+    q [L][n_sess][Hq][W][D], meank_all [L][H][nb_total][D] → fp32
     [L][H][nb_total]; session r owns blocks [blk_off[r], blk_off[r+1]).
     """
-    n_sess, L, Hq, W, D = q.shape
+    L, n_sess, Hq, W, D = q.shape
     G = Hq // H
     nb_total = meank_all.shape[2]
     out = np.zeros((L, H, nb_total), dtype=np.float32)
@@ -138,7 +138,7 @@ def score_meank(q: np.ndarray, meank_all: np.ndarray, H: int,
         for h in range(H):
             for r in range(n_sess):
                 b0, b1 = int(blk_off[r]), int(blk_off[r + 1])
-                out[l, h, b0:b1] = score_unit(q[r, l, h * G:(h + 1) * G],
+                out[l, h, b0:b1] = score_unit(q[l, r, h * G:(h + 1) * G],
                                               meank_all[l, h, b0:b1])
     return out
 

@@ -18,7 +18,7 @@ import os
 __all__ = [
     "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG",
     "kvc_status_string", "kvc_version", "kvc_device_status",
-    "kvc_build_meank", "kvc_score_workspace_size", "kvc_score",
+    "kvc_build_meank", "kvc_score_workspace_size", "kvc_score_launches", "kvc_score",
     "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
@@ -52,6 +52,7 @@ _SIGS = {
     "kvc_device_status": (_c.c_int, [_P, _P]),
     "kvc_build_meank": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _P, _P]),
     "kvc_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "kvc_score_launches": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "kvc_score": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
                              _I32, _I64, _I32, _P, _SZ, _P, _P]),
     "kvc_qmem_update": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32,
@@ -126,6 +127,10 @@ def kvc_build_meank(kraw, meank, L, H, D, n_tok, dev_status=None, stream=None):
 
 def kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max) -> int:
     return int(lib.kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max))
+
+
+def kvc_score_launches(L, H, Hq, D, W, n_sess, nb_max) -> int:
+    return int(lib.kvc_score_launches(L, H, Hq, D, W, n_sess, nb_max))
 
 
 def kvc_score(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,

@@ -88,6 +88,13 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                                            nb_total, nb_max, ws, dev_status, stream));
 }
 
+int32_t kvc_score_launches(int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                           int32_t n_sess, int32_t nb_max) {
+  if (L < 1 || H < 1 || Hq < H || Hq % H || W < 1 || n_sess < 1 || nb_max < 1 || !head_dim_ok(D))
+    return 0;
+  return kvc::score_meank_launches(H, Hq, D, W, nb_max);
+}
+
 kvc_status kvc_qmem_update(float *M, const kvc_bf16 *q_turn, int32_t n_sess,
                            int32_t L, int32_t Hq, int32_t D, int32_t T,
                            float decay, float gain, int32_t renorm,

@@ -84,7 +84,7 @@ __device__ __forceinline__ bool session_range(const ScoreArgs &a, int r,
 __device__ void stage_q(const ScoreArgs &a, float *qT, int RP, int l, int h,
                         int r) {
   const uint16_t *src =
-      a.q + ((((int64_t)r * a.L + l) * a.Hq + (int64_t)h * a.G) * a.W) * a.D;
+      a.q + ((((int64_t)l * a.n_sess + r) * a.Hq + (int64_t)h * a.G) * a.W) * a.D;
   int n = RP * a.D;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     int row = i / a.D, d = i - row * a.D;
@@ -283,6 +283,15 @@ size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
 static bool prefer_cuda_cores() {
   const char *e = getenv("KVC_SCORE_PATH");
   return e && e[0] == 'c' && e[1] == 'c';
+}
+
+int score_meank_launches(int H, int Hq, int D, int W, int nb_max) {
+  int R = (Hq / H) * W;
+  if (!prefer_cuda_cores() && score_tc_supported(R, W, D)) {
+    int n = score_tc_launches(R, W, D, nb_max);
+    if (n > 0) return n;
+  }
+  return 2;
 }
 
 cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,

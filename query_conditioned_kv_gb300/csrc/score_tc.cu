@@ -22,6 +22,8 @@
 //           each thread owns one block and forms max over g and the mean
 //           over w of 2^(z−LSE) from its own TMEM lane — W exponentials
 //           per block, no cross-lane traffic.
+// Two CTAs share each SM (≤ 256 TMEM columns and ≈ 100 KB of shared memory
+// each), so one CTA's TMA load overlaps the other's epilogue.
 // Warp roles: warps 0–3 read TMEM (warp i owns lanes 32i…32i+31), warp 4
 // issues TMA and MMA.  Every wait is bounded; on a timeout the CTA records
 // KVC_ERR_TIMEOUT, skips the remaining math, still meets every cluster
@@ -36,11 +38,12 @@ namespace {
 
 constexpr int kEpiThreads = 128;
 constexpr int kThreadsTC = kEpiThreads + 32;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 256;  // two CTAs share an SM's 512 columns
 constexpr float kLog2eTC = 1.4426950408889634f;
 constexpr uint32_t kWaitLimit = 1u << 24;  // ≈ 1–2 s with the back-off below
 
 enum Mode { kCluster = 0, kPass1 = 1, kPass2 = 2 };
+constexpr int kMaxCluster = 16;  // non-portable above 8
 
 struct TcArgs {
   float *scores;
@@ -240,7 +243,7 @@ k_score_tc(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CU
   if (!sess_ok && chunk == 0 && threadIdx.x == 0) record_error(a.status, KVC_ERR_BOUNDS);
 
   const int mk_row0 = (int)(((int64_t)l * a.H + h) * a.nb_total + b0 + blk_base);
-  const int q_row0 = (int)((((int64_t)r * a.L + l) * a.Hq + (int64_t)h * a.G) * a.W);
+  const int q_row0 = (int)((((int64_t)l * a.n_sess + r) * a.Hq + (int64_t)h * a.G) * a.W);
   const uint32_t bar0 = smem_u32(bars);
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
@@ -344,18 +347,32 @@ k_score_tc(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CU
             float v[32];
             tmem_ld32(tmem + lane_base + (uint32_t)((rt * S + s) * 128 + 32 * c), v);
             const int col0 = s * 128 + 32 * c;  // block offset within the CTA
-            float cm = -INFINITY;
+            const int nv = min(32, valid - col0);
+            if (nv <= 0) continue;
+            if (nv < 32) {
 #pragma unroll
-            for (int j = 0; j < 32; j++)
-              if (col0 + j < valid) cm = fmaxf(cm, v[j] * zs);
-            if (cm == -INFINITY) continue;
-            float mn = fmaxf(pm[rt], cm);
-            float acc = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * exp2f(pm[rt] - mn);
+              for (int j = 0; j < 32; j++)
+                if (j >= nv) v[j] = -INFINITY;
+            }
+            // max of the raw products (zs > 0), then 2^(v·zs − max·zs) by FFMA
+            float m01 = fmaxf(v[0], v[1]), m23 = fmaxf(v[2], v[3]);
 #pragma unroll
-            for (int j = 0; j < 32; j++)
-              if (col0 + j < valid) acc += exp2f(v[j] * zs - mn);
+            for (int j = 4; j < 32; j += 4) {
+              m01 = fmaxf(m01, fmaxf(v[j], v[j + 1]));
+              m23 = fmaxf(m23, fmaxf(v[j + 2], v[j + 3]));
+            }
+            const float mn = fmaxf(pm[rt], fmaxf(m01, m23) * zs);
+            float a0 = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * exp2f(pm[rt] - mn);
+            float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              a0 += exp2f(fmaf(v[j], zs, -mn));
+              a1 += exp2f(fmaf(v[j + 1], zs, -mn));
+              a2 += exp2f(fmaf(v[j + 2], zs, -mn));
+              a3 += exp2f(fmaf(v[j + 3], zs, -mn));
+            }
             pm[rt] = mn;
-            ps[rt] = acc;
+            ps[rt] = (a0 + a1) + (a2 + a3);
           }
         }
       }
@@ -379,10 +396,13 @@ k_score_tc(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CU
     for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads) {
       float m = -INFINITY, s = 0.f;
       if (MODE == kCluster) {
-        for (int c = 0; c < n_ct; c++) {
-          float2 p = ld_dsmem_f2(smem_u32(part + rr), (uint32_t)c);
-          lse_merge(m, s, p.x, p.y);
-        }
+        float2 pv[16];
+#pragma unroll
+        for (int c = 0; c < 16; c++)
+          pv[c] = c < n_ct ? ld_dsmem_f2(smem_u32(part + rr), (uint32_t)c)
+                           : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int c = 0; c < 16; c++) lse_merge(m, s, pv[c].x, pv[c].y);
       } else {
         const float2 *src = a.part + (int64_t)unit * a.n_chunk * (RT * 128) + rr;
         for (int c = 0; c < n_ct; c++) {
@@ -487,7 +507,7 @@ Plan plan(int R, int W, int D, int nb_max) {
   Plan p{};
   p.ok = (D == 64 || D == 128) && (W == 8 || W == 16 || W == 32) && R >= 1 && R <= 256;
   p.RT = R <= 128 ? 1 : 2;
-  p.S = p.RT == 1 ? 4 : 2;
+  p.S = p.RT == 1 ? 2 : 1;  // TMEM: RT·S·128 ≤ 256 and S·n2c ≤ 256
   p.C = (nb_max + p.S * 128 - 1) / (p.S * 128);
   p.n2 = (R + 15) / 16 * 16;
   p.n2c = (p.n2 + 31) / 32 * 32;
@@ -498,8 +518,8 @@ size_t smem_bytes(int RT, int S, int D) {
   int KB = D / 64;
   size_t b = 1024 /*align slack*/ + (size_t)S * KB * 16384 + (size_t)KB * RT * 16384 +
              (3 * S + 2) * 8 + 4 + 16 + 16 + RT * 128 * 8 + 256 * 4;
-  // one CTA per SM: its 512 TMEM columns are then always free
-  return b < 120 * 1024 ? 120 * 1024 : b;
+  // at most two CTAs per SM, so their 2 × 256 TMEM columns always fit
+  return b < 80 * 1024 ? 80 * 1024 : b;
 }
 
 template <int MODE, int RT, int S, int W>
@@ -510,6 +530,10 @@ cudaError_t launch_mode(const CUtensorMap &mk, const CUtensorMap &qm, const TcAr
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  if (MODE == kCluster && C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(kThreadsTC);
@@ -530,23 +554,69 @@ cudaError_t launch_mode(const CUtensorMap &mk, const CUtensorMap &qm, const TcAr
   return cudaLaunchKernelEx(&cfg, kern, mk, qm, a);
 }
 
+// Whether clusters of C CTAs of this kernel can be resident at all.
+template <int RT, int S, int W>
+bool cluster_fits(int C, int D) {
+  auto kern = k_score_tc<kCluster, RT, S, W>;
+  size_t smem = smem_bytes(RT, S, D);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return false;
+  if (C > 8 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3(kThreadsTC);
+  cfg.dynamicSmemBytes = smem;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return n > 0;
+}
+
 template <int RT, int S, int W>
 cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, const TcArgs &a,
                         int n_units, int C, cudaStream_t s) {
-  if (C <= 8) return launch_mode<kCluster, RT, S, W>(mk, qm, a, n_units, C, s);
+  if (C <= kMaxCluster && cluster_fits<RT, S, W>(C, a.D))
+    return launch_mode<kCluster, RT, S, W>(mk, qm, a, n_units, C, s);
   cudaError_t e = launch_mode<kPass1, RT, S, W>(mk, qm, a, n_units, C, s);
   if (e != cudaSuccess) return e;
   return launch_mode<kPass2, RT, S, W>(mk, qm, a, n_units, C, s);
+}
+
+template <int RT, int S>
+int launches_rt(int C, int W, int D) {
+  bool fits = W == 8    ? cluster_fits<RT, S, 8>(C, D)
+              : W == 16 ? cluster_fits<RT, S, 16>(C, D)
+                        : cluster_fits<RT, S, 32>(C, D);
+  return (C <= kMaxCluster && fits) ? 1 : 2;
 }
 
 }  // namespace
 
 bool score_tc_supported(int R, int W, int D) { return plan(R, W, D, 1).ok; }
 
+int score_tc_launches(int R, int W, int D, int nb_max) {
+  Plan p = plan(R, W, D, nb_max);
+  if (!p.ok) return 0;
+  return p.RT == 1 ? launches_rt<1, 2>(p.C, W, D) : launches_rt<2, 1>(p.C, W, D);
+}
+
 size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max) {
   int R = (Hq / H) * W;
   Plan p = plan(R, W, 128, nb_max);
-  if (!p.ok || p.C <= 8) return 0;
+  if (!p.ok) return 0;  // split-mode partials (also reserved when clusters would do)
   return (size_t)L * H * n_sess * p.C * p.RT * 128 * sizeof(float2);
 }
 
@@ -591,9 +661,9 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
     default: return launch_plan<RTv, Sv, 32>(mk_map, q_map, a, n_units, p.C, s); \
   }
   if (p.RT == 1) {
-    KVC_TC_W(1, 4)
+    KVC_TC_W(1, 2)
   } else {
-    KVC_TC_W(2, 2)
+    KVC_TC_W(2, 1)
   }
 #undef KVC_TC_W
 }

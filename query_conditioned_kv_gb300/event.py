@@ -4,8 +4,15 @@
 ``SlotMapEvent`` score (QueryMemory) → select → redirect + free
 
 Both only allocate caller-side buffers with torch and call the library's
-entry points in order on one stream; an event can be captured in a CUDA
-graph (``capture()``) so that its launches replay without host overhead.
+entry points; an event can be captured in a CUDA graph (``capture()``) so
+that its launches replay without host overhead.
+
+``MeanKEvent.run`` pipelines over groups of layers: the score and select of
+group g+1 (tensor-core and exponential heavy) run on the caller's stream
+while the pack of group g (HBM-bound streaming) runs on a second stream, so
+the two kinds of work share the SMs instead of taking turns.  Every call
+covers whole layers, which is possible because every tensor is laid out
+layer-major.
 """
 from __future__ import annotations
 
@@ -28,10 +35,16 @@ def _ws(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+def groups_hint(L: int) -> int:
+    """Layer groups of the pipelined event: enough to overlap score and
+    pack, few enough that each launch still fills the GPU."""
+    return max(1, min(6, L // 4))
+
+
 class MeanKEvent:
     """Buffers and calls of a Mean-K-mode event over ragged sessions.
 
-    Layouts (see include/kvc.h): q [n_sess][L][Hq][W][D], meank
+    Layouts (see include/kvc.h): q [L][n_sess][Hq][W][D], meank
     [L][H][nb_total][D], kraw/vraw [L_pack][H][n_tok][D]; outputs scores
     [L][H][nb_total], kept [L][H][n_sess][budget], kview/vview
     [L_pack][H][n_sess][32·budget][D].  Pack runs on the first L_pack layers.
@@ -81,31 +94,83 @@ class MeanKEvent:
         self.vview = torch.empty(shape, dtype=torch.bfloat16, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
+        self.side = torch.cuda.Stream(device=dev)
+        self.groups = self._layer_groups(groups_hint(L))
 
-    # -- the three steps -------------------------------------------------
-    def score(self, q, meank, stream=None):
-        kvc_score(q, meank, self.scores, self.L, self.H, self.Hq, self.D, self.W,
-                  self.blk_off, self.n_sess, self.nb_total, self.nb_max, self.ws,
-                  self.dev_status, stream)
+    @staticmethod
+    def _split(L: int, n: int):
+        n = max(1, min(n, L))
+        edges = [round(i * L / n) for i in range(n + 1)]
+        return [(edges[i], edges[i + 1]) for i in range(n) if edges[i + 1] > edges[i]]
 
-    def select(self, scores=None, stream=None):
-        kvc_select(self.scores if scores is None else scores, self.seg_off,
-                   self.n_seg, self.nb_max, self.budget, self.n_sink,
-                   self.n_recent, self.kept, self.kept_count, self.keepmask,
+    def _layer_groups(self, n: int):
+        return self._split(self.L, n)
+
+    # -- the three steps, on a range of layers [l0, l1) ------------------
+    def score(self, q, meank, stream=None, l0=0, l1=None):
+        l1 = self.L if l1 is None else l1
+        kvc_score(q[l0:l1], meank[l0:l1], self.scores[l0:l1], l1 - l0, self.H, self.Hq,
+                  self.D, self.W, self.blk_off, self.n_sess, self.nb_total, self.nb_max,
+                  self.ws, self.dev_status, stream)
+
+    def select(self, scores=None, stream=None, l0=0, l1=None):
+        l1 = self.L if l1 is None else l1
+        per = self.H * self.n_sess
+        kvc_select(self.scores if scores is None else scores,
+                   self.seg_off[l0 * per:l1 * per + 1], (l1 - l0) * per, self.nb_max,
+                   self.budget, self.n_sink, self.n_recent, self.kept[l0:l1],
+                   self.kept_count[l0:l1],
+                   None if self.keepmask is None else self.keepmask[l0 * per:l1 * per],
                    self.dev_status, stream)
 
-    def pack(self, kraw, vraw, kept=None, kept_count=None, stream=None):
-        kvc_pack_rerope(kraw, vraw, self.kept if kept is None else kept,
-                        self.kept_count if kept_count is None else kept_count,
-                        self.L_pack, self.H, self.D, self.tok_off, self.n_sess,
-                        self.n_tok, self.budget, self.rope_tab, self.kview,
-                        self.vview, self.dev_status, stream)
+    def pack(self, kraw, vraw, kept=None, kept_count=None, stream=None, l0=0, l1=None):
+        l1 = self.L_pack if l1 is None else min(l1, self.L_pack)
+        if l1 <= l0:
+            return
+        kept = self.kept if kept is None else kept
+        kept_count = self.kept_count if kept_count is None else kept_count
+        kvc_pack_rerope(kraw[l0:l1], vraw[l0:l1], kept[l0:l1], kept_count[l0:l1],
+                        l1 - l0, self.H, self.D, self.tok_off, self.n_sess, self.n_tok,
+                        self.budget, self.rope_tab, self.kview[l0:l1], self.vview[l0:l1],
+                        self.dev_status, stream)
 
-    def run(self, q, meank, kraw, vraw, stream=None):
-        """score → select → pack on one stream (asynchronous)."""
+    def run_serial(self, q, meank, kraw, vraw, stream=None):
+        """score → select → pack over all layers, one stream."""
         self.score(q, meank, stream)
         self.select(stream=stream)
         self.pack(kraw, vraw, stream=stream)
+
+    def run(self, q, meank, kraw, vraw, timers=None):
+        """The event, layer groups pipelined over two streams (asynchronous
+        with respect to the host; ordered after prior work on the current
+        stream, and the current stream waits for all of it).  `timers`, if
+        given, is a list that receives (stage, start, end) CUDA events around
+        every launch, recorded on the launching stream."""
+        main = torch.cuda.current_stream(self.device)
+        side = self.side
+        side.wait_stream(main)
+
+        def timed(stage, stream, fn):
+            if timers is None:
+                fn()
+                return
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            timers.append((stage, a, b))
+
+        for (l0, l1) in self.groups:
+            timed("score", main, lambda: self.score(q, meank, main, l0, l1))
+            timed("select", main, lambda: self.select(None, main, l0, l1))
+            if l0 < self.L_pack:
+                done = torch.cuda.Event()
+                done.record(main)
+                side.wait_event(done)
+                with torch.cuda.stream(side):
+                    timed("pack", side, lambda: self.pack(kraw, vraw, stream=side, l0=l0, l1=l1))
+        main.wait_stream(side)
 
     # -- CUDA graph ----------------------------------------------------
     def capture(self, q, meank, kraw, vraw):

@@ -1,0 +1,69 @@
+"""Small, self-contained launches of one kernel family for profiling.
+
+Each case builds a reduced 8B-class workload (fewer layers, so a capture
+holds a few GB at most while its inputs still exceed the 129 MB L2), runs the
+event once to produce realistic inputs for the stage, then launches the stage
+`--iters` times.
+
+  python -m query_conditioned_kv_gb300.profile_cases score --layers 16 --iters 3
+  python -m query_conditioned_kv_gb300.profile_cases pack  --layers 4  --iters 3
+  python -m query_conditioned_kv_gb300.profile_cases select --layers 16 --iters 3
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["score", "select", "pack", "event"])
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import MeanKEvent
+
+    dev = torch.device("cuda", 0)
+    cfg = W.scaled(W.config_8b(), L=args.layers)
+    q = cfg.q(dev)
+    meank = torch.empty(cfg.L, cfg.H, cfg.nb_total, cfg.D, dtype=torch.bfloat16, device=dev)
+    if args.case in ("pack", "event"):
+        kraw, vraw = cfg.kv_raw(dev)
+        kvc.kvc_build_meank(kraw, meank, cfg.L, cfg.H, cfg.D, cfg.n_tok)
+    else:
+        # score/select only need the index: draw it directly (same distribution)
+        for l in range(cfg.L):
+            for h in range(cfg.H):
+                meank[l, h] = cfg.meank_direct_unit(l, h, 0, dev)
+        kraw = vraw = None
+    ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                    cfg.n_recent, theta=cfg.theta, device=dev)
+    ev.score(q, meank)
+    ev.select()
+    torch.cuda.synchronize()
+    for _ in range(args.iters):
+        if args.case == "score":
+            ev.score(q, meank)
+        elif args.case == "select":
+            ev.select()
+        elif args.case == "pack":
+            ev.pack(kraw, vraw)
+        else:
+            ev.run(q, meank, kraw, vraw)
+    torch.cuda.synchronize()
+    st = kvc.kvc_device_status(ev.dev_status)
+    if st != 0:
+        raise SystemExit(f"device status {st}: {kvc.kvc_status_string(st)}")
+    print(f"profile case {args.case}: {args.iters} launches on {args.layers} layers ok")
+
+
+if __name__ == "__main__":
+    main()

@@ -187,12 +187,13 @@ class MeanKConfig:
 
     # --- whole tensors --------------------------------------------------
     def q(self, device="cpu") -> torch.Tensor:
-        out = torch.empty(self.n_sess, self.L, self.Hq, self.W, self.D,
+        """bf16 [L][n_sess][Hq][W][D] query windows (layer-major)."""
+        out = torch.empty(self.L, self.n_sess, self.Hq, self.W, self.D,
                           dtype=torch.bfloat16, device=device)
-        for r in range(self.n_sess):
-            for l in range(self.L):
+        for l in range(self.L):
+            for r in range(self.n_sess):
                 for hq in range(self.Hq):
-                    out[r, l, hq] = self.q_unit(r, l, hq, device)
+                    out[l, r, hq] = self.q_unit(r, l, hq, device)
         return out
 
     def kv_raw(self, device="cpu"):
