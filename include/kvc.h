@@ -128,7 +128,7 @@ kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
  * KVC_ERR_ALIGN, KVC_ERR_WORKSPACE.
  * ---------------------------------------------------------------------- */
 size_t kvc_score_workspace_size(int32_t L, int32_t H, int32_t Hq, int32_t W,
-                                int32_t n_sess, int32_t nb_max);
+                                int32_t n_sess, int32_t nb_max, int64_t nb_total);
 kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                      int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
                      const int64_t *blk_off, int32_t n_sess, int64_t nb_total,

@@ -51,7 +51,7 @@ _SIGS = {
     "kvc_version": (_c.c_char_p, []),
     "kvc_device_status": (_c.c_int, [_P, _P]),
     "kvc_build_meank": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _P, _P]),
-    "kvc_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "kvc_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I64]),
     "kvc_score_launches": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "kvc_score": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
                              _I32, _I64, _I32, _P, _SZ, _P, _P]),
@@ -125,8 +125,8 @@ def kvc_build_meank(kraw, meank, L, H, D, n_tok, dev_status=None, stream=None):
                             _ptr(dev_status), _stream(stream)), "kvc_build_meank")
 
 
-def kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max) -> int:
-    return int(lib.kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max))
+def kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max, nb_total) -> int:
+    return int(lib.kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max, nb_total))
 
 
 def kvc_score_launches(L, H, Hq, D, W, n_sess, nb_max) -> int:

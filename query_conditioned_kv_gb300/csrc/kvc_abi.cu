@@ -63,9 +63,11 @@ kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
 }
 
 size_t kvc_score_workspace_size(int32_t L, int32_t H, int32_t Hq, int32_t W,
-                                int32_t n_sess, int32_t nb_max) {
-  if (L < 1 || H < 1 || Hq < H || Hq % H || W < 1 || n_sess < 1 || nb_max < 1) return 0;
-  return kvc::score_meank_ws_bytes(L, H, Hq, W, n_sess, nb_max);
+                                int32_t n_sess, int32_t nb_max, int64_t nb_total) {
+  if (L < 1 || H < 1 || Hq < H || Hq % H || W < 1 || n_sess < 1 || nb_max < 1 ||
+      nb_total < nb_max)
+    return 0;
+  return kvc::score_meank_ws_bytes(L, H, Hq, W, n_sess, nb_max, nb_total);
 }
 
 kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
@@ -82,7 +84,7 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
     return KVC_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(meank) || !aligned16(scores) || !aligned16(ws))
     return KVC_ERR_ALIGN;
-  if (ws_bytes < kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max))
+  if (ws_bytes < kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max, nb_total))
     return KVC_ERR_WORKSPACE;
   return from_cuda(kvc::launch_score_meank(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
                                            nb_total, nb_max, ws, dev_status, stream));
@@ -92,7 +94,7 @@ int32_t kvc_score_launches(int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t 
                            int32_t n_sess, int32_t nb_max) {
   if (L < 1 || H < 1 || Hq < H || Hq % H || W < 1 || n_sess < 1 || nb_max < 1 || !head_dim_ok(D))
     return 0;
-  return kvc::score_meank_launches(H, Hq, D, W, nb_max);
+  return kvc::score_meank_launches(H, Hq, D, W, n_sess, nb_max);
 }
 
 kvc_status kvc_qmem_update(float *M, const kvc_bf16 *q_turn, int32_t n_sess,

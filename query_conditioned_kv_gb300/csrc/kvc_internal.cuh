@@ -50,14 +50,14 @@ cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
                                int64_t nb_total, int nb_max, void *ws,
                                int32_t *status, cudaStream_t s);
 size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
-                            int nb_max);
+                            int nb_max, int64_t nb_total);
 
 // tcgen05 scorer (score_tc.cu); cudaErrorNotSupported if the shape is not
 // covered (the caller then uses the CUDA-core scorer).
 bool score_tc_supported(int R, int W, int D);
-int score_tc_launches(int R, int W, int D, int nb_max);  // 1 (cluster) or 2 (split)
-int score_meank_launches(int H, int Hq, int D, int W, int nb_max);
-size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max);
+int score_tc_launches(int R, int W, int D, int n_sess, int nb_max);  // 1 persistent, 2 split
+int score_meank_launches(int H, int Hq, int D, int W, int n_sess, int nb_max);
+size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max, int64_t nb_total);
 cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *scores, int L,
                             int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
                             int64_t nb_total, int nb_max, void *ws, int32_t *status,

@@ -269,12 +269,12 @@ cudaError_t launch_rpg(const ScoreArgs &a, int n_units, cudaStream_t s) {
 }  // namespace
 
 size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
-                            int nb_max) {
+                            int nb_max, int64_t nb_total) {
   int n_units = L * H * n_sess;
   int R = (Hq / H) * W;
   int split = pick_split(n_units, nb_max);
   size_t cc = (size_t)n_units * split * R * sizeof(float2);
-  size_t tc = score_tc_ws_bytes(L, H, Hq, W, n_sess, nb_max);
+  size_t tc = score_tc_ws_bytes(L, H, Hq, W, n_sess, nb_max, nb_total);
   return cc > tc ? cc : tc;
 }
 
@@ -285,10 +285,10 @@ static bool prefer_cuda_cores() {
   return e && e[0] == 'c' && e[1] == 'c';
 }
 
-int score_meank_launches(int H, int Hq, int D, int W, int nb_max) {
+int score_meank_launches(int H, int Hq, int D, int W, int n_sess, int nb_max) {
   int R = (Hq / H) * W;
   if (!prefer_cuda_cores() && score_tc_supported(R, W, D)) {
-    int n = score_tc_launches(R, W, D, nb_max);
+    int n = score_tc_launches(R, W, D, n_sess, nb_max);
     if (n > 0) return n;
   }
   return 2;

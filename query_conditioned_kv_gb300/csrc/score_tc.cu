@@ -6,28 +6,34 @@
 //   z[ρ,b] = q[ρ]·meank[b]/sqrt(D),  LSE[ρ] = log Σ_b e^z,
 //   score[b] = (1/W) Σ_w max_g exp(z[g·W+w,b] − LSE[g·W+w]).
 //
-// A CTA owns CH = S·128 consecutive blocks of one unit.  Its Mean-K tile
-// (CH × D bf16) and the unit's query rows are brought into shared memory by
-// TMA (128-byte swizzle, the UMMA K-major layout) and stay there for both
-// passes, so Mean-K is read from HBM once.  Both logit products run as
-// tcgen05.mma (bf16 × bf16 → fp32 in TMEM), issued by one thread:
-//   pass 1  D[ρ][b] (M = 128 query rows, N = 128 blocks per MMA): each
-//           epilogue thread owns one query row (one TMEM lane) and keeps an
-//           online (max, Σ2^(z−max)) over its CH columns;
-//   LSE     the per-CTA partials are combined across the unit's CTAs —
-//           through distributed shared memory inside a thread-block cluster
-//           (cluster mode), or through global scratch between two launches
-//           (split mode, histories longer than 8 CTAs' worth);
+// Work item = (unit, chunk of CH = S·128 consecutive blocks).  A CTA brings
+// the chunk's Mean-K (CH × D bf16) and the unit's query rows into shared
+// memory with TMA (128-byte swizzle = the UMMA K-major layout); they stay
+// there for both passes, so Mean-K is read from HBM once.  Both logit
+// products are tcgen05.mma (bf16 × bf16 → fp32 in TMEM) issued by one thread:
+//   pass 1  D[ρ][b] (M = 128 query rows, N = 128 blocks): each epilogue
+//           thread owns one query row (one TMEM lane) and keeps an online
+//           (max, Σ2^(z−max)) over the chunk;
+//   LSE     the chunk partials of a unit are combined through L2: every
+//           item publishes its partials and bumps the unit's counter, then
+//           waits (bounded) until all of the unit's chunks have published;
 //   pass 2  D[b][ρ] (operands swapped: M = 128 blocks, N = R query rows):
 //           each thread owns one block and forms max over g and the mean
-//           over w of 2^(z−LSE) from its own TMEM lane — W exponentials
-//           per block, no cross-lane traffic.
-// Two CTAs share each SM (≤ 256 TMEM columns and ≈ 100 KB of shared memory
-// each), so one CTA's TMA load overlaps the other's epilogue.
+//           over w of 2^(z−LSE) from its own TMEM lane — W exponentials per
+//           block, no cross-lane traffic.
+//
+// Persistent kernel: two CTAs per SM (≤ 256 TMEM columns, ≈ 100 KB shared
+// memory each), items claimed in order from an atomic counter.  A claimed
+// item is always held by a running CTA and pass 1 waits on nothing, so the
+// only CTAs that can wait are those of the last, partially claimed unit; as
+// long as a unit has no more chunks than CTAs fit on the GPU, every wait
+// ends.  Longer units use the two-launch split mode (pass 1 → partials in
+// global memory → pass 2, Mean-K read twice).
+//
 // Warp roles: warps 0–3 read TMEM (warp i owns lanes 32i…32i+31), warp 4
 // issues TMA and MMA.  Every wait is bounded; on a timeout the CTA records
-// KVC_ERR_TIMEOUT, skips the remaining math, still meets every cluster
-// barrier, waits (bounded) for its own copies/MMAs and frees its TMEM.
+// KVC_ERR_TIMEOUT, stops claiming work, waits (bounded) for its own copies
+// and MMAs and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,14 +47,16 @@ constexpr int kThreadsTC = kEpiThreads + 32;
 constexpr uint32_t kTmemCols = 256;  // two CTAs share an SM's 512 columns
 constexpr float kLog2eTC = 1.4426950408889634f;
 constexpr uint32_t kWaitLimit = 1u << 24;  // ≈ 1–2 s with the back-off below
+constexpr int kMaxSessPersist = 2048;      // per-session chunk prefix in smem
 
-enum Mode { kCluster = 0, kPass1 = 1, kPass2 = 2 };
-constexpr int kMaxCluster = 16;  // non-portable above 8
+enum Mode { kPass1 = 1, kPass2 = 2 };
 
 struct TcArgs {
   float *scores;
   const int64_t *blk_off;
-  float2 *part;  // split mode: [unit][chunk][RT·128]
+  float2 *part;    // persistent: [item][RT·128]; split: [unit][chunk][RT·128]
+  int *counter;    // persistent: next item
+  int *unit_done;  // persistent: [n_units] chunks published
   int32_t *status;
   int L, H, Hq, W, G, R, D, n_sess, n_chunk;
   int64_t nb_total;
@@ -88,7 +96,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on phase `parity`; false after the limit.
+// Bounded wait for the completion of the phase with parity `parity`.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitLimit; i++) {
     if (mbar_try(bar, parity)) return true;
@@ -153,30 +161,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
-               : "=f"(v.x), "=f"(v.y)
-               : "r"(remote)
-               : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // (max, sum) ⊕ (max, sum) in base 2.
@@ -192,275 +184,445 @@ __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2
   m = mn;
 }
 
-// ------------------------------------------------------------ the kernel
+// ------------------------------------------------------------ the stages
 
-// Shared memory: [mk: S·KB boxes of 128 rows × 128 B][q: KB boxes of
-// RT·128 rows × 128 B][barriers][tmem holder][part float2 RT·128][lse 256]
-template <int MODE, int RT, int S, int W>
-__global__ void __launch_bounds__(kThreadsTC, 1)
-k_score_tc(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CUtensorMap tm_q,
-           TcArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int KB = a.D / 64;                   // 64-element k-blocks
-  const uint32_t mk_box = 128 * 128;         // bytes per Mean-K box
-  const uint32_t q_box = RT * 128 * 128;     // bytes per query box
-  uint8_t *mk_s = smem;
-  uint8_t *q_s = mk_s + S * KB * mk_box;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(q_s + KB * q_box);
-  // bars: 0 tma_q | 1..S tma_mk | S+1..2S mma1 | 2S+1..3S mma2 | 3S+1 tmem_free
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 3 * S + 2);
-  static_assert(W == 8 || W == 16 || W == 32, "W divides 32");
-  volatile int *flags = reinterpret_cast<volatile int *>(tmem_holder + 1);  // [0] failed
-  float2 *part = reinterpret_cast<float2 *>(
-      (reinterpret_cast<uintptr_t>(tmem_holder + 5) + 15) & ~uintptr_t(15));
-  float *lse_s = reinterpret_cast<float *>(part + RT * 128);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int unit, chunk;
-  if (MODE == kCluster) {
-    chunk = (int)cluster_rank();
-    unit = blockIdx.x / a.n_chunk;
-  } else {
-    chunk = blockIdx.x;
-    unit = blockIdx.y;
+// Shared memory of a CTA: [mk: S·KB boxes of 128 rows × 128 B][q: KB boxes
+// of RT·128 rows × 128 B][barriers][tmem holder, flags][lse][prefix]
+template <int RT, int S>
+struct Smem {
+  uint8_t *mk, *q;
+  uint64_t *bars;  // 0 tma, 1 mma1, 2 mma2, 3 tmem_free
+  uint32_t *tmem_holder;
+  volatile int *flags;  // [0] failed, [1] claimed item
+  float *lse;
+  int *prefix;
+  __device__ Smem(uint8_t *raw, int KB) {
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    mk = base;
+    q = mk + S * KB * 16384;
+    bars = reinterpret_cast<uint64_t *>(q + KB * RT * 16384);
+    tmem_holder = reinterpret_cast<uint32_t *>(bars + 4);
+    flags = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    lse = reinterpret_cast<float *>(tmem_holder + 8);
+    prefix = reinterpret_cast<int *>(lse + 256);
   }
-  const int r = unit % a.n_sess;
-  const int lh = unit / a.n_sess;
-  const int h = lh % a.H, l = lh / a.H;
-  const int64_t b0 = a.blk_off[r], b1 = a.blk_off[r + 1];
-  bool sess_ok = b0 >= 0 && b1 > b0 && b1 <= a.nb_total;
-  const int nb = sess_ok ? (int)(b1 - b0) : 0;
-  const int CH = S * 128;
-  const int blk_base = chunk * CH;
-  const int valid = max(0, min(CH, nb - blk_base));
-  // Split-mode CTAs past the unit's end have nothing to do.
-  if (MODE != kCluster && valid == 0) {
-    if (!sess_ok && chunk == 0 && threadIdx.x == 0) record_error(a.status, KVC_ERR_BOUNDS);
-    return;
+  static size_t bytes(int D, int n_prefix) {
+    int KB = D / 64;
+    return 1024 + (size_t)S * KB * 16384 + (size_t)KB * RT * 16384 + 4 * 8 + 8 * 4 + 256 * 4 +
+           (size_t)n_prefix * 4;
   }
-  if (!sess_ok && chunk == 0 && threadIdx.x == 0) record_error(a.status, KVC_ERR_BOUNDS);
+};
 
-  const int mk_row0 = (int)(((int64_t)l * a.H + h) * a.nb_total + b0 + blk_base);
-  const int q_row0 = (int)((((int64_t)l * a.n_sess + r) * a.Hq + (int64_t)h * a.G) * a.W);
-  const uint32_t bar0 = smem_u32(bars);
-  auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+template <int RT, int S>
+__device__ __forceinline__ void issue_loads(const CUtensorMap *tm_q, const CUtensorMap *tm_mk,
+                                            const Smem<RT, S> &sm, int KB, int q_row0,
+                                            int mk_row0, uint32_t bar) {
+  mbar_expect_tx(bar, (uint32_t)(KB * RT * 16384 + S * KB * 16384));
+  for (int kb = 0; kb < KB; kb++)
+    tma_load_2d(smem_u32(sm.q + kb * RT * 16384), tm_q, kb * 64, q_row0, bar);
+  for (int s = 0; s < S; s++)
+    for (int kb = 0; kb < KB; kb++)
+      tma_load_2d(smem_u32(sm.mk + (s * KB + kb) * 16384), tm_mk, kb * 64, mk_row0 + s * 128, bar);
+}
 
-  if (threadIdx.x == 0) {
-    flags[0] = 0;
-    for (int i = 0; i < 3 * S + 1; i++) mbar_init(BAR(i), 1);
-    mbar_init(BAR(3 * S + 1), 4);  // tmem_free: one arrive per epilogue warp
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_holder)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
+// pass 1: D[ρ][b] = Q · Mean-Kᵀ into TMEM columns (rt·S + s)·128
+template <int RT, int S>
+__device__ __forceinline__ void issue_pass1(uint32_t tmem, const Smem<RT, S> &sm, int KB,
+                                            uint32_t idesc) {
+  for (int s = 0; s < S; s++)
+    for (int rt = 0; rt < RT; rt++)
+      for (int kk = 0; kk < 4 * KB; kk++) {
+        const uint32_t koff = (uint32_t)(kk & 3) * 32u;
+        uint64_t a = smem_desc(smem_u32(sm.q + (kk >> 2) * RT * 16384 + rt * 16384) + koff);
+        uint64_t b = smem_desc(smem_u32(sm.mk + (s * KB + (kk >> 2)) * 16384) + koff);
+        mma_bf16(tmem + (uint32_t)((rt * S + s) * 128), a, b, idesc, kk > 0);
+      }
+}
 
-  // ------------------------------------------------------------ producer
-  if (warp == 4) {
-    if (lane == 0 && valid > 0) {
-      bool ok = true;
-      // loads
-      mbar_expect_tx(BAR(0), KB * q_box);
-      for (int kb = 0; kb < KB; kb++)
-        tma_load_2d(smem_u32(q_s + kb * q_box), &tm_q, kb * 64, q_row0, BAR(0));
-      for (int s = 0; s < S; s++) {
-        mbar_expect_tx(BAR(1 + s), KB * mk_box);
-        for (int kb = 0; kb < KB; kb++)
-          tma_load_2d(smem_u32(mk_s + (s * KB + kb) * mk_box), &tm_mk, kb * 64,
-                      mk_row0 + s * 128, BAR(1 + s));
-      }
-      ok = mbar_wait(BAR(0), 0);
-      if (MODE != kPass2) {
-        // pass 1: D[ρ][b] = Q · Mean-Kᵀ, TMEM columns (rt·S + s)·128
-        for (int s = 0; s < S && ok; s++) {
-          ok = mbar_wait(BAR(1 + s), 0);
-          if (!ok) break;
-          tc_fence_after();
-          for (int rt = 0; rt < RT; rt++)
-            for (int kk = 0; kk < 4 * KB; kk++) {
-              uint32_t koff = (uint32_t)(kk & 3) * 32u;
-              uint64_t adesc = smem_desc(smem_u32(q_s + (kk >> 2) * q_box + rt * 128 * 128) + koff);
-              uint64_t bdesc = smem_desc(smem_u32(mk_s + (s * KB + (kk >> 2)) * mk_box) + koff);
-              mma_bf16(tmem + (uint32_t)((rt * S + s) * 128), adesc, bdesc, a.idesc1, kk > 0);
-            }
-          mma_commit(BAR(1 + S + s));
-        }
-        if (MODE == kCluster && ok) {
-          ok = mbar_wait(BAR(3 * S + 1), 0);  // pass-1 TMEM reads finished
-          tc_fence_after();
-        }
-      } else {
-        for (int s = 0; s < S && ok; s++) ok = mbar_wait(BAR(1 + s), 0);
-        tc_fence_after();
-      }
-      if (MODE != kPass1 && ok) {
-        // pass 2: D[b][ρ] = Mean-K · Qᵀ, TMEM columns s·n2c
-        for (int s = 0; s < S; s++) {
-          for (int kk = 0; kk < 4 * KB; kk++) {
-            uint32_t koff = (uint32_t)(kk & 3) * 32u;
-            uint64_t adesc = smem_desc(smem_u32(mk_s + (s * KB + (kk >> 2)) * mk_box) + koff);
-            uint64_t bdesc = smem_desc(smem_u32(q_s + (kk >> 2) * q_box) + koff);
-            mma_bf16(tmem + (uint32_t)(s * a.n2c), adesc, bdesc, a.idesc2, kk > 0);
-          }
-          mma_commit(BAR(1 + 2 * S + s));
-        }
-      }
-      if (!ok) {
-        flags[0] = 1;
-        record_error(a.status, KVC_ERR_TIMEOUT);
-      }
+// pass 2: D[b][ρ] = Mean-K · Qᵀ into TMEM columns s·n2c
+template <int RT, int S>
+__device__ __forceinline__ void issue_pass2(uint32_t tmem, const Smem<RT, S> &sm, int KB,
+                                            uint32_t idesc, int n2c) {
+  for (int s = 0; s < S; s++)
+    for (int kk = 0; kk < 4 * KB; kk++) {
+      const uint32_t koff = (uint32_t)(kk & 3) * 32u;
+      uint64_t a = smem_desc(smem_u32(sm.mk + (s * KB + (kk >> 2)) * 16384) + koff);
+      uint64_t b = smem_desc(smem_u32(sm.q + (kk >> 2) * RT * 16384) + koff);
+      mma_bf16(tmem + (uint32_t)(s * n2c), a, b, idesc, kk > 0);
     }
-    __syncwarp();
-  }
+}
 
-  // ------------------------------------------------------------ epilogue
-  const float zs = a.zscale;
-  float pm[RT], ps[RT];
+// Pass-1 epilogue: online (max, Σ2^(z−max)) of this thread's query row(s)
+// over the item's `valid` blocks (base 2, z₂ = raw · zs).
+template <int RT, int S>
+__device__ __forceinline__ void epi_pass1(uint32_t tmem, uint32_t lane_base, int valid, float zs,
+                                          float (&pm)[RT], float (&ps)[RT]) {
 #pragma unroll
   for (int rt = 0; rt < RT; rt++) {
     pm[rt] = -INFINITY;
     ps[rt] = 0.f;
   }
-  if (warp < 4) {
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    if (MODE != kPass2 && valid > 0) {
-      for (int s = 0; s < S; s++) {
-        bool ok = __all_sync(0xFFFFFFFFu, flags[0] == 0 && mbar_wait(BAR(1 + S + s), 0));
-        if (!ok) {  // warp-uniform
-          if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
-          flags[0] = 1;
-          break;
+  for (int s = 0; s < S; s++)
+#pragma unroll
+    for (int rt = 0; rt < RT; rt++)
+      for (int c = 0; c < 4; c++) {
+        const int col0 = s * 128 + 32 * c;
+        const int nv = min(32, valid - col0);
+        if (nv <= 0) continue;  // warp-uniform
+        float v[32];
+        tmem_ld32(tmem + lane_base + (uint32_t)((rt * S + s) * 128 + 32 * c), v);
+        if (nv < 32) {
+#pragma unroll
+          for (int j = 0; j < 32; j++)
+            if (j >= nv) v[j] = -INFINITY;
         }
-        tc_fence_after();
+        // max of the raw products (zs > 0), then 2^(v·zs − max) by FFMA
+        float m01 = fmaxf(v[0], v[1]), m23 = fmaxf(v[2], v[3]);
 #pragma unroll
-        for (int rt = 0; rt < RT; rt++) {
-          for (int c = 0; c < 4; c++) {
-            float v[32];
-            tmem_ld32(tmem + lane_base + (uint32_t)((rt * S + s) * 128 + 32 * c), v);
-            const int col0 = s * 128 + 32 * c;  // block offset within the CTA
-            const int nv = min(32, valid - col0);
-            if (nv <= 0) continue;
-            if (nv < 32) {
-#pragma unroll
-              for (int j = 0; j < 32; j++)
-                if (j >= nv) v[j] = -INFINITY;
-            }
-            // max of the raw products (zs > 0), then 2^(v·zs − max·zs) by FFMA
-            float m01 = fmaxf(v[0], v[1]), m23 = fmaxf(v[2], v[3]);
-#pragma unroll
-            for (int j = 4; j < 32; j += 4) {
-              m01 = fmaxf(m01, fmaxf(v[j], v[j + 1]));
-              m23 = fmaxf(m23, fmaxf(v[j + 2], v[j + 3]));
-            }
-            const float mn = fmaxf(pm[rt], fmaxf(m01, m23) * zs);
-            float a0 = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * exp2f(pm[rt] - mn);
-            float a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              a0 += exp2f(fmaf(v[j], zs, -mn));
-              a1 += exp2f(fmaf(v[j + 1], zs, -mn));
-              a2 += exp2f(fmaf(v[j + 2], zs, -mn));
-              a3 += exp2f(fmaf(v[j + 3], zs, -mn));
-            }
-            pm[rt] = mn;
-            ps[rt] = (a0 + a1) + (a2 + a3);
-          }
+        for (int j = 4; j < 32; j += 4) {
+          m01 = fmaxf(m01, fmaxf(v[j], v[j + 1]));
+          m23 = fmaxf(m23, fmaxf(v[j + 2], v[j + 3]));
         }
+        const float mn = fmaxf(pm[rt], fmaxf(m01, m23) * zs);
+        float a0 = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * exp2f(pm[rt] - mn);
+        float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          a0 += exp2f(fmaf(v[j], zs, -mn));
+          a1 += exp2f(fmaf(v[j + 1], zs, -mn));
+          a2 += exp2f(fmaf(v[j + 2], zs, -mn));
+          a3 += exp2f(fmaf(v[j + 3], zs, -mn));
+        }
+        pm[rt] = mn;
+        ps[rt] = (a0 + a1) + (a2 + a3);
       }
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(BAR(3 * S + 1));
-#pragma unroll
-    for (int rt = 0; rt < RT; rt++) part[rt * 128 + threadIdx.x] = make_float2(pm[rt], ps[rt]);
-    if (MODE == kPass1) {
-      float2 *dst = a.part + ((int64_t)unit * a.n_chunk + chunk) * (RT * 128);
-#pragma unroll
-      for (int rt = 0; rt < RT; rt++) dst[rt * 128 + threadIdx.x] = make_float2(pm[rt], ps[rt]);
-    }
-  }
-  if (MODE == kCluster) cluster_sync_all();  // partials visible cluster-wide
+}
 
-  if (warp < 4 && MODE != kPass1) {
-    // LSE of every query row (thread t combines rows t and t+128)
-    const int n_ct = (nb + CH - 1) / CH;
-    for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads) {
-      float m = -INFINITY, s = 0.f;
-      if (MODE == kCluster) {
-        float2 pv[16];
+// Pass-2 epilogue: thread = block; writes the item's block scores.
+template <int S, int W>
+__device__ __forceinline__ void epi_pass2(uint32_t tmem, uint32_t lane_base, int warp, int lane,
+                                          int valid, int n2c, int R, float zs, float invW,
+                                          const float *lse, float *out) {
+  for (int s = 0; s < S; s++) {
+    if (s * 128 >= valid) break;  // uniform
+    float mw[W];
 #pragma unroll
-        for (int c = 0; c < 16; c++)
-          pv[c] = c < n_ct ? ld_dsmem_f2(smem_u32(part + rr), (uint32_t)c)
-                           : make_float2(-INFINITY, 0.f);
+    for (int w = 0; w < W; w++) mw[w] = -INFINITY;
+    for (int c = 0; c < n2c / 32; c++) {
+      float v[32];
+      tmem_ld32(tmem + lane_base + (uint32_t)(s * n2c + 32 * c), v);
 #pragma unroll
-        for (int c = 0; c < 16; c++) lse_merge(m, s, pv[c].x, pv[c].y);
-      } else {
-        const float2 *src = a.part + (int64_t)unit * a.n_chunk * (RT * 128) + rr;
-        for (int c = 0; c < n_ct; c++) {
-          float2 p = src[(int64_t)c * (RT * 128)];
-          lse_merge(m, s, p.x, p.y);
-        }
-      }
-      lse_s[rr] = (m == -INFINITY) ? INFINITY : m + log2f(s);
-    }
-    named_sync_epi();
-    // pass 2 epilogue: thread = block
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    if (valid > 0) {
-      const int n_chunks2 = a.n2c / 32;
-      for (int s = 0; s < S; s++) {
-        bool ok = __all_sync(0xFFFFFFFFu, flags[0] == 0 && mbar_wait(BAR(1 + 2 * S + s), 0));
-        if (!ok) {  // warp-uniform
-          if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
-          flags[0] = 1;
-          break;
-        }
-        tc_fence_after();
-        float mw[W];
-#pragma unroll
-        for (int w = 0; w < W; w++) mw[w] = -INFINITY;
-        for (int c = 0; c < n_chunks2; c++) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + (uint32_t)(s * a.n2c + 32 * c), v);
-#pragma unroll
-          for (int j = 0; j < 32; j++) {
-            const int rho = 32 * c + j;
-            if (rho < a.R) mw[j % W] = fmaxf(mw[j % W], v[j] * zs - lse_s[rho]);
-          }
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < W; w++) acc += exp2f(mw[w]);
-        const int bl = s * 128 + warp * 32 + lane;
-        if (bl < valid)
-          a.scores[((int64_t)l * a.H + h) * a.nb_total + b0 + blk_base + bl] = acc / (float)a.W;
+      for (int j = 0; j < 32; j++) {
+        const int rho = 32 * c + j;
+        if (rho < R) mw[j % W] = fmaxf(mw[j % W], fmaf(v[j], zs, -lse[rho]));
       }
     }
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; w++) acc += exp2f(mw[w]);
+    const int bl = s * 128 + warp * 32 + lane;
+    if (bl < valid) out[bl] = acc * invW;
   }
+}
 
-  // ------------------------------------------------------------ teardown
+__device__ __forceinline__ void alloc_tmem(uint32_t *holder) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(holder)),
+               "r"(kTmemCols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+
+__device__ __forceinline__ void free_tmem(uint32_t tmem) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+               "r"(kTmemCols));
+}
+
+// ------------------------------------------------------ persistent kernel
+
+template <int RT, int S, int W>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+k_score_tc(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CUtensorMap tm_q,
+           TcArgs a) {
+  static_assert(W == 8 || W == 16 || W == 32, "W divides 32");
+  extern __shared__ uint8_t smem_raw[];
+  const int KB = a.D / 64;
+  Smem<RT, S> sm(smem_raw, KB);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int CH = S * 128;
+  const uint32_t bar0 = smem_u32(sm.bars);
+  const uint32_t BAR_TMA = bar0, BAR_MMA1 = bar0 + 8, BAR_MMA2 = bar0 + 16, BAR_FREE = bar0 + 24;
+
+  // per-session chunk counts → prefix (items of one (layer, KV head))
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < a.n_sess; base += 32) {
+      int r = base + lane, cnt = 0;
+      if (r < a.n_sess) {
+        int64_t b0 = a.blk_off[r], b1 = a.blk_off[r + 1];
+        if (b0 >= 0 && b1 > b0 && b1 <= a.nb_total && b1 - b0 <= (int64_t)a.n_chunk * CH)
+          cnt = (int)((b1 - b0 + CH - 1) / CH);
+        else if (blockIdx.x == 0)
+          record_error(a.status, KVC_ERR_BOUNDS);
+      }
+      int x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (r < a.n_sess) sm.prefix[r] = carry + x - cnt;
+      carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) sm.prefix[a.n_sess] = carry;
+  }
+  if (threadIdx.x == 0) {
+    sm.flags[0] = 0;
+    mbar_init(BAR_TMA, 1);
+    mbar_init(BAR_MMA1, 1);
+    mbar_init(BAR_MMA2, 1);
+    mbar_init(BAR_FREE, 4);  // one arrive per epilogue warp
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) alloc_tmem(sm.tmem_holder);
   tc_fence_before();
   __syncthreads();
-  if (warp == 4 && lane == 0 && valid > 0 && flags[0] != 0) {
-    // a wait gave up: let this CTA's own copies and MMAs drain (bounded)
-    for (int i = 0; i < 3 * S + 1; i++) mbar_wait(BAR(i), 0);
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_holder;
+  const int per_lh = sm.prefix[a.n_sess];
+  const int total = a.L * a.H * per_lh;
+  const float zs = a.zscale, invW = 1.f / (float)a.W;
+  bool committed = false;
+
+  for (uint32_t iter = 0;; iter++) {
+    if (threadIdx.x == kEpiThreads) sm.flags[1] = atomicAdd(a.counter, 1);
+    __syncthreads();
+    const int item = sm.flags[1];
+    if (item >= total || sm.flags[0] != 0) break;  // CTA-uniform
+    const uint32_t ph = iter & 1u;
+    // item → (layer, head, session, chunk)
+    const int lh = item / per_lh, rem = item - lh * per_lh;
+    int lo = 0, hi = a.n_sess - 1;  // last r with prefix[r] <= rem
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (sm.prefix[mid] <= rem)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int r = lo, chunk = rem - sm.prefix[r];
+    const int n_chunks = sm.prefix[r + 1] - sm.prefix[r];
+    const int h = lh % a.H, l = lh / a.H;
+    const int unit = lh * a.n_sess + r;
+    const int64_t b0 = a.blk_off[r];
+    const int nb = (int)(a.blk_off[r + 1] - b0);
+    const int valid = min(CH, nb - chunk * CH);
+    const int mk_row0 = (int)(((int64_t)l * a.H + h) * a.nb_total + b0 + (int64_t)chunk * CH);
+    const int q_row0 = (int)((((int64_t)l * a.n_sess + r) * a.Hq + (int64_t)h * a.G) * a.W);
+
+    if (warp == 4) {
+      if (lane == 0) {
+        issue_loads<RT, S>(&tm_q, &tm_mk, sm, KB, q_row0, mk_row0, BAR_TMA);
+        bool ok = mbar_wait(BAR_TMA, ph);
+        if (ok) {
+          tc_fence_after();
+          issue_pass1<RT, S>(tmem, sm, KB, a.idesc1);
+          mma_commit(BAR_MMA1);
+          committed = true;
+          ok = mbar_wait(BAR_FREE, ph);  // pass-1 TMEM reads done
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_pass2<RT, S>(tmem, sm, KB, a.idesc2, a.n2c);
+          mma_commit(BAR_MMA2);
+        } else {
+          sm.flags[0] = 1;
+          record_error(a.status, KVC_ERR_TIMEOUT);
+        }
+      }
+      __syncwarp();
+    } else {
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      float pm[RT], ps[RT];
+      bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(BAR_MMA1, ph));
+      if (ok) {
+        tc_fence_after();
+        epi_pass1<RT, S>(tmem, lane_base, valid, zs, pm, ps);
+      } else {
+#pragma unroll
+        for (int rt = 0; rt < RT; rt++) {
+          pm[rt] = -INFINITY;
+          ps[rt] = 0.f;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR_FREE);
+      // publish this chunk's partials, then wait for the unit's other chunks
+      float2 *mine = a.part + (int64_t)item * (RT * 128);
+#pragma unroll
+      for (int rt = 0; rt < RT; rt++) mine[rt * 128 + threadIdx.x] = make_float2(pm[rt], ps[rt]);
+      __threadfence();
+      named_sync_epi();
+      if (threadIdx.x == 0) {
+        atomicAdd(&a.unit_done[unit], 1);
+        uint32_t i = 0;
+        while (ld_acquire(&a.unit_done[unit]) < n_chunks && ++i < kWaitLimit)
+          if (i > 32) __nanosleep(128);
+        if (i >= kWaitLimit) {
+          sm.flags[0] = 1;
+          record_error(a.status, KVC_ERR_TIMEOUT);
+        }
+      }
+      named_sync_epi();
+      __threadfence();
+      if (!ok) {
+        sm.flags[0] = 1;
+        if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+      }
+      // LSE of every query row (thread t: rows t and t + 128)
+      const float2 *unit_part = a.part + (int64_t)(item - chunk) * (RT * 128);
+      for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads) {
+        float m = -INFINITY, s = 0.f;
+        for (int c = 0; c < n_chunks; c++) {
+          float2 p = __ldcg(unit_part + (int64_t)c * (RT * 128) + rr);
+          lse_merge(m, s, p.x, p.y);
+        }
+        sm.lse[rr] = (m == -INFINITY) ? INFINITY : m + log2f(s);
+      }
+      named_sync_epi();
+      bool ok2 = __all_sync(0xFFFFFFFFu, ok && mbar_wait(BAR_MMA2, ph));
+      if (ok2) {
+        tc_fence_after();
+        float *out = a.scores + ((int64_t)l * a.H + h) * a.nb_total + b0 + (int64_t)chunk * CH;
+        epi_pass2<S, W>(tmem, lane_base, warp, lane, valid, a.n2c, a.R, zs, invW, sm.lse, out);
+      } else {
+        sm.flags[0] = 1;
+      }
+      tc_fence_before();
+    }
+    __syncthreads();  // item done: TMEM and shared memory are free again
+    tc_fence_after();
   }
+
+  // teardown
+  if (warp == 4 && lane == 0 && committed && sm.flags[0] != 0) {
+    // a wait gave up: let this CTA's own copies and MMAs drain (bounded)
+    mbar_wait(BAR_TMA, 0);
+    mbar_wait(BAR_TMA, 1);
+    mbar_wait(BAR_MMA1, 0);
+    mbar_wait(BAR_MMA2, 0);
+  }
+  tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols));
+    free_tmem(tmem);
   }
-  if (MODE == kCluster) cluster_sync_all();  // peers are done reading `part`
+}
+
+// --------------------------------------------------- split-mode kernels
+
+// One item per CTA (grid: chunk × unit).  kPass1 publishes the chunk's
+// partials to global memory; kPass2 (a second launch) combines them, reloads
+// the chunk and writes its scores.
+template <int MODE, int RT, int S, int W>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+k_score_split(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CUtensorMap tm_q,
+              TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const int KB = a.D / 64;
+  Smem<RT, S> sm(smem_raw, KB);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int CH = S * 128;
+  const int chunk = blockIdx.x, unit = blockIdx.y;
+  const int r = unit % a.n_sess, lh = unit / a.n_sess;
+  const int h = lh % a.H, l = lh / a.H;
+  const int64_t b0 = a.blk_off[r], b1 = a.blk_off[r + 1];
+  if (!(b0 >= 0 && b1 > b0 && b1 <= a.nb_total)) {
+    if (chunk == 0 && threadIdx.x == 0) record_error(a.status, KVC_ERR_BOUNDS);
+    return;
+  }
+  const int nb = (int)(b1 - b0);
+  const int valid = min(CH, nb - chunk * CH);
+  if (valid <= 0) return;  // CTA-uniform, before any barrier
+  const int n_chunks = (nb + CH - 1) / CH;
+  const int mk_row0 = (int)(((int64_t)l * a.H + h) * a.nb_total + b0 + (int64_t)chunk * CH);
+  const int q_row0 = (int)((((int64_t)l * a.n_sess + r) * a.Hq + (int64_t)h * a.G) * a.W);
+  const uint32_t bar0 = smem_u32(sm.bars);
+  const uint32_t BAR_TMA = bar0, BAR_MMA = bar0 + 8;
+  if (threadIdx.x == 0) {
+    sm.flags[0] = 0;
+    mbar_init(BAR_TMA, 1);
+    mbar_init(BAR_MMA, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) alloc_tmem(sm.tmem_holder);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.tmem_holder;
+  const float zs = a.zscale;
+  bool committed = false;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      issue_loads<RT, S>(&tm_q, &tm_mk, sm, KB, q_row0, mk_row0, BAR_TMA);
+      if (mbar_wait(BAR_TMA, 0)) {
+        tc_fence_after();
+        if (MODE == kPass1)
+          issue_pass1<RT, S>(tmem, sm, KB, a.idesc1);
+        else
+          issue_pass2<RT, S>(tmem, sm, KB, a.idesc2, a.n2c);
+        mma_commit(BAR_MMA);
+        committed = true;
+      } else {
+        sm.flags[0] = 1;
+        record_error(a.status, KVC_ERR_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (MODE == kPass2) {
+      const float2 *unit_part = a.part + (int64_t)unit * a.n_chunk * (RT * 128);
+      for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads) {
+        float m = -INFINITY, s = 0.f;
+        for (int c = 0; c < n_chunks; c++) {
+          float2 p = unit_part[(int64_t)c * (RT * 128) + rr];
+          lse_merge(m, s, p.x, p.y);
+        }
+        sm.lse[rr] = (m == -INFINITY) ? INFINITY : m + log2f(s);
+      }
+      named_sync_epi();
+    }
+    bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(BAR_MMA, 0));
+    if (ok) {
+      tc_fence_after();
+      if (MODE == kPass1) {
+        float pm[RT], ps[RT];
+        epi_pass1<RT, S>(tmem, lane_base, valid, zs, pm, ps);
+        float2 *dst = a.part + ((int64_t)unit * a.n_chunk + chunk) * (RT * 128);
+#pragma unroll
+        for (int rt = 0; rt < RT; rt++) dst[rt * 128 + threadIdx.x] = make_float2(pm[rt], ps[rt]);
+      } else {
+        float *out = a.scores + ((int64_t)l * a.H + h) * a.nb_total + b0 + (int64_t)chunk * CH;
+        epi_pass2<S, W>(tmem, lane_base, warp, lane, valid, a.n2c, a.R, zs, 1.f / (float)a.W,
+                        sm.lse, out);
+      }
+    } else {
+      sm.flags[0] = 1;
+      if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 4 && lane == 0 && committed && sm.flags[0] != 0) mbar_wait(BAR_MMA, 0);
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    free_tmem(tmem);
+  }
 }
 
 // --------------------------------------------------------------- host
@@ -499,7 +661,7 @@ uint32_t make_idesc(int M, int N) {
 }
 
 struct Plan {
-  int RT, S, C, n2, n2c;
+  int RT, S, CH, C, n2, n2c;
   bool ok;
 };
 
@@ -508,116 +670,104 @@ Plan plan(int R, int W, int D, int nb_max) {
   p.ok = (D == 64 || D == 128) && (W == 8 || W == 16 || W == 32) && R >= 1 && R <= 256;
   p.RT = R <= 128 ? 1 : 2;
   p.S = p.RT == 1 ? 2 : 1;  // TMEM: RT·S·128 ≤ 256 and S·n2c ≤ 256
-  p.C = (nb_max + p.S * 128 - 1) / (p.S * 128);
+  p.CH = p.S * 128;
+  p.C = (nb_max + p.CH - 1) / p.CH;
   p.n2 = (R + 15) / 16 * 16;
   p.n2c = (p.n2 + 31) / 32 * 32;
   return p;
 }
 
-size_t smem_bytes(int RT, int S, int D) {
-  int KB = D / 64;
-  size_t b = 1024 /*align slack*/ + (size_t)S * KB * 16384 + (size_t)KB * RT * 16384 +
-             (3 * S + 2) * 8 + 4 + 16 + 16 + RT * 128 * 8 + 256 * 4;
+size_t smem_bytes(int RT, int D, int n_sess) {
+  size_t b = RT == 1 ? Smem<1, 2>::bytes(D, n_sess + 1) : Smem<2, 1>::bytes(D, n_sess + 1);
   // at most two CTAs per SM, so their 2 × 256 TMEM columns always fit
   return b < 80 * 1024 ? 80 * 1024 : b;
 }
 
-template <int MODE, int RT, int S, int W>
-cudaError_t launch_mode(const CUtensorMap &mk, const CUtensorMap &qm, const TcArgs &a,
-                        int n_units, int C, cudaStream_t s) {
-  auto kern = k_score_tc<MODE, RT, S, W>;
-  size_t smem = smem_bytes(RT, S, a.D);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  if (MODE == kCluster && C > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kThreadsTC);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  if (MODE == kCluster) {
-    cfg.gridDim = dim3(n_units * C);
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  } else {
-    cfg.gridDim = dim3(C, n_units);
-    cfg.numAttrs = 0;
-  }
-  return cudaLaunchKernelEx(&cfg, kern, mk, qm, a);
-}
-
-// Whether clusters of C CTAs of this kernel can be resident at all.
+// Resident CTAs of the persistent kernel on this device (0 if it cannot run).
 template <int RT, int S, int W>
-bool cluster_fits(int C, int D) {
-  auto kern = k_score_tc<kCluster, RT, S, W>;
-  size_t smem = smem_bytes(RT, S, D);
+int persistent_capacity(size_t smem) {
+  auto kern = k_score_tc<RT, S, W>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return false;
-  if (C > 8 &&
-      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return false;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(C);
-  cfg.blockDim = dim3(kThreadsTC);
-  cfg.dynamicSmemBytes = smem;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-  if (e != cudaSuccess) {
+      cudaSuccess) {
     (void)cudaGetLastError();
-    return false;
+    return 0;
   }
-  return n > 0;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreadsTC, smem) !=
+          cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return sms * (per_sm > 2 ? 2 : per_sm);
 }
 
 template <int RT, int S, int W>
-cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, const TcArgs &a,
-                        int n_units, int C, cudaStream_t s) {
-  if (C <= kMaxCluster && cluster_fits<RT, S, W>(C, a.D))
-    return launch_mode<kCluster, RT, S, W>(mk, qm, a, n_units, C, s);
-  cudaError_t e = launch_mode<kPass1, RT, S, W>(mk, qm, a, n_units, C, s);
-  if (e != cudaSuccess) return e;
-  return launch_mode<kPass2, RT, S, W>(mk, qm, a, n_units, C, s);
+cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, int n_units,
+                        const Plan &p, void *ws, cudaStream_t s) {
+  const size_t smem = smem_bytes(RT, a.D, a.n_sess);
+  const int cap = a.n_sess <= kMaxSessPersist ? persistent_capacity<RT, S, W>(smem) : 0;
+  cudaError_t e;
+  if (cap > 0 && cap >= p.C) {
+    // ws: [counter, pad to 256 B][unit_done[n_units], pad][partials]
+    char *w = static_cast<char *>(ws);
+    size_t done_bytes = ((size_t)n_units * 4 + 255) / 256 * 256;
+    a.counter = reinterpret_cast<int *>(w);
+    a.unit_done = reinterpret_cast<int *>(w + 256);
+    a.part = reinterpret_cast<float2 *>(w + 256 + done_bytes);
+    e = cudaMemsetAsync(w, 0, 256 + done_bytes, s);
+    if (e != cudaSuccess) return e;
+    k_score_tc<RT, S, W><<<cap, kThreadsTC, smem, s>>>(mk, qm, a);
+    return cudaGetLastError();
+  }
+  a.part = reinterpret_cast<float2 *>(ws);
+  auto k1 = k_score_split<kPass1, RT, S, W>;
+  auto k2 = k_score_split<kPass2, RT, S, W>;
+  if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  dim3 grid(p.C, n_units);
+  k1<<<grid, kThreadsTC, smem, s>>>(mk, qm, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k2<<<grid, kThreadsTC, smem, s>>>(mk, qm, a);
+  return cudaGetLastError();
 }
 
 template <int RT, int S>
-int launches_rt(int C, int W, int D) {
-  bool fits = W == 8    ? cluster_fits<RT, S, 8>(C, D)
-              : W == 16 ? cluster_fits<RT, S, 16>(C, D)
-                        : cluster_fits<RT, S, 32>(C, D);
-  return (C <= kMaxCluster && fits) ? 1 : 2;
+int launches_rt(const Plan &p, int W, int D, int n_sess) {
+  size_t smem = smem_bytes(RT, D, n_sess);
+  int cap = n_sess > kMaxSessPersist ? 0
+            : W == 8              ? persistent_capacity<RT, S, 8>(smem)
+            : W == 16             ? persistent_capacity<RT, S, 16>(smem)
+                                  : persistent_capacity<RT, S, 32>(smem);
+  return (cap > 0 && cap >= p.C) ? 1 : 2;
 }
 
 }  // namespace
 
 bool score_tc_supported(int R, int W, int D) { return plan(R, W, D, 1).ok; }
 
-int score_tc_launches(int R, int W, int D, int nb_max) {
+int score_tc_launches(int R, int W, int D, int n_sess, int nb_max) {
   Plan p = plan(R, W, D, nb_max);
   if (!p.ok) return 0;
-  return p.RT == 1 ? launches_rt<1, 2>(p.C, W, D) : launches_rt<2, 1>(p.C, W, D);
+  return p.RT == 1 ? launches_rt<1, 2>(p, W, D, n_sess) : launches_rt<2, 1>(p, W, D, n_sess);
 }
 
-size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max) {
+size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max, int64_t nb_total) {
   int R = (Hq / H) * W;
   Plan p = plan(R, W, 128, nb_max);
-  if (!p.ok) return 0;  // split-mode partials (also reserved when clusters would do)
-  return (size_t)L * H * n_sess * p.C * p.RT * 128 * sizeof(float2);
+  if (!p.ok) return 0;
+  const int64_t n_units = (int64_t)L * H * n_sess;
+  const size_t row_bytes = (size_t)p.RT * 128 * sizeof(float2);
+  // persistent: one partial row set per item (≤ L·H·(nb_total/CH + n_sess) items)
+  int64_t items = (int64_t)L * H * ((nb_total + p.CH - 1) / p.CH + n_sess);
+  size_t persist = 256 + ((size_t)n_units * 4 + 255) / 256 * 256 + (size_t)items * row_bytes;
+  size_t split = (size_t)n_units * p.C * row_bytes;
+  return persist > split ? persist : split;
 }
 
 cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *scores, int L,
@@ -629,14 +779,13 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
   if (!p.ok) return cudaErrorNotSupported;
   CUtensorMap mk_map, q_map;
   uint64_t mk_rows = (uint64_t)L * H * nb_total;
-  uint64_t q_rows = (uint64_t)n_sess * L * Hq * W;
+  uint64_t q_rows = (uint64_t)L * n_sess * Hq * W;
   if (!make_map(&mk_map, meank, mk_rows, D, 128) ||
       !make_map(&q_map, q, q_rows, D, (uint32_t)(p.RT * 128)))
     return cudaErrorNotSupported;
-  TcArgs a;
+  TcArgs a{};
   a.scores = scores;
   a.blk_off = blk_off;
-  a.part = reinterpret_cast<float2 *>(ws);
   a.status = status;
   a.L = L;
   a.H = H;
@@ -654,11 +803,11 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
   a.n2 = p.n2;
   a.n2c = p.n2c;
   const int n_units = L * H * n_sess;
-#define KVC_TC_W(RTv, Sv)                                                         \
-  switch (W) {                                                                    \
-    case 8: return launch_plan<RTv, Sv, 8>(mk_map, q_map, a, n_units, p.C, s);   \
-    case 16: return launch_plan<RTv, Sv, 16>(mk_map, q_map, a, n_units, p.C, s); \
-    default: return launch_plan<RTv, Sv, 32>(mk_map, q_map, a, n_units, p.C, s); \
+#define KVC_TC_W(RTv, Sv)                                                           \
+  switch (W) {                                                                      \
+    case 8: return launch_plan<RTv, Sv, 8>(mk_map, q_map, a, n_units, p, ws, s);   \
+    case 16: return launch_plan<RTv, Sv, 16>(mk_map, q_map, a, n_units, p, ws, s); \
+    default: return launch_plan<RTv, Sv, 32>(mk_map, q_map, a, n_units, p, ws, s); \
   }
   if (p.RT == 1) {
     KVC_TC_W(1, 2)

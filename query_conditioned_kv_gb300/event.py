@@ -84,7 +84,8 @@ class MeanKEvent:
         words = (self.nb_max + 31) // 32
         self.keepmask = (torch.empty(self.n_seg, words, dtype=torch.int32, device=dev)
                          if keepmask else None)
-        self.ws = _ws(kvc_score_workspace_size(L, H, Hq, W, self.n_sess, self.nb_max), dev)
+        self.ws = _ws(kvc_score_workspace_size(L, H, Hq, W, self.n_sess, self.nb_max,
+                                               self.nb_total), dev)
         self.view_tokens = BLOCK_TOKENS * budget
         self.rope_tab = torch.empty(self.view_tokens, D // 2, 2, dtype=torch.float32,
                                     device=dev)

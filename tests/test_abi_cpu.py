@@ -52,8 +52,8 @@ def test_status_strings(kvc):
 
 
 def test_workspace_queries(kvc):
-    assert kvc.kvc_score_workspace_size(36, 8, 32, 32, 1, 4096) > 0
-    assert kvc.kvc_score_workspace_size(1, 3, 4, 1, 1, 1) == 0  # Hq % H
+    assert kvc.kvc_score_workspace_size(36, 8, 32, 32, 1, 4096, 4096) > 0
+    assert kvc.kvc_score_workspace_size(1, 3, 4, 1, 1, 1, 1) == 0  # Hq % H
     assert kvc.kvc_score_qmem_workspace_size(64, 36, 32, 32768) >= 64 * 36 * 32 * 32768 * 4
     assert kvc.kvc_redirect_free_workspace_size(64, 32768, 1839120) >= 1839120 * 4
 

@@ -66,13 +66,14 @@ def test_select_bad_segment_offsets(kvc):
     assert cnt.cpu().tolist()[1] == 0 and kept.cpu().tolist()[1] == [-1] * 4
 
 
-def test_score_bad_block_offsets(kvc):
-    L, H, Hq, D, W, nb = 1, 1, 2, 64, 4, 8
+@pytest.mark.parametrize("W", [4, 8])  # CUDA-core and tensor-core scorers
+def test_score_bad_block_offsets(kvc, W):
+    L, H, Hq, D, nb = 1, 1, 2, 64, 8
     q = torch.randn(1, L, Hq, W, D, device=DEV).to(torch.bfloat16)
     mk = torch.randn(L, H, nb, D, device=DEV).to(torch.bfloat16)
     sc = torch.full((L, H, nb), -5.0, device=DEV)
     off = torch.tensor([0, nb + 4], dtype=torch.int64, device=DEV)  # past nb_total
-    ws = torch.empty(kvc.kvc_score_workspace_size(L, H, Hq, W, 1, nb) + 256,
+    ws = torch.empty(kvc.kvc_score_workspace_size(L, H, Hq, W, 1, nb, nb) + 256,
                      dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     kvc.kvc_score(q, mk, sc, L, H, Hq, D, W, off, 1, nb, nb, ws, st)
