@@ -184,6 +184,21 @@ __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2
   m = mn;
 }
 
+// LSE (base 2) of one query row from its per-chunk partials p[c·stride],
+// c < n; loads are issued 16 at a time so their L2 latencies overlap.
+__device__ __forceinline__ float combine_partials(const float2 *p, int n, int stride) {
+  float m = -INFINITY, s = 0.f;
+  for (int c0 = 0; c0 < n; c0 += 16) {
+    float2 v[16];
+#pragma unroll
+    for (int k = 0; k < 16; k++)
+      v[k] = c0 + k < n ? __ldcg(p + (int64_t)(c0 + k) * stride) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; k++) lse_merge(m, s, v[k].x, v[k].y);
+  }
+  return (m == -INFINITY) ? INFINITY : m + log2f(s);
+}
+
 // ------------------------------------------------------------ the stages
 
 // Shared memory of a CTA: [mk: S·KB boxes of 128 rows × 128 B][q: KB boxes
@@ -482,14 +497,8 @@ k_score_tc(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CU
       }
       // LSE of every query row (thread t: rows t and t + 128)
       const float2 *unit_part = a.part + (int64_t)(item - chunk) * (RT * 128);
-      for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads) {
-        float m = -INFINITY, s = 0.f;
-        for (int c = 0; c < n_chunks; c++) {
-          float2 p = __ldcg(unit_part + (int64_t)c * (RT * 128) + rr);
-          lse_merge(m, s, p.x, p.y);
-        }
-        sm.lse[rr] = (m == -INFINITY) ? INFINITY : m + log2f(s);
-      }
+      for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads)
+        sm.lse[rr] = combine_partials(unit_part + rr, n_chunks, RT * 128);
       named_sync_epi();
       bool ok2 = __all_sync(0xFFFFFFFFu, ok && mbar_wait(BAR_MMA2, ph));
       if (ok2) {
@@ -586,14 +595,8 @@ k_score_split(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     if (MODE == kPass2) {
       const float2 *unit_part = a.part + (int64_t)unit * a.n_chunk * (RT * 128);
-      for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads) {
-        float m = -INFINITY, s = 0.f;
-        for (int c = 0; c < n_chunks; c++) {
-          float2 p = unit_part[(int64_t)c * (RT * 128) + rr];
-          lse_merge(m, s, p.x, p.y);
-        }
-        sm.lse[rr] = (m == -INFINITY) ? INFINITY : m + log2f(s);
-      }
+      for (int rr = threadIdx.x; rr < RT * 128; rr += kEpiThreads)
+        sm.lse[rr] = combine_partials(unit_part + rr, n_chunks, RT * 128);
       named_sync_epi();
     }
     bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(BAR_MMA, 0));
@@ -688,7 +691,9 @@ template <int RT, int S, int W>
 int persistent_capacity(size_t smem) {
   auto kern = k_score_tc<RT, S, W>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess) {
+          cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -724,12 +729,14 @@ cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
   a.part = reinterpret_cast<float2 *>(ws);
   auto k1 = k_score_split<kPass1, RT, S, W>;
   auto k2 = k_score_split<kPass2, RT, S, W>;
-  if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
-    return e;
+  for (auto k : {k1, k2}) {
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+  }
   dim3 grid(p.C, n_units);
   k1<<<grid, kThreadsTC, smem, s>>>(mk, qm, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
