@@ -686,7 +686,11 @@ size_t smem_bytes(int RT, int D, int n_sess) {
   return b < 80 * 1024 ? 80 * 1024 : b;
 }
 
-// Resident CTAs of the persistent kernel on this device (0 if it cannot run).
+// CTAs of the persistent kernel: two per SM (its shared memory allows two
+// and its TMEM allocation is sized for two).  Launching more CTAs than can
+// be resident at once is safe for this kernel — a CTA that is not running
+// holds no item — so the count does not rely on the occupancy calculator
+// (which may report one).  0 if the kernel cannot run on this device.
 template <int RT, int S, int W>
 int persistent_capacity(size_t smem) {
   auto kern = k_score_tc<RT, S, W>;
@@ -705,7 +709,7 @@ int persistent_capacity(size_t smem) {
     (void)cudaGetLastError();
     return 0;
   }
-  return sms * (per_sm > 2 ? 2 : per_sm);
+  return per_sm > 0 ? 2 * sms : 0;
 }
 
 template <int RT, int S, int W>
