@@ -135,6 +135,32 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                      int32_t nb_max, void *ws, size_t ws_bytes,
                      int32_t *dev_status, cudaStream_t stream);
 
+/* kvc_score for callers that cannot allocate device memory (no counterpart
+ * on the pages; this is a convenience of the library).  Some hosts cannot
+ * pass a workspace: a serving runtime that carves all of HBM into its own
+ * pool at start-up and forbids device allocations afterwards, or a plugin
+ * inside such a runtime that receives tensors but no allocator.  This call
+ * takes the same inputs and outputs as kvc_score and computes the same
+ * scores, but its scratch is a fixed array of KVC_SCORE_STATIC_SCRATCH_BYTES
+ * compiled into the library (held by every GPU that loads the library until
+ * the process exits); it calls no cudaMalloc/cudaFree.
+ *  - Sizes whose scratch (kvc_score_workspace_size) exceeds the array are
+ *    rejected with KVC_ERR_WORKSPACE before anything is launched; the 8B-
+ *    class 128K-token event (36 layers, 8/32 heads, W 32) needs about 5 MB.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture on the device.
+ *  - Every call shares the one array per device: calls whose kernels overlap
+ *    on the GPU (different streams, no ordering between them) race and give
+ *    undefined scores.  Serialise them (one stream, or events).
+ * Errors: those of kvc_score, plus KVC_ERR_WORKSPACE as above and
+ * KVC_ERR_CUDA if the device address cannot be obtained. */
+#define KVC_SCORE_STATIC_SCRATCH_BYTES (8u << 20)
+kvc_status kvc_score_static(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
+                            int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                            const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
+                            int32_t nb_max, int32_t *dev_status, cudaStream_t stream);
+
 /* Number of kernels one kvc_score call with these sizes launches on this
  * device (1: tensor-core scorer with a thread-block-cluster LSE exchange;
  * 2: two-launch scoring), 0 for invalid sizes.  Host-only query. */

@@ -19,6 +19,7 @@ __all__ = [
     "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG",
     "kvc_status_string", "kvc_version", "kvc_device_status",
     "kvc_build_meank", "kvc_score_workspace_size", "kvc_score_launches", "kvc_score",
+    "kvc_score_static", "SCORE_STATIC_SCRATCH_BYTES",
     "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
@@ -28,6 +29,7 @@ BLOCK_TOKENS = 32
 SENTINEL_K_BITS = 0xC61C
 SELECT_MAX_SEG = 49152
 SCORE_MAX_ROWS = 256
+SCORE_STATIC_SCRATCH_BYTES = 8 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvc.so")
@@ -53,6 +55,8 @@ _SIGS = {
     "kvc_build_meank": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _P, _P]),
     "kvc_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I64]),
     "kvc_score_launches": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "kvc_score_static": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
+                                    _I32, _I64, _I32, _P, _P]),
     "kvc_score": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
                              _I32, _I64, _I32, _P, _SZ, _P, _P]),
     "kvc_qmem_update": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32,
@@ -139,6 +143,15 @@ def kvc_score(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,
                       _ptr(blk_off), n_sess, nb_total, nb_max, _ptr(ws),
                       ws.numel() * ws.element_size(), _ptr(dev_status),
                       _stream(stream)), "kvc_score")
+
+
+def kvc_score_static(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,
+                     nb_max, dev_status=None, stream=None):
+    """kvc_score with the library's fixed scratch array instead of a caller
+    workspace, for callers that cannot allocate device memory."""
+    _ok(lib.kvc_score_static(_ptr(q), _ptr(meank), _ptr(scores), L, H, Hq, D, W,
+                             _ptr(blk_off), n_sess, nb_total, nb_max, _ptr(dev_status),
+                             _stream(stream)), "kvc_score_static")
 
 
 def kvc_qmem_update(M, q_turn, n_sess, L, Hq, D, T, decay=0.9, gain=0.1,
