@@ -112,10 +112,22 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
       const int shift = 24 - 8 * pass;
       for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      for (int i = tid; i < n; i += blockDim.x) {
-        if (i < n_sink || i >= rec0) continue;
-        uint32_t key = keys[i];
-        if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      // warp-aggregated: lanes with the same digit add once (scores of one
+      // segment share their leading bits, so plain atomics would serialise)
+      for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + tid;
+        bool cand = false;
+        uint32_t digit = 0;
+        if (i < n && i >= n_sink && i < rec0) {
+          uint32_t key = keys[i];
+          cand = (key & hi_mask) == prefix;
+          digit = (key >> shift) & 255u;
+        }
+        const uint32_t active = __ballot_sync(0xFFFFFFFFu, cand);
+        if (cand) {
+          const uint32_t peers = __match_any_sync(active, digit);
+          if ((int)(__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
+        }
       }
       __syncthreads();
       if (tid < 32) {

@@ -7,10 +7,11 @@ Both only allocate caller-side buffers with torch and call the library's
 entry points; an event can be captured in a CUDA graph (``capture()``) so
 that its launches replay without host overhead.
 
-``MeanKEvent.run`` pipelines over groups of layers: the score and select of
-group g+1 (tensor-core and exponential heavy) run on the caller's stream
-while the pack of group g (HBM-bound streaming) runs on a second stream, so
-the two kinds of work share the SMs instead of taking turns.  Every call
+``MeanKEvent.run`` pipelines over groups of layers: the score of group g+1
+(tensor-core and exponential heavy) runs on the caller's stream while the
+select and pack of group g (latency-bound, then HBM-bound streaming) run on a
+second stream, so the two kinds of work share the SMs instead of taking
+turns.  Every call
 covers whole layers, which is possible because every tensor is laid out
 layer-major.
 """
@@ -164,12 +165,12 @@ class MeanKEvent:
 
         for (l0, l1) in self.groups:
             timed("score", main, lambda: self.score(q, meank, main, l0, l1))
-            timed("select", main, lambda: self.select(None, main, l0, l1))
-            if l0 < self.L_pack:
-                done = torch.cuda.Event()
-                done.record(main)
-                side.wait_event(done)
-                with torch.cuda.stream(side):
+            done = torch.cuda.Event()
+            done.record(main)
+            side.wait_event(done)
+            with torch.cuda.stream(side):
+                timed("select", side, lambda: self.select(None, side, l0, l1))
+                if l0 < self.L_pack:
                     timed("pack", side, lambda: self.pack(kraw, vraw, stream=side, l0=l0, l1=l1))
         main.wait_stream(side)
 
