@@ -36,6 +36,8 @@
 // and MMAs and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "kvc_internal.cuh"
 
@@ -353,6 +355,17 @@ __device__ __forceinline__ void free_tmem(uint32_t tmem) {
                "r"(kTmemCols));
 }
 
+__device__ __forceinline__ void alloc_tmem_cols(uint32_t *holder, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(holder)),
+               "r"(cols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+
+__device__ __forceinline__ void free_tmem_cols(uint32_t tmem, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols));
+}
+
 // ------------------------------------------------------ persistent kernel
 
 template <int RT, int S, int W>
@@ -628,6 +641,382 @@ k_score_split(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
   }
 }
 
+// ------------------------------------------------ pipelined cluster kernel
+//
+// k_score_ring: a cluster of C CTAs (C ≤ 4) owns one unit at a time and
+// walks the units round-robin; CTA `rank` of the cluster takes the unit's
+// 128-block tiles rank, rank + C, …  Roles inside a CTA:
+//   warp 0      TMA producer: the unit's query rows (double-buffered), then
+//               its tiles twice (pass 1, pass 2) through an NS-stage ring;
+//   warp 1      MMA issuer: per tile, pass-1 or pass-2 tcgen05.mma into one
+//               of NBUF TMEM accumulators;
+//   warps 2–9   two epilogue warpgroups that take alternate tiles: pass-1
+//               online row LSE, then (after the exchange) pass-2 scores.
+// Between a unit's two passes the CTAs exchange their row partials through
+// distributed shared memory: every CTA stores its partials into each peer's
+// receive slot and arrives on the peer's mbarrier (release at cluster
+// scope); no full-cluster barrier stalls the producer or the MMA warp, which
+// keep prefetching the pass-2 tiles.  The second read of a tile usually hits
+// L2 (a CTA's share of a unit is ≤ 1/C of its Mean-K).
+
+constexpr int kRingThreads = 320;
+constexpr int kRingMaxC = 4;
+
+__device__ __forceinline__ uint32_t cluster_nrank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void fence_acqrel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA failed.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *failed,
+                                              bool cluster_scope = false) {
+  for (uint32_t i = 0; i < kWaitLimit; i++) {
+    if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+    if (*failed) return false;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+template <int RT>
+struct RingSmem {
+  static constexpr int NS = RT == 1 ? 4 : 2;    // Mean-K ring stages
+  static constexpr int NBUF = RT == 1 ? 4 : 2;  // TMEM accumulators
+  static constexpr int BUFCOLS = 128 * RT;      // columns per accumulator
+  uint8_t *ring, *q;
+  uint64_t *full, *empty, *tfull, *tempty, *qfull, *qempty, *recv;
+  uint32_t *tmem_holder;
+  volatile int *failed;
+  float2 *egpart;  // [2 groups][256 rows]
+  float2 *rbuf;    // [2 parities][kRingMaxC ranks][256 rows]
+  float *lse;      // [256 rows]
+  __device__ RingSmem(uint8_t *raw, int KB) {
+    uint8_t *p = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    ring = p;
+    p += NS * KB * 16384;
+    q = p;
+    p += 2 * KB * RT * 16384;
+    uint64_t *b = reinterpret_cast<uint64_t *>(p);
+    full = b;
+    empty = full + NS;
+    tfull = empty + NS;
+    tempty = tfull + NBUF;
+    qfull = tempty + NBUF;
+    qempty = qfull + 2;
+    recv = qempty + 2;
+    tmem_holder = reinterpret_cast<uint32_t *>(recv + 2);
+    failed = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    egpart = reinterpret_cast<float2 *>(tmem_holder + 4);  // 16-byte aligned
+    rbuf = egpart + 2 * 256;
+    lse = reinterpret_cast<float *>(rbuf + 2 * kRingMaxC * 256);
+  }
+  static size_t bytes(int D) {
+    int KB = D / 64;
+    return 1024 + (size_t)NS * KB * 16384 + (size_t)2 * KB * RT * 16384 +
+           (2 * NS + 2 * NBUF + 6) * 8 + 16 + (2 * 256 + 2 * kRingMaxC * 256) * 8 + 256 * 4;
+  }
+};
+
+struct UnitInfo {
+  int l, h, r, nb, n_tiles, my_tiles, mk_row0, q_row0;
+  int64_t b0;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const TcArgs &a, int unit, int C, int rank) {
+  UnitInfo u;
+  u.r = unit % a.n_sess;
+  const int lh = unit / a.n_sess;
+  u.h = lh % a.H;
+  u.l = lh / a.H;
+  const int64_t b0 = a.blk_off[u.r], b1 = a.blk_off[u.r + 1];
+  const bool ok = b0 >= 0 && b1 > b0 && b1 <= a.nb_total && b1 - b0 <= (int64_t)a.n_chunk * 128;
+  u.b0 = ok ? b0 : 0;
+  u.nb = ok ? (int)(b1 - b0) : 0;
+  u.n_tiles = (u.nb + 127) / 128;
+  u.my_tiles = u.n_tiles > rank ? (u.n_tiles - rank + C - 1) / C : 0;
+  u.mk_row0 = (int)(((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0);
+  u.q_row0 = (int)((((int64_t)u.l * a.n_sess + u.r) * a.Hq + (int64_t)u.h * a.G) * a.W);
+  return u;
+}
+
+template <int RT, int W>
+__global__ void __launch_bounds__(kRingThreads, 1)
+k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CUtensorMap tm_q,
+             TcArgs a) {
+  static_assert(W == 8 || W == 16 || W == 32, "W divides 32");
+  using SM = RingSmem<RT>;
+  constexpr int NS = SM::NS, NBUF = SM::NBUF, BUFCOLS = SM::BUFCOLS;
+  extern __shared__ uint8_t smem_raw[];
+  const int KB = a.D / 64;
+  SM sm(smem_raw, KB);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = (int)cluster_nrank(), rank = (int)cluster_rank();
+  const int cluster_id = blockIdx.x / C, n_clusters = gridDim.x / C;
+  const int n_units = a.L * a.H * a.n_sess;
+  const uint32_t stage_bytes = (uint32_t)KB * 16384u, q_bytes = (uint32_t)(KB * RT) * 16384u;
+
+  if (threadIdx.x == 0) {
+    *sm.failed = 0;
+    for (int i = 0; i < NS; i++) {
+      mbar_init(smem_u32(sm.full + i), 1);
+      mbar_init(smem_u32(sm.empty + i), 1);
+    }
+    for (int i = 0; i < NBUF; i++) {
+      mbar_init(smem_u32(sm.tfull + i), 1);
+      mbar_init(smem_u32(sm.tempty + i), 4);  // the 4 warps of one epilogue group
+    }
+    for (int i = 0; i < 2; i++) {
+      mbar_init(smem_u32(sm.qfull + i), 1);
+      mbar_init(smem_u32(sm.qempty + i), 1);
+      mbar_init(smem_u32(sm.recv + i), C > 1 ? C - 1 : 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) alloc_tmem_cols(sm.tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (C > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
+  const uint32_t tmem = *sm.tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t s = 0, qi = 0;
+      for (int unit = cluster_id; unit < n_units && !*sm.failed; unit += n_clusters) {
+        const UnitInfo u = unit_info(a, unit, C, rank);
+        if (u.nb == 0 && rank == 0) record_error(a.status, KVC_ERR_BOUNDS);
+        if (u.my_tiles == 0) continue;
+        const int qb = qi & 1;
+        if (!wait_or_abort(smem_u32(sm.qempty + qb), ((qi >> 1) & 1) ^ 1, sm.failed)) break;
+        mbar_expect_tx(smem_u32(sm.qfull + qb), q_bytes);
+        for (int kb = 0; kb < KB; kb++)
+          tma_load_2d(smem_u32(sm.q + qb * q_bytes + kb * RT * 16384), &tm_q, kb * 64, u.q_row0,
+                      smem_u32(sm.qfull + qb));
+        qi++;
+        bool ok = true;
+        for (int pass = 0; pass < 2 && ok; pass++)
+          for (int j = 0; j < u.my_tiles; j++, s++) {
+            const int slot = s % NS;
+            if (!wait_or_abort(smem_u32(sm.empty + slot), ((s / NS) & 1) ^ 1, sm.failed)) {
+              ok = false;
+              break;
+            }
+            const int tile = rank + j * C;
+            mbar_expect_tx(smem_u32(sm.full + slot), stage_bytes);
+            for (int kb = 0; kb < KB; kb++)
+              tma_load_2d(smem_u32(sm.ring + slot * stage_bytes + kb * 16384), &tm_mk, kb * 64,
+                          u.mk_row0 + tile * 128, smem_u32(sm.full + slot));
+          }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t s = 0, t = 0, qi = 0;
+      bool ok = true;
+      for (int unit = cluster_id; unit < n_units && ok; unit += n_clusters) {
+        const UnitInfo u = unit_info(a, unit, C, rank);
+        if (u.my_tiles == 0) continue;
+        const int qb = qi & 1;
+        if (!(ok = wait_or_abort(smem_u32(sm.qfull + qb), (qi >> 1) & 1, sm.failed))) break;
+        const uint8_t *qbase = sm.q + qb * q_bytes;
+        for (int pass = 0; pass < 2 && ok; pass++)
+          for (int j = 0; j < u.my_tiles; j++, s++, t++) {
+            const int slot = s % NS, buf = t % NBUF;
+            if (!(ok = wait_or_abort(smem_u32(sm.full + slot), (s / NS) & 1, sm.failed))) break;
+            if (!(ok = wait_or_abort(smem_u32(sm.tempty + buf), ((t / NBUF) & 1) ^ 1,
+                                     sm.failed)))
+              break;
+            tc_fence_after();
+            const uint8_t *mk = sm.ring + slot * stage_bytes;
+            const uint32_t d = tmem + (uint32_t)(buf * BUFCOLS);
+            for (int kk = 0; kk < 4 * KB; kk++) {
+              const uint32_t koff = (uint32_t)(kk & 3) * 32u;
+              const uint64_t mdesc = smem_desc(smem_u32(mk + (kk >> 2) * 16384) + koff);
+              if (pass == 0) {
+                for (int rt = 0; rt < RT; rt++) {
+                  const uint64_t qdesc =
+                      smem_desc(smem_u32(qbase + (kk >> 2) * RT * 16384 + rt * 16384) + koff);
+                  mma_bf16(d + (uint32_t)(rt * 128), qdesc, mdesc, a.idesc1, kk > 0);
+                }
+              } else {
+                const uint64_t qdesc = smem_desc(smem_u32(qbase + (kk >> 2) * RT * 16384) + koff);
+                mma_bf16(d, mdesc, qdesc, a.idesc2, kk > 0);
+              }
+            }
+            mma_commit(smem_u32(sm.empty + slot));
+            mma_commit(smem_u32(sm.tfull + buf));
+          }
+        if (ok) mma_commit(smem_u32(sm.qempty + qb));  // after the unit's last MMA
+        qi++;
+      }
+      if (!ok) *sm.failed = 1;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- epilogue
+    const int eg = (warp - 2) >> 2;             // epilogue group 0 or 1
+    const int row = 32 * (warp & 3) + lane;     // this thread's TMEM lane
+    const int et = (warp - 2) * 32 + lane;      // 0 … 255
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const float zs = a.zscale, invW = 1.f / (float)a.W;
+    uint32_t t = 0, ui = 0;
+    bool ok = true;
+    for (int unit = cluster_id; unit < n_units; unit += n_clusters, ui++) {
+      const UnitInfo u = unit_info(a, unit, C, rank);
+      if (C == 1 && u.my_tiles == 0) continue;
+      // pass 1: this group's tiles
+      float pm[RT], ps[RT];
+#pragma unroll
+      for (int rt = 0; rt < RT; rt++) {
+        pm[rt] = -INFINITY;
+        ps[rt] = 0.f;
+      }
+      for (int j = 0; j < u.my_tiles; j++, t++) {
+        if ((int)(t & 1) != eg) continue;
+        const int buf = t % NBUF;
+        ok = __all_sync(0xFFFFFFFFu,
+                        ok && wait_or_abort(smem_u32(sm.tfull + buf), (t / NBUF) & 1, sm.failed));
+        if (ok) {
+          tc_fence_after();
+          const int valid = min(128, u.nb - (rank + j * C) * 128);
+          float qm[RT], qs[RT];
+          epi_pass1<RT, 1>(tmem + (uint32_t)(buf * BUFCOLS), lane_base, valid, zs, qm, qs);
+#pragma unroll
+          for (int rt = 0; rt < RT; rt++) lse_merge(pm[rt], ps[rt], qm[rt], qs[rt]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sm.tempty + buf));
+      }
+      // exchange: group partials → CTA partial → every CTA of the cluster
+      const int par = ui & 1;
+#pragma unroll
+      for (int rt = 0; rt < RT; rt++) sm.egpart[eg * 256 + rt * 128 + row] = make_float2(pm[rt], ps[rt]);
+      named_sync(2, 256);
+      if (eg == 0) {
+        for (int rt = 0; rt < RT; rt++) {
+          float m = pm[rt], s2 = ps[rt];
+          const float2 o = sm.egpart[256 + rt * 128 + row];
+          lse_merge(m, s2, o.x, o.y);
+          const float2 v = make_float2(m, s2);
+          float2 *mine = sm.rbuf + (par * kRingMaxC + rank) * 256 + rt * 128 + row;
+          *mine = v;
+          for (int p = 0; p < C; p++)
+            if (p != rank) st_cluster_f2(mapa_u32(smem_u32(mine), (uint32_t)p), v);
+        }
+        if (C > 1) {
+          fence_acqrel_cluster();
+          named_sync(3, 128);
+          if (et == 0)
+            for (int p = 0; p < C; p++)
+              if (p != rank) mbar_arrive_remote(mapa_u32(smem_u32(sm.recv + par), (uint32_t)p));
+        }
+      }
+      if (C > 1)
+        ok = __all_sync(0xFFFFFFFFu,
+                        ok && wait_or_abort(smem_u32(sm.recv + par), (ui >> 1) & 1, sm.failed, true));
+      named_sync(2, 256);
+      if (et < RT * 128) {
+        float m = -INFINITY, s2 = 0.f;
+        for (int c = 0; c < C; c++) {
+          const float2 v = sm.rbuf[(par * kRingMaxC + c) * 256 + et];
+          lse_merge(m, s2, v.x, v.y);
+        }
+        sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);
+      }
+      named_sync(2, 256);
+      // pass 2: this group's tiles
+      for (int j = 0; j < u.my_tiles; j++, t++) {
+        if ((int)(t & 1) != eg) continue;
+        const int buf = t % NBUF;
+        ok = __all_sync(0xFFFFFFFFu,
+                        ok && wait_or_abort(smem_u32(sm.tfull + buf), (t / NBUF) & 1, sm.failed));
+        if (ok) {
+          tc_fence_after();
+          const int tile = rank + j * C;
+          const int valid = min(128, u.nb - tile * 128);
+          float *out = a.scores + ((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0 + tile * 128;
+          epi_pass2<1, W>(tmem + (uint32_t)(buf * BUFCOLS), lane_base, warp & 3, lane, valid, a.n2c,
+                          a.R, zs, invW, sm.lse, out);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sm.tempty + buf));
+      }
+      if (!ok) {
+        *sm.failed = 1;
+        if (et == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*sm.failed && threadIdx.x == 0) {
+    record_error(a.status, KVC_ERR_TIMEOUT);
+    // let this CTA's own copies and MMAs drain (bounded; stale phases return at once)
+    for (int i = 0; i < NS; i++) {
+      mbar_wait(smem_u32(sm.full + i), 0);
+      mbar_wait(smem_u32(sm.full + i), 1);
+    }
+    for (int i = 0; i < NBUF; i++) {
+      mbar_wait(smem_u32(sm.tfull + i), 0);
+      mbar_wait(smem_u32(sm.tfull + i), 1);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    free_tmem_cols(tmem, 512);
+  }
+  if (C > 1) cluster_sync_all();  // no peer still writes into this CTA's memory
+}
+
 // --------------------------------------------------------------- host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -712,11 +1101,95 @@ int persistent_capacity(size_t smem) {
   return per_sm > 0 ? 2 * sms : 0;
 }
 
+// Which tensor-core kernel runs: KVC_SCORE_PATH=ring|persist|split forces one
+// (tests use this); by default the pipelined cluster kernel, else the
+// persistent one, else split mode.
+enum TcPath { kAuto, kRing, kPersist, kSplit };
+TcPath forced_path() {
+  const char *e = getenv("KVC_SCORE_PATH");
+  if (!e) return kAuto;
+  if (!strcmp(e, "ring")) return kRing;
+  if (!strcmp(e, "persist")) return kPersist;
+  if (!strcmp(e, "split")) return kSplit;
+  return kAuto;
+}
+
+int ring_cluster(int nb_max) {
+  int c = (nb_max + 2047) / 2048;
+  return c < 1 ? 1 : (c > kRingMaxC ? kRingMaxC : c);
+}
+
+size_t ring_smem(int RT, int D) {
+  size_t b = RT == 1 ? RingSmem<1>::bytes(D) : RingSmem<2>::bytes(D);
+  return b < 120 * 1024 ? 120 * 1024 : b;  // one CTA per SM: 512 TMEM columns are free
+}
+
+// Clusters of the pipelined kernel that can be resident at once (0: none).
+template <int RT, int W>
+int ring_clusters(int C, int D) {
+  auto kern = k_score_ring<RT, W>;
+  const size_t smem = ring_smem(RT, D);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3(kRingThreads);
+  cfg.dynamicSmemBytes = smem;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int RT, int W>
+cudaError_t launch_ring(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, int n_units,
+                        int C, int n_clusters, cudaStream_t s) {
+  auto kern = k_score_ring<RT, W>;
+  const size_t smem = ring_smem(RT, a.D);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((n_clusters < n_units ? n_clusters : n_units) * C);
+  cfg.blockDim = dim3(kRingThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mk, qm, a);
+}
+
 template <int RT, int S, int W>
 cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, int n_units,
                         const Plan &p, void *ws, cudaStream_t s) {
+  const TcPath forced = forced_path();
+  if (forced == kAuto || forced == kRing) {
+    const int C = ring_cluster(p.C * p.CH);
+    const int nc = ring_clusters<RT, W>(C, a.D);
+    if (nc > 0) {
+      TcArgs b = a;
+      b.n_chunk = (p.C * p.CH + 127) / 128;  // session length limit in 128-block tiles
+      return launch_ring<RT, W>(mk, qm, b, n_units, C, nc, s);
+    }
+  }
   const size_t smem = smem_bytes(RT, a.D, a.n_sess);
-  const int cap = a.n_sess <= kMaxSessPersist ? persistent_capacity<RT, S, W>(smem) : 0;
+  const int cap = (a.n_sess <= kMaxSessPersist && forced != kSplit)
+                      ? persistent_capacity<RT, S, W>(smem)
+                      : 0;
   cudaError_t e;
   if (cap > 0 && cap >= p.C) {
     // ws: [counter, pad to 256 B][unit_done[n_units], pad][partials]
@@ -750,6 +1223,15 @@ cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
 
 template <int RT, int S>
 int launches_rt(const Plan &p, int W, int D, int n_sess) {
+  const TcPath forced = forced_path();
+  if (forced == kAuto || forced == kRing) {
+    const int C = ring_cluster(p.C * p.CH);
+    const int nc = W == 8    ? ring_clusters<RT, 8>(C, D)
+                   : W == 16 ? ring_clusters<RT, 16>(C, D)
+                             : ring_clusters<RT, 32>(C, D);
+    if (nc > 0) return 1;
+  }
+  if (forced == kSplit) return 2;
   size_t smem = smem_bytes(RT, D, n_sess);
   int cap = n_sess > kMaxSessPersist ? 0
             : W == 8              ? persistent_capacity<RT, S, 8>(smem)

@@ -131,12 +131,15 @@ def test_score_parity(kvc, orc, name):
     assert_scores_close(got.reshape(-1), c.scores_ref.reshape(-1))
 
 
-@pytest.mark.parametrize("name", ["tiny", "8b_scaled", "gqa6_rows192", "split_long"])
-def test_score_parity_cuda_core_scorer(kvc, orc, name, monkeypatch):
-    """The CUDA-core scorer (used for shapes the tensor-core one does not
-    cover) against the oracle on the same inputs."""
+@pytest.mark.parametrize("path", ["cc", "ring", "persist", "split"])
+@pytest.mark.parametrize("name", ["tiny", "8b_scaled", "ragged_scaled", "gqa6_rows192",
+                                  "split_long"])
+def test_score_parity_every_scorer(kvc, orc, name, path, monkeypatch):
+    """Every scorer the library can pick — CUDA cores (shapes the tensor-core
+    kernels do not cover), the pipelined cluster kernel, the persistent
+    kernel and the two-launch split mode — against the oracle."""
     c = case(kvc, orc, name)
-    monkeypatch.setenv("KVC_SCORE_PATH", "cc")
+    monkeypatch.setenv("KVC_SCORE_PATH", path)
     out = torch.full_like(c.ev.scores, -1.0)
     kvc.kvc_score(c.q, c.meank, out, c.cfg.L, c.cfg.H, c.cfg.Hq, c.cfg.D, c.cfg.W,
                   c.ev.blk_off, c.cfg.n_sess, c.cfg.nb_total, c.ev.nb_max, c.ev.ws,
