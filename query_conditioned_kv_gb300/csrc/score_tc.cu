@@ -163,6 +163,40 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
+// 2^x with the hardware approximation, flushing subnormal results to zero
+// (every argument here is ≤ 0, so a flushed term is below 2^-126 of the sum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 64 consecutive TMEM columns of this thread's lane (waits for completion).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+        "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+        "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+        "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; i++) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void named_sync_epi() {
   asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
 }
@@ -712,7 +746,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   for (uint32_t i = 0; i < kWaitLimit; i++) {
     if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
     if (*failed) return false;
-    if (i > 64) __nanosleep(64);
+    if (i > 8) __nanosleep(32);
   }
   return false;
 }
@@ -777,6 +811,89 @@ __device__ __forceinline__ UnitInfo unit_info(const TcArgs &a, int unit, int C, 
   u.mk_row0 = (int)(((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0);
   u.q_row0 = (int)((((int64_t)u.l * a.n_sess + u.r) * a.Hq + (int64_t)u.h * a.G) * a.W);
   return u;
+}
+
+// Pass-1 epilogue of one 128-block tile: (max, Σ2^(z−max)) of this lane's
+// query row(s), in 64-column halves.
+template <int RT>
+__device__ __forceinline__ void ring_pass1(uint32_t taddr, int valid, float zs, float (&pm)[RT],
+                                           float (&ps)[RT]) {
+#pragma unroll
+  for (int rt = 0; rt < RT; rt++) {
+    pm[rt] = -INFINITY;
+    ps[rt] = 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; half++) {
+      const int nv = min(64, valid - 64 * half);
+      if (nv <= 0) break;  // warp-uniform
+      float v[64];
+      tmem_ld64(taddr + (uint32_t)(rt * 128 + 64 * half), v);
+      if (nv < 64) {
+#pragma unroll
+        for (int j = 0; j < 64; j++)
+          if (j >= nv) v[j] = -INFINITY;
+      }
+      float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
+#pragma unroll
+      for (int j = 4; j < 64; j += 4) {
+        m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
+        m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
+      }
+      const float mn = fmaxf(pm[rt], fmaxf(m0, m1) * zs);
+      float a0 = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * ex2(pm[rt] - mn);
+      float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        a0 += ex2(fmaf(v[j], zs, -mn));
+        a1 += ex2(fmaf(v[j + 1], zs, -mn));
+        a2 += ex2(fmaf(v[j + 2], zs, -mn));
+        a3 += ex2(fmaf(v[j + 3], zs, -mn));
+      }
+      pm[rt] = mn;
+      ps[rt] = (a0 + a1) + (a2 + a3);
+    }
+  }
+}
+
+// Pass-2 epilogue of one tile: this lane is block `row`; max over g of
+// z·zs − LSE (LSE read four at a time), then the mean over w of 2^max.
+template <int W>
+__device__ __forceinline__ void ring_pass2(uint32_t taddr, int row, int valid, int n2c, int R,
+                                           float zs, float invW, const float *lse, float *out) {
+  float mw[W];
+#pragma unroll
+  for (int w = 0; w < W; w++) mw[w] = -INFINITY;
+  for (int c = 0; c < n2c / 64; c++) {
+    float v[64];
+    tmem_ld64(taddr + (uint32_t)(64 * c), v);
+    const float4 *l4 = reinterpret_cast<const float4 *>(lse + 64 * c);
+    if (64 * c + 64 <= R) {
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        const float4 L = l4[j / 4];
+        mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(v[j + 0], zs, -L.x));
+        mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(v[j + 1], zs, -L.y));
+        mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(v[j + 2], zs, -L.z));
+        mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(v[j + 3], zs, -L.w));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64; j++)
+        if (64 * c + j < R) mw[j % W] = fmaxf(mw[j % W], fmaf(v[j], zs, -lse[64 * c + j]));
+    }
+  }
+  if (n2c % 64) {  // a trailing 32-column chunk
+    float v[32];
+    const int c0 = n2c - 32;
+    tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+    for (int j = 0; j < 32; j++)
+      if (c0 + j < R) mw[j % W] = fmaxf(mw[j % W], fmaf(v[j], zs, -lse[c0 + j]));  // W | 32
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int w = 0; w < W; w++) acc += ex2(mw[w]);
+  if (row < valid) out[row] = acc * invW;
 }
 
 template <int RT, int W>
@@ -924,7 +1041,7 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
           tc_fence_after();
           const int valid = min(128, u.nb - (rank + j * C) * 128);
           float qm[RT], qs[RT];
-          epi_pass1<RT, 1>(tmem + (uint32_t)(buf * BUFCOLS), lane_base, valid, zs, qm, qs);
+          ring_pass1<RT>(tmem + lane_base + (uint32_t)(buf * BUFCOLS), valid, zs, qm, qs);
 #pragma unroll
           for (int rt = 0; rt < RT; rt++) lse_merge(pm[rt], ps[rt], qm[rt], qs[rt]);
         }
@@ -980,8 +1097,8 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
           const int tile = rank + j * C;
           const int valid = min(128, u.nb - tile * 128);
           float *out = a.scores + ((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0 + tile * 128;
-          epi_pass2<1, W>(tmem + (uint32_t)(buf * BUFCOLS), lane_base, warp & 3, lane, valid, a.n2c,
-                          a.R, zs, invW, sm.lse, out);
+          ring_pass2<W>(tmem + lane_base + (uint32_t)(buf * BUFCOLS), row, valid, a.n2c, a.R, zs,
+                        invW, sm.lse, out);
         }
         tc_fence_before();
         __syncwarp();
