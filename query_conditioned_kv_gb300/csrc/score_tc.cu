@@ -813,29 +813,51 @@ __device__ __forceinline__ UnitInfo unit_info(const TcArgs &a, int unit, int C, 
   return u;
 }
 
+// Split TMEM load: issue now, wait later.  The wait names the destination
+// registers as in/out operands, so no use of them can move above it.
+__device__ __forceinline__ void tmem_issue32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
 // Pass-1 epilogue of one 128-block tile: (max, Σ2^(z−max)) of this lane's
-// query row(s), in 64-column halves.
+// query row(s), in 32-column chunks whose TMEM loads are double-buffered.
 template <int RT>
 __device__ __forceinline__ void ring_pass1(uint32_t taddr, int valid, float zs, float (&pm)[RT],
                                            float (&ps)[RT]) {
+  constexpr int NCH = 4 * RT;  // (row tile, 32-column chunk)
+  const int nvc = (valid + 31) / 32;  // chunks with at least one valid column
+  uint32_t r[2][32];
 #pragma unroll
   for (int rt = 0; rt < RT; rt++) {
     pm[rt] = -INFINITY;
     ps[rt] = 0.f;
+  }
+  tmem_issue32(taddr, r[0]);
+  tmem_wait32(r[0]);
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const int nv = min(64, valid - 64 * half);
-      if (nv <= 0) break;  // warp-uniform
-      float v[64];
-      tmem_ld64(taddr + (uint32_t)(rt * 128 + 64 * half), v);
-      if (nv < 64) {
+  for (int ch = 0; ch < NCH; ch++) {
+    const int rt = ch / 4, c = ch % 4;
+    const bool have_next = ch + 1 < NCH && ((ch + 1) % 4) < nvc;
+    if (have_next)  // warp-uniform
+      tmem_issue32(taddr + (uint32_t)(((ch + 1) / 4) * 128 + 32 * ((ch + 1) % 4)), r[(ch + 1) & 1]);
+    if (c < nvc) {
+      float v[32];
 #pragma unroll
-        for (int j = 0; j < 64; j++)
+      for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[ch & 1][j]);
+      const int nv = valid - 32 * c;
+      if (nv < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
           if (j >= nv) v[j] = -INFINITY;
       }
       float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
 #pragma unroll
-      for (int j = 4; j < 64; j += 4) {
+      for (int j = 4; j < 32; j += 4) {
         m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
         m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
       }
@@ -843,7 +865,7 @@ __device__ __forceinline__ void ring_pass1(uint32_t taddr, int valid, float zs, 
       float a0 = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * ex2(pm[rt] - mn);
       float a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
+      for (int j = 0; j < 32; j += 4) {
         a0 += ex2(fmaf(v[j], zs, -mn));
         a1 += ex2(fmaf(v[j + 1], zs, -mn));
         a2 += ex2(fmaf(v[j + 2], zs, -mn));
@@ -852,6 +874,7 @@ __device__ __forceinline__ void ring_pass1(uint32_t taddr, int valid, float zs, 
       pm[rt] = mn;
       ps[rt] = (a0 + a1) + (a2 + a3);
     }
+    if (have_next) tmem_wait32(r[(ch + 1) & 1]);
   }
 }
 
@@ -863,32 +886,56 @@ __device__ __forceinline__ void ring_pass2(uint32_t taddr, int row, int valid, i
   float mw[W];
 #pragma unroll
   for (int w = 0; w < W; w++) mw[w] = -INFINITY;
-  for (int c = 0; c < n2c / 64; c++) {
-    float v[64];
-    tmem_ld64(taddr + (uint32_t)(64 * c), v);
-    const float4 *l4 = reinterpret_cast<const float4 *>(lse + 64 * c);
-    if (64 * c + 64 <= R) {
+  const int nch = n2c / 32;
+  uint32_t r[2][32];
+  tmem_issue32(taddr, r[0]);
+  tmem_wait32(r[0]);
+#pragma unroll 1
+  for (int c = 0; c < nch; c += 2) {
+    // chunk c in r[0]; c + 1 (if any) into r[1] while c is reduced
+    const bool n1 = c + 1 < nch, n2 = c + 2 < nch;
+    if (n1) tmem_issue32(taddr + (uint32_t)(32 * (c + 1)), r[1]);
+    {
+      const float4 *l4 = reinterpret_cast<const float4 *>(lse + 32 * c);
+      if (32 * c + 32 <= R) {
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        const float4 L = l4[j / 4];
-        mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(v[j + 0], zs, -L.x));
-        mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(v[j + 1], zs, -L.y));
-        mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(v[j + 2], zs, -L.z));
-        mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(v[j + 3], zs, -L.w));
+        for (int j = 0; j < 32; j += 4) {
+          const float4 L = l4[j / 4];
+          mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(__uint_as_float(r[0][j + 0]), zs, -L.x));
+          mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(__uint_as_float(r[0][j + 1]), zs, -L.y));
+          mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(__uint_as_float(r[0][j + 2]), zs, -L.z));
+          mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(__uint_as_float(r[0][j + 3]), zs, -L.w));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+          if (32 * c + j < R)
+            mw[j % W] = fmaxf(mw[j % W], fmaf(__uint_as_float(r[0][j]), zs, -lse[32 * c + j]));
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 64; j++)
-        if (64 * c + j < R) mw[j % W] = fmaxf(mw[j % W], fmaf(v[j], zs, -lse[64 * c + j]));
     }
-  }
-  if (n2c % 64) {  // a trailing 32-column chunk
-    float v[32];
-    const int c0 = n2c - 32;
-    tmem_ld32(taddr + (uint32_t)c0, v);
+    if (!n1) break;
+    tmem_wait32(r[1]);
+    if (n2) tmem_issue32(taddr + (uint32_t)(32 * (c + 2)), r[0]);
+    {
+      const float4 *l4 = reinterpret_cast<const float4 *>(lse + 32 * (c + 1));
+      if (32 * (c + 1) + 32 <= R) {
 #pragma unroll
-    for (int j = 0; j < 32; j++)
-      if (c0 + j < R) mw[j % W] = fmaxf(mw[j % W], fmaf(v[j], zs, -lse[c0 + j]));  // W | 32
+        for (int j = 0; j < 32; j += 4) {
+          const float4 L = l4[j / 4];
+          mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(__uint_as_float(r[1][j + 0]), zs, -L.x));
+          mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(__uint_as_float(r[1][j + 1]), zs, -L.y));
+          mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(__uint_as_float(r[1][j + 2]), zs, -L.z));
+          mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(__uint_as_float(r[1][j + 3]), zs, -L.w));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+          if (32 * (c + 1) + j < R)
+            mw[j % W] =
+                fmaxf(mw[j % W], fmaf(__uint_as_float(r[1][j]), zs, -lse[32 * (c + 1) + j]));
+      }
+    }
+    if (n2) tmem_wait32(r[0]);
   }
   float acc = 0.f;
 #pragma unroll
