@@ -684,8 +684,9 @@ k_score_split(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
 //               its tiles twice (pass 1, pass 2) through an NS-stage ring;
 //   warp 1      MMA issuer: per tile, pass-1 or pass-2 tcgen05.mma into one
 //               of NBUF TMEM accumulators;
-//   warps 2–9   two epilogue warpgroups that take alternate tiles: pass-1
-//               online row LSE, then (after the exchange) pass-2 scores.
+//   warps 2…     epilogue warpgroups (three, or two for > 128 query rows)
+//               taking tiles round-robin: pass-1 online row LSE, then
+//               (after the exchange) pass-2 scores.
 // Between a unit's two passes the CTAs exchange their row partials through
 // distributed shared memory: every CTA stores its partials into each peer's
 // receive slot and arrives on the peer's mbarrier (release at cluster
@@ -693,8 +694,13 @@ k_score_split(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
 // keep prefetching the pass-2 tiles.  The second read of a tile usually hits
 // L2 (a CTA's share of a unit is ≤ 1/C of its Mean-K).
 
-constexpr int kRingThreads = 320;
 constexpr int kRingMaxC = 4;
+// Epilogue warpgroups: three for ≤ 128 query rows (4 TMEM accumulators of
+// 128 columns), two for up to 256 rows (2 accumulators of 256 columns); two
+// more warps produce and issue.  Three groups keep ≤ 4 warps per SM
+// sub-partition, so each thread can hold 128 registers without spilling.
+template <int RT> constexpr int ring_groups() { return RT == 1 ? 3 : 2; }
+template <int RT> constexpr int ring_threads() { return 64 + 128 * ring_groups<RT>(); }
 
 __device__ __forceinline__ uint32_t cluster_nrank() {
   uint32_t r;
@@ -740,27 +746,37 @@ __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Bounded wait that also gives up as soon as another role of the CTA failed.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for a phase, bounded at one second of wall time, giving up at once if
+// another role of the CTA failed.  No sleep between polls: try_wait itself
+// suspends the thread until the phase completes or a short hardware limit
+// passes, so a hand-off between roles costs no extra wake-up latency.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *failed,
                                               bool cluster_scope = false) {
-  for (uint32_t i = 0; i < kWaitLimit; i++) {
+  if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
     if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    if (*failed) return false;
-    if (i > 8) __nanosleep(32);
+    if (*failed || global_ns() - t0 > 1000000000ull) return false;
   }
-  return false;
 }
 
 template <int RT>
 struct RingSmem {
   static constexpr int NS = RT == 1 ? 4 : 2;    // Mean-K ring stages
   static constexpr int NBUF = RT == 1 ? 4 : 2;  // TMEM accumulators
+  static constexpr int NEG = ring_groups<RT>();  // epilogue warpgroups
   static constexpr int BUFCOLS = 128 * RT;      // columns per accumulator
   uint8_t *ring, *q;
   uint64_t *full, *empty, *tfull, *tempty, *qfull, *qempty, *recv;
   uint32_t *tmem_holder;
   volatile int *failed;
-  float2 *egpart;  // [2 groups][256 rows]
+  float2 *egpart;  // [NEG groups][256 rows]
   float2 *rbuf;    // [2 parities][kRingMaxC ranks][256 rows]
   float *lse;      // [256 rows]
   __device__ RingSmem(uint8_t *raw, int KB) {
@@ -781,13 +797,13 @@ struct RingSmem {
     tmem_holder = reinterpret_cast<uint32_t *>(recv + 2);
     failed = reinterpret_cast<volatile int *>(tmem_holder + 1);
     egpart = reinterpret_cast<float2 *>(tmem_holder + 4);  // 16-byte aligned
-    rbuf = egpart + 2 * 256;
+    rbuf = egpart + NEG * 256;
     lse = reinterpret_cast<float *>(rbuf + 2 * kRingMaxC * 256);
   }
   static size_t bytes(int D) {
     int KB = D / 64;
     return 1024 + (size_t)NS * KB * 16384 + (size_t)2 * KB * RT * 16384 +
-           (2 * NS + 2 * NBUF + 6) * 8 + 16 + (2 * 256 + 2 * kRingMaxC * 256) * 8 + 256 * 4;
+           (2 * NS + 2 * NBUF + 6) * 8 + 16 + (NEG * 256 + 2 * kRingMaxC * 256) * 8 + 256 * 4;
   }
 };
 
@@ -862,17 +878,14 @@ __device__ __forceinline__ void ring_pass1(uint32_t taddr, int valid, float zs, 
         m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
       }
       const float mn = fmaxf(pm[rt], fmaxf(m0, m1) * zs);
-      float a0 = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * ex2(pm[rt] - mn);
-      float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      float acc[8];
+      acc[0] = (pm[rt] == -INFINITY) ? 0.f : ps[rt] * ex2(pm[rt] - mn);
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        a0 += ex2(fmaf(v[j], zs, -mn));
-        a1 += ex2(fmaf(v[j + 1], zs, -mn));
-        a2 += ex2(fmaf(v[j + 2], zs, -mn));
-        a3 += ex2(fmaf(v[j + 3], zs, -mn));
-      }
+      for (int k = 1; k < 8; k++) acc[k] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j++) acc[j & 7] += ex2(fmaf(v[j], zs, -mn));
       pm[rt] = mn;
-      ps[rt] = (a0 + a1) + (a2 + a3);
+      ps[rt] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
     if (have_next) tmem_wait32(r[(ch + 1) & 1]);
   }
@@ -886,56 +899,27 @@ __device__ __forceinline__ void ring_pass2(uint32_t taddr, int row, int valid, i
   float mw[W];
 #pragma unroll
   for (int w = 0; w < W; w++) mw[w] = -INFINITY;
-  const int nch = n2c / 32;
-  uint32_t r[2][32];
-  tmem_issue32(taddr, r[0]);
-  tmem_wait32(r[0]);
 #pragma unroll 1
-  for (int c = 0; c < nch; c += 2) {
-    // chunk c in r[0]; c + 1 (if any) into r[1] while c is reduced
-    const bool n1 = c + 1 < nch, n2 = c + 2 < nch;
-    if (n1) tmem_issue32(taddr + (uint32_t)(32 * (c + 1)), r[1]);
-    {
+  for (int c = 0; c < n2c / 32; c++) {
+    uint32_t r[32];
+    tmem_issue32(taddr + (uint32_t)(32 * c), r);
+    tmem_wait32(r);
+    if (32 * c + 32 <= R) {
       const float4 *l4 = reinterpret_cast<const float4 *>(lse + 32 * c);
-      if (32 * c + 32 <= R) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 L = l4[j / 4];
-          mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(__uint_as_float(r[0][j + 0]), zs, -L.x));
-          mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(__uint_as_float(r[0][j + 1]), zs, -L.y));
-          mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(__uint_as_float(r[0][j + 2]), zs, -L.z));
-          mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(__uint_as_float(r[0][j + 3]), zs, -L.w));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; j++)
-          if (32 * c + j < R)
-            mw[j % W] = fmaxf(mw[j % W], fmaf(__uint_as_float(r[0][j]), zs, -lse[32 * c + j]));
+      for (int j = 0; j < 32; j += 4) {
+        const float4 L = l4[j / 4];
+        mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(__uint_as_float(r[j + 0]), zs, -L.x));
+        mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(__uint_as_float(r[j + 1]), zs, -L.y));
+        mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(__uint_as_float(r[j + 2]), zs, -L.z));
+        mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(__uint_as_float(r[j + 3]), zs, -L.w));
       }
-    }
-    if (!n1) break;
-    tmem_wait32(r[1]);
-    if (n2) tmem_issue32(taddr + (uint32_t)(32 * (c + 2)), r[0]);
-    {
-      const float4 *l4 = reinterpret_cast<const float4 *>(lse + 32 * (c + 1));
-      if (32 * (c + 1) + 32 <= R) {
+    } else {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 L = l4[j / 4];
-          mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(__uint_as_float(r[1][j + 0]), zs, -L.x));
-          mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(__uint_as_float(r[1][j + 1]), zs, -L.y));
-          mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(__uint_as_float(r[1][j + 2]), zs, -L.z));
-          mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(__uint_as_float(r[1][j + 3]), zs, -L.w));
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; j++)
-          if (32 * (c + 1) + j < R)
-            mw[j % W] =
-                fmaxf(mw[j % W], fmaf(__uint_as_float(r[1][j]), zs, -lse[32 * (c + 1) + j]));
-      }
+      for (int j = 0; j < 32; j++)
+        if (32 * c + j < R)
+          mw[j % W] = fmaxf(mw[j % W], fmaf(__uint_as_float(r[j]), zs, -lse[32 * c + j]));
     }
-    if (n2) tmem_wait32(r[0]);
   }
   float acc = 0.f;
 #pragma unroll
@@ -944,7 +928,7 @@ __device__ __forceinline__ void ring_pass2(uint32_t taddr, int row, int valid, i
 }
 
 template <int RT, int W>
-__global__ void __launch_bounds__(kRingThreads, 1)
+__global__ void __launch_bounds__(ring_threads<RT>(), 1)
 k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CUtensorMap tm_q,
              TcArgs a) {
   static_assert(W == 8 || W == 16 || W == 32, "W divides 32");
@@ -1062,9 +1046,10 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
     __syncwarp();
   } else {
     // ------------------------------------------------------- epilogue
-    const int eg = (warp - 2) >> 2;             // epilogue group 0 or 1
+    constexpr int NEG = SM::NEG;                // epilogue groups
+    const int eg = (warp - 2) >> 2;             // this thread's group
     const int row = 32 * (warp & 3) + lane;     // this thread's TMEM lane
-    const int et = (warp - 2) * 32 + lane;      // 0 … 255
+    const int et = (warp - 2) * 32 + lane;      // 0 … 128·NEG − 1
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const float zs = a.zscale, invW = 1.f / (float)a.W;
     uint32_t t = 0, ui = 0;
@@ -1080,7 +1065,7 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
         ps[rt] = 0.f;
       }
       for (int j = 0; j < u.my_tiles; j++, t++) {
-        if ((int)(t & 1) != eg) continue;
+        if ((int)(t % NEG) != eg) continue;
         const int buf = t % NBUF;
         ok = __all_sync(0xFFFFFFFFu,
                         ok && wait_or_abort(smem_u32(sm.tfull + buf), (t / NBUF) & 1, sm.failed));
@@ -1100,12 +1085,14 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
       const int par = ui & 1;
 #pragma unroll
       for (int rt = 0; rt < RT; rt++) sm.egpart[eg * 256 + rt * 128 + row] = make_float2(pm[rt], ps[rt]);
-      named_sync(2, 256);
+      named_sync(2, 128 * NEG);
       if (eg == 0) {
         for (int rt = 0; rt < RT; rt++) {
           float m = pm[rt], s2 = ps[rt];
-          const float2 o = sm.egpart[256 + rt * 128 + row];
-          lse_merge(m, s2, o.x, o.y);
+          for (int g2 = 1; g2 < NEG; g2++) {
+            const float2 o = sm.egpart[g2 * 256 + rt * 128 + row];
+            lse_merge(m, s2, o.x, o.y);
+          }
           const float2 v = make_float2(m, s2);
           float2 *mine = sm.rbuf + (par * kRingMaxC + rank) * 256 + rt * 128 + row;
           *mine = v;
@@ -1123,7 +1110,7 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
       if (C > 1)
         ok = __all_sync(0xFFFFFFFFu,
                         ok && wait_or_abort(smem_u32(sm.recv + par), (ui >> 1) & 1, sm.failed, true));
-      named_sync(2, 256);
+      named_sync(2, 128 * NEG);
       if (et < RT * 128) {
         float m = -INFINITY, s2 = 0.f;
         for (int c = 0; c < C; c++) {
@@ -1132,10 +1119,10 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
         }
         sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);
       }
-      named_sync(2, 256);
+      named_sync(2, 128 * NEG);
       // pass 2: this group's tiles
       for (int j = 0; j < u.my_tiles; j++, t++) {
-        if ((int)(t & 1) != eg) continue;
+        if ((int)(t % NEG) != eg) continue;
         const int buf = t % NBUF;
         ok = __all_sync(0xFFFFFFFFu,
                         ok && wait_or_abort(smem_u32(sm.tfull + buf), (t / NBUF) & 1, sm.failed));
@@ -1301,7 +1288,7 @@ int ring_clusters(int C, int D) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(C);
-  cfg.blockDim = dim3(kRingThreads);
+  cfg.blockDim = dim3(ring_threads<RT>());
   cfg.dynamicSmemBytes = smem;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
@@ -1325,7 +1312,7 @@ cudaError_t launch_ring(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3((n_clusters < n_units ? n_clusters : n_units) * C);
-  cfg.blockDim = dim3(kRingThreads);
+  cfg.blockDim = dim3(ring_threads<RT>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
