@@ -177,7 +177,8 @@ def run_ours(args, rank, world, local_rank):
     meank = torch.empty(cfg.L, cfg.H, cfg.nb_total, cfg.D, dtype=torch.bfloat16, device=dev)
     kvc.kvc_build_meank(kraw, meank, cfg.L, cfg.H, cfg.D, cfg.n_tok)
     ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
-                    cfg.n_recent, theta=cfg.theta, pos0=cfg.pos0, device=dev)
+                    cfg.n_recent, theta=cfg.theta, pos0=cfg.pos0, device=dev,
+                    groups=args.groups)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
@@ -381,6 +382,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-units", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--groups", type=int, default=None,
+                    help="layer groups of the pipelined event (default: the library's choice)")
     args = ap.parse_args()
     args.steps_ref = max(1, min(args.steps, 2))
     args.warmup_ref = 1

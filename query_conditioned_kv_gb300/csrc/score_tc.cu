@@ -768,7 +768,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 
 template <int RT>
 struct RingSmem {
-  static constexpr int NS = RT == 1 ? 4 : 2;    // Mean-K ring stages
+  // Ring depth: the loaded latency of a 32 KB tile is ≈ 3 µs, so the ring
+  // holds as many tiles as shared memory allows (5 with one query buffer).
+  static constexpr int NS = RT == 1 ? 5 : 2;    // Mean-K ring stages
+  static constexpr int QB = RT == 1 ? 1 : 2;    // query-row buffers
+  static constexpr int ROWS = 128 * RT;         // query rows (padded)
   static constexpr int NBUF = RT == 1 ? 4 : 2;  // TMEM accumulators
   static constexpr int NEG = ring_groups<RT>();  // epilogue warpgroups
   static constexpr int BUFCOLS = 128 * RT;      // columns per accumulator
@@ -776,16 +780,16 @@ struct RingSmem {
   uint64_t *full, *empty, *tfull, *tempty, *qfull, *qempty, *recv;
   uint32_t *tmem_holder;
   volatile int *failed;
-  float2 *egpart;  // [NEG groups][256 rows]
-  float2 *rbuf;    // [2 parities][kRingMaxC ranks][256 rows]
-  float *lse;      // [256 rows]
+  float2 *egpart;  // [NEG groups][ROWS]
+  float2 *rbuf;    // [2 parities][kRingMaxC ranks][ROWS]
+  float *lse;      // [ROWS]
   __device__ RingSmem(uint8_t *raw, int KB) {
     uint8_t *p = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     ring = p;
     p += NS * KB * 16384;
     q = p;
-    p += 2 * KB * RT * 16384;
+    p += QB * KB * RT * 16384;
     uint64_t *b = reinterpret_cast<uint64_t *>(p);
     full = b;
     empty = full + NS;
@@ -797,13 +801,13 @@ struct RingSmem {
     tmem_holder = reinterpret_cast<uint32_t *>(recv + 2);
     failed = reinterpret_cast<volatile int *>(tmem_holder + 1);
     egpart = reinterpret_cast<float2 *>(tmem_holder + 4);  // 16-byte aligned
-    rbuf = egpart + NEG * 256;
-    lse = reinterpret_cast<float *>(rbuf + 2 * kRingMaxC * 256);
+    rbuf = egpart + NEG * ROWS;
+    lse = reinterpret_cast<float *>(rbuf + 2 * kRingMaxC * ROWS);
   }
   static size_t bytes(int D) {
     int KB = D / 64;
-    return 1024 + (size_t)NS * KB * 16384 + (size_t)2 * KB * RT * 16384 +
-           (2 * NS + 2 * NBUF + 6) * 8 + 16 + (NEG * 256 + 2 * kRingMaxC * 256) * 8 + 256 * 4;
+    return 1024 + (size_t)NS * KB * 16384 + (size_t)QB * KB * RT * 16384 +
+           (2 * NS + 2 * NBUF + 6) * 8 + 16 + (NEG * ROWS + 2 * kRingMaxC * ROWS) * 8 + ROWS * 4;
   }
 };
 
@@ -975,8 +979,8 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
         const UnitInfo u = unit_info(a, unit, C, rank);
         if (u.nb == 0 && rank == 0) record_error(a.status, KVC_ERR_BOUNDS);
         if (u.my_tiles == 0) continue;
-        const int qb = qi & 1;
-        if (!wait_or_abort(smem_u32(sm.qempty + qb), ((qi >> 1) & 1) ^ 1, sm.failed)) break;
+        const int qb = qi % SM::QB;
+        if (!wait_or_abort(smem_u32(sm.qempty + qb), ((qi / SM::QB) & 1) ^ 1, sm.failed)) break;
         mbar_expect_tx(smem_u32(sm.qfull + qb), q_bytes);
         for (int kb = 0; kb < KB; kb++)
           tma_load_2d(smem_u32(sm.q + qb * q_bytes + kb * RT * 16384), &tm_q, kb * 64, u.q_row0,
@@ -1008,8 +1012,8 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
       for (int unit = cluster_id; unit < n_units && ok; unit += n_clusters) {
         const UnitInfo u = unit_info(a, unit, C, rank);
         if (u.my_tiles == 0) continue;
-        const int qb = qi & 1;
-        if (!(ok = wait_or_abort(smem_u32(sm.qfull + qb), (qi >> 1) & 1, sm.failed))) break;
+        const int qb = qi % SM::QB;
+        if (!(ok = wait_or_abort(smem_u32(sm.qfull + qb), (qi / SM::QB) & 1, sm.failed))) break;
         const uint8_t *qbase = sm.q + qb * q_bytes;
         for (int pass = 0; pass < 2 && ok; pass++)
           for (int j = 0; j < u.my_tiles; j++, s++, t++) {
@@ -1084,17 +1088,17 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
       // exchange: group partials → CTA partial → every CTA of the cluster
       const int par = ui & 1;
 #pragma unroll
-      for (int rt = 0; rt < RT; rt++) sm.egpart[eg * 256 + rt * 128 + row] = make_float2(pm[rt], ps[rt]);
+      for (int rt = 0; rt < RT; rt++) sm.egpart[eg * SM::ROWS + rt * 128 + row] = make_float2(pm[rt], ps[rt]);
       named_sync(2, 128 * NEG);
       if (eg == 0) {
         for (int rt = 0; rt < RT; rt++) {
           float m = pm[rt], s2 = ps[rt];
           for (int g2 = 1; g2 < NEG; g2++) {
-            const float2 o = sm.egpart[g2 * 256 + rt * 128 + row];
+            const float2 o = sm.egpart[g2 * SM::ROWS + rt * 128 + row];
             lse_merge(m, s2, o.x, o.y);
           }
           const float2 v = make_float2(m, s2);
-          float2 *mine = sm.rbuf + (par * kRingMaxC + rank) * 256 + rt * 128 + row;
+          float2 *mine = sm.rbuf + (par * kRingMaxC + rank) * SM::ROWS + rt * 128 + row;
           *mine = v;
           for (int p = 0; p < C; p++)
             if (p != rank) st_cluster_f2(mapa_u32(smem_u32(mine), (uint32_t)p), v);
@@ -1114,7 +1118,7 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
       if (et < RT * 128) {
         float m = -INFINITY, s2 = 0.f;
         for (int c = 0; c < C; c++) {
-          const float2 v = sm.rbuf[(par * kRingMaxC + c) * 256 + et];
+          const float2 v = sm.rbuf[(par * kRingMaxC + c) * SM::ROWS + et];
           lse_merge(m, s2, v.x, v.y);
         }
         sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);

@@ -54,7 +54,8 @@ class MeanKEvent:
     def __init__(self, L: int, H: int, Hq: int, D: int, W: int,
                  hist: Sequence[int], budget: int, n_sink: int, n_recent: int,
                  L_pack: Optional[int] = None, theta: float = 1e6,
-                 pos0: int = 0, keepmask: bool = False, device="cuda"):
+                 pos0: int = 0, keepmask: bool = False, device="cuda",
+                 groups: Optional[int] = None):
         self.L, self.H, self.Hq, self.D, self.W = L, H, Hq, D, W
         self.hist = [int(n) for n in hist]
         if any(n % BLOCK_TOKENS for n in self.hist):
@@ -97,7 +98,7 @@ class MeanKEvent:
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
         self.side = torch.cuda.Stream(device=dev)
-        self.groups = self._layer_groups(groups_hint(L))
+        self.groups = self._layer_groups(groups_hint(L) if groups is None else groups)
 
     @staticmethod
     def _split(L: int, n: int):
