@@ -96,9 +96,15 @@ def kvc_version() -> str:
 
 
 def _ptr(t):
-    """Device pointer of a CUDA tensor (None → NULL)."""
+    """Device pointer of a dense row-major CUDA tensor (None → NULL).  The
+    library indexes every buffer as packed row-major, so a strided view
+    (a transpose, a Fortran-ordered array brought over from numpy) is
+    refused rather than read in the wrong order."""
     if t is None:
         return None
+    if not t.is_contiguous():
+        raise ValueError("libkvc takes contiguous row-major tensors only "
+                         f"(got shape {tuple(t.shape)}, strides {t.stride()})")
     if not t.is_cuda:
         raise ValueError("libkvc takes device tensors only")
     return t.data_ptr()

@@ -108,3 +108,22 @@ def test_binding_raises_on_error(kvc):
     with pytest.raises(kvc.KvcError) as ei:
         kvc._ok(3, "kvc_select")
     assert ei.value.code == 3 and "budget" in str(ei.value)
+
+
+def test_binding_refuses_strided_tensors(kvc):
+    """Every buffer crosses the boundary as a packed row-major pointer, so a
+    transposed view must be refused, not read in storage order."""
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="contiguous"):
+        kvc._ptr(torch.zeros(4, 6).t())
+    # a column-major numpy array keeps its strides through from_numpy
+    import numpy as np
+    with pytest.raises(ValueError, match="contiguous"):
+        kvc._ptr(torch.from_numpy(np.asfortranarray(np.zeros((3, 5), np.int32))))
+
+
+def test_slot_map_generator_is_row_major():
+    import workloads as W
+    cfg = W.SlotMapConfig(name="t", n_sess=3, N=1008, prefix=256, page=16, L=1, H=8,
+                          Hq=32, D=128, T=4, turns=1, budget=300)
+    assert cfg.slot_maps().flags["C_CONTIGUOUS"]

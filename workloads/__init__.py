@@ -345,7 +345,9 @@ class SlotMapConfig:
         bt[p / page]·page + p % page)."""
         bt = self.block_tables() if block_tables is None else block_tables
         p = np.arange(self.N)
-        return (bt[:, p // self.page] * self.page + p % self.page).astype(np.int32)
+        # the fancy index leaves a column-major array: hand out row-major
+        return np.ascontiguousarray(
+            (bt[:, p // self.page] * self.page + p % self.page).astype(np.int32))
 
     def refcounts(self, slot_maps: np.ndarray) -> np.ndarray:
         """One count per slot-map reference; the dead slot holds none."""
