@@ -8,6 +8,7 @@ event once to produce realistic inputs for the stage, then launches the stage
   python -m query_conditioned_kv_gb300.profile_cases score --layers 16 --iters 3
   python -m query_conditioned_kv_gb300.profile_cases pack  --layers 4  --iters 3
   python -m query_conditioned_kv_gb300.profile_cases select --layers 16 --iters 3
+  python -m query_conditioned_kv_gb300.profile_cases meank  --layers 2  --iters 3
 """
 from __future__ import annotations
 
@@ -18,7 +19,7 @@ import sys
 
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["score", "select", "pack", "event"])
+    ap.add_argument("case", choices=["score", "select", "pack", "event", "meank"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args(argv)
@@ -35,6 +36,13 @@ def main(argv=None) -> None:
     cfg = W.scaled(W.config_8b(), L=args.layers)
     q = cfg.q(dev)
     meank = torch.empty(cfg.L, cfg.H, cfg.nb_total, cfg.D, dtype=torch.bfloat16, device=dev)
+    if args.case == "meank":
+        kraw, _ = cfg.kv_raw(dev)
+        for _ in range(args.iters):
+            kvc.kvc_build_meank(kraw, meank, cfg.L, cfg.H, cfg.D, cfg.n_tok)
+        torch.cuda.synchronize()
+        print(f"profile case meank: {args.iters} launches on {args.layers} layers ok")
+        return
     if args.case in ("pack", "event"):
         kraw, vraw = cfg.kv_raw(dev)
         kvc.kvc_build_meank(kraw, meank, cfg.L, cfg.H, cfg.D, cfg.n_tok)
