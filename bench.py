@@ -8,7 +8,11 @@ bf16 tensors resident in HBM (see workloads/).
 
 One step = one event: score (Mean-K) → select → pack.  The metric is KV
 history tokens compressed per second; the roofline is algorithmic bytes over
-measured kernel time against the measured HBM copy bandwidth.
+measured kernel time against the measured HBM copy bandwidth.  The Mean-K
+index build and, on its own workload (64 sessions × 32768 positions over a
+paged, refcounted K pool), the QueryMemory event (memory update; rule score
+→ select → redirect + free) are measured after the timed steps and reported
+beside them (`meank_build`, `slotmap_event`; `--no-slotmap` skips the latter).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -318,6 +322,113 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# --------------------------------------------------- QueryMemory event
+
+SLOTMAP_WORKLOAD = ("slotmap_64x32k: 64 sessions x 32768 positions (4096-position shared, "
+                    "refcounted prefix; page 16), 36 layers, 8 KV / 32 query heads, d 128, "
+                    "4 memory turns of 32 queries, 8192 kept positions per session")
+
+
+def slot_map_event(args, dev, peak, reps: int = 3):
+    """The QueryMemory-mode event (rule score over the paged K pool → token
+    select → redirect + free) on the full 64 x 32768 workload, each stage
+    timed with CUDA events; the memory update is timed on its own.  The
+    slot maps and refcounts are restored before every rep (outside the
+    timed span); the inputs (135.6 GB of K) are far larger than L2."""
+    import numpy as np
+    import torch
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+
+    cfg = W.config_slotmap()
+    kp = torch.empty(cfg.L, cfg.n_slots, cfg.H, cfg.D, dtype=torch.bfloat16, device=dev)
+    for l in range(cfg.L):
+        kp[l] = cfg.kpool_layer(l, dev)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    sm_np = cfg.slot_maps()
+    sm0 = torch.from_numpy(sm_np).to(dev)
+    rc0 = torch.from_numpy(cfg.refcounts(sm_np)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        return a, b
+
+    # memory recurrence: one update per turn
+    M = torch.zeros(cfg.n_sess, cfg.L, cfg.Hq, cfg.D, dtype=torch.float32, device=dev)
+    upd = []
+    for t in range(cfg.turns):
+        qt = cfg.q_turn(t, dev)
+        upd.append(timed(lambda: kvc.kvc_qmem_update(M, qt, cfg.n_sess, cfg.L, cfg.Hq, cfg.D,
+                                                      cfg.T, cfg.decay, cfg.gain, 1)))
+        torch.cuda.synchronize(dev)
+        q_bytes = qt.numel() * 2
+        del qt
+    upd_ms = statistics.median(a.elapsed_time(b) for a, b in upd)
+    upd_bytes = q_bytes + 2 * M.numel() * 4
+
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots, cfg.budget,
+                      cfg.prefix, cfg.sentinel, device=dev)
+    sm = torch.empty_like(sm0)
+    rc = torch.empty_like(rc0)
+    stages = {"score": [], "select": [], "redirect": []}
+    events = []
+    for r in range(1 + reps):
+        sm.copy_(sm0)
+        rc.copy_(rc0)
+        torch.cuda.synchronize(dev)
+        t_all = timed(lambda: None)[0]
+        st = {"score": timed(lambda: ev.score(M, kp, sm)),
+              "select": timed(lambda: ev.select()),
+              "redirect": timed(lambda: ev.redirect(sm, rc))}
+        end = timed(lambda: None)[1]
+        torch.cuda.synchronize(dev)
+        if r == 0:
+            continue  # warm-up
+        for k, (a, b) in st.items():
+            stages[k].append(a.elapsed_time(b))
+        events.append(t_all.elapsed_time(end))
+    if kvc.kvc_device_status(ev.dev_status) != 0:
+        raise RuntimeError("device status error in the QueryMemory event")
+    n_freed = int(ev.n_freed.item())
+
+    n_unique = cfg.prefix + cfg.n_sess * (cfg.N - cfg.prefix)
+    k_bytes = n_unique * cfg.L * cfg.H * cfg.D * 2
+    sm_bytes = sm0.numel() * 4
+    score_bytes = k_bytes + M.numel() * 4 + sm_bytes
+    event_bytes = score_bytes + sm_bytes + rc0.numel() * 4
+    ms = statistics.median(events)
+    sc_ms = statistics.median(stages["score"])
+    tokens = cfg.n_sess * cfg.N
+    out = {
+        "workload": SLOTMAP_WORKLOAD, "tokens_per_event": tokens,
+        "value": tokens / (ms * 1e-3), "unit": UNIT, "ms_per_event": ms,
+        "algorithmic_bytes": event_bytes,
+        "hbm_roofline_event": {"achieved_gbs": event_bytes / (ms * 1e-3) / 1e9,
+                               "frac": event_bytes / (ms * 1e-3) / 1e9 / peak},
+        "stages_ms": {k: round(statistics.median(v), 4) for k, v in stages.items()},
+        "score_roofline": {"kernels": "k_qmem_logits + k_qmem_lse + k_qmem_rule",
+                           "algorithmic_bytes": score_bytes,
+                           "achieved": score_bytes / (sc_ms * 1e-3) / 1e9,
+                           "frac": score_bytes / (sc_ms * 1e-3) / 1e9 / peak,
+                           "note": "unique K rows read once (shared prefix counted once); "
+                                   "the fp32 logit spill (9.7 GB written + read) is overhead"},
+        "qmem_update": {"ms": upd_ms, "algorithmic_bytes": upd_bytes,
+                        "achieved_gbs": upd_bytes / (upd_ms * 1e-3) / 1e9,
+                        "frac": upd_bytes / (upd_ms * 1e-3) / 1e9 / peak,
+                        "note": "one turn: queries read once, M read and written once"},
+        "freed_slots": n_freed, "reps": reps,
+        "l2": "inputs (135.6 GB of K) far exceed the 129 MB L2; no flush",
+    }
+    del kp, ev, M
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------ oracle arm
 
 def _oracle_sample(n_units, dev):
@@ -409,6 +520,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-units", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-slotmap", action="store_true",
+                    help="skip the QueryMemory (slot-map) event measurement")
     ap.add_argument("--groups", type=int, default=None,
                     help="layer groups of the pipelined event (default: the library's choice)")
     args = ap.parse_args()
@@ -431,6 +544,11 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, local_rank)
+    if not args.no_slotmap:
+        import torch
+        torch.cuda.empty_cache()
+        line["slotmap_event"] = slot_map_event(args, torch.device("cuda", local_rank),
+                                               peaks()[0])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -194,7 +194,8 @@ kvc_status kvc_qmem_update(float *M, const kvc_bf16 *q_turn, int32_t n_sess,
  *   rule     device fp32 [n_sess][N]          out
  *   ws       device scratch of kvc_score_qmem_workspace_size() bytes
  * A slot outside [0, n_slots) is recorded as KVC_ERR_BOUNDS and treated as
- * dead.  Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE, KVC_ERR_ALIGN,
+ * dead.  Shapes: D ∈ {64, 128}; H divides 32; Hq a multiple of H with
+ * G = Hq/H ≤ 8.  Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE, KVC_ERR_ALIGN,
  * KVC_ERR_WORKSPACE.
  * ---------------------------------------------------------------------- */
 size_t kvc_score_qmem_workspace_size(int32_t n_sess, int32_t L, int32_t Hq,

@@ -123,8 +123,8 @@ kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
   if (!M || !kpool || !slot_map || !rule || !ws) return KVC_ERR_INVALID_ARG;
   if (n_sess < 1 || L < 1 || H < 1 || Hq < 1 || N < 1 || n_slots < 1 || n_slots > INT32_MAX)
     return KVC_ERR_INVALID_ARG;
-  if (!head_dim_ok(D) || Hq % H || H > 32 || 32 % H || (H * D) % 256 || (H * D) / 32 > 64 ||
-      n_sess > 65535 || (N + 127) / 128 > 65535 || L > 65535)
+  if (!head_dim_ok(D) || Hq % H || H > 32 || 32 % H || Hq / H > 8 || n_sess > 65535 ||
+      (N + 255) / 256 > 65535 || L > 65535)
     return KVC_ERR_SHAPE;
   if (!aligned16(M) || !aligned16(kpool) || !aligned16(ws)) return KVC_ERR_ALIGN;
   if (ws_bytes < kvc_score_qmem_workspace_size(n_sess, L, Hq, N)) return KVC_ERR_WORKSPACE;

@@ -12,11 +12,11 @@
 // once all normalisers are known.  The pool is read once:
 //   k_qmem_logits  grid (session, position tile, layer), session fastest so
 //                  that the sessions' reads of the shared prefix rows meet in
-//                  L2.  A warp takes one position at a time, reads the
-//                  slot's H·D K row (one 16-byte-vector sweep per lane) and
-//                  forms the Hq logits against M staged in shared memory;
-//                  the tile's logits go to ws (coalesced along positions)
-//                  with a per-tile (max, Σ2^(z−max)) per (l, hq);
+//                  L2.  A lane takes one KV head of one position, reads its
+//                  D-element K slice and forms its GQA group's logits against
+//                  M staged in shared memory; the tile's logits go to ws
+//                  (coalesced along positions) with a per-tile
+//                  (max, Σ2^(z−max)) per (l, hq);
 //   k_qmem_lse     combines the tiles into one LSE per (session, l, hq);
 //   k_qmem_rule    re-reads the logits (1/16 of the K bytes) and sums
 //                  2^(z − LSE) over (l, hq) per position.
@@ -27,7 +27,7 @@ namespace kvc {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kTJ = 128;        // positions per logits tile
+constexpr int kTJ = 256;        // positions per logits tile
 constexpr int kLogitThreads = 256;
 
 // ----------------------------------------------------------- update
@@ -77,85 +77,159 @@ struct QArgs {
   float zscale;
 };
 
-// E = H·D/32 contiguous K elements per lane (a multiple of 8); the lanes of
-// one KV head are 32/H consecutive lanes.
-template <int E>
-__global__ void __launch_bounds__(kLogitThreads)
+// Logits of one (session, position tile, layer).
+//
+// A warp is split into S = 32/NC slices of NC = D/8 lanes; lane c of a slice
+// owns head-dim elements [8c, 8c+8).  A slice works through items of kPB
+// positions of one KV head h: per position its NC lanes read the head's K
+// slice as one contiguous 2·D-byte segment (16 bytes per lane), and each
+// lane keeps its 8 elements of M for the GP query heads of h's GQA group in
+// registers.  A batch of kB = 16/GP positions gives each lane 16 partial
+// dot products; a recursive-halving reduce-scatter over the slice's lanes
+// (log2 NC shuffle stages) sums them, leaving the finished logits spread
+// over the lanes.  K streams kPF batches ahead of the arithmetic.  The
+// tile's logits are transposed through shared memory ([hq][position],
+// padded) and written coalesced along positions, with a per-tile
+// (max, Σ2^(z−max)) per query head reduced by whole warps.
+constexpr int kPB = 32;  // positions per item
+constexpr int kPF = 2;   // batches of K in flight ahead of the one in use
+
+template <int D, int GP>
+__global__ void __launch_bounds__(kLogitThreads, 2)
 k_qmem_logits(QArgs a) {
   extern __shared__ float sm[];
-  float *Ms = sm;                            // [Hq][D]
-  float *Z = Ms + (size_t)a.Hq * a.D;        // [Hq][kTJ + 1]
+  constexpr int NC = D / 8;                // lanes per slice
+  constexpr int S = 32 / NC;               // slices per warp
+  constexpr int kB = 16 / GP;              // positions per batch
+  constexpr int NV = kB * GP;              // partial sums per lane per batch
+  constexpr int ZS = kTJ + 1;              // row stride of Z
+  constexpr int n_warps = kLogitThreads / 32;
+  static_assert(NV % NC == 0, "reduce-scatter leaves whole values per lane");
+  constexpr int NOUT = NV / NC;            // finished logits per lane per batch
+  float *Z = sm;                           // [Hq][ZS]
   const int r = blockIdx.x, tile = blockIdx.y, l = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n_warps = kLogitThreads / 32;
-  const int lanes_per_head = 32 / a.H;
-  const int h = lane / lanes_per_head;
-  const int d0 = (lane % lanes_per_head) * E;
-
-  const float *Msrc = a.M + ((int64_t)r * a.L + l) * a.Hq * a.D;
-  for (int i = threadIdx.x; i < a.Hq * a.D; i += blockDim.x) Ms[i] = Msrc[i];
-  __syncthreads();
-
+  const int c = lane % NC, slice = warp * S + lane / NC;
   const int j0 = tile * kTJ;
   const int32_t *smap = a.slot_map + (int64_t)r * a.N;
-  for (int jj = warp; jj < kTJ; jj += n_warps) {
-    const int j = j0 + jj;
-    int32_t u = j < a.N ? smap[j] : a.sentinel;
-    bool live = u != a.sentinel;
-    if (live && (u < 0 || u >= a.n_slots)) {
-      if (lane == 0) record_error(a.status, KVC_ERR_BOUNDS);
-      live = false;
-    }
-    float kv[E];
-    if (live) {
-      const uint16_t *krow = a.kpool + (((int64_t)l * a.n_slots + u) * a.H) * a.D +
-                             (int64_t)lane * E;
+  const float *Mrl = a.M + ((int64_t)r * a.L + l) * a.Hq * D;
+  const uint16_t *kl = a.kpool + (int64_t)l * a.n_slots * a.H * D;
+
+  const int n_items = a.H * (kTJ / kPB);
+  for (int item = slice; item < n_items; item += n_warps * S) {
+    const int h = item % a.H, jb = (item / a.H) * kPB;
+    // this lane's 8 elements of M for the group's query heads (zero past G)
+    float m[GP][8];
 #pragma unroll
-      for (int v = 0; v < E / 8; v++) {
-        uint4 w = __ldg(reinterpret_cast<const uint4 *>(krow) + v);
-        kv[8 * v + 0] = bf16_lo(w.x);
-        kv[8 * v + 1] = bf16_hi(w.x);
-        kv[8 * v + 2] = bf16_lo(w.y);
-        kv[8 * v + 3] = bf16_hi(w.y);
-        kv[8 * v + 4] = bf16_lo(w.z);
-        kv[8 * v + 5] = bf16_hi(w.z);
-        kv[8 * v + 6] = bf16_lo(w.w);
-        kv[8 * v + 7] = bf16_hi(w.w);
+    for (int g = 0; g < GP; g++) {
+      if (g < a.G) {
+        const float4 *src = reinterpret_cast<const float4 *>(Mrl + (h * a.G + g) * D + c * 8);
+        const float4 lo = __ldg(src), hi = __ldg(src + 1);
+        m[g][0] = lo.x; m[g][1] = lo.y; m[g][2] = lo.z; m[g][3] = lo.w;
+        m[g][4] = hi.x; m[g][5] = hi.y; m[g][6] = hi.z; m[g][7] = hi.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; e++) m[g][e] = 0.f;
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; e++) kv[e] = 0.f;
     }
-    for (int g = 0; g < a.G; g++) {
-      const int hq = h * a.G + g;
-      const float *mrow = Ms + hq * a.D + d0;
-      float dot = 0.f;
+    // slot and liveness of each position (every lane of the slice reads the
+    // same slot-map word: one broadcast load)
+    const int32_t *sitem = smap + j0 + jb;
+    const bool whole = j0 + jb + kPB <= a.N;   // no position past the end
+    const uint16_t *kh = kl + (int64_t)h * D + c * 8;
+    const uint32_t row = (uint32_t)(a.H * D);
+    auto slot_of = [&](int jj, bool &live) -> uint32_t {
+      int32_t u = (whole || j0 + jb + jj < a.N) ? sitem[jj] : a.sentinel;
+      live = u != a.sentinel;
+      if (live && (u < 0 || u >= a.n_slots)) {
+        if (c == 0) record_error(a.status, KVC_ERR_BOUNDS);
+        live = false;
+      }
+      return live ? (uint32_t)u : 0u;
+    };
+    uint4 kbuf[kPF + 1][kB];
+    uint32_t lbuf[kPF + 1];  // bit i: position i of the batch is live
+    auto fetch = [&](int batch, int buf) {
+      lbuf[buf] = 0u;
 #pragma unroll
-      for (int e = 0; e < E; e++) dot = fmaf(mrow[e], kv[e], dot);
-      for (int o = lanes_per_head >> 1; o > 0; o >>= 1)
-        dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-      if ((lane % lanes_per_head) == 0)
-        Z[hq * (kTJ + 1) + jj] = live ? dot * a.zscale : -INFINITY;
+      for (int i = 0; i < kB; i++) {
+        bool live;
+        const uint32_t u = slot_of(batch * kB + i, live);
+        lbuf[buf] |= (uint32_t)live << i;
+        kbuf[buf][i] = live ? __ldg(reinterpret_cast<const uint4 *>(
+                                  kh + (uint64_t)u * row))
+                            : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    constexpr int NBATCH = kPB / kB;
+#pragma unroll
+    for (int bt = 0; bt < kPF; bt++) fetch(bt, bt);
+#pragma unroll
+    for (int bt = 0; bt < NBATCH; bt++) {
+      if (bt + kPF < NBATCH) fetch(bt + kPF, (bt + kPF) % (kPF + 1));
+      const int buf = bt % (kPF + 1);
+      float v[NV];  // [position i][g]
+#pragma unroll
+      for (int i = 0; i < kB; i++) {
+        const uint4 w4 = kbuf[buf][i];
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) x[e] = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+#pragma unroll
+        for (int g = 0; g < GP; g++) {
+          float t = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; e++) t = fmaf(m[g][e], x[e], t);
+          v[i * GP + g] = t;
+        }
+      }
+      // reduce-scatter over the NC lanes of the slice: at the stage with
+      // offset o the lane keeps the half of its values selected by bit o of
+      // its index and adds the partner's copy of that half
+#pragma unroll
+      for (int o = NC / 2, n = NV; o >= 1; o >>= 1, n >>= 1) {
+        const bool up = (c & o) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; k++) {
+          const float keep = up ? v[k + n / 2] : v[k];
+          const float send = up ? v[k] : v[k + n / 2];
+          v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+      }
+      // lane c now holds values c·NOUT … c·NOUT + NOUT − 1 of [i][g]
+#pragma unroll
+      for (int k = 0; k < NOUT; k++) {
+        const int idx = c * NOUT + k, i = idx / GP, g = idx % GP;
+        if (g < a.G) {
+          const int jj = jb + bt * kB + i;
+          Z[(h * a.G + g) * ZS + jj] = ((lbuf[buf] >> i) & 1u) ? v[k] * a.zscale : -INFINITY;
+        }
+      }
     }
   }
   __syncthreads();
+
   // logits out, coalesced along positions
   const int64_t lrow = ((int64_t)r * a.L + l) * a.Hq;
-  for (int i = threadIdx.x; i < a.Hq * kTJ; i += blockDim.x) {
-    int hq = i / kTJ, jj = i - hq * kTJ;
-    int j = j0 + jj;
-    if (j < a.N) a.logits[(lrow + hq) * a.N + j] = Z[hq * (kTJ + 1) + jj];
+  const int valid = min(kTJ, a.N - j0);
+  for (int i = threadIdx.x; i < a.Hq * kTJ; i += kLogitThreads) {
+    const int hq = i / kTJ, jj = i - hq * kTJ;
+    if (jj < valid) a.logits[(lrow + hq) * a.N + j0 + jj] = Z[hq * ZS + jj];
   }
-  // per-tile (max, Σ 2^(z − max)) per query head
-  for (int hq = threadIdx.x; hq < a.Hq; hq += blockDim.x) {
-    const float *zr = Z + hq * (kTJ + 1);
-    int valid = min(kTJ, a.N - j0);
-    float m = -INFINITY;
-    for (int jj = 0; jj < valid; jj++) m = fmaxf(m, zr[jj]);
-    float s = 0.f;
-    if (m > -INFINITY)
-      for (int jj = 0; jj < valid; jj++) s += exp2f(zr[jj] - m);
-    a.part[(lrow + hq) * a.n_tiles + tile] = make_float2(m, s);
+  // per-tile (max, Σ 2^(z − max)) per query head, one warp per head
+  for (int hq = warp; hq < a.Hq; hq += n_warps) {
+    const float *zr = Z + hq * ZS;
+    float mx = -INFINITY;
+    for (int jj = lane; jj < valid; jj += 32) mx = fmaxf(mx, zr[jj]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    float sum = 0.f;
+    if (mx > -INFINITY)
+      for (int jj = lane; jj < valid; jj += 32) sum += exp2f(zr[jj] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    if (lane == 0) a.part[(lrow + hq) * a.n_tiles + tile] = make_float2(mx, sum);
   }
 }
 
@@ -173,9 +247,13 @@ k_qmem_lse(QArgs a) {
   a.lse[row] = m > -INFINITY ? m + log2f(s) : -INFINITY;
 }
 
+// rule_j = Σ_{l,hq} 2^(z − LSE): one thread per position, reading the
+// session's L·Hq logit rows (coalesced across the warp's positions) with
+// eight independent loads and partial sums in flight.
 __global__ void __launch_bounds__(256)
 k_qmem_rule(QArgs a) {
   extern __shared__ float lse_s[];  // [L·Hq] of this session
+  constexpr int U = 8;
   const int r = blockIdx.y;
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   const int LH = a.L * a.Hq;
@@ -187,9 +265,22 @@ k_qmem_rule(QArgs a) {
   float out = -1.f;
   if (live) {
     const float *z = a.logits + (int64_t)r * LH * a.N + j;
-    float acc = 0.f;
-    for (int i = 0; i < LH; i++) acc += exp2f(__ldcs(z + (int64_t)i * a.N) - lse_s[i]);
-    out = acc;
+    float acc[U];
+#pragma unroll
+    for (int k = 0; k < U; k++) acc[k] = 0.f;
+    int i = 0;
+    for (; i + U <= LH; i += U) {
+      float zz[U];
+#pragma unroll
+      for (int k = 0; k < U; k++) zz[k] = __ldcs(z + (int64_t)(i + k) * a.N);
+#pragma unroll
+      for (int k = 0; k < U; k++) acc[k] += exp2f(zz[k] - lse_s[i + k]);
+    }
+    for (; i < LH; i++) acc[0] += exp2f(__ldcs(z + (int64_t)i * a.N) - lse_s[i]);
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < U; k++) t += acc[k];
+    out = t;
   }
   a.rule[(int64_t)r * a.N + j] = out;
 }
@@ -245,25 +336,23 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
   a.sentinel = sentinel;
   a.n_slots = n_slots;
   a.zscale = kLog2e / sqrtf((float)D);
-  const int E = H * D / 32;
-  size_t smem = ((size_t)Hq * D + (size_t)Hq * (kTJ + 1)) * sizeof(float);
+  const int GP = a.G <= 4 ? 4 : 8;
+  const size_t smem = (size_t)Hq * (kTJ + 1) * sizeof(float);
   dim3 g1(n_sess, a.n_tiles, L);
   cudaError_t e;
-#define KVC_LOGITS_CASE(EV)                                                  \
-  case EV:                                                                   \
-    e = cudaFuncSetAttribute(k_qmem_logits<EV>,                              \
+#define KVC_LOGITS_CASE(DV, GV)                                              \
+  if (D == DV && GP == GV) {                                                 \
+    e = cudaFuncSetAttribute(k_qmem_logits<DV, GV>,                          \
                              cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                              (int)smem);                                     \
     if (e != cudaSuccess) return e;                                          \
-    k_qmem_logits<EV><<<g1, kLogitThreads, smem, s>>>(a);                    \
-    break;
-  switch (E) {
-    KVC_LOGITS_CASE(8)
-    KVC_LOGITS_CASE(16)
-    KVC_LOGITS_CASE(32)
-    KVC_LOGITS_CASE(64)
-    default: return cudaErrorInvalidValue;
-  }
+    k_qmem_logits<DV, GV><<<g1, kLogitThreads, smem, s>>>(a);                \
+  } else
+  KVC_LOGITS_CASE(128, 4)
+  KVC_LOGITS_CASE(128, 8)
+  KVC_LOGITS_CASE(64, 4)
+  KVC_LOGITS_CASE(64, 8)
+  return cudaErrorInvalidValue;
 #undef KVC_LOGITS_CASE
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

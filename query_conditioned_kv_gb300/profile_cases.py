@@ -9,6 +9,11 @@ event once to produce realistic inputs for the stage, then launches the stage
   python -m query_conditioned_kv_gb300.profile_cases pack  --layers 4  --iters 3
   python -m query_conditioned_kv_gb300.profile_cases select --layers 16 --iters 3
   python -m query_conditioned_kv_gb300.profile_cases meank  --layers 2  --iters 3
+  python -m query_conditioned_kv_gb300.profile_cases qmem   --layers 4  --sessions 8 --iters 2
+
+The qmem case is the QueryMemory rule score on the 64 x 32768 slot-map
+workload's shapes (shared 4096-position prefix, page 16), reduced to
+`--sessions` sessions and `--layers` layers.
 """
 from __future__ import annotations
 
@@ -19,9 +24,10 @@ import sys
 
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["score", "select", "pack", "event", "meank"])
+    ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--sessions", type=int, default=8)
     args = ap.parse_args(argv)
 
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -33,6 +39,9 @@ def main(argv=None) -> None:
     from query_conditioned_kv_gb300.event import MeanKEvent
 
     dev = torch.device("cuda", 0)
+    if args.case == "qmem":
+        _qmem_case(args, dev)
+        return
     cfg = W.scaled(W.config_8b(), L=args.layers)
     q = cfg.q(dev)
     meank = torch.empty(cfg.L, cfg.H, cfg.nb_total, cfg.D, dtype=torch.bfloat16, device=dev)
@@ -71,6 +80,37 @@ def main(argv=None) -> None:
     if st != 0:
         raise SystemExit(f"device status {st}: {kvc.kvc_status_string(st)}")
     print(f"profile case {args.case}: {args.iters} launches on {args.layers} layers ok")
+
+
+def _qmem_case(args, dev):
+    import dataclasses
+
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+
+    cfg = dataclasses.replace(W.config_slotmap(), n_sess=args.sessions, L=args.layers)
+    kp = torch.empty(cfg.L, cfg.n_slots, cfg.H, cfg.D, dtype=torch.bfloat16, device=dev)
+    for l in range(cfg.L):
+        kp[l] = cfg.kpool_layer(l, dev)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    sm = torch.from_numpy(cfg.slot_maps()).to(dev)
+    M = torch.zeros(cfg.n_sess, cfg.L, cfg.Hq, cfg.D, dtype=torch.float32, device=dev)
+    for t in range(cfg.turns):
+        kvc.kvc_qmem_update(M, cfg.q_turn(t, dev), cfg.n_sess, cfg.L, cfg.Hq, cfg.D, cfg.T,
+                            cfg.decay, cfg.gain, 1)
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots, cfg.budget,
+                      cfg.prefix, cfg.sentinel, device=dev)
+    for _ in range(args.iters):
+        ev.score(M, kp, sm)
+    torch.cuda.synchronize()
+    st = kvc.kvc_device_status(ev.dev_status)
+    if st != 0:
+        raise SystemExit(f"device status {st}: {kvc.kvc_status_string(st)}")
+    print(f"profile case qmem: {args.iters} launches, {cfg.n_sess} sessions x {cfg.N} "
+          f"positions, {cfg.L} layers ok")
 
 
 if __name__ == "__main__":

@@ -95,8 +95,10 @@ def test_validation_rejects_before_launch(kvc):
     assert _call(kvc, "kvc_rope_table", P, 16, 0, 128, 0.5, None) == 1
     # sentinel outside the pool
     assert _call(kvc, "kvc_init_sentinel", P, None, 1, 8, 128, 10, 10, None) == 1
-    # score_qmem: H·D not a multiple of 256
-    assert _call(kvc, "kvc_score_qmem", P, P, P, 0, P, 1, 1, 1, 2, 64, 16, 10, P, 1 << 30,
+    # score_qmem: a GQA group of more than 8 query heads; H not dividing 32
+    assert _call(kvc, "kvc_score_qmem", P, P, P, 0, P, 1, 1, 1, 16, 64, 16, 10, P, 1 << 30,
+                 None, None) == 2
+    assert _call(kvc, "kvc_score_qmem", P, P, P, 0, P, 1, 1, 3, 6, 64, 16, 10, P, 1 << 30,
                  None, None) == 2
     # redirect: workspace too small
     assert _call(kvc, "kvc_redirect_free", P, P, 1, 64, P, 100, 0, 0, P, 100, P, P, 16,

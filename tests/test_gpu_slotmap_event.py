@@ -23,9 +23,9 @@ def kvc():
     return k
 
 
-def small_cfg(H=8, D=128, **kw):
+def small_cfg(H=8, D=128, Hq=None, **kw):
     base = dict(name="sm", n_sess=3, N=1008, prefix=256, page=16, L=2, H=H,
-                Hq=4 * H, D=D, T=32, turns=4, budget=300, seed=31)
+                Hq=4 * H if Hq is None else Hq, D=D, T=32, turns=4, budget=300, seed=31)
     base.update(kw)
     return W.SlotMapConfig(**base)
 
@@ -74,10 +74,13 @@ def test_qmem_update_parity(kvc, orc):
     np.testing.assert_allclose(M2.cpu().numpy(), ref, rtol=2e-5, atol=1e-8)
 
 
-@pytest.mark.parametrize("H,D", [(8, 128), (2, 128), (4, 64)])
-def test_rule_score_parity(kvc, orc, H, D):
-    cfg = small_cfg(H=H, D=D)
-    rng = np.random.default_rng(H * 1000 + D)
+@pytest.mark.parametrize("H,Hq,D", [(8, 32, 128), (2, 8, 128), (4, 16, 64), (8, 48, 128),
+                                    (4, 4, 128), (2, 16, 64), (1, 3, 64)])
+def test_rule_score_parity(kvc, orc, H, Hq, D):
+    """GQA groups of 1..8 query heads, both head sizes; 1008 positions (a
+    ragged last tile) with 5% of the private positions already dead."""
+    cfg = small_cfg(H=H, D=D, Hq=Hq)
+    rng = np.random.default_rng(H * 1000 + D + Hq)
     sm = with_prior_redirects(cfg, cfg.slot_maps(), rng)
     kp = kpool_of(cfg, DEV)
     kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
