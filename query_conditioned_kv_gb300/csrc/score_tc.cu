@@ -769,9 +769,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 template <int RT>
 struct RingSmem {
   // Ring depth: the loaded latency of a 32 KB tile is ≈ 3 µs, so the ring
-  // holds as many tiles as shared memory allows (5 with one query buffer).
-  static constexpr int NS = RT == 1 ? 5 : 2;    // Mean-K ring stages
-  static constexpr int QB = RT == 1 ? 1 : 2;    // query-row buffers
+  // holds as many tiles as shared memory allows next to two query buffers.
+  // The second query buffer lets the producer move on to the next unit's
+  // rows and tiles while this unit's last MMAs and epilogues finish, so the
+  // ring does not drain at unit boundaries.
+  static constexpr int NS = RT == 1 ? 4 : 2;    // Mean-K ring stages
+  static constexpr int QB = 2;                  // query-row buffers
   static constexpr int ROWS = 128 * RT;         // query rows (padded)
   static constexpr int NBUF = RT == 1 ? 4 : 2;  // TMEM accumulators
   static constexpr int NEG = ring_groups<RT>();  // epilogue warpgroups
@@ -831,6 +834,16 @@ __device__ __forceinline__ UnitInfo unit_info(const TcArgs &a, int unit, int C, 
   u.mk_row0 = (int)(((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0);
   u.q_row0 = (int)((((int64_t)u.l * a.n_sess + u.r) * a.Hq + (int64_t)u.h * a.G) * a.W);
   return u;
+}
+
+// Pass-2 order of a CTA's tiles (local indices).  When the CTA has at least
+// NS tiles, the last NS tiles of pass 1 are still in the ring, in the slots
+// that pass 2's first NS steps map to (FIFO slot order, NS apart): pass 2
+// takes those first, without loading them again, then the rest in order.
+template <int NS>
+__device__ __forceinline__ int pass2_tile(int j, int my_tiles) {
+  if (my_tiles < NS) return j;
+  return j < NS ? my_tiles - NS + j : j - NS;
 }
 
 // Split TMEM load: issue now, wait later.  The wait names the destination
@@ -979,27 +992,42 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
         const UnitInfo u = unit_info(a, unit, C, rank);
         if (u.nb == 0 && rank == 0) record_error(a.status, KVC_ERR_BOUNDS);
         if (u.my_tiles == 0) continue;
+        // The unit's query rows.  With one buffer they wait for the previous
+        // unit's last MMA, so the unit's first tiles are issued before them
+        // (at most NS steps: every slot wait up to that point depends only
+        // on earlier units' MMAs, never on this unit's).
         const int qb = qi % SM::QB;
-        if (!wait_or_abort(smem_u32(sm.qempty + qb), ((qi / SM::QB) & 1) ^ 1, sm.failed)) break;
-        mbar_expect_tx(smem_u32(sm.qfull + qb), q_bytes);
-        for (int kb = 0; kb < KB; kb++)
-          tma_load_2d(smem_u32(sm.q + qb * q_bytes + kb * RT * 16384), &tm_q, kb * 64, u.q_row0,
-                      smem_u32(sm.qfull + qb));
-        qi++;
+        const int q_at = SM::QB == 1 ? min(NS, u.my_tiles) : 0;
+        auto load_q = [&]() -> bool {
+          if (!wait_or_abort(smem_u32(sm.qempty + qb), ((qi / SM::QB) & 1) ^ 1, sm.failed))
+            return false;
+          mbar_expect_tx(smem_u32(sm.qfull + qb), q_bytes);
+          for (int kb = 0; kb < KB; kb++)
+            tma_load_2d(smem_u32(sm.q + qb * q_bytes + kb * RT * 16384), &tm_q, kb * 64, u.q_row0,
+                        smem_u32(sm.qfull + qb));
+          return true;
+        };
         bool ok = true;
         for (int pass = 0; pass < 2 && ok; pass++)
           for (int j = 0; j < u.my_tiles; j++, s++) {
+            if (pass * u.my_tiles + j == q_at && !(ok = load_q())) break;
             const int slot = s % NS;
             if (!wait_or_abort(smem_u32(sm.empty + slot), ((s / NS) & 1) ^ 1, sm.failed)) {
               ok = false;
               break;
             }
-            const int tile = rank + j * C;
+            if (pass == 1 && u.my_tiles >= NS && j < NS) {
+              // the tile is still in this slot from pass 1: re-arm, no copy
+              mbar_arrive(smem_u32(sm.full + slot));
+              continue;
+            }
+            const int tile = rank + (pass == 0 ? j : pass2_tile<NS>(j, u.my_tiles)) * C;
             mbar_expect_tx(smem_u32(sm.full + slot), stage_bytes);
             for (int kb = 0; kb < KB; kb++)
               tma_load_2d(smem_u32(sm.ring + slot * stage_bytes + kb * 16384), &tm_mk, kb * 64,
                           u.mk_row0 + tile * 128, smem_u32(sm.full + slot));
           }
+        qi++;
         if (!ok) break;
       }
     }
@@ -1132,7 +1160,7 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
                         ok && wait_or_abort(smem_u32(sm.tfull + buf), (t / NBUF) & 1, sm.failed));
         if (ok) {
           tc_fence_after();
-          const int tile = rank + j * C;
+          const int tile = rank + pass2_tile<NS>(j, u.my_tiles) * C;
           const int valid = min(128, u.nb - tile * 128);
           float *out = a.scores + ((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0 + tile * 128;
           ring_pass2<W>(tmem + lane_base + (uint32_t)(buf * BUFCOLS), row, valid, a.n2c, a.R, zs,
