@@ -7,15 +7,20 @@
 // survivors are restored in chronological order; ActKV §3.3: the eviction
 // output is a Boolean keep mask.  Ties rank by index (lower first).
 //
-// Per segment of n items (n > budget):
+// Per segment of n items (n > budget), thread t owning the contiguous
+// items [t·ipt, (t+1)·ipt), ipt = ⌈n / threads⌉:
 //   1. the scores are mapped to order-preserving uint32 keys (−0.0 folded
 //      onto +0.0, NaN below −inf) and staged in shared memory;
-//   2. a 4-pass, 8-bit MSB radix select over the non-forced keys finds the
-//      k-th largest key T and how many items equal to T are still needed;
-//   3. one ordered sweep (tiles of blockDim items, two block-wide scans
-//      per tile) keeps forced ∪ {key > T} ∪ {the first `need`
-//      items with key == T}, writes their indices ascending and the mask
-//      words (one warp ballot per 32 items).
+//   2. the k-th largest non-forced key T is the largest T with
+//      #(key ≥ T) ≥ k: it is found bit by bit, from the highest bit where
+//      the candidates differ, two bits per step (counts against three
+//      thresholds, summed with warp reductions), then the number of items
+//      equal to T still needed is k − #(key > T);
+//   3. an ordered sweep in two block scans (equal-to-T counts, then keep
+//      counts, from per-thread bit masks) keeps forced ∪ {key > T} ∪ {the
+//      first `need` items with key == T} and writes their indices
+//      ascending; the keep mask is built in shared memory and written out
+//      word by word.
 // No global scratch; the output is exact and deterministic.
 #include "kvc_internal.cuh"
 
@@ -23,6 +28,13 @@ namespace kvc {
 namespace {
 
 constexpr int kSelThreads = 1024;
+// Items per thread the launch aims for (at most 64: the sweep's bit masks).
+// Fewer threads per segment mean cheaper barriers in the threshold search.
+constexpr int kSelIPT = 16;
+
+// Keys are stored with one pad word per 32: a thread's contiguous chunk and
+// the strided sweeps both read distinct banks.
+__device__ __forceinline__ int kp(int i) { return i + (i >> 5); }
 
 __device__ __forceinline__ uint32_t order_key(float s, bool &nan) {
   if (s != s) {
@@ -68,14 +80,16 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
          int max_seg_len, int budget, int n_sink, int n_recent,
          int32_t *__restrict__ kept, int32_t *__restrict__ kept_count,
          uint32_t *__restrict__ keepmask, int words, int32_t *status) {
-  extern __shared__ uint32_t keys[];
-  __shared__ uint32_t hist[256];
+  extern __shared__ uint32_t dyn[];
+  uint32_t *keys = dyn;                               // [kp(max_seg_len)]
+  uint32_t *mask_s = dyn + kp(max_seg_len) + 1;       // [words]
+  __shared__ uint32_t s_red[3][32];
   __shared__ uint32_t warp_tot[32];
-  __shared__ uint32_t s_digit, s_need;
+  __shared__ uint32_t s_kmax, s_kmin, s_prefix, s_need;
   __shared__ int s_nan;
 
   const int seg = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nt = blockDim.x;
   int32_t *kept_row = kept + (int64_t)seg * budget;
   uint32_t *mask_row = keepmask ? keepmask + (int64_t)seg * words : nullptr;
 
@@ -85,9 +99,9 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
   if (bad && tid == 0) record_error(status, KVC_ERR_BOUNDS);
 
   if (n <= budget) {  // keep everything (or nothing, on a bad segment)
-    for (int i = tid; i < budget; i += blockDim.x) kept_row[i] = i < n ? i : -1;
+    for (int i = tid; i < budget; i += nt) kept_row[i] = i < n ? i : -1;
     if (mask_row)
-      for (int w = tid; w < words; w += blockDim.x) {
+      for (int w = tid; w < words; w += nt) {
         int lo = w * 32;
         uint32_t m = lo >= n ? 0u : (n - lo >= 32 ? 0xFFFFFFFFu : ((1u << (n - lo)) - 1u));
         mask_row[w] = m;
@@ -102,98 +116,150 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
   if (tid == 0) s_nan = 0;
   __syncthreads();
   bool nan = false;
-  for (int i = tid; i < n; i += blockDim.x) keys[i] = order_key(scores[off + i], nan);
+  for (int i = tid; i < n; i += nt) keys[kp(i)] = order_key(scores[off + i], nan);
   if (nan) s_nan = 1;
+  for (int w = tid; w < words; w += nt) mask_s[w] = 0u;
 
-  // Radix select: the k-th largest non-forced key.
-  uint32_t prefix = 0, hi_mask = 0, need = (uint32_t)k;
+  // T = the k-th largest non-forced key: the largest T with #(key ≥ T) ≥ k,
+  // found bit by bit from the most significant bit where the candidates
+  // differ (the bits above it are common to all of them), two bits per
+  // step, counting the candidates against three thresholds at once.
+  uint32_t prefix = 0, need = (uint32_t)k;
+  const int lane = tid & 31, warp = tid >> 5, n_warps = nt >> 5;
   if (k > 0) {
-    for (int pass = 0; pass < 4; pass++) {
-      const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      // warp-aggregated: lanes with the same digit add once (scores of one
-      // segment share their leading bits, so plain atomics would serialise)
-      for (int base = 0; base < n; base += blockDim.x) {
-        const int i = base + tid;
-        bool cand = false;
-        uint32_t digit = 0;
-        if (i < n && i >= n_sink && i < rec0) {
-          uint32_t key = keys[i];
-          cand = (key & hi_mask) == prefix;
-          digit = (key >> shift) & 255u;
-        }
-        const uint32_t active = __ballot_sync(0xFFFFFFFFu, cand);
-        if (cand) {
-          const uint32_t peers = __match_any_sync(active, digit);
-          if ((int)(__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
-        }
-      }
-      __syncthreads();
-      if (tid < 32) {
-        // lane owns bins 255-8·lane … 248-8·lane (descending)
-        uint32_t loc = 0;
-#pragma unroll
-        for (int e = 0; e < 8; e++) loc += hist[255 - 8 * tid - e];
-        uint32_t inc = loc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-          if (tid >= o) inc += y;
-        }
-        uint32_t run = inc - loc;  // count of keys in higher bins
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-          int bin = 255 - 8 * tid - e;
-          uint32_t hcount = hist[bin];
-          if (run < need && run + hcount >= need) {
-            s_digit = (uint32_t)bin;
-            s_need = need - run;
-          }
-          run += hcount;
-        }
-      }
-      __syncthreads();
-      prefix |= s_digit << shift;
-      hi_mask |= 0xFFu << shift;
-      need = s_need;
-      __syncthreads();
+    uint32_t lmax = 0u, lmin = 0xFFFFFFFFu;
+    for (int i = n_sink + tid; i < rec0; i += nt) {
+      const uint32_t key = keys[kp(i)];
+      lmax = max(lmax, key);
+      lmin = min(lmin, key);
     }
+    lmax = __reduce_max_sync(0xFFFFFFFFu, lmax);
+    lmin = __reduce_min_sync(0xFFFFFFFFu, lmin);
+    if (lane == 0) {
+      s_red[0][warp] = lmax;
+      s_red[1][warp] = lmin;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, lane < n_warps ? s_red[0][lane] : 0u);
+      const uint32_t mn =
+          __reduce_min_sync(0xFFFFFFFFu, lane < n_warps ? s_red[1][lane] : 0xFFFFFFFFu);
+      if (lane == 0) {
+        s_kmax = mx;
+        s_kmin = mn;
+      }
+    }
+    __syncthreads();
+    const uint32_t kmax = s_kmax, kmin = s_kmin;
+    int bit = kmax == kmin ? -1 : 31 - __clz(kmax ^ kmin);
+    prefix = bit < 0 ? kmax : bit == 31 ? 0u : (kmax >> (bit + 1)) << (bit + 1);
+    while (bit >= 0) {
+      const int b0 = bit >= 1 ? bit - 1 : 0;  // lowest bit decided in this step
+      const bool two = bit >= 1;
+      uint32_t c1 = 0, c2 = 0, c3 = 0;
+      const uint32_t t1 = prefix | (1u << b0), t2 = prefix | (2u << b0), t3 = prefix | (3u << b0);
+      for (int i = n_sink + tid; i < rec0; i += nt) {
+        const uint32_t key = keys[kp(i)];
+        c1 += key >= t1 ? 1u : 0u;
+        c2 += key >= t2 ? 1u : 0u;
+        c3 += key >= t3 ? 1u : 0u;
+      }
+      c1 = __reduce_add_sync(0xFFFFFFFFu, c1);
+      c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
+      c3 = __reduce_add_sync(0xFFFFFFFFu, c3);
+      if (lane == 0) {
+        s_red[0][warp] = c1;
+        s_red[1][warp] = c2;
+        s_red[2][warp] = c3;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t C1 = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[0][lane] : 0u);
+        const uint32_t C2 = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[1][lane] : 0u);
+        const uint32_t C3 = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[2][lane] : 0u);
+        if (lane == 0) {
+          // #(key ≥ prefix) ≥ k holds; take the largest threshold that keeps it
+          uint32_t v = 0;
+          if (two && C3 >= need) v = 3;
+          else if (two && C2 >= need) v = 2;
+          else if (C1 >= need) v = 1;
+          s_prefix = prefix | (v << b0);
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      bit = b0 - 1;
+    }
+    // items equal to T still needed: k − #(key > T)
+    uint32_t gt = 0;
+    for (int i = n_sink + tid; i < rec0; i += nt) gt += keys[kp(i)] > prefix ? 1u : 0u;
+    gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+    if (lane == 0) s_red[0][warp] = gt;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t G = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[0][lane] : 0u);
+      if (lane == 0) s_need = (uint32_t)k - G;
+    }
+    __syncthreads();
+    need = s_need;
   }
   const uint32_t T = prefix;  // threshold key (valid when k > 0)
 
-  // Ordered sweep: forced ∪ {key > T} ∪ first `need` of {key == T}.
-  uint32_t eq_before = 0, out_pos = 0;
-  const int lane = tid & 31, warp = tid >> 5;
-  for (int base = 0; base < n; base += blockDim.x) {
-    int i = base + tid;
-    bool valid = i < n;
-    bool forced = valid && (i < n_sink || i >= rec0);
-    uint32_t key = valid ? keys[i] : 0u;
-    bool is_eq = valid && !forced && k > 0 && key == T;
-    bool above = valid && !forced && k > 0 && key > T;
-    uint32_t tot;
-    uint32_t rank_eq = eq_before + block_excl_scan(is_eq ? 1u : 0u, &tot, warp_tot);
-    bool keep = forced || above || (is_eq && rank_eq < need);
-    uint32_t tot2;
-    uint32_t pos = out_pos + block_excl_scan(keep ? 1u : 0u, &tot2, warp_tot);
-    if (keep && pos < (uint32_t)budget) kept_row[pos] = i;
-    uint32_t ballot = __ballot_sync(0xFFFFFFFFu, keep);
-    if (mask_row && lane == 0) {
-      int w = (base >> 5) + warp;
-      if (w < words) mask_row[w] = ballot;
+  // Ordered sweep over this thread's contiguous items (ipt ≤ 64, bit e of a
+  // mask = item i0 + e): forced ∪ {key > T} ∪ the first `need` of
+  // {key == T} in index order.  Ranks come from popcounts of the masks, so
+  // the items can be read in any order.
+  const int ipt = (n + nt - 1) / nt;
+  const int i0 = min(n, tid * ipt), cnt = min(n, i0 + ipt) - i0;
+  uint64_t eqm = 0, km = 0;
+  for (int e = 0; e < cnt; e++) {
+    const int i = i0 + e;
+    bool keep = i < n_sink || i >= rec0, eq = false;
+    if (!keep && k > 0) {
+      const uint32_t key = keys[kp(i)];
+      keep = key > T;
+      eq = key == T;
     }
-    eq_before += tot;
-    out_pos += tot2;
+    km |= (uint64_t)keep << e;
+    eqm |= (uint64_t)eq << e;
   }
-  // mask words past the last tile
-  if (mask_row) {
-    int first = (n + blockDim.x - 1) / blockDim.x * (blockDim.x / 32);
-    for (int w = first + tid; w < words; w += blockDim.x) mask_row[w] = 0u;
+  uint32_t tot_eq;
+  const uint32_t eq_before = block_excl_scan((uint32_t)__popcll(eqm), &tot_eq, warp_tot);
+  // equal items in rank order: keep while the running rank is below `need`
+  if (eq_before < need) {
+    const uint32_t take = min((uint32_t)__popcll(eqm), need - eq_before);
+    uint64_t m = eqm;
+    for (uint32_t t = 0; t < take; t++) {
+      km |= m & (~m + 1);  // lowest remaining equal item
+      m &= m - 1;
+    }
   }
-  for (int i = (int)out_pos + tid; i < budget; i += blockDim.x) kept_row[i] = -1;
+  uint32_t tot_keep;
+  const uint32_t pos0 = block_excl_scan((uint32_t)__popcll(km), &tot_keep, warp_tot);
+  {
+    uint64_t m = km;
+    uint32_t pos = pos0;
+    while (m) {
+      const int e = __ffsll((long long)m) - 1;
+      m &= m - 1;
+      if (pos < (uint32_t)budget) kept_row[pos] = i0 + e;
+      pos++;
+    }
+    // this chunk's keep bits into the mask words it overlaps
+    if (cnt > 0)
+      for (int w = i0 >> 5; w <= (i0 + cnt - 1) >> 5; w++) {
+        const int lo = w * 32 - i0;  // bit of item w·32 in km (may be < 0)
+        const uint64_t part = lo >= 0 ? (km >> lo) : (km << -lo);
+        const uint32_t bits = (uint32_t)part;
+        if (bits) atomicOr(&mask_s[w], bits);
+      }
+  }
+  __syncthreads();
+  if (mask_row)
+    for (int w = tid; w < words; w += nt) mask_row[w] = mask_s[w];
+  for (int i = (int)tot_keep + tid; i < budget; i += nt) kept_row[i] = -1;
   if (tid == 0) {
-    kept_count[seg] = (int32_t)out_pos;
+    kept_count[seg] = (int32_t)tot_keep;
     if (s_nan) record_error(status, KVC_ERR_NAN);
   }
 }
@@ -206,12 +272,17 @@ cudaError_t launch_select(const float *scores, const int64_t *seg_off,
                           uint32_t *keepmask, int32_t *status,
                           cudaStream_t s) {
   int words = (max_seg_len + 31) / 32;
-  size_t smem = (size_t)max_seg_len * sizeof(uint32_t);
-  int threads = max_seg_len >= 4 * kSelThreads ? kSelThreads
-                : max_seg_len >= 1024          ? 512
-                                               : 256;
+  size_t smem = ((size_t)max_seg_len + max_seg_len / 32 + 1 + words) * sizeof(uint32_t);
+  // Segments are independent and latency-bound: CTAs small enough that
+  // several fit on an SM (registers and shared memory) put a few hundred
+  // segments in one wave; long segments get more threads per CTA.
+  int threads = 128;
+  while (threads < kSelThreads && (max_seg_len + threads - 1) / threads > kSelIPT) threads *= 2;
   cudaError_t e = cudaFuncSetAttribute(
       k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_select, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   k_select<<<n_seg, threads, smem, s>>>(scores, seg_off, max_seg_len, budget,
                                         n_sink, n_recent, kept, kept_count,

@@ -149,12 +149,14 @@ class MeanKEvent:
     def run(self, q, meank, kraw, vraw, timers=None):
         """The event, layer groups pipelined over two streams (asynchronous
         with respect to the host; ordered after prior work on the current
-        stream, and the current stream waits for all of it).  `timers`, if
+        stream, and the current stream waits for all of it).  With one layer
+        group every launch stays on the current stream.  `timers`, if
         given, is a list that receives (stage, start, end) CUDA events around
         every launch, recorded on the launching stream."""
         main = torch.cuda.current_stream(self.device)
-        side = self.side
-        side.wait_stream(main)
+        side = self.side if len(self.groups) > 1 else main
+        if side is not main:
+            side.wait_stream(main)
 
         def timed(stage, stream, fn):
             if timers is None:
@@ -169,14 +171,16 @@ class MeanKEvent:
 
         for (l0, l1) in self.groups:
             timed("score", main, lambda: self.score(q, meank, main, l0, l1))
-            done = torch.cuda.Event()
-            done.record(main)
-            side.wait_event(done)
+            if side is not main:
+                done = torch.cuda.Event()
+                done.record(main)
+                side.wait_event(done)
             with torch.cuda.stream(side):
                 timed("select", side, lambda: self.select(None, side, l0, l1))
                 if l0 < self.L_pack:
                     timed("pack", side, lambda: self.pack(kraw, vraw, stream=side, l0=l0, l1=l1))
-        main.wait_stream(side)
+        if side is not main:
+            main.wait_stream(side)
 
     # -- CUDA graph ----------------------------------------------------
     def capture(self, q, meank, kraw, vraw):

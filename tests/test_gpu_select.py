@@ -1,0 +1,77 @@
+"""GPU select against the oracle on segments built to stress the selection
+rule: many equal scores (ties broken by index), signed zeros, forced sink
+and recent items, ragged lengths from below the budget up to the longest
+segment the call accepts, and the keep mask.  Indices, counts and masks are
+compared bit for bit."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import query_conditioned_kv_gb300 as k
+    return k
+
+
+def _run(kvc, scores, lens, budget, n_sink, n_recent):
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    n_seg, max_len = len(lens), int(max(lens))
+    words = (max_len + 31) // 32
+    kept = torch.empty(n_seg, budget, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(n_seg, dtype=torch.int32, device=DEV)
+    mask = torch.empty(n_seg, words, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvc.kvc_select(torch.from_numpy(scores).to(DEV), torch.from_numpy(off).to(DEV), n_seg,
+                   max_len, budget, n_sink, n_recent, kept, cnt, mask, st)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(st) == 0
+    return off, kept.cpu().numpy(), cnt.cpu().numpy(), mask.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("budget,n_sink,n_recent", [(256, 1, 4), (64, 0, 0), (512, 3, 9),
+                                                     (8192, 0, 0), (20, 10, 10)])
+def test_select_ties_ragged_bit_exact(kvc, orc, budget, n_sink, n_recent):
+    rng = np.random.default_rng(budget + 7 * n_sink + n_recent)
+    lens = [1, budget, budget + 1, 300, 4096, 4097, 9000, 33, 32768, 49152]
+    lens = [n for n in lens if n >= 1]
+    parts = []
+    for j, n in enumerate(lens):
+        if j % 3 == 0:   # few distinct values: ties everywhere
+            s = rng.integers(0, 6, n).astype(np.float32)
+        elif j % 3 == 1:  # signed zeros among a few values
+            s = rng.choice(np.array([0.0, -0.0, 1.0, 0.5], np.float32), n)
+        else:             # continuous scores with a block of equal ones
+            s = rng.random(n).astype(np.float32)
+            s[n // 3: n // 3 + min(n, 50)] = s[n // 2]
+        parts.append(s)
+    scores = np.concatenate(parts)
+    off, kept, cnt, mask = _run(kvc, scores, lens, budget, n_sink, n_recent)
+    kref, cref, mref = orc.select_segments(scores, off, budget, n_sink, n_recent,
+                                           mask_words=mask.shape[1])
+    assert np.array_equal(cnt, cref)
+    assert np.array_equal(kept, kref)
+    assert np.array_equal(mask, mref)
+
+
+def test_select_all_equal_and_monotone(kvc, orc):
+    """All scores equal (the lowest indices win) and strictly increasing
+    scores (the latest items win), on 4096-item segments."""
+    n, budget = 4096, 256
+    scores = np.concatenate([np.full(n, 0.25, np.float32),
+                             np.arange(n, dtype=np.float32),
+                             -np.arange(n, dtype=np.float32)])
+    lens = [n, n, n]
+    off, kept, cnt, mask = _run(kvc, scores, lens, budget, 1, 4)
+    kref, cref, mref = orc.select_segments(scores, off, budget, 1, 4, mask_words=mask.shape[1])
+    assert np.array_equal(kept, kref) and np.array_equal(cnt, cref)
+    assert np.array_equal(mask, mref)
+    assert kept[0, :5].tolist() == [0, 1, 2, 3, 4]
