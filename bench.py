@@ -46,14 +46,9 @@ L2_NOTE = "L2 flushed between steps (256 MiB write outside the event's timed spa
 
 def algorithmic_bytes(cfg):
     """Bytes the method must move per event (HBM), by stage."""
-    D = cfg.D
-    meank = cfg.L * cfg.H * cfg.nb_total * D * 2
-    q = cfg.n_sess * cfg.L * cfg.Hq * cfg.W * D * 2
-    view_elems = cfg.lp * cfg.H * cfg.n_sess * cfg.view_tokens * D
-    pack_rw = 2 * 2 * view_elems * 2          # K and V, read and write
-    kept = cfg.L * cfg.H * cfg.n_sess * cfg.budget * 4
-    return {"score": meank + q, "select": 0, "pack": pack_rw + kept,
-            "event": meank + q + pack_rw + kept}
+    from query_conditioned_kv_gb300.event import event_bytes
+    return event_bytes(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.nb_total, cfg.n_sess, cfg.lp,
+                       cfg.view_tokens, cfg.budget)
 
 
 def peaks():

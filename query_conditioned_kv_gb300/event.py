@@ -200,6 +200,19 @@ class MeanKEvent:
         self.graph.replay()
 
 
+def event_bytes(L: int, H: int, Hq: int, D: int, W: int, nb_total: int, n_sess: int,
+                L_pack: int, view_tokens: int, budget: int) -> dict:
+    """Bytes a Mean-K event must move through HBM, by stage: the Mean-K index
+    and the query windows read once (score); the kept K and V rows read once
+    and the execution views written once, plus the kept indices (pack).
+    Select reads only the scores, which the score stage has just written."""
+    meank = L * H * nb_total * D * 2
+    q = n_sess * L * Hq * W * D * 2
+    view = L_pack * H * n_sess * view_tokens * D
+    pack = 2 * 2 * view * 2 + L * H * n_sess * budget * 4
+    return {"score": meank + q, "select": 0, "pack": pack, "event": meank + q + pack}
+
+
 class SlotMapEvent:
     """Buffers and calls of a QueryMemory-mode event: rule score over the
     paged K pool, token-level select (no forced set), redirect + free."""

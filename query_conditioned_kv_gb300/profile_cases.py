@@ -10,8 +10,12 @@ event once to produce realistic inputs for the stage, then launches the stage
   python -m query_conditioned_kv_gb300.profile_cases select --layers 16 --iters 3
   python -m query_conditioned_kv_gb300.profile_cases meank  --layers 2  --iters 3
   python -m query_conditioned_kv_gb300.profile_cases qmem   --layers 4  --sessions 8 --iters 2
+  python -m query_conditioned_kv_gb300.profile_cases event_timing --config 27b --iters 10
 
-The qmem case is the QueryMemory rule score on the 64 x 32768 slot-map
+event_timing times a whole Mean-K event (score → select → pack, one CUDA
+graph) on a full workload — tiny, 8b, 27b or ragged — with L2 flushed
+between replays, and prints one JSON line: time, tokens/s and the fraction
+of the measured HBM peak.  The qmem case is the QueryMemory rule score on the 64 x 32768 slot-map
 workload's shapes (shared 4096-position prefix, page 16), reduced to
 `--sessions` sessions and `--layers` layers.
 """
@@ -24,10 +28,12 @@ import sys
 
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem"])
+    ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem",
+                                     "event_timing"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sessions", type=int, default=8)
+    ap.add_argument("--config", choices=["tiny", "8b", "27b", "ragged"], default="8b")
     args = ap.parse_args(argv)
 
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -41,6 +47,9 @@ def main(argv=None) -> None:
     dev = torch.device("cuda", 0)
     if args.case == "qmem":
         _qmem_case(args, dev)
+        return
+    if args.case == "event_timing":
+        _event_timing(args, dev, root)
         return
     cfg = W.scaled(W.config_8b(), L=args.layers)
     q = cfg.q(dev)
@@ -80,6 +89,70 @@ def main(argv=None) -> None:
     if st != 0:
         raise SystemExit(f"device status {st}: {kvc.kvc_status_string(st)}")
     print(f"profile case {args.case}: {args.iters} launches on {args.layers} layers ok")
+
+
+def _event_timing(args, dev, root):
+    import json
+    import statistics
+
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import MeanKEvent, event_bytes
+
+    cfg = {"tiny": W.config_tiny, "8b": W.config_8b, "27b": W.config_27b,
+           "ragged": W.config_ragged}[args.config]()
+    q = cfg.q(dev)
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = cfg.meank_direct(dev)  # layers without raw K keep the drawn index
+    kvc.kvc_build_meank(kraw, meank[:cfg.lp], cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                    cfg.n_recent, cfg.lp, cfg.theta, cfg.pos0, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        ev.run(q, meank, kraw, vraw)
+    ev.capture(q, meank, kraw, vraw)
+    ev.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ms = []
+    for k in range(args.iters):
+        flush.fill_(k & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ev.replay()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    # per-stage kernel time from an eager pass with an event pair per launch
+    stages = {}
+    for k in range(3):
+        flush.fill_(k & 0xFF)
+        timers = []
+        ev.run(q, meank, kraw, vraw, timers=timers)
+        torch.cuda.synchronize()
+        for stage, a, b in timers:
+            stages.setdefault(stage, []).append(a.elapsed_time(b))
+    st = kvc.kvc_device_status(ev.dev_status)
+    if st != 0:
+        raise SystemExit(f"device status {st}: {kvc.kvc_status_string(st)}")
+    peak = 6800.0
+    peaks = os.path.join(root, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks):
+        with open(peaks) as f:
+            peak = float(json.load(f)["hbm_gbs"])
+    nbytes = event_bytes(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.nb_total, cfg.n_sess, cfg.lp,
+                         cfg.view_tokens, cfg.budget)["event"]
+    med = statistics.median(ms)
+    print(json.dumps({"config": cfg.name, "sessions": cfg.n_sess, "history_tokens": cfg.n_tok,
+                      "layers_scored": cfg.L, "layers_packed": cfg.lp,
+                      "ms_median": med, "ms_min": min(ms), "ms_max": max(ms),
+                      "tokens_per_s": cfg.n_tok / (med * 1e-3),
+                      "stages_ms": {k: round(statistics.median(v), 4) for k, v in stages.items()},
+                      "algorithmic_bytes": nbytes,
+                      "achieved_gbs": nbytes / (med * 1e-3) / 1e9,
+                      "frac_of_measured_hbm": nbytes / (med * 1e-3) / 1e9 / peak}))
 
 
 def _qmem_case(args, dev):
