@@ -63,9 +63,18 @@ def lib():
         L.orc_redirect_free.argtypes = [_i32p, _u32p, c.c_int, c.c_int, _i32p,
                                         c.c_int64, c.c_int, c.c_int32, _i32p,
                                         c.c_int, _i32p]
+        L.orc_attention_lse.argtypes = [_u16p, _u16p, c.c_int64, _i32p, c.c_int, c.c_int,
+                                        c.c_int, c.c_int, c.c_int, c.c_int, _f64p]
+        L.orc_recover_step.argtypes = [_u16p, _f64p, _u16p, c.c_int64, _i32p, c.c_int,
+                                       c.c_int, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                                       c.c_int, _f64p]
+        L.orc_tail_plan.argtypes = [_u32p, c.c_int, _i32p, c.c_int, _i32p, _i32p,
+                                    c.POINTER(c.c_int), c.POINTER(c.c_int), _i32p,
+                                    c.POINTER(c.c_int), _i32p, _u32p]
         for name in ("orc_meank", "orc_score_unit", "orc_qmem_update",
                      "orc_rule_session", "orc_select", "orc_rope_f64",
-                     "orc_pack_unit", "orc_slot_map", "orc_redirect_free"):
+                     "orc_pack_unit", "orc_slot_map", "orc_redirect_free",
+                     "orc_attention_lse", "orc_recover_step", "orc_tail_plan"):
             getattr(L, name).restype = c.c_int
         _lib = L
     return _lib
@@ -261,3 +270,53 @@ def redirect_free(slot_map_all, keepmask, refcnt, prefix_len: int,
     if rc not in (0, 4, 6):
         raise OracleError(f"orc_redirect_free returned {rc}")
     return sm, rc_arr, freed[:min(int(nf[0]), cap)].copy(), int(rc), int(nf[0])
+
+
+# ----------------------------------------------- LSE recovery, compaction
+
+def attention_lse(q, kpool, block_table, BS: int, seq_len: int, H: int) -> np.ndarray:
+    """The attention backend's LSE of one request's step: q [L][Hq][D] and
+    kpool [L][n_slots][H][D] bf16 bits → lse [L][Hq] (natural log)."""
+    q = _c(q, np.uint16)
+    kpool = _c(kpool, np.uint16)
+    bt = _c(block_table, np.int32)
+    L, Hq, D = q.shape
+    out = np.empty((L, Hq), dtype=np.float64)
+    _check(lib().orc_attention_lse(q, kpool, kpool.shape[1], bt, BS, seq_len, L, H, Hq, D,
+                                   out), "orc_attention_lse")
+    return out
+
+
+def recover_step(q, lse, kpool, block_table, BS: int, seq_len: int, count: int, H: int,
+                 state) -> np.ndarray:
+    """One decode step of one request's action score (state [n_blocks·BS]
+    float64, updated copy returned)."""
+    q = _c(q, np.uint16)
+    kpool = _c(kpool, np.uint16)
+    bt = _c(block_table, np.int32)
+    L, Hq, D = q.shape
+    st = np.array(state, dtype=np.float64, copy=True)
+    _check(lib().orc_recover_step(q, _c(lse, np.float64), kpool, kpool.shape[1], bt,
+                                  bt.shape[0], BS, seq_len, count, L, H, Hq, D, st),
+           "orc_recover_step")
+    return st
+
+
+def tail_plan(keepmask, n: int, block_table, BS: int) -> dict:
+    """Compaction plan of one request (see orc_tail_plan)."""
+    import ctypes as c
+    km = _c(keepmask, np.uint32)
+    bt = _c(block_table, np.int32)
+    Y = (n + BS - 1) // BS
+    src = np.zeros(max(n, 1), np.int32)
+    dst = np.zeros(max(n, 1), np.int32)
+    freed = np.zeros(max(Y, 1), np.int32)
+    new_table = np.zeros(max(Y, 1), np.int32)
+    tail = np.zeros(max((Y * BS + 31) // 32, 1), np.uint32)
+    npairs, X, nfreed = c.c_int(0), c.c_int(0), c.c_int(0)
+    _check(lib().orc_tail_plan(km, n, bt, BS, src, dst, c.byref(npairs), c.byref(X), freed,
+                               c.byref(nfreed), new_table, tail), "orc_tail_plan")
+    x = X.value
+    return {"src": src[:npairs.value], "dst": dst[:npairs.value], "X": x,
+            "freed": freed[:nfreed.value], "new_table": new_table[:x],
+            "tail_mask": tail[:(x * BS + 31) // 32]}

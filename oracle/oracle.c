@@ -449,3 +449,155 @@ int orc_redirect_free(int32_t *slot_map, const uint32_t *keepmask, int n_sess,
   *n_freed = nf;
   return rc;
 }
+
+/* ------------------------------------------------ LSE-recovery scoring */
+
+/* The attention backend's by-product: for one request's query rows q
+ * [L][Hq][D] (bf16, the current decode step) against its first seq_len
+ * cached keys (paged: position p in slot block_table[p / BS]·BS + p % BS of
+ * kpool [L][n_slots][H][D]), lse[l][hq] = ln Σ_p exp(q·k/√D), query head hq
+ * reading KV head hq / G.  [ActKV] §7.1: the LSE of the softmax
+ * normalisation over the keys the query attends to. */
+int orc_attention_lse(const uint16_t *q, const uint16_t *kpool, int64_t n_slots,
+                      const int32_t *block_table, int BS, int seq_len, int L, int H,
+                      int Hq, int D, double *lse) {
+  if (!q || !kpool || !block_table || !lse || BS < 1 || seq_len < 1 || L < 1 ||
+      H < 1 || Hq < H || Hq % H || D < 1)
+    return 1;
+  const int G = Hq / H;
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  double *s = (double *)malloc(sizeof(double) * (size_t)seq_len);
+  if (!s) return 3;
+  for (int l = 0; l < L; l++)
+    for (int hq = 0; hq < Hq; hq++) {
+      const int h = hq / G;
+      double mx = -INFINITY;
+      for (int p = 0; p < seq_len; p++) {
+        const int64_t slot = (int64_t)block_table[p / BS] * BS + p % BS;
+        if (slot < 0 || slot >= n_slots) {
+          free(s);
+          return 4;
+        }
+        const uint16_t *k = kpool + (((int64_t)l * n_slots + slot) * H + h) * D;
+        const uint16_t *qq = q + ((int64_t)l * Hq + hq) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; d++) dot += orc_bf16_to_f64(qq[d]) * orc_bf16_to_f64(k[d]);
+        s[p] = dot * inv_sqrt_d;
+        if (s[p] > mx) mx = s[p];
+      }
+      double sum = 0.0;
+      for (int p = 0; p < seq_len; p++) sum += exp(s[p] - mx);
+      lse[l * Hq + hq] = mx + log(sum);
+    }
+  free(s);
+  return 0;
+}
+
+/* One decode step of the action score of one request.
+ * [ActKV] §7.1 (Algorithm 3): for each cached key, the attention
+ * probability of the current query token is recovered from the backend's
+ * LSE as exp(q·k/√D − LSE); the maximum is taken over the query heads of
+ * the key's GQA group, and a running mean over the action tokens is
+ * updated in place (no past queries are kept); the state restarts at the
+ * first token of an action region.
+ * Readings: a token's score sums that group maximum over the layers and KV
+ * heads (a slot holds every layer's KV of one token, so eviction on paged
+ * memory is per token); keys at positions ≥ seq_len are not visible to the
+ * query and contribute 0; the mean is state ← state + (x − state)/count,
+ * with count the number of action tokens so far, this one included
+ * (count = 1 restarts it: state ← x).
+ *   q [L][Hq][D] bf16;  lse [L][Hq] (natural log);  kpool [L][n_slots][H][D]
+ *   block_table [n_blocks];  state [n_blocks·BS] in/out */
+int orc_recover_step(const uint16_t *q, const double *lse, const uint16_t *kpool,
+                     int64_t n_slots, const int32_t *block_table, int n_blocks, int BS,
+                     int seq_len, int count, int L, int H, int Hq, int D, double *state) {
+  if (!q || !lse || !kpool || !block_table || !state || BS < 1 || n_blocks < 1 ||
+      seq_len < 0 || seq_len > n_blocks * BS || count < 1 || L < 1 || H < 1 || Hq < H ||
+      Hq % H || D < 1)
+    return 1;
+  const int G = Hq / H;
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  for (int p = 0; p < n_blocks * BS; p++) {
+    double x = 0.0;
+    if (p < seq_len) {
+      const int64_t slot = (int64_t)block_table[p / BS] * BS + p % BS;
+      if (slot < 0 || slot >= n_slots) return 4;
+      for (int l = 0; l < L; l++)
+        for (int h = 0; h < H; h++) {
+          const uint16_t *k = kpool + (((int64_t)l * n_slots + slot) * H + h) * D;
+          double best = 0.0;
+          for (int g = 0; g < G; g++) {
+            const int hq = h * G + g;
+            const uint16_t *qq = q + ((int64_t)l * Hq + hq) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; d++) dot += orc_bf16_to_f64(qq[d]) * orc_bf16_to_f64(k[d]);
+            const double prob = exp(dot * inv_sqrt_d - lse[l * Hq + hq]);
+            if (prob > best) best = prob;
+          }
+          x += best;
+        }
+    }
+    state[p] = count == 1 ? x : state[p] + (x - state[p]) / count;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------- tail compaction plan */
+
+/* Conflict-free slot plan of one request.  [ActKV] §7.2 (Algorithm 4):
+ * after eviction, every retained entry is compacted into the last X logical
+ * blocks of the request; destinations are the evicted slots inside that
+ * tail region, sources the retained entries outside it, and the two sets
+ * are disjoint, so one pass of copies needs no buffer; the blocks before
+ * the region are returned.
+ * Readings (the region's formula is lost on the page): with Y = ⌈n/BS⌉
+ * blocks holding the request's n tokens and m retained tokens, X = ⌈m/BS⌉
+ * and the region is logical blocks [Y−X, Y); a destination is any slot of
+ * the region not holding a retained token (slots past n in the last block
+ * included); the k-th source in position order goes to the k-th
+ * destination in position order; logical slots are translated to physical
+ * ones through the block table.
+ *   keepmask [⌈n/32⌉] (bit p%32 of word p/32: token p retained)
+ *   src, dst [≤ m] physical slots;  *n_pairs
+ *   *X;  freed [Y] the physical blocks given back, in logical order; *n_freed
+ *   new_table [X] the region's physical blocks;  tail_mask [⌈X·BS/32⌉]
+ *   (bit i: slot i of the region holds a retained token afterwards) */
+int orc_tail_plan(const uint32_t *keepmask, int n, const int32_t *block_table, int BS,
+                  int32_t *src, int32_t *dst, int *n_pairs, int *X, int32_t *freed,
+                  int *n_freed, int32_t *new_table, uint32_t *tail_mask) {
+  if (!keepmask || !block_table || !src || !dst || !n_pairs || !X || !freed || !n_freed ||
+      !new_table || !tail_mask || BS < 1 || n < 0)
+    return 1;
+  const int Y = (n + BS - 1) / BS;
+  int m = 0;
+  for (int p = 0; p < n; p++) m += (keepmask[p / 32] >> (p % 32)) & 1u;
+  const int x = (m + BS - 1) / BS;
+  const int start = (Y - x) * BS;
+  *X = x;
+  /* sources: retained tokens before the region, in position order */
+  int ns = 0;
+  for (int p = 0; p < start; p++)
+    if ((keepmask[p / 32] >> (p % 32)) & 1u) src[ns++] = p;
+  /* destinations: region slots not holding a retained token, in order */
+  int nd = 0;
+  for (int p = start; p < Y * BS && nd < ns; p++) {
+    const int kept = p < n && ((keepmask[p / 32] >> (p % 32)) & 1u);
+    if (!kept) dst[nd++] = p;
+  }
+  if (nd != ns) return 5; /* cannot happen: the region has ≥ m − (kept inside) holes */
+  for (int i = 0; i < (x * BS + 31) / 32; i++) tail_mask[i] = 0u;
+  for (int p = start; p < Y * BS; p++)
+    if (p < n && ((keepmask[p / 32] >> (p % 32)) & 1u))
+      tail_mask[(p - start) / 32] |= 1u << ((p - start) % 32);
+  for (int k = 0; k < ns; k++) {
+    const int t = dst[k] - start;
+    tail_mask[t / 32] |= 1u << (t % 32);
+    src[k] = block_table[src[k] / BS] * BS + src[k] % BS;
+    dst[k] = block_table[dst[k] / BS] * BS + dst[k] % BS;
+  }
+  *n_pairs = ns;
+  for (int b = 0; b < Y - x; b++) freed[b] = block_table[b];
+  *n_freed = Y - x;
+  for (int b = 0; b < x; b++) new_table[b] = block_table[Y - x + b];
+  return 0;
+}
