@@ -13,7 +13,10 @@ measured kernel time against the measured HBM copy bandwidth.  The Mean-K
 index build and, on its own workload (64 sessions × 32768 positions over a
 paged, refcounted K pool), the QueryMemory event (memory update; rule score
 → select → redirect + free) are measured after the timed steps and reported
-beside them (`meank_build`, `slotmap_event`; `--no-slotmap` skips the latter).
+beside them (`meank_build`, `slotmap_event`; `--no-slotmap` skips the latter),
+and so is ActKV's paged compression operation (LSE-recovery score → select →
+tail plan → in-place compaction) at 1, 4, 16 and 64 requests of 6K → 4K
+tokens (`actkv_event`; `--no-paged` skips it).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -441,6 +444,94 @@ def slot_map_event(args, dev, peak, reps: int = 3):
     return out
 
 
+# ------------------------------------------------- ActKV paged operation
+
+PAGED_WORKLOAD = ("paged_6k_to_4k: ActKV Table 1 shapes (block size 16, 8 KV heads, d 128), "
+                  "36 layers, 32 query heads; r requests of 6144 tokens each compressed to "
+                  "4096; LSE-recovery score of one action token (restart), top-4096 select, "
+                  "tail plan, in-place compaction of K and V")
+
+
+def paged_event(args, dev, peak, reqs=(1, 4, 16, 64), reps: int = 5):
+    """ActKV's compression operation on a paged KV cache, at the request
+    counts of ActKV Table 1: each stage timed with CUDA events on the
+    launching stream, the operation as their sum.  Every rep restarts the
+    score (count 1); the compaction of a rep moves rows inside the pool, so
+    the next rep's plan can differ slightly: each rep's compaction bytes use
+    its own pair count (read after the rep).  The K and V pools (0.9–58 GB)
+    exceed the 129 MB L2."""
+    import torch
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import PagedEvent, paged_bytes
+
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        return a, b
+
+    rows = []
+    for n_req in reqs:
+        cfg = W.config_paged(n_req)
+        kp, vp = cfg.pools(dev)
+        q = cfg.q(dev)
+        lse = cfg.lse(q)
+        bt = torch.from_numpy(cfg.block_tables()).to(dev)
+        seq = torch.from_numpy(cfg.seqused()).to(dev)
+        cnt = torch.ones(n_req, dtype=torch.int32, device=dev)
+        ev = PagedEvent(n_req, cfg.max_blocks, cfg.BS, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                        cfg.keep, device=dev)
+        stages = {"score": [], "select": [], "plan": [], "compact": []}
+        events, fracs, pairs = [], [], []
+        for r in range(args.warmup + reps):
+            torch.cuda.synchronize(dev)
+            st = {"score": timed(lambda: ev.score(q, lse, kp, bt, seq, cnt)),
+                  "select": timed(lambda: ev.select()),
+                  "plan": timed(lambda: ev.plan(seq, bt)),
+                  "compact": timed(lambda: ev.compact(kp, vp))}
+            torch.cuda.synchronize(dev)
+            if r < args.warmup:
+                continue
+            ms = {k: a.elapsed_time(b) for k, (a, b) in st.items()}
+            for k, v in ms.items():
+                stages[k].append(v)
+            total = st["score"][0].elapsed_time(st["compact"][1])
+            np_ = int(ev.n_pairs.sum().item())
+            pairs.append(np_)
+            events.append(total)
+            b = paged_bytes(n_req, cfg.seq, cfg.L, cfg.H, cfg.Hq, cfg.D, np_)
+            fracs.append(b["event"] / (total * 1e-3) / 1e9 / peak)
+        if kvc.kvc_device_status(ev.dev_status) != 0:
+            raise RuntimeError("device status error in the paged operation")
+        ms = statistics.median(events)
+        np_med = int(statistics.median(pairs))
+        b = paged_bytes(n_req, cfg.seq, cfg.L, cfg.H, cfg.Hq, cfg.D, np_med)
+        sc = statistics.median(stages["score"])
+        cp = statistics.median(stages["compact"])
+        tokens = n_req * cfg.seq
+        rows.append({
+            "n_req": n_req, "tokens_per_op": tokens, "ms_per_op": round(ms, 4),
+            "value": tokens / (ms * 1e-3), "unit": UNIT,
+            "pairs_moved": np_med, "algorithmic_bytes": b["event"],
+            "hbm_frac_op": round(statistics.median(fracs), 4),
+            "stages_ms": {k: round(statistics.median(v), 4) for k, v in stages.items()},
+            "score_roofline": {"kernel": "k_recover_tc", "algorithmic_bytes": b["score"],
+                               "achieved": b["score"] / (sc * 1e-3) / 1e9,
+                               "frac": b["score"] / (sc * 1e-3) / 1e9 / peak},
+            "compact_roofline": {"kernel": "k_tail_compact", "algorithmic_bytes": b["compact"],
+                                 "achieved": b["compact"] / (cp * 1e-3) / 1e9,
+                                 "frac": b["compact"] / (cp * 1e-3) / 1e9 / peak},
+        })
+        del kp, vp, q, ev
+        torch.cuda.empty_cache()
+    return {"workload": PAGED_WORKLOAD, "reps": reps, "rows": rows,
+            "l2": "pools (0.9-58 GB) exceed the 129 MB L2; no flush"}
+
+
 # ------------------------------------------------------------ oracle arm
 
 def _oracle_sample(n_units, dev):
@@ -534,6 +625,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-slotmap", action="store_true",
                     help="skip the QueryMemory (slot-map) event measurement")
+    ap.add_argument("--no-paged", action="store_true",
+                    help="skip the ActKV paged-operation measurement")
     ap.add_argument("--groups", type=int, default=None,
                     help="layer groups of the pipelined event (default: the library's choice)")
     args = ap.parse_args()
@@ -561,6 +654,10 @@ def main():
         torch.cuda.empty_cache()
         line["slotmap_event"] = slot_map_event(args, torch.device("cuda", local_rank),
                                                peaks()[0])
+    if not args.no_paged:
+        import torch
+        torch.cuda.empty_cache()
+        line["actkv_event"] = paged_event(args, torch.device("cuda", local_rank), peaks()[0])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

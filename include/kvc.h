@@ -323,6 +323,124 @@ kvc_status kvc_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
                              size_t ws_bytes, int32_t *dev_status,
                              cudaStream_t stream);
 
+/* ========================================================================
+ * ActKV paged primitives (ActKV: Efficient LLM Agents through Action-Guided
+ * KV Cache Management, §3.3 workflow on the paged layout of §2): the same
+ * score → keep mask → compaction sequence, for a serving engine whose KV
+ * cache lives in pages.  Layout (§2 "Background"): a K pool and a V pool of
+ * [L][n_slots][H][D] bf16, one H·D row per (layer, physical slot); request
+ * r's logical position p lives in slot block_table[r][p / block_size] ·
+ * block_size + p % block_size (the page's worked example: block_size 2,
+ * block_table [17, 9], 3 tokens → slots 34, 35, 18).
+ * ====================================================================== */
+
+/* Longest request (max_blocks · block_size) kvc_tail_plan accepts. */
+#define KVC_TAIL_MAX_TOKENS (1 << 20)
+
+/* ------------------------------------------------------------------------
+ * LSE-recovery action score, one decode step (ActKV §7.1, Algorithm 3).
+ * The attention backend has already produced, for the current query token
+ * of each request, lse[r][l][hq] = ln Σ_p exp(q·k_p/√D) over the keys it
+ * attended to; each probability is recovered as exp(q·k/√D − LSE) without
+ * materialising the attention matrix.  For request r with count[r] ≥ 1 and
+ * every position p < max_blocks·block_size:
+ *   x[p] = Σ_l Σ_h max_{g<G} exp(q[r,l,hG+g]·K[l, slot(p), h]/√D − lse[r,l,hG+g])
+ *          for p < seqused_k[r] (the keys visible to the query), else 0;
+ *   state[r][p] ← x[p]                               if count[r] == 1
+ *   state[r][p] ← state + (x[p] − state)/count[r]    otherwise
+ * i.e. the running mean over the action tokens of the region (count[r] = the
+ * index of this action token, 1 at the region's first token, which restarts
+ * the state).  Requests with count[r] < 1 are not generating an action and
+ * are left untouched.  A slot holds every layer's KV of one token, so one
+ * score per position sums over layers and KV heads.
+ *   q            device bf16 [n_req][L][Hq][D]   the current query token
+ *   lse          device fp32 [n_req][L][Hq]      natural-log LSE per head
+ *   kpool        device bf16 [L][n_slots][H][D]
+ *   block_table  device int32 [n_req][max_blocks] physical block ids
+ *   seqused_k    device int32 [n_req]  keys visible (≤ max_blocks·block_size)
+ *   count        device int32 [n_req]  action-token index (< 1: skip)
+ *   state        device fp32 [n_req][max_blocks·block_size]  in/out
+ * G = Hq/H.  Arithmetic: fp32 products and sums, exp as 2^(log2 e·(…)) with
+ * the hardware ex2, the group maximum taken before the exponential.
+ * Shapes with H = 8, block_size = 16, G ∈ {2, 4, 8} run on the tensor cores
+ * (one 128-row page tile per MMA, brought in by TMA from the block table);
+ * any other shape runs on a CUDA-core kernel (kvc_recover_tensor_core tells
+ * which).  A visible position whose block id is outside the pool, or a
+ * seqused_k outside [0, max_blocks·block_size], is recorded as
+ * KVC_ERR_BOUNDS: the page scores 0 (the request is skipped).
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D ∉ {64,128}, Hq % H,
+ * Hq > 256, block_size > 64), KVC_ERR_ALIGN (q, kpool, lse, state).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
+                             int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
+                             const int32_t *seqused_k, const int32_t *count, int32_t n_req,
+                             int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
+                             float *state, int32_t *dev_status, cudaStream_t stream);
+
+/* 1 if kvc_recover_score runs these sizes on the tensor cores, else 0. */
+int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size);
+
+/* ------------------------------------------------------------------------
+ * Conflict-free tail slot plan (ActKV §7.2, Algorithm 4, planning step).
+ * Request r holds n = seqused_k[r] tokens in Y = ⌈n/block_size⌉ logical
+ * blocks, m of them retained (keep-mask bits).  All retained tokens are
+ * consolidated into the last X = ⌈m/block_size⌉ logical blocks [Y−X, Y):
+ *   sources       retained positions before the region, ascending;
+ *   destinations  positions of the region that hold no retained token
+ *                 (including the unused slots past n), ascending;
+ * the k-th source goes to the k-th destination, so the two sets are
+ * disjoint and all copies can run at once without a buffer.  Logical
+ * positions are translated to physical slots through the block table.
+ *   keepmask      device uint32 [n_req][mask_words]: bit p%32 of word p/32
+ *                 = position p retained (bits at or past n are ignored)
+ *   src_slot, dst_slot  device int32 [n_req][max_blocks·block_size] out:
+ *                 the pairs, then −1
+ *   n_pairs       device int32 [n_req] out
+ *   n_tail_blocks device int32 [n_req] out: X
+ *   freed_blocks  device int32 [n_req][max_blocks] out: block_table[r][0 …
+ *                 Y−X−1] (returned to the allocator), then −1
+ *   n_freed       device int32 [n_req] out: Y − X
+ *   new_table     device int32 [n_req][max_blocks] out: block_table[r][Y−X
+ *                 … Y−1], then −1
+ *   tail_mask     device uint32 [n_req][⌈max_blocks·block_size/32⌉] out:
+ *                 bit i = slot i of the region holds a retained token after
+ *                 the copies
+ * The result is unique and exact (integer work only).  A seqused_k outside
+ * [0, max_blocks·block_size] or longer than mask_words·32 is recorded as
+ * KVC_ERR_BOUNDS and that request gets an empty plan; a block id outside
+ * the pool is recorded and its slot written as −1.
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (max_blocks·block_size >
+ * KVC_TAIL_MAX_TOKENS).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_tail_plan(const uint32_t *keepmask, int32_t mask_words,
+                         const int32_t *seqused_k, const int32_t *block_table,
+                         int32_t max_blocks, int32_t n_req, int32_t block_size, int64_t n_slots,
+                         int32_t *src_slot, int32_t *dst_slot, int32_t *n_pairs,
+                         int32_t *n_tail_blocks, int32_t *freed_blocks, int32_t *n_freed,
+                         int32_t *new_table, uint32_t *tail_mask, int32_t *dev_status,
+                         cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * One-shot in-place compaction (ActKV §7.2, Algorithm 4, copy step): for
+ * every request r, pair k < n_pairs[r] and layer l,
+ *   kpool[l][dst_slot[r][k]] ← kpool[l][src_slot[r][k]]   (H·D elements)
+ *   vpool[l][dst_slot[r][k]] ← vpool[l][src_slot[r][k]]
+ * as bit copies, all at once.  The pairs must come from kvc_tail_plan (or
+ * any plan whose sources and destinations are disjoint); with overlapping
+ * pairs the result is undefined.
+ *   kpool, vpool  device bf16 [L][n_slots][H][D]  in/out
+ *   src_slot, dst_slot  device int32 [n_req][pair_cap]; n_pairs device
+ *                 int32 [n_req] (clamped to [0, pair_cap])
+ * A slot outside [0, n_slots) is recorded as KVC_ERR_BOUNDS and that pair
+ * is skipped.
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D, n_req > 65535),
+ * KVC_ERR_ALIGN (pools).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_tail_compact(kvc_bf16 *kpool, kvc_bf16 *vpool, int64_t n_slots, int32_t L,
+                            int32_t H, int32_t D, const int32_t *src_slot,
+                            const int32_t *dst_slot, const int32_t *n_pairs, int32_t pair_cap,
+                            int32_t n_req, int32_t *dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,8 @@ __all__ = [
     "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
+    "kvc_recover_score", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
+    "TAIL_MAX_TOKENS",
 ]
 
 BLOCK_TOKENS = 32
@@ -30,6 +32,7 @@ SENTINEL_K_BITS = 0xC61C
 SELECT_MAX_SEG = 49152
 SCORE_MAX_ROWS = 256
 SCORE_STATIC_SCRATCH_BYTES = 8 << 20
+TAIL_MAX_TOKENS = 1 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvc.so")
@@ -74,6 +77,13 @@ _SIGS = {
     "kvc_redirect_free_workspace_size": (_SZ, [_I32, _I32, _I64]),
     "kvc_redirect_free": (_c.c_int, [_P, _P, _I32, _I32, _P, _I64, _I32, _I32,
                                      _P, _I32, _P, _P, _SZ, _P, _P]),
+    "kvc_recover_score": (_c.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _P, _I32,
+                                     _I32, _I32, _I32, _I32, _I32, _P, _P, _P]),
+    "kvc_recover_tensor_core": (_I32, [_I32, _I32, _I32, _I32]),
+    "kvc_tail_plan": (_c.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I64, _P, _P,
+                                 _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvc_tail_compact": (_c.c_int, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P,
+                                    _I32, _I32, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -219,3 +229,33 @@ def kvc_redirect_free(slot_map, keepmask, n_sess, N, refcnt, n_slots,
                               _ptr(freed), freed_cap, _ptr(n_freed), _ptr(ws),
                               ws.numel() * ws.element_size(), _ptr(dev_status),
                               _stream(stream)), "kvc_redirect_free")
+
+
+def kvc_recover_score(q, lse, kpool, n_slots, block_table, max_blocks, seqused_k, count,
+                      n_req, L, H, Hq, D, block_size, state, dev_status=None, stream=None):
+    _ok(lib.kvc_recover_score(_ptr(q), _ptr(lse), _ptr(kpool), n_slots, _ptr(block_table),
+                              max_blocks, _ptr(seqused_k), _ptr(count), n_req, L, H, Hq, D,
+                              block_size, _ptr(state), _ptr(dev_status), _stream(stream)),
+        "kvc_recover_score")
+
+
+def kvc_recover_tensor_core(H, Hq, D, block_size) -> bool:
+    return bool(lib.kvc_recover_tensor_core(H, Hq, D, block_size))
+
+
+def kvc_tail_plan(keepmask, mask_words, seqused_k, block_table, max_blocks, n_req,
+                  block_size, n_slots, src_slot, dst_slot, n_pairs, n_tail_blocks,
+                  freed_blocks, n_freed, new_table, tail_mask, dev_status=None, stream=None):
+    _ok(lib.kvc_tail_plan(_ptr(keepmask), mask_words, _ptr(seqused_k), _ptr(block_table),
+                          max_blocks, n_req, block_size, n_slots, _ptr(src_slot),
+                          _ptr(dst_slot), _ptr(n_pairs), _ptr(n_tail_blocks),
+                          _ptr(freed_blocks), _ptr(n_freed), _ptr(new_table),
+                          _ptr(tail_mask), _ptr(dev_status), _stream(stream)),
+        "kvc_tail_plan")
+
+
+def kvc_tail_compact(kpool, vpool, n_slots, L, H, D, src_slot, dst_slot, n_pairs, pair_cap,
+                     n_req, dev_status=None, stream=None):
+    _ok(lib.kvc_tail_compact(_ptr(kpool), _ptr(vpool), n_slots, L, H, D, _ptr(src_slot),
+                             _ptr(dst_slot), _ptr(n_pairs), pair_cap, n_req,
+                             _ptr(dev_status), _stream(stream)), "kvc_tail_compact")

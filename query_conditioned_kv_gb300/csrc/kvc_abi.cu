@@ -215,4 +215,61 @@ kvc_status kvc_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
                                              ws, dev_status, stream));
 }
 
+kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
+                             int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
+                             const int32_t *seqused_k, const int32_t *count, int32_t n_req,
+                             int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
+                             float *state, int32_t *dev_status, cudaStream_t stream) {
+  if (!q || !lse || !kpool || !block_table || !seqused_k || !count || !state)
+    return KVC_ERR_INVALID_ARG;
+  if (n_req < 1 || L < 1 || H < 1 || Hq < 1 || block_size < 1 || max_blocks < 1 ||
+      n_slots < block_size)
+    return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D) || Hq % H || Hq > 256 || block_size > 64 || H > 256 ||
+      (int64_t)block_size * H > 4096 || (int64_t)max_blocks * block_size > INT32_MAX ||
+      (int64_t)n_req * max_blocks > INT32_MAX || (int64_t)n_req * L * Hq > INT32_MAX)
+    return KVC_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(kpool) || !aligned16(lse) || !aligned16(state))
+    return KVC_ERR_ALIGN;
+  return from_cuda(kvc::launch_recover_score(q, lse, kpool, n_slots, block_table, max_blocks,
+                                             seqused_k, count, n_req, L, H, Hq, D, block_size,
+                                             state, dev_status, stream));
+}
+
+int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size) {
+  return kvc::recover_tc_supported(H, Hq, D, block_size) ? 1 : 0;
+}
+
+kvc_status kvc_tail_plan(const uint32_t *keepmask, int32_t mask_words,
+                         const int32_t *seqused_k, const int32_t *block_table,
+                         int32_t max_blocks, int32_t n_req, int32_t block_size, int64_t n_slots,
+                         int32_t *src_slot, int32_t *dst_slot, int32_t *n_pairs,
+                         int32_t *n_tail_blocks, int32_t *freed_blocks, int32_t *n_freed,
+                         int32_t *new_table, uint32_t *tail_mask, int32_t *dev_status,
+                         cudaStream_t stream) {
+  if (!keepmask || !seqused_k || !block_table || !src_slot || !dst_slot || !n_pairs ||
+      !n_tail_blocks || !freed_blocks || !n_freed || !new_table || !tail_mask)
+    return KVC_ERR_INVALID_ARG;
+  if (n_req < 1 || mask_words < 1 || max_blocks < 1 || block_size < 1 || n_slots < 1 ||
+      n_slots > INT32_MAX)
+    return KVC_ERR_INVALID_ARG;
+  if ((int64_t)max_blocks * block_size > KVC_TAIL_MAX_TOKENS) return KVC_ERR_SHAPE;
+  return from_cuda(kvc::launch_tail_plan(keepmask, mask_words, seqused_k, block_table,
+                                         max_blocks, n_req, block_size, n_slots, src_slot,
+                                         dst_slot, n_pairs, n_tail_blocks, freed_blocks, n_freed,
+                                         new_table, tail_mask, dev_status, stream));
+}
+
+kvc_status kvc_tail_compact(kvc_bf16 *kpool, kvc_bf16 *vpool, int64_t n_slots, int32_t L,
+                            int32_t H, int32_t D, const int32_t *src_slot,
+                            const int32_t *dst_slot, const int32_t *n_pairs, int32_t pair_cap,
+                            int32_t n_req, int32_t *dev_status, cudaStream_t stream) {
+  if (!kpool || !vpool || !src_slot || !dst_slot || !n_pairs) return KVC_ERR_INVALID_ARG;
+  if (n_slots < 1 || L < 1 || H < 1 || pair_cap < 1 || n_req < 1) return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D) || n_req > 65535) return KVC_ERR_SHAPE;
+  if (!aligned16(kpool) || !aligned16(vpool)) return KVC_ERR_ALIGN;
+  return from_cuda(kvc::launch_tail_compact(kpool, vpool, n_slots, L, H, D, src_slot, dst_slot,
+                                            n_pairs, pair_cap, n_req, dev_status, stream));
+}
+
 }  // extern "C"

@@ -103,4 +103,22 @@ cudaError_t launch_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
                                  int32_t *status, cudaStream_t s);
 size_t redirect_free_ws_bytes(int n_sess, int N, int64_t n_slots);
 
+// ActKV paged primitives (recover.cu)
+bool recover_tc_supported(int H, int Hq, int D, int BS);
+cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint16_t *kpool,
+                                 int64_t n_slots, const int32_t *block_table, int max_blocks,
+                                 const int32_t *seqused, const int32_t *count, int n_req, int L,
+                                 int H, int Hq, int D, int BS, float *state, int32_t *status,
+                                 cudaStream_t s);
+cudaError_t launch_tail_plan(const uint32_t *keepmask, int mask_words, const int32_t *seqused,
+                             const int32_t *block_table, int max_blocks, int n_req, int BS,
+                             int64_t n_slots, int32_t *src, int32_t *dst, int32_t *n_pairs,
+                             int32_t *n_tail, int32_t *freed, int32_t *n_freed,
+                             int32_t *new_table, uint32_t *tail_mask, int32_t *status,
+                             cudaStream_t s);
+cudaError_t launch_tail_compact(uint16_t *kpool, uint16_t *vpool, int64_t n_slots, int L, int H,
+                                int D, const int32_t *src, const int32_t *dst,
+                                const int32_t *n_pairs, int cap, int n_req, int32_t *status,
+                                cudaStream_t s);
+
 }  // namespace kvc

@@ -2,6 +2,7 @@
 
 ``MeanKEvent``   score (Mean-K) → select → pack + re-RoPE
 ``SlotMapEvent`` score (QueryMemory) → select → redirect + free
+``PagedEvent``   LSE-recovery score → select → tail plan → in-place compaction
 
 Both only allocate caller-side buffers with torch and call the library's
 entry points; an event can be captured in a CUDA graph (``capture()``) so
@@ -22,10 +23,10 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_redirect_free,
+from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_recover_score, kvc_redirect_free,
                kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
                kvc_score_qmem, kvc_score_qmem_workspace_size,
-               kvc_score_workspace_size, kvc_select)
+               kvc_score_workspace_size, kvc_select, kvc_tail_compact, kvc_tail_plan)
 
 
 def _dev_i64(x, device) -> torch.Tensor:
@@ -257,3 +258,75 @@ class SlotMapEvent:
         self.score(M, kpool, slot_map, stream)
         self.select(stream=stream)
         self.redirect(slot_map, refcnt, stream=stream)
+
+
+class PagedEvent:
+    """Buffers and calls of an ActKV compression operation on a paged KV
+    cache (ActKV §3.3 on the §2 layout): LSE-recovery score of the current
+    action token (§7.1), token-level select of `keep` tokens per request (no
+    forced set), conflict-free tail plan and one-shot in-place compaction
+    (§7.2).  All requests have max_blocks·block_size positions; select takes
+    each request's whole row as its segment."""
+
+    def __init__(self, n_req: int, max_blocks: int, block_size: int, L: int, H: int,
+                 Hq: int, D: int, n_slots: int, keep: int, device="cuda"):
+        self.n_req, self.max_blocks, self.BS = n_req, max_blocks, block_size
+        self.L, self.H, self.Hq, self.D = L, H, Hq, D
+        self.n_slots, self.keep = n_slots, keep
+        self.cap = max_blocks * block_size
+        dev = self.device = torch.device(device)
+        self.state = torch.zeros(n_req, self.cap, dtype=torch.float32, device=dev)
+        self.seg_off = _dev_i64(np.arange(n_req + 1) * self.cap, dev)
+        self.kept = torch.empty(n_req, keep, dtype=torch.int32, device=dev)
+        self.kept_count = torch.empty(n_req, dtype=torch.int32, device=dev)
+        self.words = (self.cap + 31) // 32
+        self.keepmask = torch.empty(n_req, self.words, dtype=torch.int32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.src = torch.empty(n_req, self.cap, **i32)
+        self.dst = torch.empty(n_req, self.cap, **i32)
+        self.n_pairs = torch.empty(n_req, **i32)
+        self.n_tail = torch.empty(n_req, **i32)
+        self.freed = torch.empty(n_req, max_blocks, **i32)
+        self.n_freed = torch.empty(n_req, **i32)
+        self.new_table = torch.empty(n_req, max_blocks, **i32)
+        self.tail_mask = torch.empty(n_req, self.words, **i32)
+        self.dev_status = torch.zeros(1, **i32)
+
+    def score(self, q, lse, kpool, block_table, seqused, count, stream=None):
+        kvc_recover_score(q, lse, kpool, self.n_slots, block_table, self.max_blocks, seqused,
+                          count, self.n_req, self.L, self.H, self.Hq, self.D, self.BS,
+                          self.state, self.dev_status, stream)
+
+    def select(self, stream=None):
+        kvc_select(self.state, self.seg_off, self.n_req, self.cap, self.keep, 0, 0, self.kept,
+                   self.kept_count, self.keepmask, self.dev_status, stream)
+
+    def plan(self, seqused, block_table, stream=None):
+        kvc_tail_plan(self.keepmask, self.words, seqused, block_table, self.max_blocks,
+                      self.n_req, self.BS, self.n_slots, self.src, self.dst, self.n_pairs,
+                      self.n_tail, self.freed, self.n_freed, self.new_table, self.tail_mask,
+                      self.dev_status, stream)
+
+    def compact(self, kpool, vpool, stream=None):
+        kvc_tail_compact(kpool, vpool, self.n_slots, self.L, self.H, self.D, self.src,
+                         self.dst, self.n_pairs, self.cap, self.n_req, self.dev_status, stream)
+
+    def run(self, q, lse, kpool, vpool, block_table, seqused, count, stream=None):
+        self.score(q, lse, kpool, block_table, seqused, count, stream)
+        self.select(stream)
+        self.plan(seqused, block_table, stream)
+        self.compact(kpool, vpool, stream)
+
+
+def paged_bytes(n_req: int, seq: int, L: int, H: int, Hq: int, D: int, n_pairs: int) -> dict:
+    """Bytes an ActKV operation must move through HBM, by stage: every
+    visible key row read once, the query token, LSE and the state read and
+    written (score); the scores read (select); the keep mask and block table
+    (plan); K and V rows of every planned pair read and written once per
+    layer (compact)."""
+    score = n_req * seq * L * H * D * 2 + n_req * L * Hq * (D * 2 + 4) + n_req * seq * 8
+    select = n_req * seq * 4
+    plan = n_req * (seq // 8 + seq // 4)
+    compact = n_pairs * L * 2 * H * D * 2 * 2
+    return {"score": score, "select": select, "plan": plan, "compact": compact,
+            "event": score + select + plan + compact}

@@ -11,13 +11,17 @@ event once to produce realistic inputs for the stage, then launches the stage
   python -m query_conditioned_kv_gb300.profile_cases meank  --layers 2  --iters 3
   python -m query_conditioned_kv_gb300.profile_cases qmem   --layers 4  --sessions 8 --iters 2
   python -m query_conditioned_kv_gb300.profile_cases event_timing --config 27b --iters 10
+  python -m query_conditioned_kv_gb300.profile_cases paged  --sessions 4 --iters 3
 
 event_timing times a whole Mean-K event (score → select → pack, one CUDA
 graph) on a full workload — tiny, 8b, 27b or ragged — with L2 flushed
 between replays, and prints one JSON line: time, tokens/s and the fraction
 of the measured HBM peak.  The qmem case is the QueryMemory rule score on the 64 x 32768 slot-map
 workload's shapes (shared 4096-position prefix, page 16), reduced to
-`--sessions` sessions and `--layers` layers.
+`--sessions` sessions and `--layers` layers.  The paged case is ActKV's
+compression operation at the Table 1 shapes (6K → 4K tokens per request,
+36 layers) on `--sessions` requests: score → select → plan → compaction,
+`--iters` times.
 """
 from __future__ import annotations
 
@@ -29,7 +33,7 @@ import sys
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem",
-                                     "event_timing"])
+                                     "event_timing", "paged"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sessions", type=int, default=8)
@@ -50,6 +54,9 @@ def main(argv=None) -> None:
         return
     if args.case == "event_timing":
         _event_timing(args, dev, root)
+        return
+    if args.case == "paged":
+        _paged_case(args, dev)
         return
     cfg = W.scaled(W.config_8b(), L=args.layers)
     q = cfg.q(dev)
@@ -188,3 +195,28 @@ def _qmem_case(args, dev):
 
 if __name__ == "__main__":
     main()
+
+
+def _paged_case(args, dev):
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import PagedEvent
+
+    cfg = W.config_paged(args.sessions)
+    kp, vp = cfg.pools(dev)
+    q = cfg.q(dev)
+    lse = cfg.lse(q)
+    bt = torch.from_numpy(cfg.block_tables()).to(dev)
+    seq = torch.from_numpy(cfg.seqused()).to(dev)
+    cnt = torch.ones(cfg.n_req, dtype=torch.int32, device=dev)
+    ev = PagedEvent(cfg.n_req, cfg.max_blocks, cfg.BS, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                    cfg.keep, device=dev)
+    for _ in range(args.iters):
+        ev.run(q, lse, kp, vp, bt, seq, cnt)
+    torch.cuda.synchronize(dev)
+    st = kvc.kvc_device_status(ev.dev_status)
+    print(f"paged: {cfg.n_req} requests, pairs {int(ev.n_pairs.sum().item())}, status {st}")
+    if st != 0:
+        raise SystemExit(1)

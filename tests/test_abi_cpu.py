@@ -34,7 +34,8 @@ def test_header_declares_the_event_calls():
     for n in ("kvc_build_meank", "kvc_score", "kvc_select", "kvc_pack_rerope",
               "kvc_redirect_free", "kvc_qmem_update", "kvc_score_qmem",
               "kvc_rope_table", "kvc_init_sentinel", "kvc_status_string",
-              "kvc_device_status"):
+              "kvc_device_status", "kvc_recover_score", "kvc_tail_plan",
+              "kvc_tail_compact"):
         assert n in names
 
 
@@ -103,7 +104,38 @@ def test_validation_rejects_before_launch(kvc):
     # redirect: workspace too small
     assert _call(kvc, "kvc_redirect_free", P, P, 1, 64, P, 100, 0, 0, P, 100, P, P, 16,
                  None, None) == 5
+    # recover: D, Hq % H, a NULL state, misaligned pool
+    assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 96, 16,
+                 P, None, None) == 2
+    assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 30, 128, 16,
+                 P, None, None) == 2
+    assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128, 16,
+                 None, None, None) == 1
+    assert _call(kvc, "kvc_recover_score", P, P, U, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128, 16,
+                 P, None, None) == 4
+    # tail plan: a request longer than the plan accepts; no mask
+    assert _call(kvc, "kvc_tail_plan", P, 4, P, P, 1 << 17, 1, 16, 1 << 22, P, P, P, P, P, P,
+                 P, P, None, None) == 2
+    assert _call(kvc, "kvc_tail_plan", None, 4, P, P, 8, 1, 16, 1 << 12, P, P, P, P, P, P,
+                 P, P, None, None) == 1
+    # compaction: D, misaligned pool, no pair capacity
+    assert _call(kvc, "kvc_tail_compact", P, P, 1 << 12, 2, 8, 96, P, P, P, 16, 1, None,
+                 None) == 2
+    assert _call(kvc, "kvc_tail_compact", P, U, 1 << 12, 2, 8, 128, P, P, P, 16, 1, None,
+                 None) == 4
+    assert _call(kvc, "kvc_tail_compact", P, P, 1 << 12, 2, 8, 128, P, P, P, 0, 1, None,
+                 None) == 1
     assert _call(kvc, "kvc_device_status", None, None) == 1
+
+
+def test_recover_tensor_core_coverage(kvc):
+    """The page tile of ActKV's Table 1 shapes (block 16, 8 KV heads, d 128)
+    runs on the tensor cores; other page shapes take the CUDA-core kernel."""
+    assert kvc.kvc_recover_tensor_core(8, 32, 128, 16)
+    assert kvc.kvc_recover_tensor_core(8, 64, 64, 16)
+    assert not kvc.kvc_recover_tensor_core(4, 16, 128, 16)
+    assert not kvc.kvc_recover_tensor_core(8, 24, 128, 16)
+    assert not kvc.kvc_recover_tensor_core(8, 32, 128, 32)
 
 
 def test_binding_raises_on_error(kvc):

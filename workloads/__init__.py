@@ -23,7 +23,14 @@ none are available, so these stand in for them):
   * Mean-K of layers whose raw K is not resident is drawn directly as bf16
     of N(0, 1/32) + alpha·u (the distribution of a 32-token mean);
   * slot-map config: page size 16, a shared refcounted prefix, private pages
-    in a seeded shuffled order, slot 0 the dead slot.
+    in a seeded shuffled order, slot 0 the dead slot;
+  * paged (ActKV) config: K/V pools of N(0,1) rows drawn for a window of
+    pages and repeated periodically over the pool (the values are data, the
+    periodicity changes no arithmetic and keeps generation of tens of GB
+    quick), 3 % of the slots of each (layer, KV head) planted with +alpha·u,
+    each request's pages a seeded shuffled subset of the pool, the current
+    query token N(0,1) + gamma·u, and the attention LSE of the step stood in
+    by its value for Gaussian keys, ln(n) + |q|²/(2D).
 """
 from __future__ import annotations
 
@@ -51,7 +58,7 @@ def _mix(*parts: int) -> int:
 
 
 _TAGS = {"u": 1, "plant": 2, "k": 3, "v": 4, "q": 5, "mk": 6, "hist": 7,
-         "qturn": 8, "pages": 9, "kpool": 10}
+         "qturn": 8, "pages": 9, "kpool": 10, "vpool": 11, "lse": 12, "keep": 13}
 
 
 def _gen(device, seed: int, tag: str, *idx: int) -> torch.Generator:
@@ -385,6 +392,114 @@ def config_slotmap() -> SlotMapConfig:
     return SlotMapConfig(name="slotmap_64x32k", n_sess=64, N=32768,
                          prefix=4096, page=16, L=36, H=8, Hq=32, D=128, T=32,
                          turns=4, budget=8192)
+
+
+# ------------------------------------------------------------ paged (ActKV)
+
+@dataclasses.dataclass
+class PagedConfig:
+    """An ActKV compression operation on a paged KV cache: one LSE-recovery
+    step, keep the top `keep` tokens of each request, tail compaction."""
+    name: str
+    n_req: int
+    seq: int               # tokens per request before compression
+    keep: int              # tokens kept per request
+    BS: int = 16           # slots per block
+    L: int = 36
+    H: int = 8
+    Hq: int = 32
+    D: int = 128
+    spare_blocks: int = 64  # free blocks of the pool (not owned by a request)
+    count: int = 1         # action-token index of the timed step
+    plant_frac: float = 0.03
+    alpha: tuple = (2.0, 4.0)
+    gamma: float = 3.0
+    window_blocks: int = 4096  # distinct pages drawn per layer (then repeated)
+    seed: int = 5
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.H
+
+    @property
+    def max_blocks(self) -> int:
+        return (self.seq + self.BS - 1) // self.BS
+
+    @property
+    def cap(self) -> int:
+        return self.max_blocks * self.BS
+
+    @property
+    def n_blocks(self) -> int:
+        return self.n_req * self.max_blocks + self.spare_blocks
+
+    @property
+    def n_slots(self) -> int:
+        return self.n_blocks * self.BS
+
+    def block_tables(self) -> np.ndarray:
+        """[n_req][max_blocks] int32: a seeded shuffled assignment of the
+        pool's blocks (row-major)."""
+        perm = _np_rng(self.seed, "pages").permutation(self.n_blocks)
+        bt = perm[:self.n_req * self.max_blocks].reshape(self.n_req, self.max_blocks)
+        return np.ascontiguousarray(bt.astype(np.int32))
+
+    def seqused(self) -> np.ndarray:
+        return np.full(self.n_req, self.seq, dtype=np.int32)
+
+    def direction(self, l: int, h: int) -> np.ndarray:
+        g = _np_rng(self.seed, "u", l, h).standard_normal(self.D)
+        return (g / math.sqrt(float(np.dot(g, g)))).astype(np.float32)
+
+    def _pool_layer(self, tag: str, l: int, device, plant: bool) -> torch.Tensor:
+        n_win = min(self.window_blocks, self.n_blocks) * self.BS
+        base = torch.randn(n_win, self.H, self.D, dtype=torch.float32, device=device,
+                           generator=_gen(device, self.seed, tag, l))
+        if plant:
+            rng = _np_rng(self.seed, "plant", l)
+            for h in range(self.H):
+                cnt = int(round(self.plant_frac * n_win))
+                idx = torch.from_numpy(rng.choice(n_win, size=cnt, replace=False)).to(device)
+                a = torch.from_numpy(rng.uniform(*self.alpha, size=cnt).astype(np.float32))
+                u = torch.from_numpy(self.direction(l, h)).to(device)
+                base[idx, h] += a.to(device)[:, None] * u[None, :]
+        base = base.to(torch.bfloat16)
+        out = torch.empty(self.n_slots, self.H, self.D, dtype=torch.bfloat16, device=device)
+        for c0 in range(0, self.n_slots, n_win):
+            c1 = min(self.n_slots, c0 + n_win)
+            out[c0:c1] = base[:c1 - c0]
+        return out
+
+    def pools(self, device="cpu"):
+        """(kpool, vpool) bf16 [L][n_slots][H][D]."""
+        shape = (self.L, self.n_slots, self.H, self.D)
+        kp = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        vp = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        for l in range(self.L):
+            kp[l] = self._pool_layer("kpool", l, device, True)
+            vp[l] = self._pool_layer("vpool", l, device, False)
+        return kp, vp
+
+    def q(self, device="cpu") -> torch.Tensor:
+        """bf16 [n_req][L][Hq][D]: the current (action) query token."""
+        x = torch.randn(self.n_req, self.L, self.Hq, self.D, dtype=torch.float32,
+                        device=device, generator=_gen(device, self.seed, "q"))
+        u = torch.stack([torch.stack([torch.from_numpy(self.direction(l, hq // self.G))
+                                      for hq in range(self.Hq)]) for l in range(self.L)])
+        return (x + self.gamma * u.to(device)[None]).to(torch.bfloat16)
+
+    def lse(self, q: torch.Tensor) -> torch.Tensor:
+        """fp32 [n_req][L][Hq] stand-in for the backend's LSE of the step:
+        ln(seq) + |q|²/(2D), the log-partition of Gaussian keys."""
+        qf = q.float()
+        return (math.log(self.seq) + (qf * qf).sum(-1) / (2.0 * self.D)).contiguous()
+
+
+def config_paged(n_req: int = 64) -> PagedConfig:
+    """ActKV Table 1 shapes: block size 16, 8 KV heads, head dim 128; n_req
+    concurrent requests, each compressed from 6K to 4K entries; 8B-class
+    depth (36 layers, 32 query heads)."""
+    return PagedConfig(name=f"paged_r{n_req}_6k_to_4k", n_req=n_req, seq=6144, keep=4096)
 
 
 # ---------------------------------------------------------------- helpers
