@@ -193,9 +193,6 @@ def _qmem_case(args, dev):
           f"positions, {cfg.L} layers ok")
 
 
-if __name__ == "__main__":
-    main()
-
 
 def _paged_case(args, dev):
     import torch
@@ -220,3 +217,7 @@ def _paged_case(args, dev):
     print(f"paged: {cfg.n_req} requests, pairs {int(ev.n_pairs.sum().item())}, status {st}")
     if st != 0:
         raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main()
