@@ -73,6 +73,14 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
                               int D, int N, int64_t n_slots, void *ws,
                               int32_t *status, cudaStream_t s);
 size_t score_qmem_ws_bytes(int n_sess, int L, int Hq, int N);
+// tensor-core logits of the rule score (qmem_tc.cu)
+bool qmem_tc_supported(int H, int Hq, int D, int64_t L, int64_t n_slots);
+size_t qmem_tc_mb_bytes(int n_sess, int L, int Hq);
+cudaError_t launch_qmem_logits_tc(const float *M, const uint16_t *kpool, const int32_t *slot_map,
+                                  int32_t sentinel, float *logits, float2 *part, uint16_t *mb,
+                                  int n_sess, int L, int H, int Hq, int D, int N,
+                                  int64_t n_slots, int n_tiles, int32_t *status,
+                                  cudaStream_t s);
 
 cudaError_t launch_select(const float *scores, const int64_t *seg_off,
                           int n_seg, int max_seg_len, int budget, int n_sink,

@@ -21,6 +21,11 @@
 //   k_qmem_rule    re-reads the logits (1/16 of the K bytes) and sums
 //                  2^(z − LSE) over (l, hq) per position.
 // Dead positions (slot = sentinel) carry z = −inf and rule = −1.
+// For 8 KV heads and groups of 2, 4 or 8 query heads the logits come from
+// the tensor-core kernel of qmem_tc.cu instead (same outputs); the CUDA-core
+// kernel below covers every other shape.
+#include <stdlib.h>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -285,6 +290,24 @@ k_qmem_rule(QArgs a) {
   a.rule[(int64_t)r * a.N + j] = out;
 }
 
+// LSE per (session, layer, query head) from the tile partials, then the
+// rule sum over (layer, query head) per position.
+cudaError_t launch_qmem_reduce(const QArgs &a, cudaStream_t s) {
+  const int64_t rows = (int64_t)a.n_sess * a.L * a.Hq;
+  k_qmem_lse<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g3((a.N + 255) / 256, a.n_sess);
+  size_t smem3 = (size_t)a.L * a.Hq * sizeof(float);
+  if (smem3 > 48 * 1024) {
+    e = cudaFuncSetAttribute(k_qmem_rule, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem3);
+    if (e != cudaSuccess) return e;
+  }
+  k_qmem_rule<<<g3, 256, smem3, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
@@ -303,7 +326,8 @@ size_t score_qmem_ws_bytes(int n_sess, int L, int Hq, int N) {
   size_t part = (size_t)rows * n_tiles * sizeof(float2);
   size_t lse = (size_t)rows * sizeof(float);
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-  return al(logits) + al(part) + al(lse);
+  // + the two-term bf16 copy of M that the tensor-core logits read
+  return al(logits) + al(part) + al(lse) + al(qmem_tc_mb_bytes(n_sess, L, Hq));
 }
 
 cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
@@ -321,6 +345,8 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
   a.part = reinterpret_cast<float2 *>(w);
   w += al((size_t)rows * a.n_tiles * sizeof(float2));
   a.lse = reinterpret_cast<float *>(w);
+  w += al((size_t)rows * sizeof(float));
+  uint16_t *mb = reinterpret_cast<uint16_t *>(w);
   a.M = M;
   a.kpool = kpool;
   a.slot_map = slot_map;
@@ -336,10 +362,18 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
   a.sentinel = sentinel;
   a.n_slots = n_slots;
   a.zscale = kLog2e / sqrtf((float)D);
+  cudaError_t e;
+  const char *force = getenv("KVC_QMEM_PATH");
+  const bool cc = force && force[0] == 'c' && force[1] == 'c';
+  if (!cc && qmem_tc_supported(H, Hq, D, L, n_slots)) {
+    e = launch_qmem_logits_tc(M, kpool, slot_map, sentinel, a.logits, a.part, mb, n_sess, L, H,
+                              Hq, D, N, n_slots, a.n_tiles, status, s);
+    if (e != cudaSuccess) return e;
+    return launch_qmem_reduce(a, s);
+  }
   const int GP = a.G <= 4 ? 4 : 8;
   const size_t smem = (size_t)Hq * (kTJ + 1) * sizeof(float);
   dim3 g1(n_sess, a.n_tiles, L);
-  cudaError_t e;
 #define KVC_LOGITS_CASE(DV, GV)                                              \
   if (D == DV && GP == GV) {                                                 \
     e = cudaFuncSetAttribute(k_qmem_logits<DV, GV>,                          \
@@ -356,18 +390,7 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
 #undef KVC_LOGITS_CASE
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_qmem_lse<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  dim3 g3((N + 255) / 256, n_sess);
-  size_t smem3 = (size_t)L * Hq * sizeof(float);
-  if (smem3 > 48 * 1024) {
-    e = cudaFuncSetAttribute(k_qmem_rule, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem3);
-    if (e != cudaSuccess) return e;
-  }
-  k_qmem_rule<<<g3, 256, smem3, s>>>(a);
-  return cudaGetLastError();
+  return launch_qmem_reduce(a, s);
 }
 
 }  // namespace kvc

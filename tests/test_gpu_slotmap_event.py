@@ -75,7 +75,8 @@ def test_qmem_update_parity(kvc, orc):
 
 
 @pytest.mark.parametrize("H,Hq,D", [(8, 32, 128), (2, 8, 128), (4, 16, 64), (8, 48, 128),
-                                    (4, 4, 128), (2, 16, 64), (1, 3, 64)])
+                                    (4, 4, 128), (2, 16, 64), (1, 3, 64), (8, 16, 64),
+                                    (8, 64, 128)])
 def test_rule_score_parity(kvc, orc, H, Hq, D):
     """GQA groups of 1..8 query heads, both head sizes; 1008 positions (a
     ragged last tile) with 5% of the private positions already dead."""
@@ -100,6 +101,57 @@ def test_rule_score_parity(kvc, orc, H, Hq, D):
         assert_scores_close(got[r][~dead], ref[~dead], "rule")
         live_sum = float(got[r][~dead].astype(np.float64).sum())
         assert abs(live_sum - cfg.L * cfg.Hq) < 1e-3 * cfg.L * cfg.Hq
+
+
+def _rule_gpu(kvc, cfg, M, kp, sm, path=None):
+    import os
+    from query_conditioned_kv_gb300.event import SlotMapEvent
+    ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
+                      cfg.budget, cfg.prefix, cfg.sentinel, device=DEV)
+    old = os.environ.pop("KVC_QMEM_PATH", None)
+    if path:
+        os.environ["KVC_QMEM_PATH"] = path
+    try:
+        ev.score(torch.from_numpy(M).to(DEV), kp, torch.from_numpy(sm).to(DEV))
+        torch.cuda.synchronize()
+    finally:
+        os.environ.pop("KVC_QMEM_PATH", None)
+        if old is not None:
+            os.environ["KVC_QMEM_PATH"] = old
+    assert kvc.kvc_device_status(ev.dev_status) == 0
+    return ev.rule.cpu().numpy()
+
+
+@pytest.mark.parametrize("Hq", [16, 32, 64])
+def test_rule_score_gathered_rows(kvc, orc, Hq):
+    """Slot maps that are not page-contiguous: every position of the private
+    part points at a random slot (the tensor-core kernel then gathers one
+    row per position), plus blocks whose slots are contiguous but not
+    page-aligned, dead positions inside a page, and a session whose first
+    positions are all dead.  Against the oracle, and the two logits kernels
+    against each other."""
+    cfg = small_cfg(H=8, D=128, Hq=Hq)
+    rng = np.random.default_rng(Hq)
+    sm = cfg.slot_maps()
+    priv = sm[:, cfg.prefix:]
+    flat = priv.reshape(-1).copy()
+    rng.shuffle(flat)                                  # scatter every private position
+    sm[:, cfg.prefix:] = flat.reshape(priv.shape)
+    sm[0, 300:316] = np.arange(16) + 1000              # contiguous, not page-aligned
+    sm[1, cfg.prefix + 16: cfg.prefix + 32: 3] = cfg.sentinel  # dead inside a block
+    sm[2, :64] = cfg.sentinel                          # a dead run
+    kp = kpool_of(cfg, DEV)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    M = memory_chain(orc, cfg)
+    got = _rule_gpu(kvc, cfg, M, kp, sm)
+    cc = _rule_gpu(kvc, cfg, M, kp, sm, "cc")
+    kpb = W.bf16_bits(kp)
+    for r in range(cfg.n_sess):
+        ref = orc.rule_session(M[r], kpb, sm[r], cfg.H, cfg.sentinel)
+        dead = sm[r] == cfg.sentinel
+        assert np.all(got[r][dead] == -1.0) and np.all(cc[r][dead] == -1.0)
+        assert_scores_close(got[r][~dead], ref[~dead], "rule (tensor cores)")
+        assert_scores_close(cc[r][~dead], ref[~dead], "rule (CUDA cores)")
 
 
 def _redirect_case(orc, cfg, rng):
