@@ -16,7 +16,9 @@ paged, refcounted K pool), the QueryMemory event (memory update; rule score
 beside them (`meank_build`, `slotmap_event`; `--no-slotmap` skips the latter),
 and so is ActKV's paged compression operation (LSE-recovery score → select →
 tail plan → in-place compaction) at 1, 4, 16 and 64 requests of 6K → 4K
-tokens (`actkv_event`; `--no-paged` skips it).
+tokens (`actkv_event`; `--no-paged` skips it), and KVMem's tiered view with the
+index and raw history in host memory, cold and warm steps (`tiered_event`;
+`--no-tiered` skips it).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -532,6 +534,92 @@ def paged_event(args, dev, peak, reqs=(1, 4, 16, 64), reps: int = 5):
             "l2": "pools (0.9-58 GB) exceed the 129 MB L2; no flush"}
 
 
+# ------------------------------------------------- tiered (host-resident)
+
+TIERED_WORKLOAD = ("tiered_8b_128k: the 8b_128k event with the Mean-K index (302 MB) and "
+                   "the raw K/V history (9.66 GB) in pinned host memory; score in 4-layer "
+                   "tiles copied host->device, select, tiered pack (hits from the previous "
+                   "view, misses read from host memory by the kernel); two agent steps")
+
+
+def tiered_event(args, dev, peak, reps: int = 3):
+    """KVMem's tiered view on the 8B-class workload.  Step 1 starts cold
+    (every kept block comes from host memory); step 2 scores a new query
+    window and reuses the blocks both steps keep.  Each rep replays the two
+    steps; stages are timed with CUDA events on the current stream (the
+    staging copies run on a side stream inside the score stage)."""
+    import torch
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import TieredMeanKEvent
+
+    cfg = W.config_8b()
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = cfg.meank_direct(dev)
+    kvc.kvc_build_meank(kraw, meank, cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    meank_h = meank.cpu().pin_memory()
+    kraw_h = kraw.cpu().pin_memory()
+    vraw_h = vraw.cpu().pin_memory()
+    del kraw, vraw, meank
+    torch.cuda.empty_cache()
+    qs = [cfg.q(dev, step=0), cfg.q(dev, step=1)]
+    ev = TieredMeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                          cfg.n_recent, L_pack=cfg.lp, theta=cfg.theta, pos0=cfg.pos0,
+                          device=dev, stage_layers=4)
+    stream = torch.cuda.current_stream(dev)
+
+    def ev_pair():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    rows = {"cold": [], "warm": []}
+    hits = {}
+    for rep in range(args.warmup + reps):
+        ev.steps = 0  # every rep starts cold
+        for k, q in (("cold", qs[0]), ("warm", qs[1])):
+            ev.n_hits.zero_()
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            cur = ev.cur
+            ev.kept, ev.kept_count = ev.kept_sets[cur], ev.count_sets[cur]
+            ev.vview = ev.vviews[cur]
+            torch.cuda.synchronize(dev)
+            marks[0].record(stream)
+            ev.score_tiered(q, meank_h)
+            marks[1].record(stream)
+            ev.select()
+            marks[2].record(stream)
+            ev.pack_tiered(kraw_h, vraw_h)
+            marks[3].record(stream)
+            ev.cur, ev.steps = 1 - cur, ev.steps + 1
+            torch.cuda.synchronize(dev)
+            if rep >= args.warmup:
+                rows[k].append([marks[i].elapsed_time(marks[i + 1]) for i in range(3)])
+                hits[k] = int(ev.n_hits.item())
+    if kvc.kvc_device_status(ev.dev_status) != 0:
+        raise RuntimeError("device status error in the tiered event")
+    n_units = cfg.lp * cfg.H * cfg.n_sess
+    kept_blocks = n_units * cfg.budget
+    blk_bytes = 32 * cfg.D * 2
+    meank_bytes = cfg.L * cfg.H * cfg.nb_total * cfg.D * 2
+    out = {"workload": TIERED_WORKLOAD, "reps": reps, "tokens_per_step": cfg.n_tok}
+    for k, v in rows.items():
+        sc, se, pk = (statistics.median(x[i] for x in v) for i in range(3))
+        ms = sc + se + pk
+        miss = kept_blocks - hits[k]
+        host_bytes = meank_bytes + miss * 2 * blk_bytes
+        out[k] = {
+            "ms_per_step": round(ms, 4), "value": cfg.n_tok / (ms * 1e-3), "unit": UNIT,
+            "stages_ms": {"score_tiered": round(sc, 4), "select": round(se, 4),
+                          "pack_tiered": round(pk, 4)},
+            "kept_blocks": kept_blocks, "hits": hits[k], "misses": miss,
+            "host_to_gpu_bytes": host_bytes,
+            "score_h2d_gbs": meank_bytes / (sc * 1e-3) / 1e9,
+            "pack_host_read_gbs": miss * 2 * blk_bytes / (pk * 1e-3) / 1e9,
+        }
+    del ev, meank_h, kraw_h, vraw_h
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------ oracle arm
 
 def _oracle_sample(n_units, dev):
@@ -625,6 +713,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-slotmap", action="store_true",
                     help="skip the QueryMemory (slot-map) event measurement")
+    ap.add_argument("--no-tiered", action="store_true",
+                    help="skip the host-resident (tiered) event measurement")
     ap.add_argument("--no-paged", action="store_true",
                     help="skip the ActKV paged-operation measurement")
     ap.add_argument("--groups", type=int, default=None,
@@ -654,6 +744,10 @@ def main():
         torch.cuda.empty_cache()
         line["slotmap_event"] = slot_map_event(args, torch.device("cuda", local_rank),
                                                peaks()[0])
+    if not args.no_tiered:
+        import torch
+        torch.cuda.empty_cache()
+        line["tiered_event"] = tiered_event(args, torch.device("cuda", local_rank), peaks()[0])
     if not args.no_paged:
         import torch
         torch.cuda.empty_cache()

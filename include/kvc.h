@@ -278,6 +278,46 @@ kvc_status kvc_pack_rerope(const kvc_bf16 *kraw, const kvc_bf16 *vraw,
                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Step 3a, tiered (KVMem, "Tiered movement": the raw history lives in host
+ * memory, the GPU holds only the execution view; missed blocks are brought
+ * in and re-RoPEd, and blocks shared by consecutive steps stay on the GPU).
+ * Same output as kvc_pack_rerope for the same kept lists (bit for bit), but
+ * the source of each kept block's raw K and V is
+ *   - the previous step's view, when the block is also in the previous kept
+ *     list of its (l, h, r): raw K from kcache_prev, V from vview_prev
+ *     (device memory);
+ *   - otherwise kraw_host / vraw_host, read by the kernel directly from
+ *     host memory (which must be pinned and device-accessible, e.g.
+ *     cudaHostAlloc, so that the same address works on the device; on
+ *     GB300 the reads go over NVLink-C2C).
+ * The kernel also writes this step's raw-K cache (kcache[i] = the raw K of
+ * view block i) for the next step.  Callers alternate two sets of
+ * (kcache, vview) buffers between steps; the outputs must not overlap the
+ * previous step's buffers.
+ *   kraw_host, vraw_host  host bf16 [L][H][n_tok][D], page-locked and mapped
+ *                 (cudaHostAlloc / cudaHostRegister); the call translates them
+ *                 with cudaHostGetDevicePointer and returns
+ *                 KVC_ERR_INVALID_ARG for memory that is not
+ *   kept_prev, kept_count_prev  the previous step's kvc_select output, or
+ *                 NULL (first step: every block is a miss)
+ *   kcache_prev, vview_prev, kcache, kview, vview
+ *                 device bf16 [L][H][n_sess][32·budget][D]
+ *   n_hits        device int32 [1], may be NULL: incremented once per
+ *                 (view block, l, h) found in the previous view
+ * Other arguments as kvc_pack_rerope.
+ * Errors: those of kvc_pack_rerope; KVC_ERR_INVALID_ARG if kept_prev is
+ * given without kept_count_prev, kcache_prev or vview_prev.
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
+                           const int32_t *kept_prev, const int32_t *kept_count_prev,
+                           const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
+                           const int32_t *kept, const int32_t *kept_count, int32_t L,
+                           int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
+                           int64_t n_tok, int32_t budget, const float *rope_tab,
+                           kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview, int32_t *n_hits,
+                           int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Dead slot (IntentKV §2 "Layout", §4 check 3): writes K = bf16(−1e4) =
  * −9984 (0xC61C) into every element and V = +0.0 into slot `sentinel` of
  * every layer and head.

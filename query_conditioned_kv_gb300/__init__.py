@@ -21,7 +21,7 @@ __all__ = [
     "kvc_build_meank", "kvc_score_workspace_size", "kvc_score_launches", "kvc_score",
     "kvc_score_static", "SCORE_STATIC_SCRATCH_BYTES",
     "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
-    "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_init_sentinel",
+    "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_pack_tiered", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
     "kvc_recover_score", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
     "TAIL_MAX_TOKENS",
@@ -72,6 +72,8 @@ _SIGS = {
     "kvc_rope_table": (_c.c_int, [_P, _I32, _I32, _I32, _c.c_double, _P]),
     "kvc_pack_rerope": (_c.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P, _I32,
                                    _I64, _I32, _P, _P, _P, _P, _P]),
+    "kvc_pack_tiered": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P,
+                                   _I32, _I64, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "kvc_init_sentinel": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _I32,
                                      _P]),
     "kvc_redirect_free_workspace_size": (_SZ, [_I32, _I32, _I64]),
@@ -210,6 +212,27 @@ def kvc_pack_rerope(kraw, vraw, kept, kept_count, L, H, D, tok_off, n_sess,
                             n_tok, budget, _ptr(rope_tab), _ptr(kview),
                             _ptr(vview), _ptr(dev_status), _stream(stream)),
         "kvc_pack_rerope")
+
+
+def _host_ptr(t):
+    """Address of a pinned host tensor (device-accessible at the same address
+    under unified addressing)."""
+    if not t.is_contiguous():
+        raise ValueError("libkvc takes contiguous row-major tensors only")
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("the host-resident history must be a pinned CPU tensor")
+    return t.data_ptr()
+
+
+def kvc_pack_tiered(kraw_host, vraw_host, kept_prev, kept_count_prev, kcache_prev,
+                    vview_prev, kept, kept_count, L, H, D, tok_off, n_sess, n_tok, budget,
+                    rope_tab, kcache, kview, vview, n_hits=None, dev_status=None, stream=None):
+    _ok(lib.kvc_pack_tiered(_host_ptr(kraw_host), _host_ptr(vraw_host), _ptr(kept_prev),
+                            _ptr(kept_count_prev), _ptr(kcache_prev), _ptr(vview_prev),
+                            _ptr(kept), _ptr(kept_count), L, H, D, _ptr(tok_off), n_sess,
+                            n_tok, budget, _ptr(rope_tab), _ptr(kcache), _ptr(kview),
+                            _ptr(vview), _ptr(n_hits), _ptr(dev_status), _stream(stream)),
+        "kvc_pack_tiered")
 
 
 def kvc_init_sentinel(kpool, vpool, L, H, D, n_slots, sentinel, stream=None):

@@ -178,6 +178,41 @@ kvc_status kvc_pack_rerope(const kvc_bf16 *kraw, const kvc_bf16 *vraw,
                                            dev_status, stream));
 }
 
+kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
+                           const int32_t *kept_prev, const int32_t *kept_count_prev,
+                           const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
+                           const int32_t *kept, const int32_t *kept_count, int32_t L,
+                           int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
+                           int64_t n_tok, int32_t budget, const float *rope_tab,
+                           kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview, int32_t *n_hits,
+                           int32_t *dev_status, cudaStream_t stream) {
+  if (!kraw_host || !vraw_host || !kept || !kept_count || !tok_off || !rope_tab || !kcache ||
+      !kview || !vview)
+    return KVC_ERR_INVALID_ARG;
+  if (kept_prev && (!kept_count_prev || !kcache_prev || !vview_prev)) return KVC_ERR_INVALID_ARG;
+  if (L < 1 || H < 1 || n_sess < 1 || n_tok < 1) return KVC_ERR_INVALID_ARG;
+  if (budget < 1 || budget > 65535) return KVC_ERR_BUDGET;
+  if (!head_dim_ok(D) || n_tok % KVC_BLOCK_TOKENS || (int64_t)L * n_sess > 65535)
+    return KVC_ERR_SHAPE;
+  if (!aligned16(kraw_host) || !aligned16(vraw_host) || !aligned16(rope_tab) ||
+      !aligned16(kcache) || !aligned16(kview) || !aligned16(vview) ||
+      (kcache_prev && !aligned16(kcache_prev)) || (vview_prev && !aligned16(vview_prev)))
+    return KVC_ERR_ALIGN;
+  // the host history must be page-locked and mapped: use its device-side address
+  void *kdev = nullptr, *vdev = nullptr;
+  if (cudaHostGetDevicePointer(&kdev, const_cast<kvc_bf16 *>(kraw_host), 0) != cudaSuccess ||
+      cudaHostGetDevicePointer(&vdev, const_cast<kvc_bf16 *>(vraw_host), 0) != cudaSuccess) {
+    cudaGetLastError();  // clear the query's error
+    return KVC_ERR_INVALID_ARG;
+  }
+  kraw_host = static_cast<const kvc_bf16 *>(kdev);
+  vraw_host = static_cast<const kvc_bf16 *>(vdev);
+  return from_cuda(kvc::launch_pack_tiered(kraw_host, vraw_host, kept_prev, kept_count_prev,
+                                           kcache_prev, vview_prev, kept, kept_count, L, H, D,
+                                           tok_off, n_sess, n_tok, budget, rope_tab, kcache,
+                                           kview, vview, n_hits, dev_status, stream));
+}
+
 kvc_status kvc_init_sentinel(kvc_bf16 *kpool, kvc_bf16 *vpool, int32_t L,
                              int32_t H, int32_t D, int64_t n_slots,
                              int32_t sentinel, cudaStream_t stream) {

@@ -99,6 +99,15 @@ cudaError_t launch_pack_rerope(const uint16_t *kraw, const uint16_t *vraw,
                                uint16_t *vview, int32_t *status,
                                cudaStream_t s);
 
+cudaError_t launch_pack_tiered(const uint16_t *kraw_host, const uint16_t *vraw_host,
+                               const int32_t *kept_prev, const int32_t *kept_count_prev,
+                               const uint16_t *kcache_prev, const uint16_t *vview_prev,
+                               const int32_t *kept, const int32_t *kept_count, int L, int H,
+                               int D, const int64_t *tok_off, int n_sess, int64_t n_tok,
+                               int budget, const float *rope_tab, uint16_t *kcache,
+                               uint16_t *kview, uint16_t *vview, int32_t *n_hits,
+                               int32_t *status, cudaStream_t s);
+
 cudaError_t launch_init_sentinel(uint16_t *kpool, uint16_t *vpool, int L,
                                  int H, int D, int64_t n_slots,
                                  int32_t sentinel, cudaStream_t s);

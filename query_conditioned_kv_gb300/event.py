@@ -3,6 +3,8 @@
 ``MeanKEvent``   score (Mean-K) → select → pack + re-RoPE
 ``SlotMapEvent`` score (QueryMemory) → select → redirect + free
 ``PagedEvent``   LSE-recovery score → select → tail plan → in-place compaction
+``TieredMeanKEvent`` the Mean-K event with the index and the raw history in
+                 host memory: score in bounded layer tiles, select, tiered pack
 
 Both only allocate caller-side buffers with torch and call the library's
 entry points; an event can be captured in a CUDA graph (``capture()``) so
@@ -23,7 +25,8 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_recover_score, kvc_redirect_free,
+from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_recover_score,
+               kvc_redirect_free,
                kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
                kvc_score_qmem, kvc_score_qmem_workspace_size,
                kvc_score_workspace_size, kvc_select, kvc_tail_compact, kvc_tail_plan)
@@ -199,6 +202,83 @@ class MeanKEvent:
 
     def replay(self):
         self.graph.replay()
+
+
+class TieredMeanKEvent(MeanKEvent):
+    """KVMem's tiered execution view ("Tiered movement"): the Mean-K index and
+    the raw K/V history stay in pinned host memory; only the execution view,
+    the scores and this event's scratch live on the GPU.
+
+    score   the index is scored in bounded tiles of `stage_layers` layers:
+            each tile is copied host → device into one of two staging
+            buffers on a copy stream while the previous tile is scored on
+            the current stream (the scorer is the device-resident one, so
+            the scores are the same bit for bit);
+    select  as MeanKEvent;
+    pack    kvc_pack_tiered: blocks that the previous step also kept come
+            from the previous view (raw K from a raw-K cache, V from the V
+            view), the others are read by the kernel from host memory.
+    Two sets of (kept lists, raw-K cache, V view) alternate between steps.
+    """
+
+    def __init__(self, *args, stage_layers: int = 4, **kw):
+        super().__init__(*args, **kw)
+        dev = self.device
+        self.stage_layers = max(1, min(stage_layers, self.L))
+        self.stage = [torch.empty(self.stage_layers, self.H, self.nb_total, self.D,
+                                  dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.kept_sets = [self.kept, torch.empty_like(self.kept)]
+        self.count_sets = [self.kept_count, torch.empty_like(self.kept_count)]
+        self.kcaches = [torch.empty_like(self.kview), torch.empty_like(self.kview)]
+        self.vviews = [self.vview, torch.empty_like(self.vview)]
+        self.n_hits = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.cur, self.steps = 0, 0
+
+    def score_tiered(self, q, meank_host):
+        """Scores of every layer from the host-resident index [L][H][nb][D]."""
+        main = torch.cuda.current_stream(self.device)
+        cs = self.copy_stream
+        cs.wait_stream(main)
+        free = [None, None]
+        for gi, (l0, l1) in enumerate(self._split(self.L, -(-self.L // self.stage_layers))):
+            b = gi % 2
+            n = l1 - l0
+            with torch.cuda.stream(cs):
+                if free[b] is not None:
+                    cs.wait_event(free[b])
+                self.stage[b][:n].copy_(meank_host[l0:l1], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(cs)
+            main.wait_event(ready)
+            kvc_score(q[l0:l1], self.stage[b][:n], self.scores[l0:l1], n, self.H, self.Hq,
+                      self.D, self.W, self.blk_off, self.n_sess, self.nb_total, self.nb_max,
+                      self.ws, self.dev_status, main)
+            free[b] = torch.cuda.Event()
+            free[b].record(main)
+
+    def pack_tiered(self, kraw_host, vraw_host):
+        cur, prev = self.cur, 1 - self.cur
+        first = self.steps == 0
+        kvc_pack_tiered(kraw_host, vraw_host,
+                        None if first else self.kept_sets[prev][:self.L_pack],
+                        None if first else self.count_sets[prev][:self.L_pack],
+                        None if first else self.kcaches[prev],
+                        None if first else self.vviews[prev],
+                        self.kept_sets[cur][:self.L_pack], self.count_sets[cur][:self.L_pack],
+                        self.L_pack, self.H, self.D, self.tok_off, self.n_sess, self.n_tok,
+                        self.budget, self.rope_tab, self.kcaches[cur], self.kview,
+                        self.vviews[cur], self.n_hits, self.dev_status)
+
+    def step(self, q, meank_host, kraw_host, vraw_host):
+        """One agent step; afterwards kview / vview hold this step's view."""
+        cur = self.cur
+        self.kept, self.kept_count = self.kept_sets[cur], self.count_sets[cur]
+        self.vview = self.vviews[cur]
+        self.score_tiered(q, meank_host)
+        self.select()
+        self.pack_tiered(kraw_host, vraw_host)
+        self.cur, self.steps = 1 - cur, self.steps + 1
 
 
 def event_bytes(L: int, H: int, Hq: int, D: int, W: int, nb_total: int, n_sess: int,

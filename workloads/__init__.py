@@ -185,22 +185,25 @@ class MeanKConfig:
                 torch.from_numpy(alpha).to(device)[:, None] * u[None, :]
         return x.to(torch.bfloat16)
 
-    def q_unit(self, r: int, l: int, hq: int, device="cpu") -> torch.Tensor:
+    def q_unit(self, r: int, l: int, hq: int, device="cpu", step: int = 0) -> torch.Tensor:
+        """Query window of agent step `step` (0: the event's window; later
+        steps draw new noise around the same planted directions)."""
+        key = (r, l, hq) if step == 0 else (r, l, hq, step)
         x = torch.randn(self.W, self.D,
-                        generator=_gen(device, self.seed, "q", r, l, hq),
+                        generator=_gen(device, self.seed, "q", *key),
                         device=device, dtype=torch.float32)
         u = torch.from_numpy(self.direction(l, hq // self.G)).to(device)
         return (x + self.gamma * u[None, :]).to(torch.bfloat16)
 
     # --- whole tensors --------------------------------------------------
-    def q(self, device="cpu") -> torch.Tensor:
+    def q(self, device="cpu", step: int = 0) -> torch.Tensor:
         """bf16 [L][n_sess][Hq][W][D] query windows (layer-major)."""
         out = torch.empty(self.L, self.n_sess, self.Hq, self.W, self.D,
                           dtype=torch.bfloat16, device=device)
         for l in range(self.L):
             for r in range(self.n_sess):
                 for hq in range(self.Hq):
-                    out[l, r, hq] = self.q_unit(r, l, hq, device)
+                    out[l, r, hq] = self.q_unit(r, l, hq, device, step)
         return out
 
     def kv_raw(self, device="cpu"):
