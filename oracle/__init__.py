@@ -71,10 +71,13 @@ def lib():
         L.orc_tail_plan.argtypes = [_u32p, c.c_int, _i32p, c.c_int, _i32p, _i32p,
                                     c.POINTER(c.c_int), c.POINTER(c.c_int), _i32p,
                                     c.POINTER(c.c_int), _i32p, _u32p]
+        L.orc_lrfu_update.argtypes = [_f32p, c.c_int, c.c_double, c.c_double, _f32p,
+                                      np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")]
         for name in ("orc_meank", "orc_score_unit", "orc_qmem_update",
                      "orc_rule_session", "orc_select", "orc_rope_f64",
                      "orc_pack_unit", "orc_slot_map", "orc_redirect_free",
-                     "orc_attention_lse", "orc_recover_step", "orc_tail_plan"):
+                     "orc_attention_lse", "orc_recover_step", "orc_tail_plan",
+                     "orc_lrfu_update"):
             getattr(L, name).restype = c.c_int
         _lib = L
     return _lib
@@ -320,3 +323,15 @@ def tail_plan(keepmask, n: int, block_table, BS: int) -> dict:
     return {"src": src[:npairs.value], "dst": dst[:npairs.value], "X": x,
             "freed": freed[:nfreed.value], "new_table": new_table[:x],
             "tail_mask": tail[:(x * BS + 31) // 32]}
+
+
+# ------------------------------------------------------ LRFU keep score
+
+def lrfu_update(scores, ks, p: float = 0.9, lam: float = 0.5):
+    """One LRFU step of one segment: returns (new keep scores fp32, hits bool)."""
+    sc = _c(scores, np.float32)
+    k = np.array(ks, dtype=np.float32, copy=True)
+    hits = np.zeros(len(sc), np.uint8)
+    _check(lib().orc_lrfu_update(sc, len(sc), float(p), float(lam), k, hits),
+           "orc_lrfu_update")
+    return k, hits.astype(bool)

@@ -601,3 +601,61 @@ int orc_tail_plan(const uint32_t *keepmask, int n, const int32_t *block_table, i
   for (int b = 0; b < x; b++) new_table[b] = block_table[Y - x + b];
   return 0;
 }
+
+/* ---------------------------------------------------- LRFU keep score */
+
+struct orc_mass_item {
+  double m;
+  int i;
+};
+
+static int orc_mass_desc(const void *a, const void *b) {
+  const struct orc_mass_item *x = (const struct orc_mass_item *)a;
+  const struct orc_mass_item *y = (const struct orc_mass_item *)b;
+  if (x->m > y->m) return -1;
+  if (x->m < y->m) return 1;
+  return (x->i > y->i) - (x->i < y->i);
+}
+
+/* [ActKV] §5.2 (attention-aware LRFU, Algorithm 1): after an action region
+ * each entry's keep score decays by λ and gains the entry's action-region
+ * attention score when the entry is a hit, a hit being membership of the
+ * top-p set of that region's scores (p = 90% on the page).
+ * Readings (the update's equation is lost on the page):
+ *   KS_t = λ·KS_{t−1} + hit_t·s_t — recency only at λ = 0, an undecayed sum
+ *   (frequency) at λ = 1, the two limits the page describes;
+ *   the top-p set is the shortest prefix of the entries ordered by score
+ *   (descending, lower index first among equal scores) whose score mass
+ *   reaches p·Σ s; an entry with s ≤ 0 or NaN has no mass and is never a hit.
+ * KS is computed in fp64 from the fp32 inputs and rounded once to fp32.
+ *   scores [n];  ks [n] in/out;  hits [n] out (0/1) */
+int orc_lrfu_update(const float *scores, int n, double p, double lambda, float *ks,
+                    uint8_t *hits) {
+  if (!scores || !ks || !hits || n < 0 || !(p >= 0.0 && p <= 1.0) ||
+      !(lambda >= 0.0 && lambda <= 1.0))
+    return 1;
+  struct orc_mass_item *it =
+      (struct orc_mass_item *)malloc(sizeof(struct orc_mass_item) * (size_t)(n > 0 ? n : 1));
+  if (!it) return 3;
+  double total = 0.0;
+  for (int i = 0; i < n; i++) {
+    const double s = (double)scores[i];
+    it[i].m = s > 0.0 ? s : 0.0; /* NaN compares false: no mass */
+    it[i].i = i;
+    total += it[i].m;
+    hits[i] = 0;
+  }
+  qsort(it, (size_t)n, sizeof(struct orc_mass_item), orc_mass_desc);
+  const double target = p * total;
+  double cum = 0.0;
+  for (int k = 0; k < n && cum < target && it[k].m > 0.0; k++) {
+    hits[it[k].i] = 1;
+    cum += it[k].m;
+  }
+  for (int i = 0; i < n; i++) {
+    const double s = (double)scores[i];
+    ks[i] = (float)(lambda * (double)ks[i] + (hits[i] ? (s > 0.0 ? s : 0.0) : 0.0));
+  }
+  free(it);
+  return 0;
+}
