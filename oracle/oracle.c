@@ -626,7 +626,8 @@ static int orc_mass_desc(const void *a, const void *b) {
  *   (frequency) at λ = 1, the two limits the page describes;
  *   the top-p set is the shortest prefix of the entries ordered by score
  *   (descending, lower index first among equal scores) whose score mass
- *   reaches p·Σ s; an entry with s ≤ 0 or NaN has no mass and is never a hit.
+ *   reaches p·Σ s; an entry whose score is not a positive finite number
+ *   (≤ 0, NaN, ±∞) has no mass and is never a hit.
  * KS is computed in fp64 from the fp32 inputs and rounded once to fp32.
  *   scores [n];  ks [n] in/out;  hits [n] out (0/1) */
 int orc_lrfu_update(const float *scores, int n, double p, double lambda, float *ks,
@@ -640,7 +641,7 @@ int orc_lrfu_update(const float *scores, int n, double p, double lambda, float *
   double total = 0.0;
   for (int i = 0; i < n; i++) {
     const double s = (double)scores[i];
-    it[i].m = s > 0.0 ? s : 0.0; /* NaN compares false: no mass */
+    it[i].m = (s > 0.0 && isfinite(s)) ? s : 0.0; /* NaN compares false: no mass */
     it[i].i = i;
     total += it[i].m;
     hits[i] = 0;
@@ -654,7 +655,7 @@ int orc_lrfu_update(const float *scores, int n, double p, double lambda, float *
   }
   for (int i = 0; i < n; i++) {
     const double s = (double)scores[i];
-    ks[i] = (float)(lambda * (double)ks[i] + (hits[i] ? (s > 0.0 ? s : 0.0) : 0.0));
+    ks[i] = (float)(lambda * (double)ks[i] + (hits[i] ? s : 0.0));
   }
   free(it);
   return 0;

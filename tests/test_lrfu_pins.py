@@ -75,10 +75,10 @@ def test_decay_over_two_steps(orc):
 
 
 def test_zero_mass_and_nan_are_never_hits(orc):
-    s = np.array([0.0, -1.0, np.nan, 2.0, 0.0], np.float32)
-    ks, hits = orc.lrfu_update(s, np.ones(5), p=1.0, lam=0.25)
-    assert hits.tolist() == [False, False, False, True, False]
-    assert ks.tolist() == [0.25, 0.25, 0.25, 2.25, 0.25]
+    s = np.array([0.0, -1.0, np.nan, 2.0, 0.0, np.inf], np.float32)
+    ks, hits = orc.lrfu_update(s, np.ones(6), p=1.0, lam=0.25)
+    assert hits.tolist() == [False, False, False, True, False, False]
+    assert ks.tolist() == [0.25, 0.25, 0.25, 2.25, 0.25, 0.25]
     _, hits = orc.lrfu_update(np.zeros(4, np.float32), np.zeros(4), p=0.9, lam=0.5)
     assert not hits.any()
 
