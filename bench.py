@@ -450,8 +450,9 @@ def slot_map_event(args, dev, peak, reps: int = 3):
 
 PAGED_WORKLOAD = ("paged_6k_to_4k: ActKV Table 1 shapes (block size 16, 8 KV heads, d 128), "
                   "36 layers, 32 query heads; r requests of 6144 tokens each compressed to "
-                  "4096; LSE-recovery score of one action token (restart), top-4096 select, "
-                  "tail plan, in-place compaction of K and V")
+                  "4096; LSE-recovery score of one action token (restart), LRFU keep score "
+                  "(top-p 0.9, lambda 0.5), top-4096 select by keep score, tail plan, "
+                  "in-place compaction of K and V")
 
 
 def paged_event(args, dev, peak, reqs=(1, 4, 16, 64), reps: int = 5):
@@ -487,12 +488,13 @@ def paged_event(args, dev, peak, reqs=(1, 4, 16, 64), reps: int = 5):
         cnt = torch.ones(n_req, dtype=torch.int32, device=dev)
         ev = PagedEvent(n_req, cfg.max_blocks, cfg.BS, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
                         cfg.keep, device=dev)
-        stages = {"score": [], "select": [], "plan": [], "compact": []}
+        stages = {"score": [], "lrfu": [], "select": [], "plan": [], "compact": []}
         events, fracs, pairs = [], [], []
         for r in range(args.warmup + reps):
             torch.cuda.synchronize(dev)
             st = {"score": timed(lambda: ev.score(q, lse, kp, bt, seq, cnt)),
-                  "select": timed(lambda: ev.select()),
+                  "lrfu": timed(lambda: ev.lrfu()),
+                  "select": timed(lambda: ev.select(source=ev.keep_score)),
                   "plan": timed(lambda: ev.plan(seq, bt)),
                   "compact": timed(lambda: ev.compact(kp, vp))}
             torch.cuda.synchronize(dev)

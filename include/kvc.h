@@ -421,6 +421,33 @@ kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16
 int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size);
 
 /* ------------------------------------------------------------------------
+ * LRFU keep score (ActKV §5.2, attention-aware LRFU, Algorithm 1): after an
+ * action region, every entry's keep score decays and gains its action-
+ * region attention score when the entry is a hit, so an entry is evicted
+ * only after it has not drawn high attention for a while.  Per segment s
+ * (one request's entries [seg_off[s], seg_off[s+1])):
+ *   hit_i  ⇔ i is in the shortest prefix of the entries ordered by score
+ *            (descending, lower index first among equal scores) whose score
+ *            mass reaches top_p · Σ scores (p = 0.9 on the page);
+ *   keep_score[i] ← fma(lambda, keep_score[i], hit_i ? scores[i] : 0).
+ * lambda = 0 keeps only the latest region (recency), lambda = 1 sums every
+ * region (frequency).  Scores that are not positive finite numbers carry no
+ * mass and never hit (a NaN is recorded as KVC_ERR_NAN).  The masses are
+ * summed in fp64; the boundary entry is exact up to that rounding.
+ *   scores      device fp32 (e.g. kvc_recover_score's state at the end of the
+ *               region)
+ *   seg_off     device int64 [n_seg+1], each segment ≤ max_seg_len
+ *   keep_score  device fp32, same layout as scores, in/out
+ *   hitmask     device uint32 [n_seg][⌈max_seg_len/32⌉] out, may be NULL
+ * Entries with the highest keep scores are then retained with kvc_select.
+ * Errors: KVC_ERR_INVALID_ARG (top_p or lambda outside [0, 1]),
+ * KVC_ERR_SHAPE (max_seg_len > KVC_SELECT_MAX_SEG).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t n_seg,
+                           int32_t max_seg_len, float top_p, float lambda, float *keep_score,
+                           uint32_t *hitmask, int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Conflict-free tail slot plan (ActKV §7.2, Algorithm 4, planning step).
  * Request r holds n = seqused_k[r] tokens in Y = ⌈n/block_size⌉ logical
  * blocks, m of them retained (keep-mask bits).  All retained tokens are

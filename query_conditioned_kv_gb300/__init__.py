@@ -24,6 +24,7 @@ __all__ = [
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_pack_tiered", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
     "kvc_recover_score", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
+    "kvc_lrfu_update",
     "TAIL_MAX_TOKENS",
 ]
 
@@ -82,6 +83,8 @@ _SIGS = {
     "kvc_recover_score": (_c.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _P, _I32,
                                      _I32, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "kvc_recover_tensor_core": (_I32, [_I32, _I32, _I32, _I32]),
+    "kvc_lrfu_update": (_c.c_int, [_P, _P, _I32, _I32, _c.c_float, _c.c_float, _P, _P, _P,
+                                   _P]),
     "kvc_tail_plan": (_c.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I64, _P, _P,
                                  _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvc_tail_compact": (_c.c_int, [_P, _P, _I64, _I32, _I32, _I32, _P, _P, _P,
@@ -282,3 +285,10 @@ def kvc_tail_compact(kpool, vpool, n_slots, L, H, D, src_slot, dst_slot, n_pairs
     _ok(lib.kvc_tail_compact(_ptr(kpool), _ptr(vpool), n_slots, L, H, D, _ptr(src_slot),
                              _ptr(dst_slot), _ptr(n_pairs), pair_cap, n_req,
                              _ptr(dev_status), _stream(stream)), "kvc_tail_compact")
+
+
+def kvc_lrfu_update(scores, seg_off, n_seg, max_seg_len, top_p, lam, keep_score,
+                    hitmask=None, dev_status=None, stream=None):
+    _ok(lib.kvc_lrfu_update(_ptr(scores), _ptr(seg_off), n_seg, max_seg_len, float(top_p),
+                            float(lam), _ptr(keep_score), _ptr(hitmask), _ptr(dev_status),
+                            _stream(stream)), "kvc_lrfu_update")

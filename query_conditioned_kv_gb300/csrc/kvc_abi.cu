@@ -271,6 +271,18 @@ kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16
                                              state, dev_status, stream));
 }
 
+kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t n_seg,
+                           int32_t max_seg_len, float top_p, float lambda, float *keep_score,
+                           uint32_t *hitmask, int32_t *dev_status, cudaStream_t stream) {
+  if (!scores || !seg_off || !keep_score || n_seg < 1 || max_seg_len < 1)
+    return KVC_ERR_INVALID_ARG;
+  if (!(top_p >= 0.f && top_p <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
+    return KVC_ERR_INVALID_ARG;
+  if (max_seg_len > KVC_SELECT_MAX_SEG) return KVC_ERR_SHAPE;
+  return from_cuda(kvc::launch_lrfu(scores, seg_off, n_seg, max_seg_len, top_p, lambda,
+                                    keep_score, hitmask, dev_status, stream));
+}
+
 int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size) {
   return kvc::recover_tc_supported(H, Hq, D, block_size) ? 1 : 0;
 }

@@ -120,6 +120,11 @@ cudaError_t launch_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
                                  int32_t *status, cudaStream_t s);
 size_t redirect_free_ws_bytes(int n_sess, int N, int64_t n_slots);
 
+// ActKV LRFU keep score (lrfu.cu)
+cudaError_t launch_lrfu(const float *scores, const int64_t *seg_off, int n_seg, int max_seg_len,
+                        float p, float lambda, float *ks, uint32_t *hitmask, int32_t *status,
+                        cudaStream_t s);
+
 // ActKV paged primitives (recover.cu)
 bool recover_tc_supported(int H, int Hq, int D, int BS);
 cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint16_t *kpool,

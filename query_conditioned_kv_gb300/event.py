@@ -2,7 +2,8 @@
 
 ``MeanKEvent``   score (Mean-K) → select → pack + re-RoPE
 ``SlotMapEvent`` score (QueryMemory) → select → redirect + free
-``PagedEvent``   LSE-recovery score → select → tail plan → in-place compaction
+``PagedEvent``   LSE-recovery score → LRFU keep score → select → tail plan →
+                 in-place compaction
 ``TieredMeanKEvent`` the Mean-K event with the index and the raw history in
                  host memory: score in bounded layer tiles, select, tiered pack
 
@@ -28,7 +29,7 @@ import torch
 from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_recover_score,
                kvc_redirect_free,
                kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
-               kvc_score_qmem, kvc_score_qmem_workspace_size,
+               kvc_lrfu_update, kvc_score_qmem, kvc_score_qmem_workspace_size,
                kvc_score_workspace_size, kvc_select, kvc_tail_compact, kvc_tail_plan)
 
 
@@ -343,7 +344,8 @@ class SlotMapEvent:
 class PagedEvent:
     """Buffers and calls of an ActKV compression operation on a paged KV
     cache (ActKV §3.3 on the §2 layout): LSE-recovery score of the current
-    action token (§7.1), token-level select of `keep` tokens per request (no
+    action token (§7.1), the LRFU keep score at the end of the action region
+    (§5.2), token-level select of `keep` tokens per request by keep score (no
     forced set), conflict-free tail plan and one-shot in-place compaction
     (§7.2).  All requests have max_blocks·block_size positions; select takes
     each request's whole row as its segment."""
@@ -356,6 +358,7 @@ class PagedEvent:
         self.cap = max_blocks * block_size
         dev = self.device = torch.device(device)
         self.state = torch.zeros(n_req, self.cap, dtype=torch.float32, device=dev)
+        self.keep_score = torch.zeros(n_req, self.cap, dtype=torch.float32, device=dev)
         self.seg_off = _dev_i64(np.arange(n_req + 1) * self.cap, dev)
         self.kept = torch.empty(n_req, keep, dtype=torch.int32, device=dev)
         self.kept_count = torch.empty(n_req, dtype=torch.int32, device=dev)
@@ -377,9 +380,14 @@ class PagedEvent:
                           count, self.n_req, self.L, self.H, self.Hq, self.D, self.BS,
                           self.state, self.dev_status, stream)
 
-    def select(self, stream=None):
-        kvc_select(self.state, self.seg_off, self.n_req, self.cap, self.keep, 0, 0, self.kept,
-                   self.kept_count, self.keepmask, self.dev_status, stream)
+    def lrfu(self, top_p: float = 0.9, lam: float = 0.5, stream=None):
+        kvc_lrfu_update(self.state, self.seg_off, self.n_req, self.cap, top_p, lam,
+                        self.keep_score, None, self.dev_status, stream)
+
+    def select(self, stream=None, source=None):
+        kvc_select(self.state if source is None else source, self.seg_off, self.n_req,
+                   self.cap, self.keep, 0, 0, self.kept, self.kept_count, self.keepmask,
+                   self.dev_status, stream)
 
     def plan(self, seqused, block_table, stream=None):
         kvc_tail_plan(self.keepmask, self.words, seqused, block_table, self.max_blocks,
@@ -391,9 +399,11 @@ class PagedEvent:
         kvc_tail_compact(kpool, vpool, self.n_slots, self.L, self.H, self.D, self.src,
                          self.dst, self.n_pairs, self.cap, self.n_req, self.dev_status, stream)
 
-    def run(self, q, lse, kpool, vpool, block_table, seqused, count, stream=None):
+    def run(self, q, lse, kpool, vpool, block_table, seqused, count, stream=None, lrfu=True):
         self.score(q, lse, kpool, block_table, seqused, count, stream)
-        self.select(stream)
+        if lrfu:
+            self.lrfu(stream=stream)
+        self.select(stream, self.keep_score if lrfu else None)
         self.plan(seqused, block_table, stream)
         self.compact(kpool, vpool, stream)
 
@@ -401,12 +411,14 @@ class PagedEvent:
 def paged_bytes(n_req: int, seq: int, L: int, H: int, Hq: int, D: int, n_pairs: int) -> dict:
     """Bytes an ActKV operation must move through HBM, by stage: every
     visible key row read once, the query token, LSE and the state read and
-    written (score); the scores read (select); the keep mask and block table
+    written (score); the state read and the keep score read and written
+    (lrfu); the keep scores read (select); the keep mask and block table
     (plan); K and V rows of every planned pair read and written once per
     layer (compact)."""
     score = n_req * seq * L * H * D * 2 + n_req * L * Hq * (D * 2 + 4) + n_req * seq * 8
+    lrfu = n_req * seq * 12
     select = n_req * seq * 4
     plan = n_req * (seq // 8 + seq // 4)
     compact = n_pairs * L * 2 * H * D * 2 * 2
-    return {"score": score, "select": select, "plan": plan, "compact": compact,
-            "event": score + select + plan + compact}
+    return {"score": score, "lrfu": lrfu, "select": select, "plan": plan, "compact": compact,
+            "event": score + lrfu + select + plan + compact}

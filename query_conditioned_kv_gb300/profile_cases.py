@@ -20,8 +20,8 @@ of the measured HBM peak.  The qmem case is the QueryMemory rule score on the 64
 workload's shapes (shared 4096-position prefix, page 16), reduced to
 `--sessions` sessions and `--layers` layers.  The paged case is ActKV's
 compression operation at the Table 1 shapes (6K → 4K tokens per request,
-36 layers) on `--sessions` requests: score → select → plan → compaction,
-`--iters` times.
+36 layers) on `--sessions` requests: score → LRFU → select → plan →
+compaction, `--iters` times.
 """
 from __future__ import annotations
 
