@@ -73,11 +73,17 @@ def lib():
                                     c.POINTER(c.c_int), _i32p, _u32p]
         L.orc_lrfu_update.argtypes = [_f32p, c.c_int, c.c_double, c.c_double, _f32p,
                                       np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")]
+        L.orc_token_confidence.argtypes = [_f32p, c.c_int, c.c_int, c.POINTER(c.c_double)]
+        L.orc_conf_trend.argtypes = [_f64p, c.c_int, c.c_int, c.c_int, c.c_double,
+                                     c.POINTER(c.c_double), c.POINTER(c.c_int),
+                                     c.POINTER(c.c_int)]
+        L.orc_adapt_budget.argtypes = [c.c_double, c.c_int, c.c_int, c.c_int]
         for name in ("orc_meank", "orc_score_unit", "orc_qmem_update",
                      "orc_rule_session", "orc_select", "orc_rope_f64",
                      "orc_pack_unit", "orc_slot_map", "orc_redirect_free",
                      "orc_attention_lse", "orc_recover_step", "orc_tail_plan",
-                     "orc_lrfu_update"):
+                     "orc_lrfu_update", "orc_token_confidence", "orc_conf_trend",
+                     "orc_adapt_budget"):
             getattr(L, name).restype = c.c_int
         _lib = L
     return _lib
@@ -335,3 +341,28 @@ def lrfu_update(scores, ks, p: float = 0.9, lam: float = 0.5):
     _check(lib().orc_lrfu_update(sc, len(sc), float(p), float(lam), k, hits),
            "orc_lrfu_update")
     return k, hits.astype(bool)
+
+
+# --------------------------------------------------- confidence monitor
+
+def token_confidence(logits, k: int = 20) -> float:
+    """−mean log-probability of the top-k tokens of one row of logits."""
+    import ctypes as c
+    lg = _c(logits, np.float32)
+    out = c.c_double(0.0)
+    _check(lib().orc_token_confidence(lg, len(lg), k, c.byref(out)), "orc_token_confidence")
+    return out.value
+
+
+def conf_trend(conf, w: int, s: int, b: float):
+    """(slope, n_windows, n_kept) of one trace's confidence sequence."""
+    import ctypes as c
+    cf = _c(conf, np.float64)
+    sl, nw, nk = c.c_double(0.0), c.c_int(0), c.c_int(0)
+    _check(lib().orc_conf_trend(cf, len(cf), w, s, float(b), c.byref(sl), c.byref(nw),
+                                c.byref(nk)), "orc_conf_trend")
+    return sl.value, nw.value, nk.value
+
+
+def adapt_budget(slope: float, budget: int, step: int, max_budget: int) -> int:
+    return int(lib().orc_adapt_budget(float(slope), int(budget), int(step), int(max_budget)))

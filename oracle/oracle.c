@@ -660,3 +660,112 @@ int orc_lrfu_update(const float *scores, int n, double p, double lambda, float *
   free(it);
   return 0;
 }
+
+/* ------------------------------------------------- confidence monitor */
+
+static int orc_f64_desc(const void *a, const void *b) {
+  const double x = *(const double *)a, y = *(const double *)b;
+  return (x < y) - (x > y);
+}
+
+static int orc_f64_asc(const void *a, const void *b) {
+  const double x = *(const double *)a, y = *(const double *)b;
+  return (x > y) - (x < y);
+}
+
+/* [ActKV] §6.1 "Token-level confidence": the negative average
+ * log-probability of the k most probable tokens of the predicted
+ * distribution P = softmax(logits):
+ *   C = −(1/k) Σ_{j ≤ k} log P(j) = LSE − (1/k) Σ_{j ≤ k} logit(j),
+ * with LSE = log Σ_v exp(logit_v).  fp64 throughout.
+ *   logits [V] (fp32);  *conf out */
+int orc_token_confidence(const float *logits, int V, int k, double *conf) {
+  if (!logits || !conf || V < 1 || k < 1 || k > V) return 1;
+  double mx = -INFINITY;
+  for (int v = 0; v < V; v++)
+    if ((double)logits[v] > mx) mx = (double)logits[v];
+  double sum = 0.0;
+  for (int v = 0; v < V; v++) sum += exp((double)logits[v] - mx);
+  const double lse = mx + log(sum);
+  double *sorted = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!sorted) return 3;
+  for (int v = 0; v < V; v++) sorted[v] = (double)logits[v];
+  qsort(sorted, (size_t)V, sizeof(double), orc_f64_desc);
+  double top = 0.0;
+  for (int j = 0; j < k; j++) top += sorted[j] - lse; /* log P(j) */
+  *conf = -top / (double)k;
+  free(sorted);
+  return 0;
+}
+
+/* [ActKV] §6.1 "Trace-level confidence" and "Trend detection".
+ *   R'_m = min{C_i : m·s ≤ i < m·s + w}, m = 0 … ⌊(L − w)/s⌋ (windows of w
+ *          tokens, stride s; no window if L < w);
+ *   Q_b  = the b-th percentile of R' (linear interpolation between the
+ *          order statistics at rank (b/100)·(n − 1), the common definition);
+ *   R    = the entries of R' with value ≤ Q_b, kept at their window index m;
+ *   slope = the least-squares slope of R against m (0 if R has fewer than
+ *          two distinct window indices).
+ * Readings: the percentile's interpolation and the time axis of the fit are
+ * not given on the page; these are the plainest choices.
+ *   conf [L];  *slope, *n_windows, *n_kept out */
+int orc_conf_trend(const double *conf, int L, int w, int s, double b, double *slope,
+                   int *n_windows, int *n_kept) {
+  if (!conf || !slope || !n_windows || !n_kept || L < 0 || w < 1 || s < 1 ||
+      !(b >= 0.0 && b <= 100.0))
+    return 1;
+  *slope = 0.0;
+  *n_windows = 0;
+  *n_kept = 0;
+  if (L < w) return 0;
+  const int n = (L - w) / s + 1;
+  double *rp = (double *)malloc(sizeof(double) * (size_t)n);
+  double *srt = (double *)malloc(sizeof(double) * (size_t)n);
+  if (!rp || !srt) {
+    free(rp);
+    free(srt);
+    return 3;
+  }
+  for (int m = 0; m < n; m++) {
+    double mn = INFINITY;
+    for (int i = m * s; i < m * s + w; i++)
+      if (conf[i] < mn) mn = conf[i];
+    rp[m] = mn;
+    srt[m] = mn;
+  }
+  qsort(srt, (size_t)n, sizeof(double), orc_f64_asc);
+  const double pos = b / 100.0 * (double)(n - 1);
+  const int lo = (int)floor(pos);
+  const int hi = lo + 1 < n ? lo + 1 : lo;
+  const double q = srt[lo] + (pos - (double)lo) * (srt[hi] - srt[lo]);
+  double sx = 0.0, sy = 0.0, sxx = 0.0, sxy = 0.0;
+  int cnt = 0;
+  for (int m = 0; m < n; m++)
+    if (rp[m] <= q) {
+      sx += m;
+      sy += rp[m];
+      sxx += (double)m * m;
+      sxy += (double)m * rp[m];
+      cnt++;
+    }
+  const double den = cnt * sxx - sx * sx;
+  *slope = (cnt >= 2 && den > 0.0) ? (cnt * sxy - sx * sy) / den : 0.0;
+  *n_windows = n;
+  *n_kept = cnt;
+  free(rp);
+  free(srt);
+  return 0;
+}
+
+/* [ActKV] §6.2, Algorithm 2 (confidence-driven adaptive budget): start
+ * small; when the confidence trend is falling (slope < 0) raise the
+ * budget; when it is flat or recovering keep it — it is never lowered.
+ * Reading: the page gives no increment; the budget grows by `step`, capped
+ * at `max_budget`. */
+int orc_adapt_budget(double slope, int budget, int step, int max_budget) {
+  if (slope < 0.0) {
+    const int nb = budget + step;
+    return nb < max_budget ? nb : (budget > max_budget ? budget : max_budget);
+  }
+  return budget;
+}
