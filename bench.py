@@ -18,7 +18,8 @@ and so is ActKV's paged compression operation (LSE-recovery score → select →
 tail plan → in-place compaction) at 1, 4, 16 and 64 requests of 6K → 4K
 tokens (`actkv_event`; `--no-paged` skips it), and KVMem's tiered view with the
 index and raw history in host memory, cold and warm steps (`tiered_event`;
-`--no-tiered` skips it).
+`--no-tiered` skips it), and ActKV's confidence monitor (`confidence_monitor`;
+`--no-confidence` skips it).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -638,6 +639,61 @@ def tiered_event(args, dev, peak, reps: int = 3):
     return out
 
 
+# -------------------------------------------------- confidence monitor
+
+def confidence_monitor(args, dev, peak, reps: int = 10):
+    """ActKV's confidence monitor: token confidence of one decode step (64
+    rows of 151936 fp32 logits, top-20) and the trace trend + budget update
+    over 64 traces of 8192 token confidences (window 128, stride 32, bottom
+    10%).  CUDA events on the current stream, median of `reps`, L2 flushed
+    before each logits rep (the rows are 39 MB, under the L2 size)."""
+    import torch
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+
+    cfg = W.ConfidenceConfig()
+    lg = cfg.logits(dev)
+    tr = cfg.traces(dev)
+    conf = torch.empty(cfg.n_req, dtype=torch.float32, device=dev)
+    off = torch.arange(cfg.n_req + 1, dtype=torch.int64, device=dev) * cfg.trace_len
+    slope = torch.empty(cfg.n_req, dtype=torch.float64, device=dev)
+    budget = torch.empty(cfg.n_req, dtype=torch.int32, device=dev)
+    kept = torch.empty(cfg.n_req, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    t_conf, t_trend = [], []
+    for r in range(args.warmup + reps):
+        flush.fill_(r & 255)
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        budget.fill_(cfg.budget0)
+        a.record()
+        kvc.kvc_token_confidence(lg, cfg.n_req, cfg.vocab, cfg.top_k, conf, st)
+        b.record()
+        kvc.kvc_conf_trend_budget(tr, off, cfg.n_req, cfg.trace_len, cfg.window, cfg.stride,
+                                  cfg.bottom_pct, cfg.budget_step, cfg.max_budget, slope, budget,
+                                  kept, st)
+        c.record()
+        torch.cuda.synchronize(dev)
+        if r >= args.warmup:
+            t_conf.append(a.elapsed_time(b))
+            t_trend.append(b.elapsed_time(c))
+    if kvc.kvc_device_status(st) != 0:
+        raise RuntimeError("device status error in the confidence monitor")
+    ms_c, ms_t = statistics.median(t_conf), statistics.median(t_trend)
+    lg_bytes = lg.numel() * 4
+    raised = int((budget > cfg.budget0).sum().item())
+    del lg, tr, flush
+    torch.cuda.empty_cache()
+    return {"workload": f"{cfg.name}: {cfg.n_req} rows of {cfg.vocab} fp32 logits, top-{cfg.top_k}; "
+                        f"{cfg.n_req} traces of {cfg.trace_len} confidences (w {cfg.window}, "
+                        f"s {cfg.stride}, bottom {cfg.bottom_pct}%)",
+            "token_confidence_ms": round(ms_c, 4),
+            "token_confidence_rows_per_s": cfg.n_req / (ms_c * 1e-3),
+            "logits_gbs": lg_bytes / (ms_c * 1e-3) / 1e9,
+            "logits_frac_of_hbm": lg_bytes / (ms_c * 1e-3) / 1e9 / peak,
+            "trend_budget_ms": round(ms_t, 4), "budgets_raised": raised}
+
+
 # ------------------------------------------------------------ oracle arm
 
 def _oracle_sample(n_units, dev):
@@ -733,6 +789,8 @@ def main():
                     help="skip the QueryMemory (slot-map) event measurement")
     ap.add_argument("--no-tiered", action="store_true",
                     help="skip the host-resident (tiered) event measurement")
+    ap.add_argument("--no-confidence", action="store_true",
+                    help="skip the confidence-monitor measurement")
     ap.add_argument("--no-paged", action="store_true",
                     help="skip the ActKV paged-operation measurement")
     ap.add_argument("--groups", type=int, default=None,
@@ -770,6 +828,10 @@ def main():
         import torch
         torch.cuda.empty_cache()
         line["actkv_event"] = paged_event(args, torch.device("cuda", local_rank), peaks()[0])
+    if not args.no_confidence:
+        import torch
+        line["confidence_monitor"] = confidence_monitor(args, torch.device("cuda", local_rank),
+                                                        peaks()[0])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -448,6 +448,48 @@ kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t 
                            uint32_t *hitmask, int32_t *dev_status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Confidence monitor (ActKV §6.1): token-level confidence of each predicted
+ * distribution, the negative average log-probability of its top-k tokens,
+ *   conf[t] = −(1/k) Σ_{j ≤ k} log P_t(j) = LSE_t − (1/k) Σ_{j ≤ k} logit_t(j)
+ * (P_t = softmax of row t; ties at the k-th logit count once per copy).
+ *   logits  device fp32 [n_tok][V]  (the model's output rows)
+ *   conf    device fp32 [n_tok] out
+ * fp32 arithmetic (LSE from per-thread online max/sum merged in a fixed
+ * order); the top-k set is exact.  A NaN logit is recorded as KVC_ERR_NAN.
+ * Errors: KVC_ERR_INVALID_ARG (sizes, top_k > V).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_token_confidence(const float *logits, int32_t n_tok, int32_t V, int32_t top_k,
+                                float *conf, int32_t *dev_status, cudaStream_t stream);
+
+/* Largest number of windows kvc_conf_trend_budget takes per trace. */
+#define KVC_CONF_MAX_WINDOWS 8192
+
+/* ------------------------------------------------------------------------
+ * Trace confidence, trend and adaptive budget (ActKV §6.1 "Trace-level
+ * confidence", "Trend detection"; §6.2 Algorithm 2).  For each trace t (one
+ * request's token confidences conf[trace_off[t] … trace_off[t+1])):
+ *   R'_m   = min of the window [m·stride, m·stride + window), m = 0 …
+ *            ⌊(L − window)/stride⌋ (no window if L < window);
+ *   Q      = the bottom_pct-th percentile of R' (linear interpolation between
+ *            the order statistics at rank bottom_pct/100·(n − 1));
+ *   slope[t] = least-squares slope of the windows with R'_m ≤ Q against m
+ *            (fp64; 0 with fewer than two such windows); n_kept[t] = their
+ *            number;
+ *   budget[t] ← min(budget[t] + budget_step, max_budget) if slope < 0, else
+ *            unchanged — the budget starts small and is never lowered.
+ *   conf       device fp32; trace_off device int64 [n_trace+1]
+ *   slope      device fp64 [n_trace] out; budget device int32 [n_trace]
+ *              in/out; n_kept device int32 [n_trace] out
+ * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (more than KVC_CONF_MAX_WINDOWS
+ * windows), KVC_ERR_ALIGN (slope not 8-byte aligned).
+ * ---------------------------------------------------------------------- */
+kvc_status kvc_conf_trend_budget(const float *conf, const int64_t *trace_off, int32_t n_trace,
+                                 int32_t max_trace_len, int32_t window, int32_t stride,
+                                 float bottom_pct, int32_t budget_step, int32_t max_budget,
+                                 double *slope, int32_t *budget, int32_t *n_kept,
+                                 int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Conflict-free tail slot plan (ActKV §7.2, Algorithm 4, planning step).
  * Request r holds n = seqused_k[r] tokens in Y = ⌈n/block_size⌉ logical
  * blocks, m of them retained (keep-mask bits).  All retained tokens are

@@ -24,7 +24,7 @@ __all__ = [
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_pack_tiered", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
     "kvc_recover_score", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
-    "kvc_lrfu_update",
+    "kvc_lrfu_update", "kvc_token_confidence", "kvc_conf_trend_budget",
     "TAIL_MAX_TOKENS",
 ]
 
@@ -83,6 +83,9 @@ _SIGS = {
     "kvc_recover_score": (_c.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _P, _I32,
                                      _I32, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "kvc_recover_tensor_core": (_I32, [_I32, _I32, _I32, _I32]),
+    "kvc_token_confidence": (_c.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
+    "kvc_conf_trend_budget": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _c.c_float, _I32,
+                                         _I32, _P, _P, _P, _P, _P]),
     "kvc_lrfu_update": (_c.c_int, [_P, _P, _I32, _I32, _c.c_float, _c.c_float, _P, _P, _P,
                                    _P]),
     "kvc_tail_plan": (_c.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I64, _P, _P,
@@ -292,3 +295,17 @@ def kvc_lrfu_update(scores, seg_off, n_seg, max_seg_len, top_p, lam, keep_score,
     _ok(lib.kvc_lrfu_update(_ptr(scores), _ptr(seg_off), n_seg, max_seg_len, float(top_p),
                             float(lam), _ptr(keep_score), _ptr(hitmask), _ptr(dev_status),
                             _stream(stream)), "kvc_lrfu_update")
+
+
+def kvc_token_confidence(logits, n_tok, V, top_k, conf, dev_status=None, stream=None):
+    _ok(lib.kvc_token_confidence(_ptr(logits), n_tok, V, top_k, _ptr(conf), _ptr(dev_status),
+                                 _stream(stream)), "kvc_token_confidence")
+
+
+def kvc_conf_trend_budget(conf, trace_off, n_trace, max_trace_len, window, stride, bottom_pct,
+                          budget_step, max_budget, slope, budget, n_kept, dev_status=None,
+                          stream=None):
+    _ok(lib.kvc_conf_trend_budget(_ptr(conf), _ptr(trace_off), n_trace, max_trace_len, window,
+                                  stride, float(bottom_pct), budget_step, max_budget,
+                                  _ptr(slope), _ptr(budget), _ptr(n_kept), _ptr(dev_status),
+                                  _stream(stream)), "kvc_conf_trend_budget")

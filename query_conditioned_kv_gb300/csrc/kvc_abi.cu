@@ -283,6 +283,33 @@ kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t 
                                     keep_score, hitmask, dev_status, stream));
 }
 
+kvc_status kvc_token_confidence(const float *logits, int32_t n_tok, int32_t V, int32_t top_k,
+                                float *conf, int32_t *dev_status, cudaStream_t stream) {
+  if (!logits || !conf || n_tok < 1 || V < 1 || top_k < 1 || top_k > V)
+    return KVC_ERR_INVALID_ARG;
+  if (n_tok > INT32_MAX / 2) return KVC_ERR_SHAPE;
+  return from_cuda(kvc::launch_token_confidence(logits, n_tok, V, top_k, conf, dev_status,
+                                                stream));
+}
+
+kvc_status kvc_conf_trend_budget(const float *conf, const int64_t *trace_off, int32_t n_trace,
+                                 int32_t max_trace_len, int32_t window, int32_t stride,
+                                 float bottom_pct, int32_t budget_step, int32_t max_budget,
+                                 double *slope, int32_t *budget, int32_t *n_kept,
+                                 int32_t *dev_status, cudaStream_t stream) {
+  if (!conf || !trace_off || !slope || !budget || !n_kept || n_trace < 1 || max_trace_len < 1 ||
+      window < 1 || stride < 1 || budget_step < 0 || max_budget < 1)
+    return KVC_ERR_INVALID_ARG;
+  if (!(bottom_pct >= 0.f && bottom_pct <= 100.f)) return KVC_ERR_INVALID_ARG;
+  if (max_trace_len >= window &&
+      (max_trace_len - window) / stride + 1 > kvc::conf_trend_max_windows())
+    return KVC_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(slope) & 7u) return KVC_ERR_ALIGN;
+  return from_cuda(kvc::launch_conf_trend(conf, trace_off, n_trace, max_trace_len, window,
+                                          stride, bottom_pct, budget_step, max_budget, slope,
+                                          budget, n_kept, dev_status, stream));
+}
+
 int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size) {
   return kvc::recover_tc_supported(H, Hq, D, block_size) ? 1 : 0;
 }

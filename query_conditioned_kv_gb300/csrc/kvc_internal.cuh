@@ -125,6 +125,15 @@ cudaError_t launch_lrfu(const float *scores, const int64_t *seg_off, int n_seg, 
                         float p, float lambda, float *ks, uint32_t *hitmask, int32_t *status,
                         cudaStream_t s);
 
+// ActKV confidence monitor (confidence.cu)
+cudaError_t launch_token_confidence(const float *logits, int n_tok, int V, int k, float *conf,
+                                    int32_t *status, cudaStream_t s);
+cudaError_t launch_conf_trend(const float *conf, const int64_t *trace_off, int n_trace,
+                              int max_len, int w, int stride, float b, int step, int max_budget,
+                              double *slope, int32_t *budget, int32_t *n_kept, int32_t *status,
+                              cudaStream_t s);
+int conf_trend_max_windows();
+
 // ActKV paged primitives (recover.cu)
 bool recover_tc_supported(int H, int Hq, int D, int BS);
 cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint16_t *kpool,

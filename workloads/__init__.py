@@ -58,7 +58,8 @@ def _mix(*parts: int) -> int:
 
 
 _TAGS = {"u": 1, "plant": 2, "k": 3, "v": 4, "q": 5, "mk": 6, "hist": 7,
-         "qturn": 8, "pages": 9, "kpool": 10, "vpool": 11, "lse": 12, "keep": 13}
+         "qturn": 8, "pages": 9, "kpool": 10, "vpool": 11, "lse": 12, "keep": 13,
+         "logits": 14, "conftrace": 15}
 
 
 def _gen(device, seed: int, tag: str, *idx: int) -> torch.Generator:
@@ -503,6 +504,47 @@ def config_paged(n_req: int = 64) -> PagedConfig:
     concurrent requests, each compressed from 6K to 4K entries; 8B-class
     depth (36 layers, 32 query heads)."""
     return PagedConfig(name=f"paged_r{n_req}_6k_to_4k", n_req=n_req, seq=6144, keep=4096)
+
+
+# ------------------------------------------------- confidence monitor
+
+@dataclasses.dataclass
+class ConfidenceConfig:
+    """ActKV's confidence monitor on one decode step of n_req requests (one
+    row of logits each, Qwen-class vocabulary), and the trend over each
+    request's trace of token confidences."""
+    name: str = "conf_64x151936"
+    n_req: int = 64
+    vocab: int = 151936
+    top_k: int = 20
+    trace_len: int = 8192
+    window: int = 128
+    stride: int = 32
+    bottom_pct: float = 10.0
+    budget0: int = 1024
+    budget_step: int = 256
+    max_budget: int = 8192
+    seed: int = 6
+
+    def logits(self, device="cpu") -> torch.Tensor:
+        """fp32 [n_req][vocab]: N(0, 2²) logits, plus per row a few tokens
+        lifted by U(4, 12) (a peaked head, as sampled text has)."""
+        g = _gen(device, self.seed, "logits")
+        x = torch.randn(self.n_req, self.vocab, generator=g, device=device) * 2.0
+        rng = _np_rng(self.seed, "logits", 1)
+        for r in range(self.n_req):
+            idx = torch.from_numpy(rng.choice(self.vocab, 8, replace=False)).to(device)
+            x[r, idx] += torch.from_numpy(rng.uniform(4, 12, 8).astype(np.float32)).to(device)
+        return x.contiguous()
+
+    def traces(self, device="cpu") -> torch.Tensor:
+        """fp32 [n_req][trace_len] token confidences: noise around a level
+        with a seeded drift per request (half of them falling)."""
+        rng = _np_rng(self.seed, "conftrace")
+        t = np.linspace(0.0, 1.0, self.trace_len)
+        rows = [rng.normal(12.0, 0.6, self.trace_len) - rng.normal(0.0, 1.0) * t
+                for _ in range(self.n_req)]
+        return torch.from_numpy(np.stack(rows).astype(np.float32)).to(device)
 
 
 # ---------------------------------------------------------------- helpers
