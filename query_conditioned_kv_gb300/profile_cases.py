@@ -6,6 +6,7 @@ event once to produce realistic inputs for the stage, then launches the stage
 `--iters` times.
 
   python -m query_conditioned_kv_gb300.profile_cases score --layers 16 --iters 3
+  python -m query_conditioned_kv_gb300.profile_cases score --config 27b --layers 2 --iters 3
   python -m query_conditioned_kv_gb300.profile_cases pack  --layers 4  --iters 3
   python -m query_conditioned_kv_gb300.profile_cases select --layers 16 --iters 3
   python -m query_conditioned_kv_gb300.profile_cases meank  --layers 2  --iters 3
@@ -58,7 +59,11 @@ def main(argv=None) -> None:
     if args.case == "paged":
         _paged_case(args, dev)
         return
-    cfg = W.scaled(W.config_8b(), L=args.layers)
+    base = {"8b": W.config_8b, "27b": W.config_27b, "tiny": W.config_tiny,
+            "ragged": W.config_ragged}[args.config]()
+    if args.config in ("27b", "ragged") and args.case not in ("score", "select"):
+        raise SystemExit("the 27b and ragged configs profile the score and select cases only")
+    cfg = W.scaled(base, L=args.layers, L_pack=None)
     q = cfg.q(dev)
     meank = torch.empty(cfg.L, cfg.H, cfg.nb_total, cfg.D, dtype=torch.bfloat16, device=dev)
     if args.case == "meank":
@@ -73,9 +78,11 @@ def main(argv=None) -> None:
         kvc.kvc_build_meank(kraw, meank, cfg.L, cfg.H, cfg.D, cfg.n_tok)
     else:
         # score/select only need the index: draw it directly (same distribution)
+        boff = cfg.blk_off()
         for l in range(cfg.L):
             for h in range(cfg.H):
-                meank[l, h] = cfg.meank_direct_unit(l, h, 0, dev)
+                for r in range(cfg.n_sess):
+                    meank[l, h, boff[r]:boff[r + 1]] = cfg.meank_direct_unit(l, h, r, dev)
         kraw = vraw = None
     ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
                     cfg.n_recent, theta=cfg.theta, device=dev)
