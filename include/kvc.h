@@ -405,17 +405,25 @@ kvc_status kvc_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
  * Shapes with H = 8, block_size = 16, G ∈ {2, 4, 8} run on the tensor cores
  * (one 128-row page tile per MMA, brought in by TMA from the block table);
  * any other shape runs on a CUDA-core kernel (kvc_recover_tensor_core tells
- * which).  A visible position whose block id is outside the pool, or a
+ * which).  ws is optional scratch (NULL, or ws_bytes from
+ * kvc_recover_score_workspace_size): when a few requests' pages cannot fill
+ * the GPU, the tensor-core path then splits the layers into groups, writes
+ * each group's partial sums to ws and adds them in group order in a second
+ * kernel (the result is deterministic either way; without ws, or when the
+ * size query returns 0, one kernel and no scratch).  A visible position whose block id is outside the pool, or a
  * seqused_k outside [0, max_blocks·block_size], is recorded as
  * KVC_ERR_BOUNDS: the page scores 0 (the request is skipped).
  * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D ∉ {64,128}, Hq % H,
  * Hq > 256, block_size > 64), KVC_ERR_ALIGN (q, kpool, lse, state).
  * ---------------------------------------------------------------------- */
+size_t kvc_recover_score_workspace_size(int32_t n_req, int32_t max_blocks, int32_t L, int32_t H,
+                                        int32_t Hq, int32_t D, int32_t block_size);
 kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
                              int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
                              const int32_t *seqused_k, const int32_t *count, int32_t n_req,
                              int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
-                             float *state, int32_t *dev_status, cudaStream_t stream);
+                             float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
+                             cudaStream_t stream);
 
 /* 1 if kvc_recover_score runs these sizes on the tensor cores, else 0. */
 int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size);

@@ -23,7 +23,7 @@ __all__ = [
     "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_pack_tiered", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
-    "kvc_recover_score", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
+    "kvc_recover_score", "kvc_recover_score_workspace_size", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
     "kvc_lrfu_update", "kvc_token_confidence", "kvc_conf_trend_budget",
     "TAIL_MAX_TOKENS",
 ]
@@ -80,8 +80,9 @@ _SIGS = {
     "kvc_redirect_free_workspace_size": (_SZ, [_I32, _I32, _I64]),
     "kvc_redirect_free": (_c.c_int, [_P, _P, _I32, _I32, _P, _I64, _I32, _I32,
                                      _P, _I32, _P, _P, _SZ, _P, _P]),
+    "kvc_recover_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "kvc_recover_score": (_c.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _P, _I32,
-                                     _I32, _I32, _I32, _I32, _I32, _P, _P, _P]),
+                                     _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "kvc_recover_tensor_core": (_I32, [_I32, _I32, _I32, _I32]),
     "kvc_token_confidence": (_c.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "kvc_conf_trend_budget": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _c.c_float, _I32,
@@ -260,12 +261,18 @@ def kvc_redirect_free(slot_map, keepmask, n_sess, N, refcnt, n_slots,
                               _stream(stream)), "kvc_redirect_free")
 
 
+def kvc_recover_score_workspace_size(n_req, max_blocks, L, H, Hq, D, block_size) -> int:
+    return int(lib.kvc_recover_score_workspace_size(n_req, max_blocks, L, H, Hq, D, block_size))
+
+
 def kvc_recover_score(q, lse, kpool, n_slots, block_table, max_blocks, seqused_k, count,
-                      n_req, L, H, Hq, D, block_size, state, dev_status=None, stream=None):
+                      n_req, L, H, Hq, D, block_size, state, ws=None, dev_status=None,
+                      stream=None):
     _ok(lib.kvc_recover_score(_ptr(q), _ptr(lse), _ptr(kpool), n_slots, _ptr(block_table),
                               max_blocks, _ptr(seqused_k), _ptr(count), n_req, L, H, Hq, D,
-                              block_size, _ptr(state), _ptr(dev_status), _stream(stream)),
-        "kvc_recover_score")
+                              block_size, _ptr(state), _ptr(ws),
+                              0 if ws is None else ws.numel() * ws.element_size(),
+                              _ptr(dev_status), _stream(stream)), "kvc_recover_score")
 
 
 def kvc_recover_tensor_core(H, Hq, D, block_size) -> bool:

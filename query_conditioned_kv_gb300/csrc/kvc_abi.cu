@@ -250,11 +250,19 @@ kvc_status kvc_redirect_free(int32_t *slot_map, const uint32_t *keepmask,
                                              ws, dev_status, stream));
 }
 
+size_t kvc_recover_score_workspace_size(int32_t n_req, int32_t max_blocks, int32_t L, int32_t H,
+                                        int32_t Hq, int32_t D, int32_t block_size) {
+  if (n_req < 1 || max_blocks < 1 || L < 1 || H < 1 || Hq < H || Hq % H || block_size < 1)
+    return 0;
+  return kvc::recover_ws_bytes(n_req, max_blocks, block_size, L, H, Hq, D);
+}
+
 kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
                              int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
                              const int32_t *seqused_k, const int32_t *count, int32_t n_req,
                              int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
-                             float *state, int32_t *dev_status, cudaStream_t stream) {
+                             float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
+                             cudaStream_t stream) {
   if (!q || !lse || !kpool || !block_table || !seqused_k || !count || !state)
     return KVC_ERR_INVALID_ARG;
   if (n_req < 1 || L < 1 || H < 1 || Hq < 1 || block_size < 1 || max_blocks < 1 ||
@@ -264,11 +272,12 @@ kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16
       (int64_t)block_size * H > 4096 || (int64_t)max_blocks * block_size > INT32_MAX ||
       (int64_t)n_req * max_blocks > INT32_MAX || (int64_t)n_req * L * Hq > INT32_MAX)
     return KVC_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(kpool) || !aligned16(lse) || !aligned16(state))
+  if (!aligned16(q) || !aligned16(kpool) || !aligned16(lse) || !aligned16(state) ||
+      (ws && !aligned16(ws)))
     return KVC_ERR_ALIGN;
   return from_cuda(kvc::launch_recover_score(q, lse, kpool, n_slots, block_table, max_blocks,
                                              seqused_k, count, n_req, L, H, Hq, D, block_size,
-                                             state, dev_status, stream));
+                                             state, ws, ws ? ws_bytes : 0, dev_status, stream));
 }
 
 kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t n_seg,

@@ -136,11 +136,12 @@ int conf_trend_max_windows();
 
 // ActKV paged primitives (recover.cu)
 bool recover_tc_supported(int H, int Hq, int D, int BS);
+size_t recover_ws_bytes(int n_req, int max_blocks, int BS, int L, int H, int Hq, int D);
 cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint16_t *kpool,
                                  int64_t n_slots, const int32_t *block_table, int max_blocks,
                                  const int32_t *seqused, const int32_t *count, int n_req, int L,
-                                 int H, int Hq, int D, int BS, float *state, int32_t *status,
-                                 cudaStream_t s);
+                                 int H, int Hq, int D, int BS, float *state, void *ws,
+                                 size_t ws_bytes, int32_t *status, cudaStream_t s);
 cudaError_t launch_tail_plan(const uint32_t *keepmask, int mask_words, const int32_t *seqused,
                              const int32_t *block_table, int max_blocks, int n_req, int BS,
                              int64_t n_slots, int32_t *src, int32_t *dst, int32_t *n_pairs,

@@ -54,14 +54,16 @@ struct RecArgs {
   int32_t *status;
   int n_req, L, H, Hq, G, D, BS, max_blocks;
   int P;         // pages per work item
-  int n_chunks;  // items per request = ⌈max_blocks / P⌉
+  int n_chunks;  // page chunks per request = ⌈max_blocks / P⌉
+  int n_lg;      // layer groups per chunk (> 1: partial sums, then a finalize)
+  float *partial;  // [n_lg][n_req][max_blocks·BS] when n_lg > 1
   int64_t n_slots;
   float zscale;  // log2(e)/√D
   uint32_t idesc;
 };
 
 struct Item {
-  int r, j0, seq, cnt;
+  int r, j0, seq, cnt, lg, l0, l1;
   uint32_t mask;  // bit jj: page j0 + jj is visible and maps to a valid block
   bool active;    // request generating an action token, sizes valid
 };
@@ -71,8 +73,12 @@ struct Item {
 // tiles exist.  Only the caller passing `record` reports bad inputs.
 __device__ __forceinline__ Item item_info(const RecArgs &a, int item, bool record) {
   Item it;
-  it.r = item / a.n_chunks;
-  it.j0 = (item - it.r * a.n_chunks) * a.P;
+  it.lg = item % a.n_lg;
+  const int rest = item / a.n_lg;
+  it.r = rest / a.n_chunks;
+  it.j0 = (rest - it.r * a.n_chunks) * a.P;
+  it.l0 = it.lg * a.L / a.n_lg;
+  it.l1 = (it.lg + 1) * a.L / a.n_lg;
   it.seq = a.seqused[it.r];
   it.cnt = a.count[it.r];
   it.mask = 0u;
@@ -154,7 +160,7 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
   const int KB = a.D / 64;
   RecSmem sm(smem_raw, NS, KB, NCOL);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = a.n_req * a.n_chunks;
+  const int n_items = a.n_req * a.n_chunks * a.n_lg;
   const uint32_t tile_bytes = (uint32_t)KB * 16384u;
   const uint32_t q_bytes = (uint32_t)(KB * NCOL * 128);
 
@@ -189,7 +195,7 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         const Item it = item_info(a, item, true);
         if (!it.active || !it.mask) continue;
         const int32_t *bt = a.block_table + (int64_t)it.r * a.max_blocks + it.j0;
-        for (int l = 0; l < a.L && ok; l++) {
+        for (int l = it.l0; l < it.l1 && ok; l++) {
           const int qb = qi % kRecQB;
           if (!(ok = mbar_wait_bounded(smem_u32(sm.qempty + qb), ((qi / kRecQB) & 1) ^ 1,
                                        sm.failed)))
@@ -226,7 +232,7 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const Item it = item_info(a, item, false);
         if (!it.active || !it.mask) continue;
-        for (int l = 0; l < a.L && ok; l++) {
+        for (int l = it.l0; l < it.l1 && ok; l++) {
           const int qb = qi % kRecQB;
           if (!(ok = mbar_wait_bounded(smem_u32(sm.qfull + qb), (qi / kRecQB) & 1, sm.failed)))
             break;
@@ -279,7 +285,7 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
       for (int jj = 0; jj < kRecPmax; jj++) xacc[jj] = 0.f;
       if (it.mask) {
         const float *lse_r = a.lse + (int64_t)it.r * a.L * NCOL + h * G;
-        for (int l = 0; l < a.L && ok; l++) {
+        for (int l = it.l0; l < it.l1 && ok; l++) {
           float l2[G];
 #pragma unroll
           for (int g = 0; g < G; g++) l2[g] = __ldg(lse_r + l * NCOL + g) * kLog2eR;
@@ -326,7 +332,10 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         const int p = (it.j0 + jj) * BS + s_;
         if (h == 0) {
           const float xf = (((it.mask >> jj) & 1u) && p < it.seq) ? x : 0.f;
-          update_state(a.state + (int64_t)it.r * cap + p, xf, it.cnt);
+          if (a.n_lg == 1)
+            update_state(a.state + (int64_t)it.r * cap + p, xf, it.cnt);
+          else
+            a.partial[((int64_t)it.lg * a.n_req + it.r) * cap + p] = xf;
         }
       }
     }
@@ -360,6 +369,21 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     tc_fence_after();
     free_tmem_cols(tmem, tmem_cols);
   }
+}
+
+// The layer groups' partial sums, added in group order, then the state.
+__global__ void __launch_bounds__(256)
+k_recover_finalize(RecArgs a) {
+  const int cap = a.max_blocks * a.BS;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)a.n_req * cap) return;
+  const int r = (int)(i / cap), p = (int)(i - (int64_t)r * cap);
+  const int cnt = a.count[r], seq = a.seqused[r];
+  if (cnt < 1 || seq < 0 || seq > cap) return;  // skipped (a bad length was recorded)
+  float x = 0.f;
+  if (p < seq)
+    for (int g = 0; g < a.n_lg; g++) x += a.partial[((int64_t)g * a.n_req + r) * cap + p];
+  update_state(a.state + i, x, cnt);
 }
 
 // ------------------------------------------------- CUDA-core kernel
@@ -660,11 +684,32 @@ bool recover_tc_supported(int H, int Hq, int D, int BS) {
          (D == 64 || D == 128);
 }
 
+// Work items per CTA that keep the persistent grid balanced.
+constexpr int kRecItemsPerCta = 16;
+
+// Layer groups of a launch (with a workspace): items keep kRecPmax pages,
+// so the query rows of a layer are loaded once per kRecPmax page tiles, and
+// the layers are split until there are kRecItemsPerCta items per SM (at most
+// one layer per item).  1 when the requests' pages already give that many.
+int recover_layer_groups(int n_req, int max_blocks, int BS, int L, int H, int Hq, int D) {
+  if (!recover_tc_supported(H, Hq, D, BS) || force_cc()) return 1;
+  const int64_t items = (int64_t)n_req * ((max_blocks + kRecPmax - 1) / kRecPmax);
+  const int64_t want = (int64_t)kRecItemsPerCta * sm_count();
+  if (items >= want) return 1;
+  const int64_t n = (want + items - 1) / items;
+  return n > L ? L : (int)n;
+}
+
+size_t recover_ws_bytes(int n_req, int max_blocks, int BS, int L, int H, int Hq, int D) {
+  const int n_lg = recover_layer_groups(n_req, max_blocks, BS, L, H, Hq, D);
+  return n_lg > 1 ? (size_t)n_lg * n_req * max_blocks * BS * sizeof(float) : 0;
+}
+
 cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint16_t *kpool,
                                  int64_t n_slots, const int32_t *block_table, int max_blocks,
                                  const int32_t *seqused, const int32_t *count, int n_req, int L,
-                                 int H, int Hq, int D, int BS, float *state, int32_t *status,
-                                 cudaStream_t s) {
+                                 int H, int Hq, int D, int BS, float *state, void *ws,
+                                 size_t ws_bytes, int32_t *status, cudaStream_t s) {
   RecArgs a{};
   a.q = q;
   a.kpool = kpool;
@@ -687,6 +732,8 @@ cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint
   const int n_sm = sm_count();
   const bool tc_path = recover_tc_supported(H, Hq, D, BS) && !force_cc() &&
                        (int64_t)L * n_slots * H < INT32_MAX;
+  a.n_lg = 1;
+  a.partial = nullptr;
   if (!tc_path) {
     a.P = 1;
     a.n_chunks = max_blocks;
@@ -699,14 +746,21 @@ cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint
     k_recover_cc<<<(unsigned)((int64_t)n_req * max_blocks), kRecCcThreads, smem, s>>>(a);
     return cudaGetLastError();
   }
-  // Pages per item: as many as keep ≥ 16 items per CTA (the query rows of a
-  // layer are then loaded once for P pages), at most kRecPmax.
-  const int64_t pages = (int64_t)n_req * max_blocks;
+  // Too few pages to fill the GPU: with the caller's workspace, keep
+  // kRecPmax pages per item and split the layers into groups (partial sums,
+  // then a finalize); without it, fewer pages per item (one kernel).
+  const int n_lg = recover_layer_groups(n_req, max_blocks, BS, L, H, Hq, D);
   int P = kRecPmax;
-  while (P > 1 && pages / P < 16LL * n_sm) P >>= 1;
+  if (n_lg > 1 && ws && ws_bytes >= recover_ws_bytes(n_req, max_blocks, BS, L, H, Hq, D)) {
+    a.n_lg = n_lg;
+    a.partial = static_cast<float *>(ws);
+  } else {
+    const int64_t pages = (int64_t)n_req * max_blocks;
+    while (P > 1 && pages / P < (int64_t)kRecItemsPerCta * n_sm) P >>= 1;
+  }
   a.P = P;
   a.n_chunks = (max_blocks + P - 1) / P;
-  const int64_t n_items = (int64_t)n_req * a.n_chunks;
+  const int64_t n_items = (int64_t)n_req * a.n_chunks * a.n_lg;
   const int KB = D / 64, ncol = Hq;
   a.idesc = make_idesc(128, ncol);
   CUtensorMap tm_k, tm_q;
@@ -727,6 +781,10 @@ cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint
                              (int)smem);                                                       \
     if (e != cudaSuccess) return e;                                                            \
     k_recover_tc<GV><<<grid, kRecThreads, smem, s>>>(tm_k, tm_q, a, NS, cols);                 \
+    e = cudaGetLastError();                                                                    \
+    if (e != cudaSuccess || a.n_lg == 1) return e;                                             \
+    const int64_t n_pos = (int64_t)n_req * max_blocks * BS;                                    \
+    k_recover_finalize<<<(unsigned)((n_pos + 255) / 256), 256, 0, s>>>(a);                     \
     return cudaGetLastError();                                                                 \
   }
   KVC_RECOVER_CASE(2)

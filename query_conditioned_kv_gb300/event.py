@@ -27,6 +27,7 @@ import numpy as np
 import torch
 
 from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_recover_score,
+               kvc_recover_score_workspace_size,
                kvc_redirect_free,
                kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
                kvc_lrfu_update, kvc_score_qmem, kvc_score_qmem_workspace_size,
@@ -359,6 +360,8 @@ class PagedEvent:
         dev = self.device = torch.device(device)
         self.state = torch.zeros(n_req, self.cap, dtype=torch.float32, device=dev)
         self.keep_score = torch.zeros(n_req, self.cap, dtype=torch.float32, device=dev)
+        wsb = kvc_recover_score_workspace_size(n_req, max_blocks, L, H, Hq, D, block_size)
+        self.ws = torch.empty(wsb, dtype=torch.uint8, device=dev) if wsb else None
         self.seg_off = _dev_i64(np.arange(n_req + 1) * self.cap, dev)
         self.kept = torch.empty(n_req, keep, dtype=torch.int32, device=dev)
         self.kept_count = torch.empty(n_req, dtype=torch.int32, device=dev)
@@ -378,7 +381,7 @@ class PagedEvent:
     def score(self, q, lse, kpool, block_table, seqused, count, stream=None):
         kvc_recover_score(q, lse, kpool, self.n_slots, block_table, self.max_blocks, seqused,
                           count, self.n_req, self.L, self.H, self.Hq, self.D, self.BS,
-                          self.state, self.dev_status, stream)
+                          self.state, self.ws, self.dev_status, stream)
 
     def lrfu(self, top_p: float = 0.9, lam: float = 0.5, stream=None):
         kvc_lrfu_update(self.state, self.seg_off, self.n_req, self.cap, top_p, lam,

@@ -106,13 +106,15 @@ def test_validation_rejects_before_launch(kvc):
                  None, None) == 5
     # recover: D, Hq % H, a NULL state, misaligned pool
     assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 96, 16,
-                 P, None, None) == 2
+                 P, None, 0, None, None) == 2
     assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 30, 128, 16,
-                 P, None, None) == 2
+                 P, None, 0, None, None) == 2
     assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128, 16,
-                 None, None, None) == 1
+                 None, None, 0, None, None) == 1
     assert _call(kvc, "kvc_recover_score", P, P, U, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128, 16,
-                 P, None, None) == 4
+                 P, None, 0, None, None) == 4
+    assert _call(kvc, "kvc_recover_score", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128, 16,
+                 P, U, 1 << 20, None, None) == 4  # misaligned workspace
     # tail plan: a request longer than the plan accepts; no mask
     assert _call(kvc, "kvc_tail_plan", P, 4, P, P, 1 << 17, 1, 16, 1 << 22, P, P, P, P, P, P,
                  P, P, None, None) == 2

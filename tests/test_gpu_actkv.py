@@ -57,9 +57,12 @@ def _mk_inputs(orc, rng, n_req, L, H, Hq, D, BS, max_blocks, seq, spare=3):
     return kp, q, bt, lse, kp_bits, q_bits, n_slots
 
 
-def _gpu_recover(kvc, q, lse, kp, bt, seq, cnt, state, n_slots, L, H, Hq, D, BS, path=None):
+def _gpu_recover(kvc, q, lse, kp, bt, seq, cnt, state, n_slots, L, H, Hq, D, BS, path=None,
+                 ws=True):
     n_req, max_blocks = bt.shape
     st = torch.from_numpy(state.astype(np.float32)).to(DEV)
+    wsb = kvc.kvc_recover_score_workspace_size(n_req, max_blocks, L, H, Hq, D, BS)
+    wst = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV) if ws else None
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     old = os.environ.pop("KVC_RECOVER_PATH", None)
     if path:
@@ -69,7 +72,7 @@ def _gpu_recover(kvc, q, lse, kp, bt, seq, cnt, state, n_slots, L, H, Hq, D, BS,
                               torch.from_numpy(bt).to(DEV), max_blocks,
                               torch.from_numpy(np.asarray(seq, np.int32)).to(DEV),
                               torch.from_numpy(np.asarray(cnt, np.int32)).to(DEV), n_req, L, H,
-                              Hq, D, BS, st, status)
+                              Hq, D, BS, st, wst, status)
         torch.cuda.synchronize()
     finally:
         os.environ.pop("KVC_RECOVER_PATH", None)
@@ -88,10 +91,15 @@ SHAPES = [  # H, Hq, D, BS
 
 
 @pytest.mark.parametrize("H,Hq,D,BS", SHAPES)
-@pytest.mark.parametrize("path", [None, "cc"])
+@pytest.mark.parametrize("path", [None, "cc", "one_group"])
 def test_recover_matches_oracle(kvc, orc, H, Hq, D, BS, path):
-    if path == "cc" and not kvc.kvc_recover_tensor_core(H, Hq, D, BS):
+    """Both kernels; on the tensor cores both with layer groups (few pages:
+    partial sums in the workspace, then the finalize) and without (no
+    workspace: one kernel)."""
+    if path in ("cc", "one_group") and not kvc.kvc_recover_tensor_core(H, Hq, D, BS):
         pytest.skip("already the CUDA-core path")
+    ws = path != "one_group"
+    path = None if path == "one_group" else path
     rng = np.random.default_rng(H * 1000 + Hq * 10 + D + BS)
     n_req, L, max_blocks = 5, 3, 7
     seq = [max_blocks * BS, max_blocks * BS - BS - 3, 1, 3 * BS + 2, 0]
@@ -104,7 +112,7 @@ def test_recover_matches_oracle(kvc, orc, H, Hq, D, BS, path):
     for cnt in ([1, 1, 1, 1, 1], [2, 3, 2, 0, 2]):
         prev = state
         state, status = _gpu_recover(kvc, q, lse, kp, bt, seq, cnt, state, n_slots, L, H, Hq,
-                                     D, BS, path)
+                                     D, BS, path, ws)
         assert status == 0
         for r in range(n_req):
             if cnt[r] < 1:  # not generating an action: untouched
