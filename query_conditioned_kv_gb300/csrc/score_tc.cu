@@ -962,7 +962,11 @@ k_score_ring(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ 
         ps[rt] = 0.f;
       }
       for (int j = 0; j < u.my_tiles; j++, t++) {
-        if ((int)(t % NEG) != eg) continue;
+        // the group of a tile follows its index within the unit, so a unit's
+        // partial sums merge in the same order whatever ran on this CTA
+        // before it (scores do not depend on how units are split between
+        // launches)
+        if (j % NEG != eg) continue;
         const int buf = t % NBUF;
         ok = __all_sync(0xFFFFFFFFu,
                         ok && wait_or_abort(smem_u32(sm.tfull + buf), (t / NBUF) & 1, sm.failed));

@@ -214,10 +214,9 @@ class TieredMeanKEvent(MeanKEvent):
     score   the index is scored in bounded tiles of `stage_layers` layers:
             each tile is copied host → device into one of two staging
             buffers on a copy stream while the previous tile is scored on
-            the current stream (the scorer is the device-resident one; a
-            tile launch can merge a unit's partial sums in another order,
-            so the scores may differ from one all-layer launch in the last
-            bits);
+            the current stream (the scorer is the device-resident one, and
+            a unit's partial sums merge in one order whatever else a launch
+            holds, so the scores are the same bit for bit);
     select  as MeanKEvent;
     pack    kvc_pack_tiered: blocks that the previous step also kept come
             from the previous view (raw K from a raw-K cache, V from the V
