@@ -153,10 +153,11 @@ k_lrfu(const float *__restrict__ scores, const int64_t *__restrict__ seg_off, in
   }
   const double total = m3[0];
   const double target = (double)p * total;
-  uint32_t T = 0xFFFFFFFFu;  // no hits unless the total is positive
+  uint32_t T = 0xFFFFFFFFu;  // no hits unless some mass is asked for
   double above = 0.0;
   int need = 0;
-  if (total > 0.0) {
+  const bool any = total > 0.0 && target > 0.0;  // p = 0: the empty prefix suffices
+  if (any) {
     // two bits per pass: the largest of the three candidates that still
     // holds p of the mass extends the threshold
     uint32_t prefix = 0u;
@@ -187,7 +188,7 @@ k_lrfu(const float *__restrict__ scores, const int64_t *__restrict__ seg_off, in
   for (int i = i0; i < i1; i++) {
     const uint32_t k = keys[i];
     bool hit = false;
-    if (total > 0.0 && k) {
+    if (any && k) {
       if (k > T) hit = true;
       else if (k == T) hit = rank++ < need;
     }
