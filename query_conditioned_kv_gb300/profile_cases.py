@@ -13,6 +13,8 @@ event once to produce realistic inputs for the stage, then launches the stage
   python -m query_conditioned_kv_gb300.profile_cases qmem   --layers 4  --sessions 8 --iters 2
   python -m query_conditioned_kv_gb300.profile_cases event_timing --config 27b --iters 10
   python -m query_conditioned_kv_gb300.profile_cases paged  --sessions 4 --iters 3
+  python -m query_conditioned_kv_gb300.profile_cases tiered --layers 8 --iters 2
+  python -m query_conditioned_kv_gb300.profile_cases confidence --iters 3
 
 event_timing times a whole Mean-K event (score → select → pack, one CUDA
 graph) on a full workload — tiny, 8b, 27b or ragged — with L2 flushed
@@ -22,7 +24,9 @@ workload's shapes (shared 4096-position prefix, page 16), reduced to
 `--sessions` sessions and `--layers` layers.  The paged case is ActKV's
 compression operation at the Table 1 shapes (6K → 4K tokens per request,
 36 layers) on `--sessions` requests: score → LRFU → select → plan →
-compaction, `--iters` times.
+compaction, `--iters` times.  The tiered case runs `--iters` pairs of agent
+steps of the host-resident 8B-class event reduced to `--layers` layers; the
+confidence case runs the confidence monitor on its bench workload.
 """
 from __future__ import annotations
 
@@ -34,7 +38,7 @@ import sys
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem",
-                                     "event_timing", "paged"])
+                                     "event_timing", "paged", "tiered", "confidence"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sessions", type=int, default=8)
@@ -58,6 +62,12 @@ def main(argv=None) -> None:
         return
     if args.case == "paged":
         _paged_case(args, dev)
+        return
+    if args.case == "tiered":
+        _tiered_case(args, dev)
+        return
+    if args.case == "confidence":
+        _confidence_case(args, dev)
         return
     base = {"8b": W.config_8b, "27b": W.config_27b, "tiny": W.config_tiny,
             "ragged": W.config_ragged}[args.config]()
@@ -223,6 +233,58 @@ def _paged_case(args, dev):
     st = kvc.kvc_device_status(ev.dev_status)
     print(f"paged: {cfg.n_req} requests, pairs {int(ev.n_pairs.sum().item())}, status {st}")
     if st != 0:
+        raise SystemExit(1)
+
+
+
+def _tiered_case(args, dev):
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import TieredMeanKEvent
+
+    cfg = W.scaled(W.config_8b(), L=args.layers)
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = cfg.meank_direct(dev)
+    kvc.kvc_build_meank(kraw, meank, cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    meank_h, kraw_h, vraw_h = (t.cpu().pin_memory() for t in (meank, kraw, vraw))
+    del kraw, vraw, meank
+    qs = [cfg.q(dev, step=0), cfg.q(dev, step=1)]
+    ev = TieredMeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                          cfg.n_recent, theta=cfg.theta, device=dev, stage_layers=4)
+    for i in range(2 * args.iters):
+        ev.step(qs[i % 2], meank_h, kraw_h, vraw_h)
+    torch.cuda.synchronize(dev)
+    st = kvc.kvc_device_status(ev.dev_status)
+    print(f"tiered: {2 * args.iters} steps on {cfg.L} layers, status {st}")
+    if st != 0:
+        raise SystemExit(1)
+
+
+def _confidence_case(args, dev):
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+
+    cfg = W.ConfidenceConfig()
+    lg, tr = cfg.logits(dev), cfg.traces(dev)
+    conf = torch.empty(cfg.n_req, dtype=torch.float32, device=dev)
+    off = torch.arange(cfg.n_req + 1, dtype=torch.int64, device=dev) * cfg.trace_len
+    slope = torch.empty(cfg.n_req, dtype=torch.float64, device=dev)
+    budget = torch.full((cfg.n_req,), cfg.budget0, dtype=torch.int32, device=dev)
+    kept = torch.empty(cfg.n_req, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.iters):
+        kvc.kvc_token_confidence(lg, cfg.n_req, cfg.vocab, cfg.top_k, conf, st)
+        kvc.kvc_conf_trend_budget(tr, off, cfg.n_req, cfg.trace_len, cfg.window, cfg.stride,
+                                  cfg.bottom_pct, cfg.budget_step, cfg.max_budget, slope, budget,
+                                  kept, st)
+    torch.cuda.synchronize(dev)
+    s = kvc.kvc_device_status(st)
+    print(f"confidence: {args.iters} iterations, status {s}")
+    if s != 0:
         raise SystemExit(1)
 
 
