@@ -78,12 +78,6 @@ struct QtcSmem {
   }
 };
 
-__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try(bar, parity) && global_ns() - t0 < 200000000ull) {
-  }
-}
-
 // (max, sum) ⊕ (max, sum), base 2.
 __device__ __forceinline__ void merge(float &m, float &s, float m2, float s2) {
   if (m2 == -INFINITY) return;
@@ -396,16 +390,16 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
   if (*sm.failed && threadIdx.x == 0) {
     record_error(a.status, KVC_ERR_TIMEOUT);
     for (int i = 0; i < NS; i++) {
-      drain(smem_u32(sm.full + i), 0);
-      drain(smem_u32(sm.full + i), 1);
+      mbar_drain(smem_u32(sm.full + i), 0);
+      mbar_drain(smem_u32(sm.full + i), 1);
     }
     for (int i = 0; i < kMB; i++) {
-      drain(smem_u32(sm.mfull + i), 0);
-      drain(smem_u32(sm.mfull + i), 1);
+      mbar_drain(smem_u32(sm.mfull + i), 0);
+      mbar_drain(smem_u32(sm.mfull + i), 1);
     }
     for (int i = 0; i < kNacc; i++) {
-      drain(smem_u32(sm.tfull + i), 0);
-      drain(smem_u32(sm.tfull + i), 1);
+      mbar_drain(smem_u32(sm.tfull + i), 0);
+      mbar_drain(smem_u32(sm.tfull + i), 1);
     }
   }
   __syncthreads();
@@ -432,17 +426,6 @@ k_qmem_split(const float *__restrict__ M, uint16_t *__restrict__ mb, int64_t row
 
 bool make_map_box8(CUtensorMap *m, const void *base, uint64_t rows, int D) {
   return make_map(m, base, rows, D, 8);
-}
-
-int n_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 1;
-  }
-  return n;
 }
 
 }  // namespace
@@ -495,7 +478,7 @@ cudaError_t launch_qmem_logits_tc(const float *M, const uint16_t *kpool, const i
   uint32_t cols = 32;
   while (cols < (uint32_t)(kNacc * 2 * Hq)) cols <<= 1;
   const int64_t n_items = (int64_t)n_sess * n_tiles * L;
-  const unsigned grid = (unsigned)std::min<int64_t>(n_items, n_sms());
+  const unsigned grid = (unsigned)std::min<int64_t>(n_items, device_sm_count());
 #define KVC_QTC_CASE(GV)                                                                     \
   if (a.G == GV) {                                                                           \
     e = cudaFuncSetAttribute(k_qmem_logits_tc<GV>,                                           \

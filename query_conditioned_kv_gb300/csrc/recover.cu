@@ -144,13 +144,6 @@ struct RecSmem {
   }
 };
 
-// Bounded wait that ignores the failure flag (teardown drain only).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try(bar, parity) && global_ns() - t0 < 200000000ull) {
-  }
-}
-
 template <int G>
 __global__ void __launch_bounds__(kRecThreads, 1)
 k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -352,16 +345,16 @@ k_recover_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     record_error(a.status, KVC_ERR_TIMEOUT);
     // let this CTA's own copies and MMAs finish before its memory is released
     for (int i = 0; i < NS; i++) {
-      drain_wait(smem_u32(sm.full + i), 0);
-      drain_wait(smem_u32(sm.full + i), 1);
+      mbar_drain(smem_u32(sm.full + i), 0);
+      mbar_drain(smem_u32(sm.full + i), 1);
     }
     for (int i = 0; i < kRecQB; i++) {
-      drain_wait(smem_u32(sm.qfull + i), 0);
-      drain_wait(smem_u32(sm.qfull + i), 1);
+      mbar_drain(smem_u32(sm.qfull + i), 0);
+      mbar_drain(smem_u32(sm.qfull + i), 1);
     }
     for (int i = 0; i < kRecNacc; i++) {
-      drain_wait(smem_u32(sm.tfull + i), 0);
-      drain_wait(smem_u32(sm.tfull + i), 1);
+      mbar_drain(smem_u32(sm.tfull + i), 0);
+      mbar_drain(smem_u32(sm.tfull + i), 1);
     }
   }
   __syncthreads();
@@ -660,17 +653,6 @@ k_tail_compact(uint16_t *kpool, uint16_t *vpool, int64_t n_slots, int L, int row
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 1;
-  }
-  return n;
-}
-
 bool force_cc() {
   const char *e = getenv("KVC_RECOVER_PATH");
   return e && e[0] == 'c' && e[1] == 'c';
@@ -694,7 +676,7 @@ constexpr int kRecItemsPerCta = 16;
 int recover_layer_groups(int n_req, int max_blocks, int BS, int L, int H, int Hq, int D) {
   if (!recover_tc_supported(H, Hq, D, BS) || force_cc()) return 1;
   const int64_t items = (int64_t)n_req * ((max_blocks + kRecPmax - 1) / kRecPmax);
-  const int64_t want = (int64_t)kRecItemsPerCta * sm_count();
+  const int64_t want = (int64_t)kRecItemsPerCta * device_sm_count();
   if (items >= want) return 1;
   const int64_t n = (want + items - 1) / items;
   return n > L ? L : (int)n;
@@ -729,7 +711,7 @@ cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint
   a.max_blocks = max_blocks;
   a.n_slots = n_slots;
   a.zscale = kLog2eR / sqrtf((float)D);
-  const int n_sm = sm_count();
+  const int n_sm = device_sm_count();
   const bool tc_path = recover_tc_supported(H, Hq, D, BS) && !force_cc() &&
                        (int64_t)L * n_slots * H < INT32_MAX;
   a.n_lg = 1;
@@ -835,7 +817,7 @@ cudaError_t launch_tail_compact(uint16_t *kpool, uint16_t *vpool, int64_t n_slot
                                 const int32_t *n_pairs, int cap, int n_req, int32_t *status,
                                 cudaStream_t s) {
   const int row_chunks = H * D / 8;  // 16-byte pieces per row
-  const int per_req = std::max(1, 8 * sm_count() / n_req);
+  const int per_req = std::max(1, 8 * device_sm_count() / n_req);
   dim3 grid((unsigned)per_req, (unsigned)n_req);
   k_tail_compact<<<grid, kCopyThreads, 0, s>>>(kpool, vpool, n_slots, L, row_chunks, src, dst,
                                                n_pairs, cap, status);

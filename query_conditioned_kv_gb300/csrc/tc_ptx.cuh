@@ -61,6 +61,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Teardown after a failure: wait (at most 0.2 s, ignoring the failure
+// flag) for a phase, so this CTA's own copies and MMAs finish before its
+// shared memory and TMEM are released.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try(bar, parity) && global_ns() - t0 < 200000000ull) {
+  }
+}
+
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }

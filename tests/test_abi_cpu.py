@@ -127,6 +127,24 @@ def test_validation_rejects_before_launch(kvc):
                  None) == 4
     assert _call(kvc, "kvc_tail_compact", P, P, 1 << 12, 2, 8, 128, P, P, P, 0, 1, None,
                  None) == 1
+    # tiered pack: prev lists without their buffers; misaligned history
+    assert _call(kvc, "kvc_pack_tiered", P, P, P, None, None, None, P, P, 1, 1, 128, P, 1, 128,
+                 4, P, P, P, P, None, None, None) == 1
+    assert _call(kvc, "kvc_pack_tiered", U, P, None, None, None, None, P, P, 1, 1, 128, P, 1,
+                 128, 4, P, P, P, P, None, None, None) == 4
+    # LRFU: p or lambda outside [0, 1]; a segment longer than the staging allows
+    assert _call(kvc, "kvc_lrfu_update", P, P, 1, 64, ctypes.c_float(1.5), ctypes.c_float(0.5),
+                 P, None, None, None) == 1
+    assert _call(kvc, "kvc_lrfu_update", P, P, 1, 64, ctypes.c_float(0.9), ctypes.c_float(-0.1),
+                 P, None, None, None) == 1
+    assert _call(kvc, "kvc_lrfu_update", P, P, 1, 49153, ctypes.c_float(0.9),
+                 ctypes.c_float(0.5), P, None, None, None) == 2
+    # confidence: top_k beyond the vocabulary; too many windows; misaligned slope
+    assert _call(kvc, "kvc_token_confidence", P, 4, 10, 11, P, None, None) == 1
+    assert _call(kvc, "kvc_conf_trend_budget", P, P, 1, 100000, 1, 1, ctypes.c_float(10.0),
+                 256, 8192, P, P, P, None, None) == 2
+    assert _call(kvc, "kvc_conf_trend_budget", P, P, 1, 1000, 16, 4, ctypes.c_float(10.0),
+                 256, 8192, FAKE + 4, P, P, None, None) == 4
     assert _call(kvc, "kvc_device_status", None, None) == 1
 
 
