@@ -1,0 +1,647 @@
+// score_fused.cu — single-read tensor-core Mean-K scorer for query sets of
+// 4 query heads per KV head × a 32-token window (128 query rows), D = 128.
+//
+// The quantity is the one every scorer of this library computes (KVMem
+// "Query-conditioned retrieval"; ActKV §7.1 aggregation): for a unit (layer
+// l, KV head h, session r) and query row (g, w),
+//   z[g,w,b] = q[g,w]·meank[b]/sqrt(D),   LSE[g,w] = log Σ_b e^z,
+//   score[b] = (1/W) Σ_w max_g exp(z[g,w,b] − LSE[g,w]).
+//
+// Design (Mean-K read from HBM once):
+//   * A cluster of C ≤ 8 CTAs (one per SM) owns a unit; CTA `rank` takes the
+//     unit's 256-block tiles rank, rank + C, …  A tile is one tcgen05.mma
+//     product D[ρ][b] (M = 128 query rows, N = 256 blocks, K = 128) into one
+//     of two 256-column TMEM buffers.  (N = 256 runs the tensor pipe about
+//     2.3 times faster per block than two N = 128 products.)
+//   * The query rows are loaded w-major (row ρ = 4w + g) by a 4-D tensor map
+//     whose strides walk g inside w, so TMEM lane ρ holds (w = ρ/4, g = ρ%4):
+//     the four query heads of one window position sit in four adjacent lanes.
+//   * Pass 1 (per lane = query row): online (max, Σ2^(z−max)) over the tile's
+//     blocks.  The logits of a CTA's last (up to) two tiles stay in TMEM.
+//   * The CTAs of the cluster exchange their row partials with st.async into
+//     each other's shared memory, and every CTA forms the row LSEs.
+//   * Pass 2 reads the kept logits again: x = z·log2e/√D − LSE, then a
+//     butterfly over the warp: max over g (lanes ρ^1, ρ^2), one ex2 per
+//     (w, b), and the sum over the warp's 8 window positions (ρ^4, ρ^8,
+//     ρ^16), each stage halving the columns a lane carries, so lane ℓ ends
+//     with the sum for column bitrev5(ℓ) of each 32-column chunk.  The four
+//     lane quarters (32 window positions) are added through shared memory in
+//     a fixed order.
+//   * Four epilogue warpgroups split every tile: group e takes its columns
+//     64e … 64e + 63, so each step of the chain above has 16 warps on it.
+//   * A CTA with more than two tiles multiplies its first tiles again after
+//     the exchange (they are still in L2); the last two are never reloaded.
+//     Jobs run in the order A(u) R(u−1) B(u) (A = first multiplications of
+//     the reloaded tiles, R = their second, B = kept tiles), so the next
+//     unit's first tiles stream in during a unit's exchange and pass 2.
+// Every wait is bounded (1 s of %globaltimer) and records KVC_ERR_TIMEOUT.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "kvc_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace kvc {
+namespace {
+
+using namespace tc;
+
+constexpr int kFG = 4;           // query heads per KV head
+constexpr int kFW = 32;          // window positions
+constexpr int kFD = 128;         // head dim
+constexpr int kFTB = 256;        // Mean-K blocks per tile (MMA N)
+constexpr int kFNS = 2;          // Mean-K ring stages (64 KB each)
+constexpr int kFQB = 2;          // query-row buffers (32 KB each)
+constexpr int kFNBUF = 2;        // TMEM buffers of 256 columns
+constexpr int kFKeep = kFNBUF;   // tiles whose logits stay in TMEM
+constexpr int kFTarget = 4;      // tiles per CTA and unit the cluster size aims at
+constexpr int kFNEG = 4;         // epilogue warpgroups
+constexpr int kFCols = kFTB / kFNEG;  // columns of every tile a group takes (64)
+constexpr int kFNCH = kFCols / 32;    // their 32-column chunks
+constexpr int kFMaxC = 8;        // CTAs per cluster
+constexpr int kFThreads = 64 + 128 * kFNEG;
+constexpr uint32_t kFTile = kFTB * kFD * 2;  // 64 KB
+constexpr uint32_t kFQ = 128 * kFD * 2;      // 32 KB
+
+struct FusedArgs {
+  float *scores;
+  const int64_t *blk_off;
+  int32_t *status;
+  int L, H, n_sess;
+  int max_tiles;  // longest session accepted, in tiles
+  int64_t nb_total;
+  float zscale;  // log2(e)/sqrt(D)
+  uint32_t idesc;
+};
+
+struct FusedSmem {
+  uint8_t *ring, *q;
+  uint64_t *full, *empty, *tfull, *tempty, *qfull, *qempty, *recv;
+  uint32_t *tmem_holder;
+  volatile int *failed;
+  float2 *egpart;  // [kFNEG][128] per-group row partials
+  float2 *rbuf;    // [2 parities][kFMaxC ranks][128] received partials
+  float *lse;      // [128] row LSE (base 2)
+  float *red;      // [kFNEG][2 parities][4 quarters][kFCols] pass-2 column sums
+  __device__ explicit FusedSmem(uint8_t *raw) {
+    uint8_t *p = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    ring = p;
+    p += kFNS * kFTile;
+    q = p;
+    p += kFQB * kFQ;
+    uint64_t *b = reinterpret_cast<uint64_t *>(p);
+    full = b;
+    empty = full + kFNS;
+    tfull = empty + kFNS;
+    tempty = tfull + kFNBUF;
+    qfull = tempty + kFNBUF;
+    qempty = qfull + kFQB;
+    recv = qempty + kFQB;
+    tmem_holder = reinterpret_cast<uint32_t *>(recv + 2);
+    failed = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    egpart = reinterpret_cast<float2 *>(tmem_holder + 4);  // 16-byte aligned
+    rbuf = egpart + kFNEG * 128;
+    lse = reinterpret_cast<float *>(rbuf + 2 * kFMaxC * 128);
+    red = lse + 128;
+  }
+  static constexpr size_t bytes() {
+    return 1024 + (size_t)kFNS * kFTile + (size_t)kFQB * kFQ +
+           (2 * kFNS + 2 * kFNBUF + 2 * kFQB + 2) * 8 + 16 +
+           (size_t)(kFNEG + 2 * kFMaxC) * 128 * 8 + 128 * 4 + (size_t)kFNEG * 2 * 4 * kFCols * 4;
+  }
+};
+
+struct FUnit {
+  int l, h, r, nb, n_tiles, my_tiles, n_rec, jobs, mk_row0, q_unit;
+  int64_t b0;
+};
+
+// A unit and this CTA's share of it: my_tiles tiles, of which the first
+// n_rec are multiplied twice (before and after the exchange); jobs = MMAs.
+__device__ __forceinline__ FUnit funit(const FusedArgs &a, int unit, int C, int rank) {
+  FUnit u;
+  u.r = unit % a.n_sess;
+  const int lh = unit / a.n_sess;
+  u.h = lh % a.H;
+  u.l = lh / a.H;
+  const int64_t b0 = a.blk_off[u.r], b1 = a.blk_off[u.r + 1];
+  const bool ok =
+      b0 >= 0 && b1 > b0 && b1 <= a.nb_total && b1 - b0 <= (int64_t)a.max_tiles * kFTB;
+  u.b0 = ok ? b0 : 0;
+  u.nb = ok ? (int)(b1 - b0) : 0;
+  u.n_tiles = (u.nb + kFTB - 1) / kFTB;
+  u.my_tiles = u.n_tiles > rank ? (u.n_tiles - rank + C - 1) / C : 0;
+  u.n_rec = u.my_tiles > kFKeep ? u.my_tiles - kFKeep : 0;
+  u.jobs = u.my_tiles + u.n_rec;
+  u.mk_row0 = (int)(((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0);
+  u.q_unit = (u.l * a.n_sess + u.r) * a.H + u.h;
+  return u;
+}
+
+// Remote 8-byte store into a peer's shared memory that counts its bytes on
+// the peer's mbarrier when it lands (no fence or separate arrive).
+__device__ __forceinline__ void st_async_f2(uint32_t raddr, float2 v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(raddr), "f"(v.x), "f"(v.y), "r"(rbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void merge_lse(float &m, float &s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float mn = fmaxf(m, m2);
+  s = s * exp2f(m - mn) + s2 * exp2f(m2 - mn);
+  m = mn;
+}
+
+// Pass 1 of this group's columns of one tile for this lane's query row:
+// (max, Σ2^(z·zs − max)) over the `valid` blocks, 32 columns at a time.
+__device__ __forceinline__ void fused_pass1(uint32_t taddr, int valid, float zs, float &pm,
+                                            float &ps) {
+  pm = -INFINITY;
+  ps = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < kFNCH && 32 * c < valid; c++) {
+    uint32_t r[32];
+    tmem_issue32(taddr + (uint32_t)(32 * c), r);
+    tmem_wait32(r);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+    const int nv = valid - 32 * c;
+    if (nv < 32) {
+#pragma unroll
+      for (int j = 0; j < 32; j++)
+        if (j >= nv) v[j] = -INFINITY;
+    }
+    float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
+#pragma unroll
+    for (int j = 4; j < 32; j += 4) {
+      m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
+      m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
+    }
+    const float mn = fmaxf(pm, fmaxf(m0, m1) * zs);
+    float acc[8];
+    acc[0] = (pm == -INFINITY) ? 0.f : ps * ex2(pm - mn);
+#pragma unroll
+    for (int k = 1; k < 8; k++) acc[k] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j++) acc[j & 7] += ex2(fmaf(v[j], zs, -mn));
+    pm = mn;
+    ps = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  }
+}
+
+// Bit reversal of a lane index (5 bits): the column a lane holds after the
+// five halving stages of fused_pass2.
+__device__ __forceinline__ int bitrev5(int x) {
+  return ((x & 1) << 4) | ((x & 2) << 2) | (x & 4) | ((x & 8) >> 2) | ((x & 16) >> 4);
+}
+
+// Pass 2 of one tile.  This lane is query row ρ = 32·quarter + lane, i.e.
+// window position w = 8·quarter + lane/4 and head g = lane%4.  For each
+// 32-column chunk: x = z·zs − LSE[ρ]; max over g (xor 1, 2), ex2, sum over
+// the warp's w (xor 4, 8, 16).  Each stage keeps the half of the columns
+// selected by the lane bit and receives the partner's copy of it.  The
+// warp's 32 column sums go to red[quarter][col].
+__device__ __forceinline__ void fused_pass2(uint32_t taddr, float lse_row, float zs, int lane,
+                                            float *red_q) {
+  const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4, b3 = lane & 8, b4 = lane & 16;
+  const int col_in_chunk = bitrev5(lane);
+#pragma unroll 1
+  for (int c = 0; c < kFNCH; c++) {
+    uint32_t r[32];
+    tmem_issue32(taddr + (uint32_t)(32 * c), r);
+    tmem_wait32(r);
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const float lo = fmaf(__uint_as_float(r[i]), zs, -lse_row);
+      const float hi = fmaf(__uint_as_float(r[16 + i]), zs, -lse_row);
+      a[i] = fmaxf(b0 ? hi : lo, __shfl_xor_sync(0xFFFFFFFFu, b0 ? lo : hi, 1));
+    }
+    float e[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const float keep = b1 ? a[8 + i] : a[i], send = b1 ? a[i] : a[8 + i];
+      e[i] = ex2(fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2)));
+    }
+    float s4[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const float keep = b2 ? e[4 + i] : e[i], send = b2 ? e[i] : e[4 + i];
+      s4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+    }
+    float s2[2];
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      const float keep = b3 ? s4[2 + i] : s4[i], send = b3 ? s4[i] : s4[2 + i];
+      s2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    const float keep = b4 ? s2[1] : s2[0], send = b4 ? s2[0] : s2[1];
+    red_q[32 * c + col_in_chunk] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+  }
+}
+
+__global__ void __launch_bounds__(kFThreads, 1)
+k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__ CUtensorMap tm_q,
+              FusedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  FusedSmem sm(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = (int)cluster_nrank(), rank = (int)cluster_rank();
+  const int cluster_id = blockIdx.x / C, n_clusters = gridDim.x / C;
+  const int n_units = a.L * a.H * a.n_sess;
+
+  if (threadIdx.x == 0) {
+    *sm.failed = 0;
+    for (int i = 0; i < kFNS; i++) {
+      mbar_init(smem_u32(sm.full + i), 1);
+      mbar_init(smem_u32(sm.empty + i), 1);
+    }
+    for (int i = 0; i < kFNBUF; i++) {
+      mbar_init(smem_u32(sm.tfull + i), 1);
+      mbar_init(smem_u32(sm.tempty + i), 4 * kFNEG);  // every epilogue warp reads every tile
+    }
+    for (int i = 0; i < kFQB; i++) {
+      mbar_init(smem_u32(sm.qfull + i), 1);
+      mbar_init(smem_u32(sm.qempty + i), 1);
+    }
+    // each receive barrier: one local arrival that arms it for the bytes of
+    // the C − 1 peers' row partials
+    for (int i = 0; i < 2; i++) {
+      mbar_init(smem_u32(sm.recv + i), 1);
+      if (C > 1) mbar_expect_tx(smem_u32(sm.recv + i), (uint32_t)(C - 1) * 128 * 8);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) alloc_tmem_cols(sm.tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (C > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
+  const uint32_t tmem = *sm.tmem_holder;
+
+  // Job order of a CTA (the same for all three roles).  With A(u) = the
+  // tiles of unit u multiplied twice (first n_rec), B(u) = the tiles whose
+  // logits stay in TMEM and R(u) = the second multiplication of A(u):
+  //   A(u0) B(u0) | A(u1) R(u0) B(u1) | A(u2) R(u1) B(u2) | … | R(u_last)
+  // A job waits for the TMEM buffer of the job four places earlier, so the
+  // next unit's first tiles stream in while this unit's exchange and pass 2
+  // run, and R(u) follows them out of L2.
+  if (warp == 0) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t s = 0, qi = 0;
+      bool ok = true;
+      int prev_unit = -1;
+      auto load_tile = [&](int row0, int i) -> bool {
+        const int slot = s % kFNS;
+        if (!wait_or_abort(smem_u32(sm.empty + slot), ((s / kFNS) & 1) ^ 1, sm.failed))
+          return false;
+        mbar_expect_tx(smem_u32(sm.full + slot), kFTile);
+        for (int kb = 0; kb < 2; kb++)
+          tma_load_2d(smem_u32(sm.ring + slot * kFTile + kb * (kFTile / 2)), &tm_mk, kb * 64,
+                      row0 + (rank + i * C) * kFTB, smem_u32(sm.full + slot));
+        s++;
+        return true;
+      };
+      for (int unit = cluster_id; ok; unit += n_clusters) {
+        const bool last = unit >= n_units;
+        FUnit u{};
+        if (!last) {
+          u = funit(a, unit, C, rank);
+          if (u.nb == 0 && rank == 0) record_error(a.status, KVC_ERR_BOUNDS);
+          if (u.my_tiles > 0) {
+            const int qb = qi % kFQB;
+            if (!(ok = wait_or_abort(smem_u32(sm.qempty + qb), ((qi / kFQB) & 1) ^ 1,
+                                     sm.failed)))
+              break;
+            mbar_expect_tx(smem_u32(sm.qfull + qb), kFQ);
+            for (int kb = 0; kb < 2; kb++)
+              tma_load_4d(smem_u32(sm.q + qb * kFQ + kb * (kFQ / 2)), &tm_q, kb * 64, 0, 0,
+                          u.q_unit, smem_u32(sm.qfull + qb));
+            qi++;
+          }
+        }
+        for (int i = 0; i < u.n_rec && ok; i++) ok = load_tile(u.mk_row0, i);      // A(u)
+        if (prev_unit >= 0) {
+          const FUnit prev = funit(a, prev_unit, C, rank);
+          for (int i = 0; i < prev.n_rec && ok; i++) ok = load_tile(prev.mk_row0, i);  // R(prev)
+        }
+        for (int i = u.n_rec; i < u.my_tiles && ok; i++) ok = load_tile(u.mk_row0, i);  // B(u)
+        if (last) break;
+        prev_unit = unit;
+      }
+      if (!ok) *sm.failed = 1;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t s = 0, t = 0, qi = 0;
+      bool ok = true;
+      int prev_nrec = 0, prev_qb = -1;
+      auto mma_job = [&](int qb) -> bool {
+        const int slot = s % kFNS, buf = t % kFNBUF;
+        if (!wait_or_abort(smem_u32(sm.full + slot), (s / kFNS) & 1, sm.failed)) return false;
+        if (!wait_or_abort(smem_u32(sm.tempty + buf), ((t / kFNBUF) & 1) ^ 1, sm.failed))
+          return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.q + qb * kFQ), ma = smem_u32(sm.ring + slot * kFTile);
+        const uint32_t d = tmem + (uint32_t)(buf * kFTB);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+          const uint32_t k32 = (uint32_t)(kk & 3) * 32u;
+          mma_bf16(d, smem_desc(qa + (kk >> 2) * (kFQ / 2) + k32),
+                   smem_desc(ma + (kk >> 2) * (kFTile / 2) + k32), a.idesc, kk > 0);
+        }
+        mma_commit(smem_u32(sm.empty + slot));
+        mma_commit(smem_u32(sm.tfull + buf));
+        s++;
+        t++;
+        return true;
+      };
+      for (int unit = cluster_id; ok; unit += n_clusters) {
+        const bool last = unit >= n_units;
+        FUnit u{};
+        int qb = -1;
+        if (!last) {
+          u = funit(a, unit, C, rank);
+          if (u.my_tiles > 0) {
+            qb = qi % kFQB;
+            if (!(ok = wait_or_abort(smem_u32(sm.qfull + qb), (qi / kFQB) & 1, sm.failed)))
+              break;
+            qi++;
+          }
+        }
+        for (int i = 0; i < u.n_rec && ok; i++) ok = mma_job(qb);                  // A(u)
+        if (prev_qb >= 0) {
+          for (int i = 0; i < prev_nrec && ok; i++) ok = mma_job(prev_qb);         // R(prev)
+          if (ok) mma_commit(smem_u32(sm.qempty + prev_qb));  // prev's last MMA issued
+        }
+        for (int i = u.n_rec; i < u.my_tiles && ok; i++) ok = mma_job(qb);        // B(u)
+        if (last) break;
+        prev_nrec = u.n_rec;
+        prev_qb = qb;
+      }
+      if (!ok) *sm.failed = 1;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- epilogue
+    const int eg = (warp - 2) >> 2;          // this thread's group
+    const int quarter = warp & 3;            // TMEM lane quarter of this warp
+    const int row = 32 * quarter + lane;     // query row ρ = 4w + g
+    const int gt = ((warp - 2) & 3) * 32 + lane;  // 0 … 127 within the group
+    const int et = (warp - 2) * 32 + lane;        // 0 … 128·kFNEG − 1
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    const float zs = a.zscale, invW = 1.f / (float)kFW;
+    float *red = sm.red + eg * 2 * 4 * kFCols;
+    uint32_t t = 0, ui = 0, rp = 0;
+    bool ok = true;
+    int prev_unit = -1;
+    float lse_prev = 0.f;
+    // pass 2 of one job of unit w (local tile i) with row LSE `lse`
+    auto pass2_job = [&](const FUnit &w, int i, uint32_t job, float lse, bool wait_full) {
+      const uint32_t buf = job % kFNBUF;
+      if (wait_full)
+        ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.tfull + buf),
+                                                          (job / kFNBUF) & 1, sm.failed));
+      const int tile = rank + i * C;
+      const int valid = min(kFCols, w.nb - tile * kFTB - eg * kFCols);  // this group's columns
+      float *rq = red + (rp & 1) * 4 * kFCols;
+      if (ok && valid > 0) {
+        tc_fence_after();
+        fused_pass2(tmem + lane_base + buf * kFTB + eg * kFCols, lse, zs, lane,
+                    rq + quarter * kFCols);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(sm.tempty + buf));
+      named_sync(4 + eg, 128);
+      if (ok && gt < valid) {
+        float *out = a.scores + ((int64_t)w.l * a.H + w.h) * a.nb_total + w.b0 + tile * kFTB +
+                     eg * kFCols;
+        out[gt] = ((rq[gt] + rq[kFCols + gt]) + (rq[2 * kFCols + gt] + rq[3 * kFCols + gt])) * invW;
+      }
+      rp++;
+    };
+    // pass 1 of one job of unit w (local tile i); releases the buffer unless kept
+    auto pass1_job = [&](const FUnit &w, int i, uint32_t job, float &pm, float &ps) {
+      const uint32_t buf = job % kFNBUF;
+      ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.tfull + buf),
+                                                        (job / kFNBUF) & 1, sm.failed));
+      const int valid = min(kFCols, w.nb - (rank + i * C) * kFTB - eg * kFCols);
+      if (ok && valid > 0) {  // this group's columns of the tile
+        tc_fence_after();
+        float qm, qs;
+        fused_pass1(tmem + lane_base + buf * kFTB + eg * kFCols, valid, zs, qm, qs);
+        merge_lse(pm, ps, qm, qs);
+      }
+      if (i < w.n_rec) {  // not kept: the buffer goes back to the MMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sm.tempty + buf));
+      }
+    };
+    for (int unit = cluster_id;; unit += n_clusters) {
+      const bool last = unit >= n_units;
+      FUnit u{};
+      if (!last) u = funit(a, unit, C, rank);
+      // a group merges its columns of the unit's tiles in tile order, and the
+      // groups merge in group order, so the result depends only on the unit
+      float pm = -INFINITY, ps = 0.f;
+      for (int i = 0; i < u.n_rec; i++, t++) pass1_job(u, i, t, pm, ps);         // A(u)
+      if (prev_unit >= 0) {
+        const FUnit prev = funit(a, prev_unit, C, rank);
+        for (int i = 0; i < prev.n_rec; i++, t++) pass2_job(prev, i, t, lse_prev, true);  // R(prev)
+      }
+      const uint32_t tB = t;
+      for (int i = u.n_rec; i < u.my_tiles; i++, t++) pass1_job(u, i, t, pm, ps);  // B(u)
+      if (last) break;
+      if (C > 1 || u.my_tiles > 0) {
+        // exchange: group partials → CTA partial → every CTA of the cluster
+        const int par = ui & 1;
+        sm.egpart[eg * 128 + row] = make_float2(pm, ps);
+        named_sync(2, 128 * kFNEG);
+        if (eg == 0) {
+          float m = pm, s2 = ps;
+          for (int g2 = 1; g2 < kFNEG; g2++) {
+            const float2 o = sm.egpart[g2 * 128 + row];
+            merge_lse(m, s2, o.x, o.y);
+          }
+          const float2 v = make_float2(m, s2);
+          float2 *mine = sm.rbuf + (par * kFMaxC + rank) * 128 + row;
+          *mine = v;
+          const uint32_t a_mine = smem_u32(mine), a_bar = smem_u32(sm.recv + par);
+          for (int p = 1; p < C; p++) {
+            const uint32_t peer = (uint32_t)((rank + p) % C);
+            st_async_f2(mapa_u32(a_mine, peer), v, mapa_u32(a_bar, peer));
+          }
+        }
+        if (C > 1) {
+          ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.recv + par),
+                                                            (ui >> 1) & 1, sm.failed, true));
+          // re-arm this parity for the unit after next: no peer can send that
+          // unit's partials before it has received this CTA's next ones
+          if (et == 0) mbar_expect_tx(smem_u32(sm.recv + par), (uint32_t)(C - 1) * 128 * 8);
+        }
+        named_sync(2, 128 * kFNEG);
+        if (et < 128) {
+          float m = -INFINITY, s2 = 0.f;
+          for (int c = 0; c < C; c++) {
+            const float2 v = sm.rbuf[(par * kFMaxC + c) * 128 + et];
+            merge_lse(m, s2, v.x, v.y);
+          }
+          sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);
+        }
+        named_sync(2, 128 * kFNEG);
+        const float lse_row = sm.lse[row];
+        ui++;
+        for (int i = u.n_rec; i < u.my_tiles; i++)                               // pass 2 of B(u)
+          pass2_job(u, i, tB + (uint32_t)(i - u.n_rec), lse_row, false);
+        lse_prev = lse_row;
+      }
+      prev_unit = unit;
+      if (!ok) {
+        *sm.failed = 1;
+        if (et == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+      }
+    }
+    if (!ok) {
+      *sm.failed = 1;
+      if (et == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*sm.failed && threadIdx.x == 0) {
+    record_error(a.status, KVC_ERR_TIMEOUT);
+    // let this CTA's own copies and MMAs drain (bounded; stale phases return at once)
+    for (int i = 0; i < kFNS; i++) {
+      mbar_drain(smem_u32(sm.full + i), 0);
+      mbar_drain(smem_u32(sm.full + i), 1);
+    }
+    for (int i = 0; i < kFNBUF; i++) {
+      mbar_drain(smem_u32(sm.tfull + i), 0);
+      mbar_drain(smem_u32(sm.tfull + i), 1);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    free_tmem_cols(tmem, 512);
+  }
+  if (C > 1) cluster_sync_all();  // no peer still writes into this CTA's memory
+}
+
+// --------------------------------------------------------------- host
+
+// CTAs per cluster: about kFTarget tiles of the longest session per CTA, at
+// most eight CTAs.  Fewer, longer shares spread the exchange over more
+// tiles; the tiles beyond the four kept in TMEM are multiplied twice.
+int fused_cluster(int nb_max) {
+  const int tiles = (nb_max + kFTB - 1) / kFTB;
+  int c = (tiles + kFTarget - 1) / kFTarget;
+  return c < 1 ? 1 : (c > kFMaxC ? kFMaxC : c);
+}
+
+// Clusters of C that can be resident at once (0: the kernel cannot run).
+int fused_clusters(int C) {
+  static int cached[kFMaxC + 1] = {};
+  static bool done[kFMaxC + 1] = {};
+  if (C < 1 || C > kFMaxC) return 0;
+  if (done[C]) return cached[C];
+  const size_t smem = FusedSmem::bytes();
+  int n = 0;
+  if (cudaFuncSetAttribute(k_score_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, k_score_fused, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  cached[C] = n;
+  done[C] = true;
+  return n;
+}
+
+// q as [units][W][G][D] seen through strides that walk g inside w: a box of
+// (64 columns, G, W, 1) lands in shared memory as rows ρ = w·G + g.
+bool make_q_wmajor_map(CUtensorMap *m, const void *q, uint64_t q_units) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kFD, (cuuint64_t)kFG, (cuuint64_t)kFW, (cuuint64_t)q_units};
+  cuuint64_t strides[3] = {(cuuint64_t)kFW * kFD * 2, (cuuint64_t)kFD * 2,
+                           (cuuint64_t)kFG * kFW * kFD * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kFG, (cuuint32_t)kFW, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool score_fused_supported(int G, int D, int W, int nb_max) {
+  return G == kFG && D == kFD && W == kFW && nb_max > 0 &&
+         fused_clusters(fused_cluster(nb_max)) > 0;
+}
+
+cudaError_t launch_score_fused(const uint16_t *q, const uint16_t *meank, float *scores, int L,
+                               int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
+                               int64_t nb_total, int nb_max, int32_t *status, cudaStream_t s) {
+  if (H <= 0 || Hq != kFG * H || !score_fused_supported(Hq / H, D, W, nb_max))
+    return cudaErrorNotSupported;
+  const int C = fused_cluster(nb_max), nc = fused_clusters(C);
+  const int n_units = L * H * n_sess;
+  CUtensorMap mk_map, q_map;
+  if (!make_map(&mk_map, meank, (uint64_t)L * H * nb_total, D, kFTB) ||
+      !make_q_wmajor_map(&q_map, q, (uint64_t)L * n_sess * H))
+    return cudaErrorNotSupported;
+  FusedArgs a{};
+  a.scores = scores;
+  a.blk_off = blk_off;
+  a.status = status;
+  a.L = L;
+  a.H = H;
+  a.n_sess = n_sess;
+  a.max_tiles = (nb_max + kFTB - 1) / kFTB;
+  a.nb_total = nb_total;
+  a.zscale = 1.4426950408889634f / sqrtf((float)D);
+  a.idesc = make_idesc(128, kFTB);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((nc < n_units ? nc : n_units) * C);
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = FusedSmem::bytes();
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_score_fused, mk_map, q_map, a);
+}
+
+}  // namespace kvc

@@ -576,61 +576,6 @@ constexpr int kRingMaxC = 4;
 template <int RT> constexpr int ring_groups() { return RT == 1 ? 3 : 2; }
 template <int RT> constexpr int ring_threads() { return 64 + 128 * ring_groups<RT>(); }
 
-__device__ __forceinline__ uint32_t cluster_nrank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_f2(uint32_t addr, float2 v) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void fence_acqrel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Wait for a phase, bounded at one second of wall time, giving up at once if
-// another role of the CTA failed.  No sleep between polls: try_wait itself
-// suspends the thread until the phase completes or a short hardware limit
-// passes, so a hand-off between roles costs no extra wake-up latency.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *failed,
-                                              bool cluster_scope = false) {
-  if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-    if (cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    if (*failed || global_ns() - t0 > 1000000000ull) return false;
-  }
-}
-
 template <int RT>
 struct RingSmem {
   // Ring depth: the loaded latency of a 32 KB tile is ≈ 3 µs, so the ring
@@ -709,17 +654,6 @@ template <int NS>
 __device__ __forceinline__ int pass2_tile(int j, int my_tiles) {
   if (my_tiles < NS) return j;
   return j < NS ? my_tiles - NS + j : j - NS;
-}
-
-// Split TMEM load: issue now, wait later.  The wait names the destination
-// registers as in/out operands, so no use of them can move above it.
-__device__ __forceinline__ void tmem_issue32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-               : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait32(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])::"memory");
 }
 
 // Pass-1 epilogue of one 128-block tile: (max, Σ2^(z−max)) of this lane's
@@ -1120,13 +1054,15 @@ int persistent_capacity(size_t smem) {
   return per_sm > 0 ? 2 * sms : 0;
 }
 
-// Which tensor-core kernel runs: KVC_SCORE_PATH=ring|persist|split forces one
-// (tests use this); by default the pipelined cluster kernel, else the
-// persistent one, else split mode.
-enum TcPath { kAuto, kRing, kPersist, kSplit };
+// Which tensor-core kernel runs: KVC_SCORE_PATH=fused|ring|persist|split
+// forces one (tests use this); by default the single-read kernel where the
+// shape allows it, else the pipelined cluster kernel, else the persistent
+// one, else split mode.
+enum TcPath { kAuto, kFused, kRing, kPersist, kSplit };
 TcPath forced_path() {
   const char *e = getenv("KVC_SCORE_PATH");
   if (!e) return kAuto;
+  if (!strcmp(e, "fused")) return kFused;
   if (!strcmp(e, "ring")) return kRing;
   if (!strcmp(e, "persist")) return kPersist;
   if (!strcmp(e, "split")) return kSplit;
@@ -1196,7 +1132,7 @@ template <int RT, int S, int W>
 cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, int n_units,
                         const Plan &p, void *ws, cudaStream_t s) {
   const TcPath forced = forced_path();
-  if (forced == kAuto || forced == kRing) {
+  if (forced == kAuto || forced == kRing || forced == kFused) {
     const int C = ring_cluster(p.C * p.CH);
     const int nc = ring_clusters<RT, W>(C, a.D);
     if (nc > 0) {
@@ -1243,7 +1179,7 @@ cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
 template <int RT, int S>
 int launches_rt(const Plan &p, int W, int D, int n_sess) {
   const TcPath forced = forced_path();
-  if (forced == kAuto || forced == kRing) {
+  if (forced == kAuto || forced == kRing || forced == kFused) {
     const int C = ring_cluster(p.C * p.CH);
     const int nc = W == 8    ? ring_clusters<RT, 8>(C, D)
                    : W == 16 ? ring_clusters<RT, 16>(C, D)
@@ -1266,6 +1202,10 @@ bool score_tc_supported(int R, int W, int D) { return plan(R, W, D, 1).ok; }
 int score_tc_launches(int R, int W, int D, int n_sess, int nb_max) {
   Plan p = plan(R, W, D, nb_max);
   if (!p.ok) return 0;
+  const TcPath forced = forced_path();
+  if ((forced == kAuto || forced == kFused) && R % W == 0 &&
+      score_fused_supported(R / W, D, W, nb_max))
+    return 1;
   return p.RT == 1 ? launches_rt<1, 2>(p, W, D, n_sess) : launches_rt<2, 1>(p, W, D, n_sess);
 }
 
@@ -1289,6 +1229,12 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
   const int G = Hq / H, R = G * W;
   Plan p = plan(R, W, D, nb_max);
   if (!p.ok) return cudaErrorNotSupported;
+  const TcPath forced = forced_path();
+  if (forced == kAuto || forced == kFused) {
+    cudaError_t e = launch_score_fused(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
+                                       nb_total, nb_max, status, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   CUtensorMap mk_map, q_map;
   uint64_t mk_rows = (uint64_t)L * H * nb_total;
   uint64_t q_rows = (uint64_t)L * n_sess * Hq * W;

@@ -49,6 +49,12 @@ CONFIGS = {
     "split_long": W.MeanKConfig(name="split", L=1, H=2, Hq=8, D=128, W=32,
                                 hist=[32 * 4500, 32 * 700], budget=96, n_sink=1,
                                 n_recent=4, gamma=W.GAMMA_PLANTED, L_pack=1, seed=13),
+    # 64 tiles in the longest session: eight CTAs of eight tiles each, four
+    # of which the single-read scorer multiplies again after the exchange;
+    # the 100-block session leaves seven CTAs of its cluster without a tile
+    "fused_long": W.MeanKConfig(name="fl", L=1, H=2, Hq=8, D=128, W=32,
+                                hist=[32 * 8192, 32 * 100, 32 * 1500], budget=64, n_sink=1,
+                                n_recent=4, gamma=W.GAMMA_PLANTED, L_pack=1, seed=14),
 }
 
 
@@ -131,12 +137,13 @@ def test_score_parity(kvc, orc, name):
     assert_scores_close(got.reshape(-1), c.scores_ref.reshape(-1))
 
 
-@pytest.mark.parametrize("path", ["cc", "ring", "persist", "split"])
+@pytest.mark.parametrize("path", ["cc", "fused", "ring", "persist", "split"])
 @pytest.mark.parametrize("name", ["tiny", "8b_scaled", "ragged_scaled", "gqa6_rows192",
-                                  "split_long"])
+                                  "split_long", "fused_long"])
 def test_score_parity_every_scorer(kvc, orc, name, path, monkeypatch):
     """Every scorer the library can pick — CUDA cores (shapes the tensor-core
-    kernels do not cover), the pipelined cluster kernel, the persistent
+    kernels do not cover), the single-read cluster kernel (4 query heads per
+    KV head, W = 32, D = 128), the two-pass cluster kernel, the persistent
     kernel and the two-launch split mode — against the oracle."""
     c = case(kvc, orc, name)
     monkeypatch.setenv("KVC_SCORE_PATH", path)
@@ -147,6 +154,27 @@ def test_score_parity_every_scorer(kvc, orc, name, path, monkeypatch):
     torch.cuda.synchronize()
     assert kvc.kvc_device_status(c.ev.dev_status) == 0
     assert_scores_close(out.cpu().numpy().reshape(-1), c.scores_ref.reshape(-1))
+
+
+@pytest.mark.parametrize("path", ["fused", "ring"])
+def test_scores_do_not_depend_on_launch_split(kvc, orc, path, monkeypatch):
+    """A unit's scores are the same bits whether its layer is scored alone or
+    with the others, and from one run to the next."""
+    c = case(kvc, orc, "8b_scaled")
+    cfg = c.cfg
+    monkeypatch.setenv("KVC_SCORE_PATH", path)
+    full = torch.full_like(c.ev.scores, -1.0)
+    again = torch.full_like(c.ev.scores, -1.0)
+    one = torch.full_like(c.ev.scores[1:], -1.0)
+    args = (cfg.D, cfg.W, c.ev.blk_off, cfg.n_sess, cfg.nb_total, c.ev.nb_max, c.ev.ws,
+            c.ev.dev_status)
+    kvc.kvc_score(c.q, c.meank, full, cfg.L, cfg.H, cfg.Hq, *args)
+    kvc.kvc_score(c.q, c.meank, again, cfg.L, cfg.H, cfg.Hq, *args)
+    kvc.kvc_score(c.q[1:], c.meank[1:], one, 1, cfg.H, cfg.Hq, *args)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(c.ev.dev_status) == 0
+    assert torch.equal(full.view(torch.int32), again.view(torch.int32))
+    assert torch.equal(full[1:].view(torch.int32), one.view(torch.int32))
 
 
 @pytest.mark.parametrize("name", list(CONFIGS))
