@@ -56,7 +56,7 @@ constexpr int kFNS = 2;          // Mean-K ring stages (64 KB each)
 constexpr int kFQB = 2;          // query-row buffers (32 KB each)
 constexpr int kFNBUF = 2;        // TMEM buffers of 256 columns
 constexpr int kFKeep = kFNBUF;   // tiles whose logits stay in TMEM
-constexpr int kFTarget = 4;      // tiles per CTA and unit the cluster size aims at
+constexpr int kFTarget = 8;      // tiles per CTA of a mean-length unit the cluster aims at
 constexpr int kFNEG = 4;         // epilogue warpgroups
 constexpr int kFCols = kFTB / kFNEG;  // columns of every tile a group takes (64)
 constexpr int kFNCH = kFCols / 32;    // their 32-column chunks
@@ -547,15 +547,6 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
 
 // --------------------------------------------------------------- host
 
-// CTAs per cluster: about kFTarget tiles of the longest session per CTA, at
-// most eight CTAs.  Fewer, longer shares spread the exchange over more
-// tiles; the tiles beyond the four kept in TMEM are multiplied twice.
-int fused_cluster(int nb_max) {
-  const int tiles = (nb_max + kFTB - 1) / kFTB;
-  int c = (tiles + kFTarget - 1) / kFTarget;
-  return c < 1 ? 1 : (c > kFMaxC ? kFMaxC : c);
-}
-
 // Clusters of C that can be resident at once (0: the kernel cannot run).
 int fused_clusters(int C) {
   static int cached[kFMaxC + 1] = {};
@@ -585,6 +576,19 @@ int fused_clusters(int C) {
   return n;
 }
 
+// CTAs per cluster: about kFTarget tiles of a mean-length session per CTA,
+// rounded down to a power of two (at most eight), and smaller while the
+// size cannot be scheduled.  Short sessions then leave few CTAs of their
+// cluster idle, and long ones multiply more of their tiles twice.
+int fused_cluster(int64_t nb_total, int n_sess) {
+  const int64_t mean = (nb_total + n_sess - 1) / (n_sess > 0 ? n_sess : 1);
+  const int64_t want = ((mean + kFTB - 1) / kFTB + kFTarget - 1) / kFTarget;
+  int c = 1;
+  while (2 * c <= want && 2 * c <= kFMaxC) c *= 2;
+  while (c > 1 && fused_clusters(c) == 0) c /= 2;
+  return c;
+}
+
 // q as [units][W][G][D] seen through strides that walk g inside w: a box of
 // (64 columns, G, W, 1) lands in shared memory as rows ρ = w·G + g.
 bool make_q_wmajor_map(CUtensorMap *m, const void *q, uint64_t q_units) {
@@ -603,8 +607,7 @@ bool make_q_wmajor_map(CUtensorMap *m, const void *q, uint64_t q_units) {
 }  // namespace
 
 bool score_fused_supported(int G, int D, int W, int nb_max) {
-  return G == kFG && D == kFD && W == kFW && nb_max > 0 &&
-         fused_clusters(fused_cluster(nb_max)) > 0;
+  return G == kFG && D == kFD && W == kFW && nb_max > 0 && fused_clusters(1) > 0;
 }
 
 cudaError_t launch_score_fused(const uint16_t *q, const uint16_t *meank, float *scores, int L,
@@ -612,7 +615,7 @@ cudaError_t launch_score_fused(const uint16_t *q, const uint16_t *meank, float *
                                int64_t nb_total, int nb_max, int32_t *status, cudaStream_t s) {
   if (H <= 0 || Hq != kFG * H || !score_fused_supported(Hq / H, D, W, nb_max))
     return cudaErrorNotSupported;
-  const int C = fused_cluster(nb_max), nc = fused_clusters(C);
+  const int C = fused_cluster(nb_total, n_sess), nc = fused_clusters(C);
   const int n_units = L * H * n_sess;
   CUtensorMap mk_map, q_map;
   if (!make_map(&mk_map, meank, (uint64_t)L * H * nb_total, D, kFTB) ||
