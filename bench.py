@@ -302,7 +302,7 @@ def run_ours(args, rank, world, local_rank):
     ab = algorithmic_bytes(cfg)
     peak, peak_src = peaks()
     dom = max(("score", "select", "pack"), key=lambda s: mean[s])
-    kern = {"score": "k_score_ring", "select": "k_select", "pack": "k_pack_rerope"}[dom]
+    kern = {"score": "k_score_fused", "select": "k_select", "pack": "k_pack_rerope"}[dom]
     score_kernels = kvc.kvc_score_launches(max(1, cfg.L // len(ev.groups)), cfg.H, cfg.Hq,
                                            cfg.D, cfg.W, cfg.n_sess, cfg.nb_total)
     achieved = ab[dom] / (mean[dom] * 1e-3) / 1e9 if ab[dom] else 0.0

@@ -56,7 +56,7 @@ constexpr int kFNS = 2;          // Mean-K ring stages (64 KB each)
 constexpr int kFQB = 2;          // query-row buffers (32 KB each)
 constexpr int kFNBUF = 2;        // TMEM buffers of 256 columns
 constexpr int kFKeep = kFNBUF;   // tiles whose logits stay in TMEM
-constexpr int kFTarget = 8;      // tiles per CTA of a mean-length unit the cluster aims at
+constexpr int kFTarget = 4;      // tiles per CTA of a mean-length unit the cluster aims at
 constexpr int kFNEG = 4;         // epilogue warpgroups
 constexpr int kFCols = kFTB / kFNEG;  // columns of every tile a group takes (64)
 constexpr int kFNCH = kFCols / 32;    // their 32-column chunks
@@ -161,12 +161,40 @@ __device__ __forceinline__ void merge_lse(float &m, float &s, float m2, float s2
   m = mn;
 }
 
+// Packed fp32 pairs (two lanes of one 64-bit register): each lane of
+// fma.rn.f32x2 / add.rn.f32x2 rounds exactly like the scalar instruction.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Pass 1 of this group's columns of one tile for this lane's query row:
 // (max, Σ2^(z·zs − max)) over the `valid` blocks, 32 columns at a time.
+// Column j adds into accumulator j mod 8 (held as four packed pairs).
 __device__ __forceinline__ void fused_pass1(uint32_t taddr, int valid, float zs, float &pm,
                                             float &ps) {
   pm = -INFINITY;
   ps = 0.f;
+  const uint64_t zs2 = pk2(zs, zs);
 #pragma unroll 1
   for (int c = 0; c < kFNCH && 32 * c < valid; c++) {
     uint32_t r[32];
@@ -181,21 +209,34 @@ __device__ __forceinline__ void fused_pass1(uint32_t taddr, int valid, float zs,
       for (int j = 0; j < 32; j++)
         if (j >= nv) v[j] = -INFINITY;
     }
-    float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
+    float m0 = max3(v[0], v[1], v[2]), m1 = max3(v[3], v[4], v[5]);
+    float m2 = max3(v[6], v[7], v[8]), m3 = max3(v[9], v[10], v[11]);
 #pragma unroll
-    for (int j = 4; j < 32; j += 4) {
-      m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
-      m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
+    for (int j = 12; j < 28; j += 8) {
+      m0 = max3(m0, v[j], v[j + 1]);
+      m1 = max3(m1, v[j + 2], v[j + 3]);
+      m2 = max3(m2, v[j + 4], v[j + 5]);
+      m3 = max3(m3, v[j + 6], v[j + 7]);
     }
-    const float mn = fmaxf(pm, fmaxf(m0, m1) * zs);
-    float acc[8];
-    acc[0] = (pm == -INFINITY) ? 0.f : ps * ex2(pm - mn);
+    m0 = max3(m0, v[28], v[29]);
+    m1 = max3(m1, v[30], v[31]);
+    const float mn = fmaxf(pm, fmaxf(max3(m0, m1, m2), m3) * zs);
+    const uint64_t nmn2 = pk2(-mn, -mn);
+    uint64_t acc[4];
+    acc[0] = pk2((pm == -INFINITY) ? 0.f : ps * ex2(pm - mn), 0.f);
 #pragma unroll
-    for (int k = 1; k < 8; k++) acc[k] = 0.f;
+    for (int k = 1; k < 4; k++) acc[k] = pk2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 32; j++) acc[j & 7] += ex2(fmaf(v[j], zs, -mn));
+    for (int j = 0; j < 32; j += 2) {
+      float x0, x1;
+      upk2(fma2(pk2(v[j], v[j + 1]), zs2, nmn2), x0, x1);
+      acc[(j & 7) >> 1] = add2(acc[(j & 7) >> 1], pk2(ex2(x0), ex2(x1)));
+    }
+    float a8[8];
+#pragma unroll
+    for (int k = 0; k < 4; k++) upk2(acc[k], a8[2 * k], a8[2 * k + 1]);
     pm = mn;
-    ps = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    ps = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
   }
 }
 
@@ -215,16 +256,20 @@ __device__ __forceinline__ void fused_pass2(uint32_t taddr, float lse_row, float
                                             float *red_q) {
   const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4, b3 = lane & 8, b4 = lane & 16;
   const int col_in_chunk = bitrev5(lane);
+  const uint64_t zs2 = pk2(zs, zs), nlse2 = pk2(-lse_row, -lse_row);
 #pragma unroll 1
   for (int c = 0; c < kFNCH; c++) {
     uint32_t r[32];
     tmem_issue32(taddr + (uint32_t)(32 * c), r);
     tmem_wait32(r);
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2)
+      upk2(fma2(pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), zs2, nlse2), x[j], x[j + 1]);
     float a[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-      const float lo = fmaf(__uint_as_float(r[i]), zs, -lse_row);
-      const float hi = fmaf(__uint_as_float(r[16 + i]), zs, -lse_row);
+      const float lo = x[i], hi = x[16 + i];
       a[i] = fmaxf(b0 ? hi : lo, __shfl_xor_sync(0xFFFFFFFFu, b0 ? lo : hi, 1));
     }
     float e[8];
@@ -578,8 +623,11 @@ int fused_clusters(int C) {
 
 // CTAs per cluster: about kFTarget tiles of a mean-length session per CTA,
 // rounded down to a power of two (at most eight), and smaller while the
-// size cannot be scheduled.  Short sessions then leave few CTAs of their
-// cluster idle, and long ones multiply more of their tiles twice.
+// size cannot be scheduled.  A tile multiplied twice is reloaded about one
+// round (its CTA's share of a unit, plus the next unit's first tiles) after
+// its first read; with four tiles per CTA that is ~50 MB across the GPU, so
+// the reload still hits L2 (eight tiles per CTA measured 1.57× the
+// algorithmic DRAM reads).
 int fused_cluster(int64_t nb_total, int n_sess) {
   const int64_t mean = (nb_total + n_sess - 1) / (n_sess > 0 ? n_sess : 1);
   const int64_t want = ((mean + kFTB - 1) / kFTB + kFTarget - 1) / kFTarget;
