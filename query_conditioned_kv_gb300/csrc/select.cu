@@ -276,8 +276,14 @@ cudaError_t launch_select(const float *scores, const int64_t *seg_off,
   // Segments are independent and latency-bound: CTAs small enough that
   // several fit on an SM (registers and shared memory) put a few hundred
   // segments in one wave; long segments get more threads per CTA.
+  // With many segments the GPU is full anyway: fewer threads per segment (up
+  // to 64 items each, the sweep's bit masks) put more segments in flight,
+  // while a few hundred segments want the shorter per-step passes.
+  int ipt = kSelIPT;
+  const int64_t waves_threads = (int64_t)device_sm_count() * 2048 * 4;
+  while (ipt < 64 && (int64_t)n_seg * ((max_seg_len + ipt - 1) / ipt) > waves_threads) ipt *= 2;
   int threads = 128;
-  while (threads < kSelThreads && (max_seg_len + threads - 1) / threads > kSelIPT) threads *= 2;
+  while (threads < kSelThreads && (max_seg_len + threads - 1) / threads > ipt) threads *= 2;
   cudaError_t e = cudaFuncSetAttribute(
       k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -66,9 +66,11 @@ def test_select_bad_segment_offsets(kvc):
     assert cnt.cpu().tolist()[1] == 0 and kept.cpu().tolist()[1] == [-1] * 4
 
 
-@pytest.mark.parametrize("W", [4, 8])  # CUDA-core and tensor-core scorers
-def test_score_bad_block_offsets(kvc, W):
-    L, H, Hq, D, nb = 1, 1, 2, 64, 8
+# CUDA-core scorer (W = 4), two-pass tensor-core scorer (W = 8) and the
+# single-read one (4 query heads per KV head, W = 32, D = 128)
+@pytest.mark.parametrize("W,Hq,D", [(4, 2, 64), (8, 2, 64), (32, 4, 128)])
+def test_score_bad_block_offsets(kvc, W, Hq, D):
+    L, H, nb = 1, 1, 8
     q = torch.randn(1, L, Hq, W, D, device=DEV).to(torch.bfloat16)
     mk = torch.randn(L, H, nb, D, device=DEV).to(torch.bfloat16)
     sc = torch.full((L, H, nb), -5.0, device=DEV)
@@ -80,6 +82,31 @@ def test_score_bad_block_offsets(kvc, W):
     torch.cuda.synchronize()
     assert kvc.kvc_device_status(st) == 7
     assert torch.all(sc == -5.0)
+
+
+def test_score_bad_session_leaves_the_others_scored(kvc):
+    """Single-read scorer: a session whose offsets run past the index is
+    reported (KVC_ERR_BOUNDS) and left unwritten; the other session of the
+    same launch is scored as usual."""
+    L, H, Hq, D, W, nb = 2, 2, 8, 128, 32, 600
+    q = torch.randn(L, 2, Hq, W, D, device=DEV).to(torch.bfloat16)
+    mk = (torch.randn(L, H, nb, D, device=DEV) * 0.2).to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(kvc.kvc_score_workspace_size(L, H, Hq, W, 2, 500, nb) + 256,
+                     dtype=torch.uint8, device=DEV)
+    good = torch.tensor([0, 400, 600], dtype=torch.int64, device=DEV)
+    ref = torch.full((L, H, nb), -5.0, device=DEV)
+    kvc.kvc_score(q, mk, ref, L, H, Hq, D, W, good, 2, nb, 400, ws, st)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(st) == 0
+    bad = torch.tensor([0, 400, 900], dtype=torch.int64, device=DEV)  # session 1 past nb_total
+    sc = torch.full((L, H, nb), -5.0, device=DEV)
+    kvc.kvc_score(q, mk, sc, L, H, Hq, D, W, bad, 2, nb, 500, ws, st)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(st) == 7
+    assert torch.all(sc[:, :, 400:] == -5.0)
+    # same mean session length, so the same cluster size: session 0 has the same bits
+    assert torch.equal(sc[:, :, :400].view(torch.int32), ref[:, :, :400].view(torch.int32))
 
 
 def test_host_validation_raises_before_launch(kvc):

@@ -75,3 +75,22 @@ def test_select_all_equal_and_monotone(kvc, orc):
     assert np.array_equal(kept, kref) and np.array_equal(cnt, cref)
     assert np.array_equal(mask, mref)
     assert kept[0, :5].tolist() == [0, 1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("n_seg", [3000, 7000])
+def test_select_many_segments_bit_exact(kvc, orc, n_seg):
+    """Launches with tens of millions of items: the kernel then runs fewer
+    threads per segment (32 or 64 items each) to keep more segments in
+    flight; the result is the same bits."""
+    rng = np.random.default_rng(n_seg)
+    lens = rng.integers(1, 8193, n_seg)
+    lens[:3] = [8192, 1, 300]
+    scores = rng.random(int(lens.sum())).astype(np.float32)
+    scores[::7] = 0.5  # ties
+    budget, n_sink, n_recent = 256, 1, 4
+    off, kept, cnt, mask = _run(kvc, scores, [int(n) for n in lens], budget, n_sink, n_recent)
+    kref, cref, mref = orc.select_segments(scores, off, budget, n_sink, n_recent,
+                                           mask_words=mask.shape[1])
+    assert np.array_equal(cnt, cref)
+    assert np.array_equal(kept, kref)
+    assert np.array_equal(mask, mref)
