@@ -12,10 +12,13 @@
 //   1. the scores are mapped to order-preserving uint32 keys (−0.0 folded
 //      onto +0.0, NaN below −inf) and staged in shared memory;
 //   2. the k-th largest non-forced key T is the largest T with
-//      #(key ≥ T) ≥ k: it is found bit by bit, from the highest bit where
-//      the candidates differ, two bits per step (counts against three
-//      thresholds, summed with warp reductions), then the number of items
-//      equal to T still needed is k − #(key > T);
+//      #(key ≥ T) ≥ k: it is found eight bits at a time (MSB radix levels),
+//      from the highest bit where the candidates differ.  A level counts the
+//      next digit of the keys that still match the decided bits into shared
+//      histograms (after the first level few keys match) and takes the
+//      largest digit whose count from the top reaches the number still
+//      needed.  The count left at the end is the number of items equal to T
+//      still needed, k − #(key > T);
 //   3. an ordered sweep in two block scans (equal-to-T counts, then keep
 //      counts, from per-thread bit masks) keeps forced ∪ {key > T} ∪ {the
 //      first `need` items with key == T} and writes their indices
@@ -31,6 +34,9 @@ constexpr int kSelThreads = 1024;
 // Items per thread the launch aims for (at most 64: the sweep's bit masks).
 // Fewer threads per segment mean cheaper barriers in the threshold search.
 constexpr int kSelIPT = 16;
+// Histogram copies of the radix levels (warp w counts into copy w mod 8), so
+// conflicting atomics come from at most a few warps.
+constexpr int kSelHist = 8;
 
 // Keys are stored with one pad word per 32: a thread's contiguous chunk and
 // the strided sweeps both read distinct banks.
@@ -83,6 +89,7 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
   extern __shared__ uint32_t dyn[];
   uint32_t *keys = dyn;                               // [kp(max_seg_len)]
   uint32_t *mask_s = dyn + kp(max_seg_len) + 1;       // [words]
+  uint32_t *hist = mask_s + words;                    // [kSelHist][256]
   __shared__ uint32_t s_red[3][32];
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t s_kmax, s_kmin, s_prefix, s_need;
@@ -151,57 +158,60 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
     }
     __syncthreads();
     const uint32_t kmax = s_kmax, kmin = s_kmin;
-    int bit = kmax == kmin ? -1 : 31 - __clz(kmax ^ kmin);
-    prefix = bit < 0 ? kmax : bit == 31 ? 0u : (kmax >> (bit + 1)) << (bit + 1);
-    while (bit >= 0) {
-      const int b0 = bit >= 1 ? bit - 1 : 0;  // lowest bit decided in this step
-      const bool two = bit >= 1;
-      uint32_t c1 = 0, c2 = 0, c3 = 0;
-      const uint32_t t1 = prefix | (1u << b0), t2 = prefix | (2u << b0), t3 = prefix | (3u << b0);
+    int hi = kmax == kmin ? -1 : 31 - __clz(kmax ^ kmin);  // highest undecided bit
+    prefix = hi < 0 ? kmax : hi == 31 ? 0u : (kmax >> (hi + 1)) << (hi + 1);
+    // Eight bits per level: a histogram of the next digit over the keys that
+    // still match the decided bits (after the first level, few do), then the
+    // largest digit whose count from the top reaches `need`.
+    while (hi >= 0) {
+      const int lo = hi >= 7 ? hi - 7 : 0;
+      const uint32_t dmask = (2u << (hi - lo)) - 1u;
+      const uint32_t pmask = hi == 31 ? 0u : ~((2u << hi) - 1u);
+      uint32_t *h = hist + (warp % kSelHist) * 256;
+      for (int j = tid; j < kSelHist * 256; j += nt) hist[j] = 0u;
+      __syncthreads();
       for (int i = n_sink + tid; i < rec0; i += nt) {
         const uint32_t key = keys[kp(i)];
-        c1 += key >= t1 ? 1u : 0u;
-        c2 += key >= t2 ? 1u : 0u;
-        c3 += key >= t3 ? 1u : 0u;
-      }
-      c1 = __reduce_add_sync(0xFFFFFFFFu, c1);
-      c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
-      c3 = __reduce_add_sync(0xFFFFFFFFu, c3);
-      if (lane == 0) {
-        s_red[0][warp] = c1;
-        s_red[1][warp] = c2;
-        s_red[2][warp] = c3;
+        if ((key & pmask) == prefix) atomicAdd(&h[(key >> lo) & dmask], 1u);
       }
       __syncthreads();
       if (warp == 0) {
-        const uint32_t C1 = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[0][lane] : 0u);
-        const uint32_t C2 = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[1][lane] : 0u);
-        const uint32_t C3 = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[2][lane] : 0u);
-        if (lane == 0) {
-          // #(key ≥ prefix) ≥ k holds; take the largest threshold that keeps it
+        // lane l: bins 8l … 8l+7 summed over the histogram copies
+        uint32_t loc[8], lsum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; b++) {
           uint32_t v = 0;
-          if (two && C3 >= need) v = 3;
-          else if (two && C2 >= need) v = 2;
-          else if (C1 >= need) v = 1;
-          s_prefix = prefix | (v << b0);
+          for (int c = 0; c < kSelHist; c++) v += hist[c * 256 + 8 * lane + b];
+          loc[b] = v;
+          lsum += v;
+        }
+        uint32_t sfx = lsum;  // Σ of the bins ≥ 8·lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, sfx, o);
+          if (lane + o < 32) sfx += y;
+        }
+        const uint32_t above = sfx - lsum;  // Σ of the bins ≥ 8·(lane + 1)
+        if (above < need && sfx >= need) {  // exactly one lane
+          uint32_t acc = above;
+          int d = 8 * lane;
+#pragma unroll
+          for (int b = 7; b >= 0; b--)
+            if (acc + loc[b] >= need) {
+              d = 8 * lane + b;
+              break;
+            } else {
+              acc += loc[b];
+            }
+          s_prefix = prefix | ((uint32_t)d << lo);
+          s_need = need - acc;
         }
       }
       __syncthreads();
       prefix = s_prefix;
-      bit = b0 - 1;
+      need = s_need;
+      hi = lo - 1;
     }
-    // items equal to T still needed: k − #(key > T)
-    uint32_t gt = 0;
-    for (int i = n_sink + tid; i < rec0; i += nt) gt += keys[kp(i)] > prefix ? 1u : 0u;
-    gt = __reduce_add_sync(0xFFFFFFFFu, gt);
-    if (lane == 0) s_red[0][warp] = gt;
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t G = __reduce_add_sync(0xFFFFFFFFu, lane < n_warps ? s_red[0][lane] : 0u);
-      if (lane == 0) s_need = (uint32_t)k - G;
-    }
-    __syncthreads();
-    need = s_need;
   }
   const uint32_t T = prefix;  // threshold key (valid when k > 0)
 
@@ -272,7 +282,8 @@ cudaError_t launch_select(const float *scores, const int64_t *seg_off,
                           uint32_t *keepmask, int32_t *status,
                           cudaStream_t s) {
   int words = (max_seg_len + 31) / 32;
-  size_t smem = ((size_t)max_seg_len + max_seg_len / 32 + 1 + words) * sizeof(uint32_t);
+  size_t smem = ((size_t)max_seg_len + max_seg_len / 32 + 1 + words + kSelHist * 256) *
+                sizeof(uint32_t);
   // Segments are independent and latency-bound: CTAs small enough that
   // several fit on an SM (registers and shared memory) put a few hundred
   // segments in one wave; long segments get more threads per CTA.
