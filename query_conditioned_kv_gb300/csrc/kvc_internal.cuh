@@ -37,16 +37,18 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v) {
   __stcs(reinterpret_cast<uint4 *>(p), v);
 }
 
-// SM count of the current device (cached per process; 1 if the query fails).
+// SM count of the current device (cached per device; 1 if the query fails).
 inline int device_sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 1;
-  }
-  return n;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  int *n = (dev >= 0 && dev < 64) ? &cache[dev] : nullptr;
+  if (n && *n) return *n;
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+    v = 1;
+  if (n) *n = v;
+  return v;
 }
 
 // ------------------------------------------------------------ launches

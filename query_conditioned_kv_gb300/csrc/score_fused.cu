@@ -594,10 +594,12 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
 
 // Clusters of C that can be resident at once (0: the kernel cannot run).
 int fused_clusters(int C) {
-  static int cached[kFMaxC + 1] = {};
-  static bool done[kFMaxC + 1] = {};
+  static int cached[64][kFMaxC + 1] = {};
+  static bool done[64][kFMaxC + 1] = {};
   if (C < 1 || C > kFMaxC) return 0;
-  if (done[C]) return cached[C];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (done[dev][C]) return cached[dev][C];
   const size_t smem = FusedSmem::bytes();
   int n = 0;
   if (cudaFuncSetAttribute(k_score_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -616,8 +618,8 @@ int fused_clusters(int C) {
     if (cudaOccupancyMaxActiveClusters(&n, k_score_fused, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();
-  cached[C] = n;
-  done[C] = true;
+  cached[dev][C] = n;
+  done[dev][C] = true;
   return n;
 }
 
