@@ -28,13 +28,14 @@ def _cfg(name, hist_blocks, L=1, seed=0):
                          n_recent=2, gamma=W.GAMMA_PLANTED, L_pack=0, seed=seed)
 
 
-# mean session length in 256-block tiles → CTAs per cluster (4 tiles per CTA)
+# mean session length in 256-block tiles → CTAs per cluster (4 tiles per CTA;
+# 8 when the longest session is 1.5× the mean or more)
 CASES = {
     "c1_partial": _cfg("c1", [700 + 37], L=2, seed=21),       # 3 tiles → 1 CTA
     "c2_rec": _cfg("c2", [2048 + 200], seed=22),             # 9 tiles → 2 CTAs, 3 reloads
     "c4": _cfg("c4", [4096 + 300], seed=23),                 # 18 tiles → 4 CTAs, 3 reloads
     "c8_long": _cfg("c8", [16384 + 129], seed=24),           # 65 tiles → 8 CTAs, 7 reloads
-    "mixed": _cfg("mx", [12000, 40, 3000, 256, 9000], seed=25),  # mean 19 tiles → 4 CTAs
+    "mixed": _cfg("mx", [12000, 40, 3000, 256, 9000], seed=25),  # spread lengths: 8 tiles/CTA → 2 CTAs
     "c1_long": _cfg("c1l", [1000, 900], seed=26),             # mean 4 tiles → 1 CTA, 2 reloads
 }
 
