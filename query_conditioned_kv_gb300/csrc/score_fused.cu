@@ -13,20 +13,22 @@
 //     product D[ρ][b] (M = 128 query rows, N = 256 blocks, K = 128) into one
 //     of two 256-column TMEM buffers.  (N = 256 runs the tensor pipe about
 //     2.3 times faster per block than two N = 128 products.)
-//   * The query rows are loaded w-major (row ρ = 4w + g) by a 4-D tensor map
-//     whose strides walk g inside w, so TMEM lane ρ holds (w = ρ/4, g = ρ%4):
-//     the four query heads of one window position sit in four adjacent lanes.
+//   * The query rows are loaded by a 5-D tensor map in the order
+//     ρ = g_l + 2·w_l + 8·g_h + 16·w_h (g = 2·g_h + g_l, w = 4·w_h + w_l): in
+//     each 16-lane half of TMEM, lanes ρ and ρ + 8 hold query heads g and
+//     g + 2 of one window position.
 //   * Pass 1 (per lane = query row): online (max, Σ2^(z−max)) over the tile's
 //     blocks.  The logits of a CTA's last (up to) two tiles stay in TMEM.
 //   * The CTAs of the cluster exchange their row partials with st.async into
 //     each other's shared memory, and every CTA forms the row LSEs.
-//   * Pass 2 reads the kept logits again: x = z·log2e/√D − LSE, then a
-//     butterfly over the warp: max over g (lanes ρ^1, ρ^2), one ex2 per
-//     (w, b), and the sum over the warp's 8 window positions (ρ^4, ρ^8,
-//     ρ^16), each stage halving the columns a lane carries, so lane ℓ ends
-//     with the sum for column bitrev5(ℓ) of each 32-column chunk.  The four
-//     lane quarters (32 window positions) are added through shared memory in
-//     a fixed order.
+//   * Pass 2 reads the kept logits again with the 16x256b TMEM shape, which
+//     gives a thread two rows (lanes t/4 and t/4 + 8 of a 16-lane half): the
+//     heads g_l and g_l + 2 of window position t/8.  x = z·log2e/√D − LSE; the
+//     max over those two heads in the thread, over g_l with lane t^4, one ex2
+//     per (w, b), the sum over the half's four window positions with lanes
+//     t^8 and t^16 (each stage halving the columns a lane carries), the two
+//     halves added in the thread, and the warp quarters through shared
+//     memory in a fixed order.
 //   * Four epilogue warpgroups split every tile: group e takes its columns
 //     64e … 64e + 63, so each step of the chain above has 16 warps on it.
 //   * A CTA with more than two tiles multiplies its first tiles again after
@@ -240,58 +242,77 @@ __device__ __forceinline__ void fused_pass1(uint32_t taddr, int valid, float zs,
   }
 }
 
-// Bit reversal of a lane index (5 bits): the column a lane holds after the
-// five halving stages of fused_pass2.
-__device__ __forceinline__ int bitrev5(int x) {
-  return ((x & 1) << 4) | ((x & 2) << 2) | (x & 4) | ((x & 8) >> 2) | ((x & 16) >> 4);
+// 16 lanes × 32 columns of TMEM with the 16x256b shape: register 4k + j of
+// thread t holds lane (t/4 + 8·(j ≥ 2)), column 8k + 2·(t%4) + (j & 1).
+__device__ __forceinline__ void tmem_ld16x256x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Pass 2 of one tile.  This lane is query row ρ = 32·quarter + lane, i.e.
-// window position w = 8·quarter + lane/4 and head g = lane%4.  For each
-// 32-column chunk: x = z·zs − LSE[ρ]; max over g (xor 1, 2), ex2, sum over
-// the warp's w (xor 4, 8, 16).  Each stage keeps the half of the columns
-// selected by the lane bit and receives the partner's copy of it.  The
-// warp's 32 column sums go to red[quarter][col].
-__device__ __forceinline__ void fused_pass2(uint32_t taddr, float lse_row, float zs, int lane,
+// Pass 2 of one tile for this warp's 32 query rows (TMEM lanes 32q … 32q+31 =
+// two 16-lane halves; `taddr` points at lane 32q and this group's columns).
+// Rows are ordered so that in half h, lane 2·w_l + g_l + 8·g_h is window
+// position w = 4·(2q + h) + w_l and query head g = 2·g_h + g_l: the 16x256b
+// load gives thread t heads g_l and g_l + 2 (g_l = bit 2 of t) of window
+// position w_l = t/8.  Per 32 columns and half: x = z·zs − LSE; max over g_h
+// in the thread, over g_l with lane t^4 (each stage halving the columns a
+// lane carries), one ex2, the sum over w_l with lanes t^8 and t^16; the two
+// halves are added in the thread.  Lane t ends with column
+// 16·b2 + 8·b3 + 2·(t%4) + b4 (b_i = bit i of t).
+__device__ __forceinline__ void fused_pass2(uint32_t taddr, const float *lse_q, float zs, int lane,
                                             float *red_q) {
-  const bool b0 = lane & 1, b1 = lane & 2, b2 = lane & 4, b3 = lane & 8, b4 = lane & 16;
-  const int col_in_chunk = bitrev5(lane);
-  const uint64_t zs2 = pk2(zs, zs), nlse2 = pk2(-lse_row, -lse_row);
+  const bool b2 = lane & 4, b3 = lane & 8, b4 = lane & 16;
+  const int col_in_chunk = 16 * (int)b2 + 8 * (int)b3 + 2 * (lane & 3) + (int)b4;
+  const uint64_t zs2 = pk2(zs, zs);
+  uint64_t nl2[2][2];  // [half][g_h]: −LSE of this thread's two rows, paired
+#pragma unroll
+  for (int h = 0; h < 2; h++)
+#pragma unroll
+    for (int gh = 0; gh < 2; gh++) {
+      const float l = lse_q[16 * h + (lane >> 2) + 8 * gh];
+      nl2[h][gh] = pk2(-l, -l);
+    }
 #pragma unroll 1
   for (int c = 0; c < kFNCH; c++) {
-    uint32_t r[32];
-    tmem_issue32(taddr + (uint32_t)(32 * c), r);
-    tmem_wait32(r);
-    float x[32];
+    float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; j += 2)
-      upk2(fma2(pk2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), zs2, nlse2), x[j], x[j + 1]);
-    float a[16];
+    for (int h = 0; h < 2; h++) {
+      uint32_t r[16];
+      tmem_ld16x256x4(taddr + ((uint32_t)(16 * h) << 16) + (uint32_t)(32 * c), r);
+      float v[8];  // [2k + e]: column 8k + 2·(t%4) + e, max over g_h
 #pragma unroll
-    for (int i = 0; i < 16; i++) {
-      const float lo = x[i], hi = x[16 + i];
-      a[i] = fmaxf(b0 ? hi : lo, __shfl_xor_sync(0xFFFFFFFFu, b0 ? lo : hi, 1));
+      for (int k = 0; k < 4; k++) {
+        float x0, x1, y0, y1;
+        upk2(fma2(pk2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1])), zs2, nl2[h][0]),
+             x0, x1);
+        upk2(fma2(pk2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])), zs2,
+                  nl2[h][1]),
+             y0, y1);
+        v[2 * k] = fmaxf(x0, y0);
+        v[2 * k + 1] = fmaxf(x1, y1);
+      }
+      float e[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const float keep = b2 ? v[4 + i] : v[i], send = b2 ? v[i] : v[4 + i];
+        e[i] = ex2(fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4)));
+      }
+      float s2[2];
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        const float keep = b3 ? e[2 + i] : e[i], send = b3 ? e[i] : e[2 + i];
+        s2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+      }
+      const float keep = b4 ? s2[1] : s2[0], send = b4 ? s2[0] : s2[1];
+      sum += keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
     }
-    float e[8];
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const float keep = b1 ? a[8 + i] : a[i], send = b1 ? a[i] : a[8 + i];
-      e[i] = ex2(fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2)));
-    }
-    float s4[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float keep = b2 ? e[4 + i] : e[i], send = b2 ? e[i] : e[4 + i];
-      s4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-    }
-    float s2[2];
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-      const float keep = b3 ? s4[2 + i] : s4[i], send = b3 ? s4[i] : s4[2 + i];
-      s2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-    }
-    const float keep = b4 ? s2[1] : s2[0], send = b4 ? s2[0] : s2[1];
-    red_q[32 * c + col_in_chunk] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    red_q[32 * c + col_in_chunk] = sum;
   }
 }
 
@@ -371,8 +392,8 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
               break;
             mbar_expect_tx(smem_u32(sm.qfull + qb), kFQ);
             for (int kb = 0; kb < 2; kb++)
-              tma_load_4d(smem_u32(sm.q + qb * kFQ + kb * (kFQ / 2)), &tm_q, kb * 64, 0, 0,
-                          u.q_unit, smem_u32(sm.qfull + qb));
+              tma_load_5d(smem_u32(sm.q + qb * kFQ + kb * (kFQ / 2)), &tm_q, kb * 64, 0, 0,
+                          2 * u.q_unit, 0, smem_u32(sm.qfull + qb));
             qi++;
           }
         }
@@ -444,7 +465,7 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
     // ------------------------------------------------------- epilogue
     const int eg = (warp - 2) >> 2;          // this thread's group
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
-    const int row = 32 * quarter + lane;     // query row ρ = 4w + g
+    const int row = 32 * quarter + lane;     // this thread's TMEM lane (query row)
     const int gt = ((warp - 2) & 3) * 32 + lane;  // 0 … 127 within the group
     const int et = (warp - 2) * 32 + lane;        // 0 … 128·kFNEG − 1
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
@@ -453,9 +474,10 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
     uint32_t t = 0, ui = 0, rp = 0;
     bool ok = true;
     int prev_unit = -1;
-    float lse_prev = 0.f;
     // pass 2 of one job of unit w (local tile i) with row LSE `lse`
-    auto pass2_job = [&](const FUnit &w, int i, uint32_t job, float lse, bool wait_full) {
+    // (the row LSEs are in sm.lse: a unit's reloaded tiles run before the next
+    // exchange, whose first barrier every group passes only after them)
+    auto pass2_job = [&](const FUnit &w, int i, uint32_t job, bool wait_full) {
       const uint32_t buf = job % kFNBUF;
       if (wait_full)
         ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.tfull + buf),
@@ -465,8 +487,8 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
       float *rq = red + (rp & 1) * 4 * kFCols;
       if (ok && valid > 0) {
         tc_fence_after();
-        fused_pass2(tmem + lane_base + buf * kFTB + eg * kFCols, lse, zs, lane,
-                    rq + quarter * kFCols);
+        fused_pass2(tmem + lane_base + buf * kFTB + eg * kFCols, sm.lse + 32 * quarter, zs,
+                    lane, rq + quarter * kFCols);
       }
       tc_fence_before();
       __syncwarp();
@@ -507,7 +529,7 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
       for (int i = 0; i < u.n_rec; i++, t++) pass1_job(u, i, t, pm, ps);         // A(u)
       if (prev_unit >= 0) {
         const FUnit prev = funit(a, prev_unit, C, rank);
-        for (int i = 0; i < prev.n_rec; i++, t++) pass2_job(prev, i, t, lse_prev, true);  // R(prev)
+        for (int i = 0; i < prev.n_rec; i++, t++) pass2_job(prev, i, t, true);  // R(prev)
       }
       const uint32_t tB = t;
       for (int i = u.n_rec; i < u.my_tiles; i++, t++) pass1_job(u, i, t, pm, ps);  // B(u)
@@ -549,11 +571,9 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
           sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);
         }
         named_sync(2, 128 * kFNEG);
-        const float lse_row = sm.lse[row];
         ui++;
         for (int i = u.n_rec; i < u.my_tiles; i++)                               // pass 2 of B(u)
-          pass2_job(u, i, tB + (uint32_t)(i - u.n_rec), lse_row, false);
-        lse_prev = lse_row;
+          pass2_job(u, i, tB + (uint32_t)(i - u.n_rec), false);
       }
       prev_unit = unit;
       if (!ok) {
@@ -645,17 +665,22 @@ int fused_cluster(int64_t nb_total, int n_sess, int nb_max) {
   return c;
 }
 
-// q as [units][W][G][D] seen through strides that walk g inside w: a box of
-// (64 columns, G, W, 1) lands in shared memory as rows ρ = w·G + g.
-bool make_q_wmajor_map(CUtensorMap *m, const void *q, uint64_t q_units) {
+// q rows [units][G = 4][W = 32][D] seen as five dimensions (d, g_l, w_l,
+// g_h + 2·unit, w_h) with g = 2·g_h + g_l and w = 4·w_h + w_l; g_h and the unit
+// share one dimension because the unit stride is twice the g_h stride.  A box
+// (64 columns, 2, 4, 2, 8) at (·, 0, 0, 2·unit, 0) lands in shared memory as
+// rows ρ = g_l + 2·w_l + 8·g_h + 16·w_h: within each 16-row half, rows ρ and
+// ρ + 8 are query heads g and g + 2 of one window position (the pairs the
+// 16x256b TMEM load gives one thread in pass 2).
+bool make_q_rows_map(CUtensorMap *m, const void *q, uint64_t q_units) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)kFD, (cuuint64_t)kFG, (cuuint64_t)kFW, (cuuint64_t)q_units};
-  cuuint64_t strides[3] = {(cuuint64_t)kFW * kFD * 2, (cuuint64_t)kFD * 2,
-                           (cuuint64_t)kFG * kFW * kFD * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)kFG, (cuuint32_t)kFW, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box,
+  const cuuint64_t row = (cuuint64_t)kFD * 2;  // bytes per (g, w) row
+  cuuint64_t dims[5] = {(cuuint64_t)kFD, 2, 4, 2 * q_units, (cuuint64_t)kFW / 4};
+  cuuint64_t strides[4] = {(cuuint64_t)kFW * row, row, 2 * (cuuint64_t)kFW * row, 4 * row};
+  cuuint32_t box[5] = {64, 2, 4, 2, (cuuint32_t)kFW / 4};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(q), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -675,7 +700,7 @@ cudaError_t launch_score_fused(const uint16_t *q, const uint16_t *meank, float *
   const int n_units = L * H * n_sess;
   CUtensorMap mk_map, q_map;
   if (!make_map(&mk_map, meank, (uint64_t)L * H * nb_total, D, kFTB) ||
-      !make_q_wmajor_map(&q_map, q, (uint64_t)L * n_sess * H))
+      !make_q_rows_map(&q_map, q, (uint64_t)L * n_sess * H))
     return cudaErrorNotSupported;
   FusedArgs a{};
   a.scores = scores;

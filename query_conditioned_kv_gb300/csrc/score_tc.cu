@@ -1233,7 +1233,11 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
   if (forced == kAuto || forced == kFused) {
     cudaError_t e = launch_score_fused(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
                                        nb_total, nb_max, status, s);
-    if (e != cudaErrorNotSupported) return e;
+    // forced onto a shape the single-read kernel covers: its failure is the
+    // result (tests rely on this to know that kernel ran)
+    if (e != cudaErrorNotSupported ||
+        (forced == kFused && W > 0 && R % W == 0 && score_fused_supported(R / W, D, W, nb_max)))
+      return e;
   }
   CUtensorMap mk_map, q_map;
   uint64_t mk_rows = (uint64_t)L * H * nb_total;
