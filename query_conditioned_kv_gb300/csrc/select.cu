@@ -33,7 +33,7 @@ namespace {
 constexpr int kSelThreads = 1024;
 // Items per thread the launch aims for (at most 64: the sweep's bit masks).
 // Fewer threads per segment mean cheaper barriers in the threshold search.
-constexpr int kSelIPT = 16;
+constexpr int kSelIPT = 8;
 // Histogram copies of the radix levels (warp w counts into copy w mod 8), so
 // conflicting atomics come from at most a few warps.
 constexpr int kSelHist = 8;
