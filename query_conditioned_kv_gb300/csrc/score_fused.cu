@@ -540,6 +540,9 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
         sm.egpart[eg * 128 + row] = make_float2(pm, ps);
         named_sync(2, 128 * kFNEG);
         if (eg == 0) {
+          // group 0: this row's CTA partial to every peer, then (once the
+          // peers' partials are in) the row's LSE; the other groups go on to
+          // the barrier below
           float m = pm, s2 = ps;
           for (int g2 = 1; g2 < kFNEG; g2++) {
             const float2 o = sm.egpart[g2 * 128 + row];
@@ -553,22 +556,19 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
             const uint32_t peer = (uint32_t)((rank + p) % C);
             st_async_f2(mapa_u32(a_mine, peer), v, mapa_u32(a_bar, peer));
           }
-        }
-        if (C > 1) {
-          ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.recv + par),
-                                                            (ui >> 1) & 1, sm.failed, true));
-          // re-arm this parity for the unit after next: no peer can send that
-          // unit's partials before it has received this CTA's next ones
-          if (et == 0) mbar_expect_tx(smem_u32(sm.recv + par), (uint32_t)(C - 1) * 128 * 8);
-        }
-        named_sync(2, 128 * kFNEG);
-        if (et < 128) {
-          float m = -INFINITY, s2 = 0.f;
-          for (int c = 0; c < C; c++) {
-            const float2 v = sm.rbuf[(par * kFMaxC + c) * 128 + et];
-            merge_lse(m, s2, v.x, v.y);
+          if (C > 1) {
+            ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.recv + par),
+                                                              (ui >> 1) & 1, sm.failed, true));
+            // re-arm this parity for the unit after next: no peer can send that
+            // unit's partials before it has received this CTA's next ones
+            if (et == 0) mbar_expect_tx(smem_u32(sm.recv + par), (uint32_t)(C - 1) * 128 * 8);
           }
-          sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);
+          float mm = -INFINITY, ss = 0.f;
+          for (int c = 0; c < C; c++) {
+            const float2 w = sm.rbuf[(par * kFMaxC + c) * 128 + row];
+            merge_lse(mm, ss, w.x, w.y);
+          }
+          sm.lse[row] = (mm == -INFINITY) ? INFINITY : mm + log2f(ss);
         }
         named_sync(2, 128 * kFNEG);
         ui++;
