@@ -117,12 +117,12 @@ struct FusedSmem {
 };
 
 struct FUnit {
-  int l, h, r, nb, n_tiles, my_tiles, n_rec, jobs, mk_row0, q_unit;
+  int l, h, r, nb, n_tiles, my_tiles, n_rec, mk_row0, q_unit;
   int64_t b0;
 };
 
 // A unit and this CTA's share of it: my_tiles tiles, of which the first
-// n_rec are multiplied twice (before and after the exchange); jobs = MMAs.
+// n_rec are multiplied twice (before and after the exchange).
 __device__ __forceinline__ FUnit funit(const FusedArgs &a, int unit, int C, int rank) {
   FUnit u;
   u.r = unit % a.n_sess;
@@ -137,7 +137,6 @@ __device__ __forceinline__ FUnit funit(const FusedArgs &a, int unit, int C, int 
   u.n_tiles = (u.nb + kFTB - 1) / kFTB;
   u.my_tiles = u.n_tiles > rank ? (u.n_tiles - rank + C - 1) / C : 0;
   u.n_rec = u.my_tiles > kFKeep ? u.my_tiles - kFKeep : 0;
-  u.jobs = u.my_tiles + u.n_rec;
   u.mk_row0 = (int)(((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0);
   u.q_unit = (u.l * a.n_sess + u.r) * a.H + u.h;
   return u;
@@ -474,9 +473,9 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
     uint32_t t = 0, ui = 0, rp = 0;
     bool ok = true;
     int prev_unit = -1;
-    // pass 2 of one job of unit w (local tile i) with row LSE `lse`
-    // (the row LSEs are in sm.lse: a unit's reloaded tiles run before the next
-    // exchange, whose first barrier every group passes only after them)
+    // pass 2 of one job of unit w (local tile i); the row LSEs are in sm.lse
+    // (a unit's reloaded tiles run before the next exchange, whose first
+    // barrier every group passes only after them)
     auto pass2_job = [&](const FUnit &w, int i, uint32_t job, bool wait_full) {
       const uint32_t buf = job % kFNBUF;
       if (wait_full)
