@@ -37,6 +37,10 @@ CASES = {
     "c8_long": _cfg("c8", [16384 + 129], seed=24),           # 65 tiles → 8 CTAs, 7 reloads
     "mixed": _cfg("mx", [12000, 40, 3000, 256, 9000], seed=25),  # spread lengths: 8 tiles/CTA → 2 CTAs
     "c1_long": _cfg("c1l", [1000, 900], seed=26),             # mean 4 tiles → 1 CTA, 2 reloads
+    # tile boundaries: 1 block, one short of a tile, exactly one, one over
+    "edges": _cfg("ed", [1, 255, 256, 257], L=2, seed=27),   # mean 1 tile → 1 CTA
+    # eight CTAs over several sessions; the 300-block one leaves six idle
+    "c8_multi": _cfg("c8m", [16384, 16384, 300], seed=28),   # mean 44 tiles → 8 CTAs
 }
 
 
