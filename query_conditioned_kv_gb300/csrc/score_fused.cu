@@ -42,6 +42,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kvc_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -611,14 +613,22 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
 
 // --------------------------------------------------------------- host
 
-// Clusters of C that can be resident at once (0: the kernel cannot run).
+// Clusters of C that can be resident at once (0: the kernel cannot run),
+// cached per device; −1 marks an entry not yet queried (two host threads
+// that race on one entry both run the same query and store the same value).
 int fused_clusters(int C) {
-  static int cached[64][kFMaxC + 1] = {};
-  static bool done[64][kFMaxC + 1] = {};
+  using Row = std::atomic<int>[kFMaxC + 1];
+  static Row *const cached = [] {  // initialised once, thread-safely
+    Row *rows = new Row[64];
+    for (int d = 0; d < 64; d++)
+      for (int c = 0; c <= kFMaxC; c++) rows[d][c].store(-1, std::memory_order_relaxed);
+    return rows;
+  }();
   if (C < 1 || C > kFMaxC) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (done[dev][C]) return cached[dev][C];
+  const int have = cached[dev][C].load(std::memory_order_acquire);
+  if (have >= 0) return have;
   const size_t smem = FusedSmem::bytes();
   int n = 0;
   if (cudaFuncSetAttribute(k_score_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -637,8 +647,7 @@ int fused_clusters(int C) {
     if (cudaOccupancyMaxActiveClusters(&n, k_score_fused, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();
-  cached[dev][C] = n;
-  done[dev][C] = true;
+  cached[dev][C].store(n, std::memory_order_release);
   return n;
 }
 
