@@ -307,6 +307,7 @@ def run_ours(args, rank, world, local_rank):
                                            cfg.D, cfg.W, cfg.n_sess, cfg.nb_total)
     achieved = ab[dom] / (mean[dom] * 1e-3) / 1e9 if ab[dom] else 0.0
     pack_gbs = ab["pack"] / (mean["pack"] * 1e-3) / 1e9
+    score_gbs = ab["score"] / (mean["score"] * 1e-3) / 1e9 if mean["score"] > 0 else 0.0
     event_gbs = ab["event"] / (ms_event * 1e-3) / 1e9
     traffic = ncu_traffic(dom)
     line = {
@@ -332,6 +333,8 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": ab[dom], "peak_source": peak_src},
         "pack_roofline": {"achieved": pack_gbs, "frac": pack_gbs / peak},
+        "score_roofline": {"kernel": "k_score_fused", "algorithmic_bytes": ab["score"],
+                           "achieved": score_gbs, "frac": score_gbs / peak},
         "meank_build": dict(meank_build, frac=meank_build["achieved_gbs"] / peak),
         "gpu_launches": n_launch["select"] + n_launch["pack"] + n_launch["score"] * score_kernels,
         "clocks": clk,
