@@ -1,6 +1,6 @@
 """Compile the C oracle into ``oracle/liboracle.so`` (gcc, no CUDA).
 
-The oracle is test infrastructure: this build exists so that the test-suite,
+The oracle is test infrastructure: it is compiled only so that the test-suite,
 the smoke check and the benchmark's CPU-baseline leg can load it.  Plain
 ``-O2`` and no target-specific flags, so the same source builds and gives
 the same results on x86-64 and aarch64 hosts.
