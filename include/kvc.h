@@ -124,6 +124,10 @@ kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
  *   scores   device fp32 [L][H][nb_total]  out
  *   ws       device scratch of kvc_score_workspace_size() bytes
  * G = Hq/H; W*G ≤ KVC_SCORE_MAX_ROWS.
+ * Accuracy: products accumulate in fp32 and exponentials are taken in base 2
+ * in fp32; each score lies within 1e-3 relative of the exact value for the
+ * same bf16 inputs.  Repeating a call, or scoring some layers in a call of
+ * their own, gives bit-identical scores.
  * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (Hq % H, D, W*G too wide),
  * KVC_ERR_ALIGN, KVC_ERR_WORKSPACE.
  * ---------------------------------------------------------------------- */
