@@ -16,15 +16,21 @@ SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
 
+def compile_to(src: str, out: str, quiet: bool = False) -> None:
+    """Compile one C source of the oracle into the shared library ``out``
+    (``quiet``: keep the compiler's warnings out of the output)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-Wall", "-Wextra", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=quiet)
+
+
 def build(force: bool = False) -> str:
     """Build liboracle.so if missing or older than oracle.c; return its path."""
     if (not force and os.path.exists(LIB)
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
-           "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_to(SRC, tmp)
     os.replace(tmp, LIB)
     return LIB
 

@@ -75,6 +75,20 @@ def test_bf16_rounding_matches_exact_nearest_even(orc):
         assert orc.f64_to_bf16(x) == nearest_bf16(Fraction(x)), x
 
 
+def test_bf16_rounding_of_subnormals(orc):
+    # below 2^-126 bf16 values are multiples of 2^-133: random values across
+    # that range, and the exact midpoints between subnormal neighbours
+    # (including the step from the largest subnormal to the smallest normal)
+    rng = np.random.default_rng(11)
+    xs = list(rng.uniform(-1.0, 1.0, 300) * 2.0 ** -126)
+    xs += list(rng.uniform(0.0, 1.0, 100) * 2.0 ** -130)
+    for b in (0x0001, 0x0002, 0x0040, 0x0055, 0x007F, 0x8003, 0x807F):
+        lo, hi = bf16_value(b), bf16_value(b + 1)
+        xs.append(float((lo + hi) / 2))
+    for x in xs:
+        assert orc.f64_to_bf16(x) == nearest_bf16(Fraction(x)), x
+
+
 def test_sentinel_key_bits(orc):
     # IntentKV §2 "Layout": the dead slot's K is -1e4; in bf16 that is -9984
     assert orc.f64_to_bf16(-1e4) == 0xC61C
@@ -169,6 +183,26 @@ def test_score_takes_mean_over_window(orc):
     s = orc.score_unit(qb, mb)
     sg = sigmoid1()
     np.testing.assert_allclose(s, [(sg + 0.5) / 2, (1 - sg + 0.5) / 2],
+                               rtol=1e-7)
+
+
+def test_score_reads_query_heads_major(orc):
+    # q is [G][W][D]: G = 2 heads × W = 3 window tokens, D = 16, Nb = 3 unit
+    # Mean-K rows.  Row i of q (i = g·W + w) is 4·e_t[i], a logit of 1 on
+    # block t[i] and 0 on the other two, so its softmax is A = e/(e+2) there
+    # and B = 1/(e+2) elsewhere.  With t = (0, 0, 1, 2, 2, 1) the group of
+    # token w is rows {w, W + w}: blocks {0,2}, {0,2}, {1,1}, giving scores
+    # ((2A+B)/3, (A+2B)/3, (2A+B)/3); reading q as [W][G] pairs rows
+    # {0,1}, {2,3}, {4,5} instead and gives ((A+2B)/3, (2A+B)/3, (2A+B)/3).
+    D, G, Wn = 16, 2, 3
+    t = (0, 0, 1, 2, 2, 1)
+    q = np.zeros((G, Wn, D), np.float32)
+    for i, blk in enumerate(t):
+        q[i // Wn, i % Wn, blk] = 4.0
+    mk = np.eye(3, D, dtype=np.float32)
+    s = orc.score_unit(*_unit(q, mk))
+    A, B = math.e / (math.e + 2.0), 1.0 / (math.e + 2.0)
+    np.testing.assert_allclose(s, [(2 * A + B) / 3, (A + 2 * B) / 3, (2 * A + B) / 3],
                                rtol=1e-7)
 
 

@@ -31,6 +31,20 @@ def test_lse_is_log_of_n_for_a_zero_query(orc):
     assert lse[0, 0] == pytest.approx(math.log(n), rel=1e-14)
 
 
+def test_lse_maps_query_heads_to_their_kv_head(orc):
+    """H = 2 KV heads, Hq = 4: every key of KV head 0 is zero and every key of
+    KV head 1 is 3·e0, every query row is 2·e0.  Query heads 0, 1 read KV head
+    0 (LSE = ln n) and heads 2, 3 read KV head 1 (LSE = ln n + 6/√4)."""
+    D, n, H, Hq = 4, 5, 2, 4
+    kp = np.zeros((1, n, H, D), np.float32)
+    kp[0, :, 1, 0] = 3.0
+    q = np.zeros((1, Hq, D), np.float32)
+    q[0, :, 0] = 2.0
+    lse = orc.attention_lse(_bits(q), _bits(kp), np.array([0], np.int32), 16, n, H)
+    want = [math.log(n), math.log(n), math.log(n) + 3.0, math.log(n) + 3.0]
+    np.testing.assert_allclose(lse[0], want, rtol=1e-14)
+
+
 def test_one_aligned_key_closed_form(orc):
     """q·k = c for key 0 and 0 for the other n−1 keys: p_0 = e^{c/√D}/(e^{c/√D}+n−1)."""
     D, n, c = 16, 9, 8.0
