@@ -34,14 +34,10 @@ BLOCK = 32
 
 
 def lib():
-    """Load (building if needed) liboracle.so.
-
-    ``KVC_ORACLE_LIB``, when set, names another build of ``oracle.c`` to load
-    instead; the mutation tests point it at copies with one planted mistake
-    to show that the pins catch each of them."""
+    """Load (building if needed) liboracle.so."""
     global _lib
     if _lib is None:
-        path = os.environ.get("KVC_ORACLE_LIB") or _build.build()
+        path = _build.build()
         L = ctypes.CDLL(path)
         c = ctypes
         L.orc_bf16_to_f64.argtypes = [c.c_uint16]

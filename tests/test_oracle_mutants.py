@@ -1,34 +1,40 @@
 """Mutation check of the oracle's pins.
 
-Each entry below plants one plausible mistake in a copy of ``oracle/oracle.c``
-(a dropped term, a wrong sign, index or divisor, a transposed operand, a sum
-where a max belongs, a reversed tie order), builds that copy, and runs the
-CPU pin tests against it in a child process.  A mutant passes this test only
-if some pin FAILS on it: a pin set that cannot tell the mutant from the real
-oracle leaves that step unpinned.  No mutant reads or writes outside the
-buffers its function is given (several candidate mistakes that would have
-were left out), so a child process ends in a test failure, not a crash.
+Each entry below plants one plausible mistake in a copy of the oracle (a
+dropped term, a wrong sign, index or divisor, a transposed operand, a sum
+where a max belongs, a reversed tie order, a wrong slice of the units), and
+runs the CPU pin tests against that copy in a child process.  A mutant
+passes this test only if some pin FAILS on it: a pin set that cannot tell
+the mutant from the real oracle leaves that step unpinned.  No mutant reads
+or writes outside the buffers its function is given (several candidate
+mistakes that would have were left out), so a child process ends in a test
+failure, not a crash.
 
-CPU only; the mutants run in parallel, about half a minute on 8 cores.
+Each child runs in a scratch tree holding copies of ``oracle/`` (with the
+mistake), ``workloads/`` and the pin tests, so it builds and imports only
+the mutated oracle.  CPU only; the mutants run in parallel, about a minute
+on 8 cores.
 """
 from __future__ import annotations
 
 import os
 import re
+import shutil
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
 
-import pytest
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PINS = ["tests/test_oracle_pins.py", "tests/test_meank_pins.py",
         "tests/test_recover_pins.py", "tests/test_lrfu_pins.py",
         "tests/test_confidence_pins.py"]
+COPIED = ["oracle/oracle.c", "oracle/__init__.py", "oracle/build.py",
+          "workloads/__init__.py", "tests/conftest.py", "tests/helpers.py",
+          "tests/golden/calibrate_gamma.py", "tests/golden/slot_map_example.json",
+          *PINS]
 
-# (name, the mistake it models, text in oracle.c, replacement)
-MUTANTS = [
+# (name, the mistake it models, text in oracle/oracle.c, replacement)
+C_MUTANTS = [
     # bf16 rounding
     ("bf16_truncates", "round toward zero instead of to nearest even",
      "r = ldexp(nearbyint(ldexp(m, 8)), e - 8);",
@@ -183,27 +189,55 @@ MUTANTS = [
 ]
 
 
+# (name, the mistake it models, text in oracle/__init__.py, replacement):
+# the wrappers that slice a whole event into the C functions' units
+PY_MUTANTS = [
+    ("score_meank_interleaved_group", "query heads h, h + H, ... grouped with KV head h",
+     "score_unit(q[l, r, h * G:(h + 1) * G],", "score_unit(q[l, r, h::H],"),
+    ("score_meank_layer0", "every layer scored against layer 0's Mean-K",
+     "meank_all[l, h, b0:b1])", "meank_all[0, h, b0:b1])"),
+    ("score_meank_softmax_from_zero", "softmax over every block before the session's end",
+     "meank_all[l, h, b0:b1])", "meank_all[l, h, 0:b1])[b0:]"),
+    ("select_segments_off_by_one", "each segment takes the next segment's first item",
+     "a, b = int(seg_off[s]), int(seg_off[s + 1])",
+     "a, b = int(seg_off[s]), int(seg_off[s + 1]) + 1"),
+    ("meank_first_dim_only", "only the first leading dimension's rows averaged",
+     "    rows = int(np.prod(lead)) if lead else 1\n    out = np.empty((*lead, n_tok // BLOCK",
+     "    rows = lead[0] if lead else 1\n    out = np.zeros((*lead, n_tok // BLOCK"),
+    ("qmem_first_dim_only", "only the first leading dimension's memories updated",
+     "    rows = int(np.prod(lead)) if lead else 1\n    _check(lib().orc_qmem_update",
+     "    rows = lead[0] if lead else 1\n    _check(lib().orc_qmem_update"),
+]
+
+MUTANTS = ([(n, d, "oracle/oracle.c", o, w) for n, d, o, w in C_MUTANTS] +
+           [(n, d, "oracle/__init__.py", o, w) for n, d, o, w in PY_MUTANTS])
+
+
 def test_every_mutation_site_is_in_the_oracle():
-    text = open(SRC).read()
     names = [m[0] for m in MUTANTS]
     assert len(names) == len(set(names))
-    for name, _, old, new in MUTANTS:
-        assert text.count(old) == 1, name
+    for name, _, path, old, new in MUTANTS:
+        with open(os.path.join(ROOT, path)) as f:
+            assert f.read().count(old) == 1, name
         assert old != new, name
 
 
 def _run_mutant(entry, workdir):
-    from oracle import build as obuild
-    name, _, old, new = entry
-    text = open(SRC).read().replace(old, new)
-    src = os.path.join(workdir, f"{name}.c")
-    lib = os.path.join(workdir, f"{name}.so")
-    with open(src, "w") as f:
-        f.write(text)
-    obuild.compile_to(src, lib, quiet=True)
-    env = dict(os.environ, KVC_ORACLE_LIB=lib, PYTHONDONTWRITEBYTECODE="1")
+    """Pin-test exit code of the oracle with one mistake planted (none for the
+    control entry, whose path is None), and the first pin that failed."""
+    name, _, path, old, new = entry
+    tree = os.path.join(workdir, name)
+    for rel in COPIED:
+        os.makedirs(os.path.dirname(os.path.join(tree, rel)), exist_ok=True)
+        shutil.copyfile(os.path.join(ROOT, rel), os.path.join(tree, rel))
+    if path is not None:
+        with open(os.path.join(ROOT, path)) as f:
+            text = f.read().replace(old, new)
+        with open(os.path.join(tree, path), "w") as f:
+            f.write(text)
+    env = dict(os.environ, PYTHONDONTWRITEBYTECODE="1")
     p = subprocess.run([sys.executable, "-m", "pytest", *PINS, "-x", "-q", "-m", "not gpu",
-                        "-p", "no:cacheprovider"], cwd=ROOT, env=env,
+                        "-p", "no:cacheprovider", "--rootdir", tree], cwd=tree, env=env,
                        capture_output=True, text=True, timeout=600)
     caught = re.search(r"^FAILED (\S+)", p.stdout, re.M)
     return name, p.returncode, caught.group(1) if caught else None, p.stdout[-2000:]
@@ -211,8 +245,11 @@ def _run_mutant(entry, workdir):
 
 def test_every_planted_mistake_fails_a_pin(tmp_path):
     workers = max(1, min(8, os.cpu_count() or 1))
+    control = ("control", "no mistake", None, "", "")
     with ThreadPoolExecutor(workers) as pool:
-        results = list(pool.map(lambda e: _run_mutant(e, str(tmp_path)), MUTANTS))
+        results = list(pool.map(lambda e: _run_mutant(e, str(tmp_path)), [control, *MUTANTS]))
+    _, rc, _, tail = results.pop(0)
+    assert rc == 0, f"the unchanged copy fails its pins:\n{tail}"
     survivors = [(n, rc, tail) for n, rc, pin, tail in results if rc != 1 or pin is None]
     assert not survivors, "\n\n".join(f"{n}: pytest exit {rc}\n{tail}"
                                       for n, rc, tail in survivors)

@@ -103,6 +103,21 @@ def test_meank_constant_block_is_constant(orc):
     assert mk.shape == (1, 2, 8) and np.all(mk == 0x3FC0)
 
 
+def test_meank_every_row_of_a_layered_index(orc):
+    # kraw [L=2][H=3][64][8]: every token of (l, h, block b) holds
+    # 4l + h + b/2, exact in bf16, so each block mean is that value
+    L, H = 2, 3
+    v = np.zeros((L, H, 64, 8), np.float32)
+    for l in range(L):
+        for h in range(H):
+            for b in range(2):
+                v[l, h, 32 * b:32 * (b + 1)] = 4 * l + h + b / 2
+    mk = orc.meank(bits(v))
+    want = np.array([[[4 * l + h + b / 2] * 8 for b in range(2)]
+                     for l in range(L) for h in range(H)], np.float32).reshape(L, H, 2, 8)
+    assert np.array_equal(mk, bits(want))
+
+
 def test_meank_is_exact_block_mean_rounded_once(orc):
     rng = np.random.default_rng(1)
     D = 16
@@ -206,6 +221,31 @@ def test_score_reads_query_heads_major(orc):
                                rtol=1e-7)
 
 
+def test_score_meank_slices_units_by_layer_head_and_session(orc):
+    # L = 2, H = 2 KV heads with G = 2 query heads each, W = 1, D = 16, two
+    # sessions owning blocks [0, 2) and [2, 5).  Layer 0's Mean-K row of block
+    # b is e_b in both KV heads; query head hq of session r is 4·e_t[r][hq], a
+    # logit of 1 on block t (0 elsewhere; 0 everywhere when t lies outside the
+    # session).  A softmax over n blocks with one logit of 1 is A_n = e/(e+n-1)
+    # there and B_n = 1/(e+n-1) elsewhere.  Layer 1's Mean-K is zero: uniform
+    # 1/n per session.  Query heads 2h and 2h+1 belong to KV head h.
+    L, n_sess, H, Hq, D = 2, 2, 2, 4, 16
+    t = [(0, 0, 1, 1), (2, 3, 4, 7)]
+    q = np.zeros((L, n_sess, Hq, 1, D), np.float32)
+    for r in range(n_sess):
+        for hq in range(Hq):
+            q[:, r, hq, 0, t[r][hq]] = 4.0
+    mk = np.zeros((L, H, 5, D), np.float32)
+    mk[0, :, :, :5] = np.eye(5, dtype=np.float32)
+    s = orc.score_meank(bits(q), bits(mk), H, np.array([0, 2, 5]))
+    e = math.e
+    A2, B2, A3, B3 = e / (e + 1), 1 / (e + 1), e / (e + 2), 1 / (e + 2)
+    want = np.array([[[A2, B2, A3, A3, B3],
+                      [B2, A2, 1 / 3, 1 / 3, A3]],
+                     [[1 / 2, 1 / 2, 1 / 3, 1 / 3, 1 / 3]] * 2])
+    np.testing.assert_allclose(s, want, rtol=1e-7)
+
+
 def test_score_mass_bounds(orc):
     rng = np.random.default_rng(4)
     for G in (1, 2, 4):
@@ -301,6 +341,19 @@ def test_select_invariants_large(orc):
     free_kept = [i for i in k if i not in forced]
     dropped = [i for i in range(n) if i not in set(k.tolist())]
     assert min(s[free_kept]) >= max(s[dropped])
+
+
+def test_select_segments_closed_form(orc):
+    # three segments of 5, 40 and 33 items, scores −i (the earliest item is
+    # the best); budget 6 with 1 sink and 2 recent: a segment that fits is
+    # kept whole, the others keep items 0–3 and their last two items
+    off = np.array([0, 5, 45, 78])
+    sc = np.concatenate([-np.arange(n, dtype=np.float32) for n in (5, 40, 33)])
+    kept, cnt, mask = orc.select_segments(sc, off, 6, 1, 2)
+    assert cnt.tolist() == [5, 6, 6]
+    assert kept.tolist() == [[0, 1, 2, 3, 4, -1], [0, 1, 2, 3, 38, 39],
+                             [0, 1, 2, 3, 31, 32]]
+    assert mask.tolist() == [[0x1F, 0], [0xF, 0xC0], [0x8000000F, 0x1]]
 
 
 def test_select_negative_zero_ties_positive_zero(orc):
@@ -432,6 +485,21 @@ def test_qmem_closed_forms(orc):
     q3[0, 0, 2] = 4.0
     M3 = orc.qmem_update(np.zeros((1, D), np.float32), bits(q3), renorm=False)
     assert M3[0, 2] == np.float32(0.1)
+
+
+def test_qmem_updates_every_memory_row(orc):
+    # M [n_sess=2][L=3][Hq=2][D] from zero, every token of row i equal to
+    # (i + 1)·e_(i mod D): without renormalisation each row becomes
+    # 0.1·(i + 1)·e_(i mod D)
+    D, T = 16, 3
+    q = np.zeros((2, 3, 2, T, D), np.float32)
+    for i in range(12):
+        q.reshape(12, T, D)[i, :, i % D] = i + 1
+    M = orc.qmem_update(np.zeros((2, 3, 2, D), np.float32), bits(q), renorm=False)
+    want = np.zeros((12, D), np.float32)
+    for i in range(12):
+        want[i, i % D] = np.float32(0.1 * (i + 1))
+    assert np.array_equal(M.reshape(12, D), want)
 
 
 def test_qmem_unit_norm_after_every_update(orc):
