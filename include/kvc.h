@@ -487,8 +487,9 @@ kvc_status kvc_token_confidence(const float *logits, int32_t n_tok, int32_t V, i
  *   slope[t] = least-squares slope of the windows with R'_m ≤ Q against m
  *            (fp64; 0 with fewer than two such windows); n_kept[t] = their
  *            number;
- *   budget[t] ← min(budget[t] + budget_step, max_budget) if slope < 0, else
- *            unchanged — the budget starts small and is never lowered.
+ *   budget[t] ← max(budget[t], min(budget[t] + budget_step, max_budget)) if
+ *            slope < 0, else unchanged — the budget starts small and is never
+ *            lowered (one already above max_budget is kept).
  *   conf       device fp32; trace_off device int64 [n_trace+1]
  *   slope      device fp64 [n_trace] out; budget device int32 [n_trace]
  *              in/out; n_kept device int32 [n_trace] out

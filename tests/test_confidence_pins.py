@@ -95,6 +95,8 @@ def test_budget_rises_only_on_a_falling_trend(orc):
     assert orc.adapt_budget(0.0, 1024, 256, 8192) == 1024     # flat: kept
     assert orc.adapt_budget(0.3, 1024, 256, 8192) == 1024     # recovering: never lowered
     assert orc.adapt_budget(-2.0, 8000, 256, 8192) == 8192    # capped
+    # a budget already above the cap (the cap lowered between steps) is not cut
+    assert orc.adapt_budget(-2.0, 9000, 256, 8192) == 9000
     b = 512
     for slope in (-1, 1, -1, -1, 0, 2, -1):
         nb = orc.adapt_budget(slope, b, 128, 4096)

@@ -49,6 +49,8 @@ C_MUTANTS = [
     ("meank_block_stride", "block stride of 31 tokens",
      "kraw[(r * n_tok + b * ORC_BLOCK + t) * D + d]",
      "kraw[(r * n_tok + b * (ORC_BLOCK - 1) + t) * D + d]"),
+    ("meank_double_rounding", "mean rounded to fp32 before bf16",
+     "orc_f64_to_bf16(sum / ORC_BLOCK)", "orc_f64_to_bf16((float)(sum / ORC_BLOCK))"),
     # Mean-K score
     ("score_no_inv_sqrt_d", "logits not scaled by 1/sqrt(D)",
      "zr[b] = dot * inv_sqrt_d;", "zr[b] = dot;"),
@@ -58,6 +60,9 @@ C_MUTANTS = [
      "score[b] = (float)(acc / W);", "score[b] = (float)(acc / G);"),
     ("score_lse_drops_max", "LSE without its max shift",
      "lse[g * W + w] = m + log(s);", "lse[g * W + w] = log(s);"),
+    ("score_blocks_reversed", "probability of block b taken from block Nb-1-b",
+     "double p = exp(z[((int64_t)g * W + w) * nb + b] - lse[g * W + w]);",
+     "double p = exp(z[((int64_t)g * W + w) * nb + (nb - 1 - b)] - lse[g * W + w]);"),
     ("score_q_transposed", "query read as [W][G] instead of [G][W]",
      "const uint16_t *qr = q + ((int64_t)g * W + w) * D;",
      "const uint16_t *qr = q + ((int64_t)w * G + g) * D;"),
@@ -67,12 +72,16 @@ C_MUTANTS = [
     ("qmem_decay_gain_swapped", "decay and gain swapped",
      "v[d] = decay * (double)M[r * D + d] + gain * mean;",
      "v[d] = gain * (double)M[r * D + d] + decay * mean;"),
+    ("qmem_always_renormalised", "the renorm flag ignored",
+     "    if (renorm) {\n", "    if (1) {\n"),
     ("qmem_divides_by_norm_squared", "renormalised by the squared norm",
      "for (int d = 0; d < D; d++) v[d] /= n;",
      "for (int d = 0; d < D; d++) v[d] /= n2;"),
     # rule score
     ("rule_gqa_modulo", "query head hq reads KV head hq % H",
      "      int h = hq / G;\n", "      int h = hq % H;\n"),
+    ("rule_no_inv_sqrt_d", "logits not scaled by 1/sqrt(D)",
+     "z[j] = dot * inv_sqrt_d;", "z[j] = dot;"),
     ("rule_unnormalised", "exp(z - max) instead of the softmax",
      "if (slot_map[j] != sentinel) acc[j] += exp(z[j] - lse);",
      "if (slot_map[j] != sentinel) acc[j] += exp(z[j] - zmax);"),
@@ -106,6 +115,8 @@ C_MUTANTS = [
      "      out[j + 1] = x[j + 1] * c + x[j] * s;\n"
      "    }\n"
      "    out[j + half] = x[j + half];\n"),
+    ("pack_tail_not_zeroed", "view tokens past the kept blocks left unwritten",
+     "      for (int d = 0; d < D; d++) ko[d] = vo[d] = 0;\n", "\n"),
     ("pack_old_position", "K re-RoPEd at its old position",
      "orc_rope_f64(x, y, D, (double)(pos0 + i), theta);",
      "orc_rope_f64(x, y, D, (double)(pos0 + src), theta);"),
@@ -120,6 +131,8 @@ C_MUTANTS = [
      "if (refcnt[u] == 0 && j >= prefix_len) {", "if (refcnt[u] == 0) {"),
     ("free_ignores_aliases", "slot freed while another reference holds it",
      "if (refcnt[u] == 0 && j >= prefix_len) {", "if (j >= prefix_len) {"),
+    ("redirect_sentinel_counted", "an entry already at the dead slot dropped again",
+     "      if (u == sentinel) continue;\n", "\n"),
     ("redirect_skipped", "dropped positions keep their slot",
      "      *e = sentinel;\n", "\n"),
     # attention LSE and recovery score
@@ -131,6 +144,8 @@ C_MUTANTS = [
      "s[p] = dot * inv_sqrt_d;", "s[p] = dot;"),
     ("recover_sum_over_group", "sum over the GQA group instead of max",
      "if (prob > best) best = prob;", "best += prob;"),
+    ("recover_gqa_interleaved", "KV head h's group taken as heads h, h + H, ...",
+     "const int hq = h * G + g;", "const int hq = g * H + h;"),
     ("recover_running_sum", "running sum instead of running mean",
      "state[p] = count == 1 ? x : state[p] + (x - state[p]) / count;",
      "state[p] = count == 1 ? x : state[p] + x;"),
@@ -147,6 +162,9 @@ C_MUTANTS = [
     ("tail_freed_logical", "logical block numbers freed",
      "for (int b = 0; b < Y - x; b++) freed[b] = block_table[b];",
      "for (int b = 0; b < Y - x; b++) freed[b] = b;"),
+    ("tail_mask_absolute_bit", "tail mask bit taken from the absolute position",
+     "tail_mask[(p - start) / 32] |= 1u << ((p - start) % 32);",
+     "tail_mask[(p - start) / 32] |= 1u << (p % 32);"),
     # LRFU keep score
     ("lrfu_no_hit_gate", "every entry gains its score",
      "ks[i] = (float)(lambda * (double)ks[i] + (hits[i] ? s : 0.0));",
@@ -154,6 +172,9 @@ C_MUTANTS = [
     ("lrfu_decay_complement", "decay by 1 - lambda",
      "ks[i] = (float)(lambda * (double)ks[i] + (hits[i] ? s : 0.0));",
      "ks[i] = (float)((1.0 - lambda) * (double)ks[i] + (hits[i] ? s : 0.0));"),
+    ("lrfu_negative_mass", "negative scores carry their magnitude as mass",
+     "it[i].m = (s > 0.0 && isfinite(s)) ? s : 0.0;",
+     "it[i].m = isfinite(s) ? fabs(s) : 0.0;"),
     ("lrfu_one_hit_too_many", "top-p prefix one entry past the mass",
      "for (int k = 0; k < n && cum < target && it[k].m > 0.0; k++) {",
      "for (int k = 0; k < n && cum <= target && it[k].m > 0.0; k++) {"),
@@ -166,6 +187,9 @@ C_MUTANTS = [
     ("conf_logits_not_logprobs", "logits used as log-probabilities",
      "for (int j = 0; j < k; j++) top += sorted[j] - lse; /* log P(j) */",
      "for (int j = 0; j < k; j++) top += sorted[j];"),
+    ("conf_lse_unshifted", "LSE sum not shifted by the max",
+     "for (int v = 0; v < V; v++) sum += exp((double)logits[v] - mx);",
+     "for (int v = 0; v < V; v++) sum += exp((double)logits[v]);"),
     ("conf_bottom_k", "the k least probable tokens",
      "qsort(sorted, (size_t)V, sizeof(double), orc_f64_desc);",
      "qsort(sorted, (size_t)V, sizeof(double), orc_f64_asc);"),
@@ -183,6 +207,9 @@ C_MUTANTS = [
      "*slope = (cnt >= 2 && den > 0.0) ? (sx * sy - cnt * sxy) / den : 0.0;"),
     ("budget_raised_on_rise", "budget raised on a rising trend",
      "  if (slope < 0.0) {\n", "  if (slope > 0.0) {\n"),
+    ("budget_lowered_to_cap", "a budget above the cap lowered to it",
+     "return nb < max_budget ? nb : (budget > max_budget ? budget : max_budget);",
+     "return nb < max_budget ? nb : max_budget;"),
     ("budget_uncapped", "budget not capped",
      "return nb < max_budget ? nb : (budget > max_budget ? budget : max_budget);",
      "return nb;"),
