@@ -88,6 +88,16 @@ kvc_status kvc_device_status(const int32_t *dev_status, int32_t *host_out);
 /* Library version, "major.minor.patch". */
 const char *kvc_version(void);
 
+/* Self-test of the bounded waits (a diagnostic of this library; no
+ * counterpart on the pages).  Launches one CTA whose first thread waits on a
+ * shared-memory mbarrier that nothing arrives on.  The wait is the same
+ * bounded wait the tensor-core kernels use: it polls against %globaltimer and
+ * gives up after one second.  The kernel then records KVC_ERR_TIMEOUT in
+ * *dev_status and returns.  The launch takes about a second; no fault or trap
+ * is raised, and the context stays usable.
+ * Errors: KVC_ERR_INVALID_ARG (dev_status NULL), KVC_ERR_CUDA (launch). */
+kvc_status kvc_selftest_bounded_wait(int32_t *dev_status, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * Index maintenance (not part of the timed event).
  *

@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG",
-    "kvc_status_string", "kvc_version", "kvc_device_status",
+    "kvc_status_string", "kvc_version", "kvc_device_status", "kvc_selftest_bounded_wait",
     "kvc_build_meank", "kvc_score_workspace_size", "kvc_score_launches", "kvc_score",
     "kvc_score_static", "SCORE_STATIC_SCRATCH_BYTES",
     "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
@@ -56,6 +56,7 @@ _SIGS = {
     "kvc_status_string": (_c.c_char_p, [_c.c_int]),
     "kvc_version": (_c.c_char_p, []),
     "kvc_device_status": (_c.c_int, [_P, _P]),
+    "kvc_selftest_bounded_wait": (_c.c_int, [_P, _P]),
     "kvc_build_meank": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _P, _P]),
     "kvc_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I64]),
     "kvc_score_launches": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
@@ -147,6 +148,11 @@ def kvc_device_status(dev_status) -> int:
     _ok(lib.kvc_device_status(_ptr(dev_status), _c.addressof(out)),
         "kvc_device_status")
     return int(out.value)
+
+
+def kvc_selftest_bounded_wait(dev_status, stream=None):
+    _ok(lib.kvc_selftest_bounded_wait(_ptr(dev_status), _stream(stream)),
+        "kvc_selftest_bounded_wait")
 
 
 def kvc_build_meank(kraw, meank, L, H, D, n_tok, dev_status=None, stream=None):

@@ -4,6 +4,7 @@
 #include <math.h>
 
 #include "kvc_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace {
 
@@ -21,6 +22,23 @@ __global__ void k_init_sentinel(uint16_t *kpool, uint16_t *vpool, int L, int H,
   int64_t idx = (l * n_slots + sentinel) * per_layer + e;
   kpool[idx] = (uint16_t)KVC_SENTINEL_K_BITS;
   if (vpool) vpool[idx] = 0;
+}
+
+// One thread waits, through the kernels' bounded wait, on an mbarrier that no
+// thread arrives on; the wait gives up after a second and the kernel records
+// KVC_ERR_TIMEOUT.
+__global__ void k_selftest_wait(int32_t *status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int failed;
+  if (threadIdx.x == 0) {
+    kvc::tc::mbar_init(kvc::tc::smem_u32(&bar), 1);
+    failed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 &&
+      !kvc::tc::mbar_wait_bounded(kvc::tc::smem_u32(&bar), 0, (volatile int *)&failed))
+    kvc::record_error(status, KVC_ERR_TIMEOUT);
 }
 
 }  // namespace
@@ -45,6 +63,12 @@ const char *kvc_status_string(kvc_status s) {
 }
 
 const char *kvc_version(void) { return "0.1.0"; }
+
+kvc_status kvc_selftest_bounded_wait(int32_t *dev_status, cudaStream_t stream) {
+  if (!dev_status) return KVC_ERR_INVALID_ARG;
+  k_selftest_wait<<<1, 32, 0, stream>>>(dev_status);
+  return from_cuda(cudaGetLastError());
+}
 
 kvc_status kvc_device_status(const int32_t *dev_status, int32_t *host_out) {
   if (!dev_status || !host_out) return KVC_ERR_INVALID_ARG;

@@ -66,6 +66,10 @@ def _call(kvc, name, *args):
     return getattr(kvc.lib, name)(*args)
 
 
+def test_selftest_rejects_a_null_status_word(kvc):
+    assert _call(kvc, "kvc_selftest_bounded_wait", None, None) == 1
+
+
 def test_validation_rejects_before_launch(kvc):
     P, U = FAKE, FAKE + 2  # U: misaligned
     # build_meank: shape (n_tok % 32), head dim, alignment, NULL

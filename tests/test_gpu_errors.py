@@ -117,3 +117,27 @@ def test_host_validation_raises_before_launch(kvc):
     with pytest.raises(kvc.KvcError) as ei:
         kvc.kvc_select(s, off, 1, 10, 2, 2, 1, kept, cnt)
     assert ei.value.code == 3
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable(kvc):
+    """A wait that nothing completes ends after about a second with
+    KVC_ERR_TIMEOUT in the status word (no fault, no trap), and the next
+    kernels run normally."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    kvc.kvc_selftest_bounded_wait(st)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert kvc.kvc_device_status(st) == 9  # KVC_ERR_TIMEOUT
+    assert 0.9 < dt < 30.0
+    s = torch.tensor([0.5, 0.1, 0.2, 0.9, 0.3], device=DEV)
+    off = torch.tensor([0, 5], dtype=torch.int64, device=DEV)
+    kept = torch.empty(1, 3, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(1, dtype=torch.int32, device=DEV)
+    st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvc.kvc_select(s, off, 1, 5, 3, 0, 0, kept, cnt, None, st2)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(st2) == 0
+    assert kept.cpu().tolist() == [[0, 3, 4]] and cnt.cpu().tolist() == [3]
