@@ -19,7 +19,11 @@ tail plan → in-place compaction) at 1, 4, 16 and 64 requests of 6K → 4K
 tokens (`actkv_event`; `--no-paged` skips it), and KVMem's tiered view with the
 index and raw history in host memory, cold and warm steps (`tiered_event`;
 `--no-tiered` skips it), and ActKV's confidence monitor (`confidence_monitor`;
-`--no-confidence` skips it).
+`--no-confidence` skips it).  The 27B-class 1M-token event (64 layers scored, 16
+packed) and the 128-session ragged event are measured the same way as the
+headline, each with its own roofline and a scaled oracle baseline on a seeded
+sample of its units (`event_27b_1m`, `event_ragged_128`; `--no-27b`,
+`--no-ragged` skip them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -48,6 +52,14 @@ WORKLOAD = "8b_128k: 36 layers, 8 KV / 32 query heads, d 128, 131072-token histo
            "W 32, budget 256 blocks (1 sink, 4 recent), view 8192 tokens"
 L2_NOTE = "L2 flushed between steps (256 MiB write outside the event's timed span); " \
           "the event also touches 2.7 GB > 129 MB L2"
+
+
+def bench_config(cfg, world: int) -> dict:
+    """The `config` of the JSON line; both arms print the same one."""
+    return {"workload": WORKLOAD, "sessions": cfg.n_sess, "history_tokens": cfg.n_tok,
+            "layers": cfg.L, "kv_heads": cfg.H, "q_heads": cfg.Hq, "head_dim": cfg.D,
+            "window": cfg.W, "budget_blocks": cfg.budget, "parallelism": f"replicas{world}",
+            "l2": L2_NOTE}
 
 
 def algorithmic_bytes(cfg):
@@ -315,10 +327,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_event,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded, workloads/)",
-        "config": {"workload": WORKLOAD, "sessions": 1, "history_tokens": cfg.n_tok,
-                   "layers": cfg.L, "kv_heads": cfg.H, "q_heads": cfg.Hq, "head_dim": cfg.D,
-                   "window": cfg.W, "budget_blocks": cfg.budget, "parallelism": f"replicas{world}",
-                   "l2": L2_NOTE},
+        "config": bench_config(cfg, world),
         "hbm_roofline_event": {"achieved_gbs": event_gbs, "peak_gbs": peak,
                                "frac": event_gbs / peak,
                                "algorithmic_bytes": ab["event"]},
@@ -344,6 +353,139 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, dev)
     return line
+
+
+# ------------------------------------------- the other Mean-K workloads
+
+EVENT_WORKLOADS = {
+    "27b_1m": ("27b_1m: 64 layers scored (Mean-K index of 4.3 GB device-resident), 16 "
+               "layers packed (raw K/V 68.7 GB resident), 8 KV / 48 query heads, d 128, "
+               "1048576-token workspace, W 32, budget 2048 blocks (1 sink, 8 recent), "
+               "view 65536 tokens"),
+    "ragged_128": ("ragged_128: 128 sessions of U[16384, 262144] tokens (rounded to 32), "
+                   "36 layers scored, 2 packed, 8 KV / 32 query heads, d 128, W 32, budget "
+                   "512 blocks (1 sink, 4 recent), view 16384 tokens per session"),
+}
+
+
+def _oracle_config_sample(cfg, name, dev, seed=7):
+    """A seeded sample of the workload's units for the oracle baseline and the
+    share of the event's tokens it stands for.  27b_1m: 8 of the 512 (layer,
+    KV head) units, 2 of them in packed layers and 6 in scored-only layers
+    (the event's 1:3 mix).  ragged_128: every unit of 8 of the 128 sessions,
+    the shortest and the longest among them."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    if name == "27b_1m":
+        packed = rng.choice(cfg.lp * cfg.H, size=2, replace=False)
+        scored = rng.choice((cfg.L - cfg.lp) * cfg.H, size=6, replace=False) + cfg.lp * cfg.H
+        picks = [(int(u) // cfg.H, int(u) % cfg.H, 0) for u in list(packed) + list(scored)]
+        frac = len(picks) / (cfg.L * cfg.H * cfg.n_sess)
+        what = (f"8 of {cfg.L * cfg.H} (layer, KV head) units (2 of them packed), "
+                f"tokens scaled by {frac:.5f}")
+    else:
+        hist = np.asarray(cfg.hist)
+        rest = [r for r in range(cfg.n_sess) if r not in (int(hist.argmin()), int(hist.argmax()))]
+        sess = [int(hist.argmin()), int(hist.argmax())] + \
+            [int(x) for x in rng.choice(rest, size=6, replace=False)]
+        picks = [(l, h, r) for r in sess for l in range(cfg.L) for h in range(cfg.H)]
+        frac = float(hist[sess].sum()) / cfg.n_tok
+        what = (f"all {cfg.L * cfg.H} (layer, KV head) units of 8 of {cfg.n_sess} sessions "
+                f"(shortest and longest included), {int(hist[sess].sum())} of "
+                f"{cfg.n_tok} tokens: scaled by {frac:.5f}")
+    return _oracle_units(cfg, picks, dev), frac, what
+
+
+def config_event(args, dev, peak, name: str, reps: int = 20):
+    """One Mean-K event of the 27b_1m or ragged_128 workload, measured like the
+    headline: score → select → pack replayed as one CUDA graph, the L2 flushed
+    (256 MiB write) between replays outside the event span, CUDA events on the
+    stream; stages from an eager pass with an event pair per launch; the
+    oracle baseline on a seeded sample of the same workload."""
+    import torch
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import MeanKEvent, event_bytes
+
+    cfg = {"27b_1m": W.config_27b, "ragged_128": W.config_ragged}[name]()
+    q = cfg.q(dev)
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = cfg.meank_direct(dev)  # layers without raw K keep the drawn index
+    kvc.kvc_build_meank(kraw, meank[:cfg.lp], cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                    cfg.n_recent, cfg.lp, cfg.theta, cfg.pos0, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        ev.run(q, meank, kraw, vraw)
+    ev.capture(q, meank, kraw, vraw)
+    ev.replay()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for k in range(reps):
+        flush.fill_(k & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ev.replay()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    stages = {}
+    n_launch = {}
+    for k in range(5):
+        flush.fill_(k & 0xFF)
+        timers = []
+        ev.run(q, meank, kraw, vraw, timers=timers)
+        torch.cuda.synchronize(dev)
+        for stage, a, b in timers:
+            stages.setdefault(stage, []).append(a.elapsed_time(b))
+            if k == 0:
+                n_launch[stage] = n_launch.get(stage, 0) + 1
+    if kvc.kvc_device_status(ev.dev_status) != 0:
+        raise RuntimeError(f"device status error in the {name} event")
+    ab = event_bytes(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.nb_total, cfg.n_sess, cfg.lp,
+                     cfg.view_tokens, cfg.budget)
+    ms_sorted = sorted(ms)
+    med = statistics.median(ms)
+    st = {k: statistics.median(v) for k, v in stages.items()}
+    score_kernels = kvc.kvc_score_launches(cfg.L // len(ev.groups), cfg.H, cfg.Hq, cfg.D, cfg.W,
+                                           cfg.n_sess, ev.nb_max)
+    out = {
+        "workload": EVENT_WORKLOADS[name], "sessions": cfg.n_sess, "history_tokens": cfg.n_tok,
+        "layers_scored": cfg.L, "layers_packed": cfg.lp,
+        "value": cfg.n_tok / (med * 1e-3), "unit": UNIT, "ms_per_event": round(med, 4),
+        "ms_p10_p50_p90": [round(ms_sorted[int(0.1 * (reps - 1))], 4), round(med, 4),
+                           round(ms_sorted[int(0.9 * (reps - 1))], 4)],
+        "reps": reps,
+        "hbm_roofline_event": {"achieved_gbs": ab["event"] / (med * 1e-3) / 1e9,
+                               "peak_gbs": peak,
+                               "frac": ab["event"] / (med * 1e-3) / 1e9 / peak,
+                               "algorithmic_bytes": ab["event"]},
+        "stages_ms": {k: round(v, 4) for k, v in st.items()},
+        "score_roofline": {"algorithmic_bytes": ab["score"],
+                           "achieved": ab["score"] / (st["score"] * 1e-3) / 1e9,
+                           "frac": ab["score"] / (st["score"] * 1e-3) / 1e9 / peak},
+        "pack_roofline": {"kernel": "k_pack_rerope", "algorithmic_bytes": ab["pack"],
+                          "achieved": ab["pack"] / (st["pack"] * 1e-3) / 1e9,
+                          "frac": ab["pack"] / (st["pack"] * 1e-3) / 1e9 / peak},
+        "gpu_launches": n_launch.get("select", 0) + n_launch.get("pack", 0)
+        + n_launch.get("score", 0) * score_kernels,
+        "l2": "L2 flushed between replays (256 MiB write outside the event span); the "
+              "event moves " f"{ab['event'] / 1e9:.1f} GB",
+    }
+    del q, kraw, vraw, meank, ev, flush
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        units, frac, what = _oracle_config_sample(cfg, name, dev)
+        secs = _oracle_event(cfg, units, cores)
+        out["cpu_baseline"] = {"value": cfg.n_tok * frac / secs, "unit": UNIT, "cores": cores,
+                               "kind": "oracle", "scaled": True,
+                               "sample": f"{what}; score+select+pack (pack in packed layers), "
+                                         f"fp64 C oracle, thread pool of {cores}, "
+                                         f"{secs:.2f} s wall"}
+    return out
 
 
 # --------------------------------------------------- QueryMemory event
@@ -759,38 +901,55 @@ def confidence_monitor(args, dev, peak, reps: int = 10):
 
 # ------------------------------------------------------------ oracle arm
 
-def _oracle_sample(n_units, dev):
-    """Oracle inputs of the first n_units (layer, KV head) units of the
-    workload: (q rows, raw K, raw V) per unit, as numpy bit patterns."""
+def _oracle_units(cfg, picks, dev):
+    """Oracle inputs of the sampled (layer, KV head, session) units, from the
+    seeded generators only: (l, h, r, q rows, raw K or None, raw V or None,
+    Mean-K or None) as numpy bit patterns.  A layer with resident raw K gets
+    its Mean-K from the oracle's own build; the others use the drawn index."""
     import numpy as np
     import torch
     import workloads as W
-    cfg = W.config_8b()
     units = []
-    for u in range(n_units):
-        l, h = divmod(u * 37 % (cfg.L * cfg.H), cfg.H)
-        k = W.bf16_bits(cfg.kraw_unit(l, h, 0, dev))
-        v = W.bf16_bits(cfg.vraw_unit(l, h, 0, dev))
-        qg = [W.bf16_bits(cfg.q_unit(0, l, h * cfg.G + g, dev)) for g in range(cfg.G)]
-        units.append((l, h, np.stack(qg), k, v))
+    for l, h, r in picks:
+        qg = np.stack([W.bf16_bits(cfg.q_unit(r, l, h * cfg.G + g, dev)) for g in range(cfg.G)])
+        if l < cfg.lp:
+            k = W.bf16_bits(cfg.kraw_unit(l, h, r, dev))
+            v = W.bf16_bits(cfg.vraw_unit(l, h, r, dev))
+            units.append((l, h, r, qg, k, v, None))
+        else:
+            mk = W.bf16_bits(cfg.meank_direct_unit(l, h, r, dev))
+            units.append((l, h, r, qg, None, None, mk))
     if dev is not None and getattr(dev, "type", "cpu") == "cuda":
         torch.cuda.synchronize(dev)
-    return cfg, units
+    return units
+
+
+def _oracle_sample(n_units, dev):
+    """The first n_units (layer, KV head) units of the 8B-class event, spread
+    over the layers (unit u → (l, h) of index 37·u mod 288)."""
+    import workloads as W
+    cfg = W.config_8b()
+    picks = []
+    for u in range(n_units):
+        l, h = divmod(u * 37 % (cfg.L * cfg.H), cfg.H)
+        picks.append((l, h, 0))
+    return cfg, _oracle_units(cfg, picks, dev)
 
 
 def _oracle_event(cfg, units, threads):
-    """score → select → pack of the sampled units with the oracle; returns
-    (seconds, units done).  Mean-K (index maintenance) is built first and is
-    not part of the timed event."""
+    """score → select → pack of the sampled units with the oracle (pack only
+    where the unit's layer has resident raw K/V); returns seconds.  The Mean-K
+    build (index maintenance) runs first and is not part of the timed event."""
     from concurrent.futures import ThreadPoolExecutor
     import oracle
-    mks = [oracle.meank(u[3][None])[0] for u in units]
+    mks = [u[6] if u[6] is not None else oracle.meank(u[4][None])[0] for u in units]
 
     def one(i):
-        l, h, qg, k, v = units[i]
+        l, h, r, qg, k, v, _ = units[i]
         s = oracle.score_unit(qg, mks[i])
         kept, cnt, _ = oracle.select(s, cfg.budget, cfg.n_sink, cfg.n_recent)
-        oracle.pack_unit(k, v, kept, cnt, cfg.budget, cfg.pos0, cfg.theta)
+        if k is not None:
+            oracle.pack_unit(k, v, kept, cnt, cfg.budget, cfg.pos0, cfg.theta)
         return cnt
 
     t0 = time.perf_counter()
@@ -800,16 +959,25 @@ def _oracle_event(cfg, units, threads):
 
 
 def cpu_baseline(args, dev=None):
+    """The oracle on a sample of the 8B-class event's units: on every host
+    core (a thread pool over the units), and on one thread."""
     cores = os.cpu_count() or 1
     n_units = args.cpu_units
     cfg, units = _oracle_sample(n_units, dev)
     secs = _oracle_event(cfg, units, cores)
     frac = n_units / (cfg.L * cfg.H)
     value = cfg.n_tok * frac / secs
+    n1 = max(1, n_units // 4)
+    secs1 = _oracle_event(cfg, units[:n1], 1)
+    value1 = cfg.n_tok * (n1 / (cfg.L * cfg.H)) / secs1
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n_units} of {cfg.L * cfg.H} (layer, KV head) units of the event "
                       f"(score+select+pack, fp64 C oracle, thread pool of {cores}); "
-                      f"{secs:.2f} s wall, tokens scaled by {frac:.4f}"}
+                      f"{secs:.2f} s wall, tokens scaled by {frac:.4f}",
+            "single_thread": {"value": value1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} of the same units on one thread; "
+                                        f"{secs1:.2f} s wall, tokens scaled by "
+                                        f"{n1 / (cfg.L * cfg.H):.4f}"}}
 
 
 def run_reference(args, rank, world):
@@ -842,7 +1010,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": n_steps, "warmup": n_warm,
             "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, workloads/)",
-            "config": {"workload": WORKLOAD, "parallelism": "host thread pool"},
+            "config": bench_config(cfg, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -858,6 +1026,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-units", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-27b", action="store_true",
+                    help="skip the 27B-class 1M-token event measurement")
+    ap.add_argument("--no-ragged", action="store_true",
+                    help="skip the 128-session ragged event measurement")
     ap.add_argument("--no-slotmap", action="store_true",
                     help="skip the QueryMemory (slot-map) event measurement")
     ap.add_argument("--no-tiered", action="store_true",
@@ -886,6 +1058,12 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, local_rank)
+    for name, flag in (("27b_1m", args.no_27b), ("ragged_128", args.no_ragged)):
+        if not flag:
+            import torch
+            torch.cuda.empty_cache()
+            line["event_" + name] = config_event(args, torch.device("cuda", local_rank), name=name,
+                                                 peak=peaks()[0])
     if not args.no_slotmap:
         import torch
         torch.cuda.empty_cache()

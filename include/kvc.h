@@ -77,6 +77,32 @@ typedef enum {
   KVC_ERR_CAPACITY = 10    /* device: the freed-slot list overflowed         */
 } kvc_status;
 
+/* Kernel choice for the entry points that have more than one kernel for the
+ * same arithmetic (a diagnostic of this library, no counterpart on the
+ * pages).  The plain entry points (kvc_score, kvc_score_qmem,
+ * kvc_recover_score) choose by shape and device, which is KVC_KERNEL_AUTO;
+ * their _ex variants take the choice as an argument so that a test or a
+ * profile can run one particular kernel.  A kernel that does not cover the
+ * call's sizes is refused with KVC_ERR_SHAPE before any launch; a value that
+ * does not belong to the entry point is KVC_ERR_INVALID_ARG.  Every kernel of
+ * one entry point computes the same quantity within the accuracy that entry
+ * point states. */
+typedef enum {
+  KVC_KERNEL_AUTO = 0,
+  /* kvc_score_ex (Mean-K scoring) */
+  KVC_KERNEL_SCORE_FUSED = 1,   /* tcgen05, Mean-K read once; G = 4, W = 32, D = 128 */
+  KVC_KERNEL_SCORE_RING = 2,    /* tcgen05, two passes in a CTA-cluster ring          */
+  KVC_KERNEL_SCORE_PERSIST = 3, /* tcgen05, persistent grid, L2 exchange              */
+  KVC_KERNEL_SCORE_SPLIT = 4,   /* tcgen05, two launches                              */
+  KVC_KERNEL_SCORE_CC = 5,      /* CUDA cores, two launches; any shape                */
+  /* kvc_score_qmem_ex (rule score) */
+  KVC_KERNEL_QMEM_TC = 16,      /* tcgen05 logits (8 KV heads, G ∈ {2, 4, 8})         */
+  KVC_KERNEL_QMEM_CC = 17,      /* CUDA-core logits; any shape                        */
+  /* kvc_recover_score_ex (LSE-recovery score) */
+  KVC_KERNEL_RECOVER_TC = 32,   /* tcgen05 page tiles (H 8, block 16, G ∈ {2, 4, 8})  */
+  KVC_KERNEL_RECOVER_CC = 33    /* CUDA cores; any shape                              */
+} kvc_kernel;
+
 /* Static, never-NULL description of a status code. */
 const char *kvc_status_string(kvc_status s);
 
@@ -106,8 +132,13 @@ kvc_status kvc_selftest_bounded_wait(int32_t *dev_status, cudaStream_t stream);
  *   kraw   device bf16 [L][H][n_tok][D]   raw (pre-RoPE) keys
  *   meank  device bf16 [L][H][n_tok/32][D] out: block means
  * Each output element is the exact mean of the 32 inputs rounded once to
- * bf16 (round-to-nearest-even); the sum is taken in fp64, which is exact
- * whenever the 32 magnitudes span less than 2^40.
+ * bf16 (round-to-nearest-even).  The kernel sums in fp32 with Knuth's
+ * TwoSum, which keeps every rounding error of the running sum, so the sum is
+ * exact while a guard holds over each thread's 8 columns: all inputs zero,
+ * or 32·max|x| in [2^-60, 2^100) with min|x| > 2^-29·max|x| (no zero,
+ * subnormal, NaN or infinity next to normal values).  Columns outside the
+ * guard are summed in fp64 in token order, which is exact whenever their
+ * magnitudes span less than about 2^40 (NaN gives the quiet NaN 0x7FC0).
  * Errors: KVC_ERR_INVALID_ARG (NULL, sizes < 1), KVC_ERR_SHAPE (n_tok % 32,
  * D ∉ {64,128}), KVC_ERR_ALIGN (pointers not 16-byte aligned).
  * ---------------------------------------------------------------------- */
@@ -148,6 +179,13 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                      const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
                      int32_t nb_max, void *ws, size_t ws_bytes,
                      int32_t *dev_status, cudaStream_t stream);
+/* kvc_score with the kernel named by `kernel` (KVC_KERNEL_AUTO or one of
+ * KVC_KERNEL_SCORE_*; see kvc_kernel).  Same arguments, result and errors. */
+kvc_status kvc_score_ex(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
+                        int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                        const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
+                        int32_t nb_max, void *ws, size_t ws_bytes,
+                        int32_t *dev_status, kvc_kernel kernel, cudaStream_t stream);
 
 /* kvc_score for callers that cannot allocate device memory (no counterpart
  * on the pages; this is a convenience of the library).  Some hosts cannot
@@ -161,15 +199,25 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
  *  - Sizes whose scratch (kvc_score_workspace_size) exceeds the array are
  *    rejected with KVC_ERR_WORKSPACE before anything is launched; the 8B-
  *    class 128K-token event (36 layers, 8/32 heads, W 32) needs about 5 MB.
+ *  - kvc_score's own argument, shape and alignment errors are reported
+ *    first, exactly as kvc_score reports them.
  *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture on the device.
+ *    per device, with that device current) and keeps it; make that first
+ *    call before any stream capture on the device.  The kept address belongs
+ *    to the context current at that call: a call under another context of
+ *    the device (one the caller created and made current) repeats the
+ *    look-up, so make such a call before capture too.  Do not call this
+ *    entry point again after a cudaDeviceReset in the same process: the
+ *    reset unloads the array, and the library does not track resets.
  *  - Every call shares the one array per device: calls whose kernels overlap
  *    on the GPU (different streams, no ordering between them) race and give
  *    undefined scores.  Serialise them (one stream, or events).
  * Errors: those of kvc_score, plus KVC_ERR_WORKSPACE as above and
  * KVC_ERR_CUDA if the device address cannot be obtained. */
 #define KVC_SCORE_STATIC_SCRATCH_BYTES (8u << 20)
+/* KVC_SCORE_STATIC_SCRATCH_BYTES as compiled into this library (bindings
+ * read the limit from here rather than repeat the constant). */
+size_t kvc_score_static_scratch_bytes(void);
 kvc_status kvc_score_static(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                             int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
                             const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
@@ -220,6 +268,14 @@ kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
                           int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
                           void *ws, size_t ws_bytes, int32_t *dev_status,
                           cudaStream_t stream);
+/* kvc_score_qmem with the logits kernel named by `kernel` (KVC_KERNEL_AUTO,
+ * KVC_KERNEL_QMEM_TC or KVC_KERNEL_QMEM_CC). */
+kvc_status kvc_score_qmem_ex(const float *M, const kvc_bf16 *kpool,
+                             const int32_t *slot_map, int32_t sentinel,
+                             float *rule, int32_t n_sess, int32_t L, int32_t H,
+                             int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
+                             void *ws, size_t ws_bytes, int32_t *dev_status,
+                             kvc_kernel kernel, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Step 2 (select): budgeted top-k with a forced set (IntentKV §4 "Top-k
@@ -438,6 +494,14 @@ kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16
                              int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
                              float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
                              cudaStream_t stream);
+/* kvc_recover_score with the kernel named by `kernel` (KVC_KERNEL_AUTO,
+ * KVC_KERNEL_RECOVER_TC or KVC_KERNEL_RECOVER_CC). */
+kvc_status kvc_recover_score_ex(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
+                                int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
+                                const int32_t *seqused_k, const int32_t *count, int32_t n_req,
+                                int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
+                                float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                kvc_kernel kernel, cudaStream_t stream);
 
 /* 1 if kvc_recover_score runs these sizes on the tensor cores, else 0. */
 int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_size);

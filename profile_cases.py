@@ -1,20 +1,22 @@
-"""Small, self-contained launches of one kernel family for profiling.
+"""Profiling cases: small, self-contained launches of one kernel family.
+
+A measurement harness beside bench.py (not part of the library package).
 
 Each case builds a reduced 8B-class workload (fewer layers, so a capture
 holds a few GB at most while its inputs still exceed the 129 MB L2), runs the
 event once to produce realistic inputs for the stage, then launches the stage
 `--iters` times.
 
-  python -m query_conditioned_kv_gb300.profile_cases score --layers 16 --iters 3
-  python -m query_conditioned_kv_gb300.profile_cases score --config 27b --layers 2 --iters 3
-  python -m query_conditioned_kv_gb300.profile_cases pack  --layers 4  --iters 3
-  python -m query_conditioned_kv_gb300.profile_cases select --layers 16 --iters 3
-  python -m query_conditioned_kv_gb300.profile_cases meank  --layers 2  --iters 3
-  python -m query_conditioned_kv_gb300.profile_cases qmem   --layers 4  --sessions 8 --iters 2
-  python -m query_conditioned_kv_gb300.profile_cases event_timing --config 27b --iters 10
-  python -m query_conditioned_kv_gb300.profile_cases paged  --sessions 4 --iters 3
-  python -m query_conditioned_kv_gb300.profile_cases tiered --layers 8 --iters 2
-  python -m query_conditioned_kv_gb300.profile_cases confidence --iters 3
+  python profile_cases.py score --layers 16 --iters 3
+  python profile_cases.py score --config 27b --layers 2 --iters 3
+  python profile_cases.py pack  --layers 4  --iters 3
+  python profile_cases.py select --layers 16 --iters 3
+  python profile_cases.py meank  --layers 2  --iters 3
+  python profile_cases.py qmem   --layers 4  --sessions 8 --iters 2
+  python profile_cases.py event_timing --config 27b --iters 10
+  python profile_cases.py paged  --sessions 4 --iters 3
+  python profile_cases.py tiered --layers 8 --iters 2
+  python profile_cases.py confidence --iters 3
 
 event_timing times a whole Mean-K event (score → select → pack, one CUDA
 graph) on a full workload — tiny, 8b, 27b or ragged — with L2 flushed
@@ -43,9 +45,12 @@ def main(argv=None) -> None:
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sessions", type=int, default=8)
     ap.add_argument("--config", choices=["tiny", "8b", "27b", "ragged"], default="8b")
+    ap.add_argument("--kernel", default="auto",
+                    help="scorer to run (a kvc_kernel name: score_fused, score_ring, "
+                         "qmem_cc, recover_cc, ...); default: the library's choice")
     args = ap.parse_args(argv)
 
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    root = os.path.dirname(os.path.abspath(__file__))
     sys.path.insert(0, root)
     import torch
 
@@ -96,12 +101,12 @@ def main(argv=None) -> None:
         kraw = vraw = None
     ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
                     cfg.n_recent, theta=cfg.theta, device=dev)
-    ev.score(q, meank)
+    ev.score(q, meank, kernel=args.kernel)
     ev.select()
     torch.cuda.synchronize()
     for _ in range(args.iters):
         if args.case == "score":
-            ev.score(q, meank)
+            ev.score(q, meank, kernel=args.kernel)
         elif args.case == "select":
             ev.select()
         elif args.case == "pack":
@@ -133,6 +138,7 @@ def _event_timing(args, dev, root):
     kvc.kvc_build_meank(kraw, meank[:cfg.lp], cfg.lp, cfg.H, cfg.D, cfg.n_tok)
     ev = MeanKEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
                     cfg.n_recent, cfg.lp, cfg.theta, cfg.pos0, device=dev)
+    ev.score_kernel = args.kernel
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(3):
         ev.run(q, meank, kraw, vraw)
@@ -201,7 +207,7 @@ def _qmem_case(args, dev):
     ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots, cfg.budget,
                       cfg.prefix, cfg.sentinel, device=dev)
     for _ in range(args.iters):
-        ev.score(M, kp, sm)
+        ev.score(M, kp, sm, kernel=args.kernel)
     torch.cuda.synchronize()
     st = kvc.kvc_device_status(ev.dev_status)
     if st != 0:

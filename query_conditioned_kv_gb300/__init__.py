@@ -19,11 +19,13 @@ __all__ = [
     "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG",
     "kvc_status_string", "kvc_version", "kvc_device_status", "kvc_selftest_bounded_wait",
     "kvc_build_meank", "kvc_score_workspace_size", "kvc_score_launches", "kvc_score",
-    "kvc_score_static", "SCORE_STATIC_SCRATCH_BYTES",
-    "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem",
+    "kvc_score_ex", "kvc_score_static", "kvc_score_static_scratch_bytes",
+    "SCORE_STATIC_SCRATCH_BYTES", "KERNELS",
+    "kvc_qmem_update", "kvc_score_qmem_workspace_size", "kvc_score_qmem", "kvc_score_qmem_ex",
     "kvc_select", "kvc_rope_table", "kvc_pack_rerope", "kvc_pack_tiered", "kvc_init_sentinel",
     "kvc_redirect_free_workspace_size", "kvc_redirect_free",
-    "kvc_recover_score", "kvc_recover_score_workspace_size", "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
+    "kvc_recover_score", "kvc_recover_score_ex", "kvc_recover_score_workspace_size",
+    "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
     "kvc_lrfu_update", "kvc_token_confidence", "kvc_conf_trend_budget",
     "TAIL_MAX_TOKENS",
 ]
@@ -32,8 +34,15 @@ BLOCK_TOKENS = 32
 SENTINEL_K_BITS = 0xC61C
 SELECT_MAX_SEG = 49152
 SCORE_MAX_ROWS = 256
-SCORE_STATIC_SCRATCH_BYTES = 8 << 20
 TAIL_MAX_TOKENS = 1 << 20
+
+# kvc_kernel values (include/kvc.h): the kernel an _ex entry point runs
+KERNELS = {
+    "auto": 0,
+    "score_fused": 1, "score_ring": 2, "score_persist": 3, "score_split": 4, "score_cc": 5,
+    "qmem_tc": 16, "qmem_cc": 17,
+    "recover_tc": 32, "recover_cc": 33,
+}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvc.so")
@@ -64,11 +73,16 @@ _SIGS = {
                                     _I32, _I64, _I32, _P, _P]),
     "kvc_score": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
                              _I32, _I64, _I32, _P, _SZ, _P, _P]),
+    "kvc_score_ex": (_c.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P,
+                                _I32, _I64, _I32, _P, _SZ, _P, _c.c_int, _P]),
+    "kvc_score_static_scratch_bytes": (_SZ, []),
     "kvc_qmem_update": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32,
                                    _c.c_float, _c.c_float, _I32, _P]),
     "kvc_score_qmem_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "kvc_score_qmem": (_c.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I32,
                                   _I32, _I32, _I32, _I64, _P, _SZ, _P, _P]),
+    "kvc_score_qmem_ex": (_c.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                     _I32, _I32, _I32, _I64, _P, _SZ, _P, _c.c_int, _P]),
     "kvc_select": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P,
                               _P, _P, _P]),
     "kvc_rope_table": (_c.c_int, [_P, _I32, _I32, _I32, _c.c_double, _P]),
@@ -84,6 +98,9 @@ _SIGS = {
     "kvc_recover_score_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "kvc_recover_score": (_c.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _P, _I32,
                                      _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "kvc_recover_score_ex": (_c.c_int, [_P, _P, _P, _I64, _P, _I32, _P, _P, _I32,
+                                        _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P,
+                                        _c.c_int, _P]),
     "kvc_recover_tensor_core": (_I32, [_I32, _I32, _I32, _I32]),
     "kvc_token_confidence": (_c.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "kvc_conf_trend_budget": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I32, _c.c_float, _I32,
@@ -99,6 +116,18 @@ for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
     _f.restype = _res
     _f.argtypes = _args
+
+
+SCORE_STATIC_SCRATCH_BYTES = int(lib.kvc_score_static_scratch_bytes())
+
+
+def _kernel(name) -> int:
+    if isinstance(name, int):
+        return name
+    try:
+        return KERNELS[name]
+    except KeyError:
+        raise ValueError(f"unknown kernel {name!r}; one of {sorted(KERNELS)}") from None
 
 
 class KvcError(RuntimeError):
@@ -176,6 +205,19 @@ def kvc_score(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,
                       _stream(stream)), "kvc_score")
 
 
+def kvc_score_ex(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,
+                 nb_max, ws, kernel="auto", dev_status=None, stream=None):
+    """kvc_score with a named kernel (a KERNELS key or value)."""
+    _ok(lib.kvc_score_ex(_ptr(q), _ptr(meank), _ptr(scores), L, H, Hq, D, W,
+                         _ptr(blk_off), n_sess, nb_total, nb_max, _ptr(ws),
+                         ws.numel() * ws.element_size(), _ptr(dev_status), _kernel(kernel),
+                         _stream(stream)), "kvc_score_ex")
+
+
+def kvc_score_static_scratch_bytes() -> int:
+    return int(lib.kvc_score_static_scratch_bytes())
+
+
 def kvc_score_static(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total,
                      nb_max, dev_status=None, stream=None):
     """kvc_score with the library's fixed scratch array instead of a caller
@@ -202,6 +244,16 @@ def kvc_score_qmem(M, kpool, slot_map, sentinel, rule, n_sess, L, H, Hq, D, N,
                            _ptr(rule), n_sess, L, H, Hq, D, N, n_slots,
                            _ptr(ws), ws.numel() * ws.element_size(),
                            _ptr(dev_status), _stream(stream)), "kvc_score_qmem")
+
+
+def kvc_score_qmem_ex(M, kpool, slot_map, sentinel, rule, n_sess, L, H, Hq, D, N,
+                      n_slots, ws, kernel="auto", dev_status=None, stream=None):
+    """kvc_score_qmem with a named logits kernel (a KERNELS key or value)."""
+    _ok(lib.kvc_score_qmem_ex(_ptr(M), _ptr(kpool), _ptr(slot_map), sentinel,
+                              _ptr(rule), n_sess, L, H, Hq, D, N, n_slots,
+                              _ptr(ws), ws.numel() * ws.element_size(),
+                              _ptr(dev_status), _kernel(kernel), _stream(stream)),
+        "kvc_score_qmem_ex")
 
 
 def kvc_select(scores, seg_off, n_seg, max_seg_len, budget, n_sink, n_recent,
@@ -279,6 +331,18 @@ def kvc_recover_score(q, lse, kpool, n_slots, block_table, max_blocks, seqused_k
                               block_size, _ptr(state), _ptr(ws),
                               0 if ws is None else ws.numel() * ws.element_size(),
                               _ptr(dev_status), _stream(stream)), "kvc_recover_score")
+
+
+def kvc_recover_score_ex(q, lse, kpool, n_slots, block_table, max_blocks, seqused_k, count,
+                         n_req, L, H, Hq, D, block_size, state, ws=None, kernel="auto",
+                         dev_status=None, stream=None):
+    """kvc_recover_score with a named kernel (a KERNELS key or value)."""
+    _ok(lib.kvc_recover_score_ex(_ptr(q), _ptr(lse), _ptr(kpool), n_slots, _ptr(block_table),
+                                 max_blocks, _ptr(seqused_k), _ptr(count), n_req, L, H, Hq, D,
+                                 block_size, _ptr(state), _ptr(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(),
+                                 _ptr(dev_status), _kernel(kernel), _stream(stream)),
+        "kvc_recover_score_ex")
 
 
 def kvc_recover_tensor_core(H, Hq, D, block_size) -> bool:

@@ -13,6 +13,19 @@ bool head_dim_ok(int D) { return D == 64 || D == 128; }
 
 kvc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
+// A launch refused because the named kernel does not cover the sizes.
+kvc_status from_cuda_kernel(cudaError_t e) {
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    return KVC_ERR_SHAPE;
+  }
+  return from_cuda(e);
+}
+
+bool score_kernel_ok(kvc_kernel k) {
+  return k == KVC_KERNEL_AUTO || (k >= KVC_KERNEL_SCORE_FUSED && k <= KVC_KERNEL_SCORE_CC);
+}
+
 __global__ void k_init_sentinel(uint16_t *kpool, uint16_t *vpool, int L, int H,
                                 int D, int64_t n_slots, int32_t sentinel) {
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -42,6 +55,24 @@ __global__ void k_selftest_wait(int32_t *status) {
 }
 
 }  // namespace
+
+namespace kvc {
+
+kvc_status score_args_status(const void *q, const void *meank, const void *scores,
+                             const int64_t *blk_off, int L, int H, int Hq, int D, int W,
+                             int n_sess, int64_t nb_total, int nb_max) {
+  if (!q || !meank || !scores || !blk_off) return KVC_ERR_INVALID_ARG;
+  if (L < 1 || H < 1 || Hq < 1 || W < 1 || n_sess < 1 || nb_total < 1 || nb_max < 1 ||
+      nb_max > nb_total)
+    return KVC_ERR_INVALID_ARG;
+  if (!head_dim_ok(D) || Hq % H || (int64_t)(Hq / H) * W > KVC_SCORE_MAX_ROWS ||
+      (int64_t)L * H * n_sess > 65535)
+    return KVC_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(meank) || !aligned16(scores)) return KVC_ERR_ALIGN;
+  return KVC_OK;
+}
+
+}  // namespace kvc
 
 extern "C" {
 
@@ -89,9 +120,27 @@ kvc_status kvc_build_meank(const kvc_bf16 *kraw, kvc_bf16 *meank, int32_t L,
 size_t kvc_score_workspace_size(int32_t L, int32_t H, int32_t Hq, int32_t W,
                                 int32_t n_sess, int32_t nb_max, int64_t nb_total) {
   if (L < 1 || H < 1 || Hq < H || Hq % H || W < 1 || n_sess < 1 || nb_max < 1 ||
-      nb_total < nb_max)
+      nb_total < nb_max || (int64_t)L * H * n_sess > 65535 ||
+      (int64_t)(Hq / H) * W > KVC_SCORE_MAX_ROWS)
     return 0;
   return kvc::score_meank_ws_bytes(L, H, Hq, W, n_sess, nb_max, nb_total);
+}
+
+kvc_status kvc_score_ex(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
+                        int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
+                        const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
+                        int32_t nb_max, void *ws, size_t ws_bytes,
+                        int32_t *dev_status, kvc_kernel kernel, cudaStream_t stream) {
+  if (!ws || !score_kernel_ok(kernel)) return KVC_ERR_INVALID_ARG;
+  const kvc_status args = kvc::score_args_status(q, meank, scores, blk_off, L, H, Hq, D, W,
+                                                 n_sess, nb_total, nb_max);
+  if (args != KVC_OK) return args;
+  if (!aligned16(ws)) return KVC_ERR_ALIGN;
+  if (ws_bytes < kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max, nb_total))
+    return KVC_ERR_WORKSPACE;
+  return from_cuda_kernel(kvc::launch_score_meank(q, meank, scores, L, H, Hq, D, W, blk_off,
+                                                  n_sess, nb_total, nb_max, ws, dev_status,
+                                                  (int)kernel, stream));
 }
 
 kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
@@ -99,19 +148,8 @@ kvc_status kvc_score(const kvc_bf16 *q, const kvc_bf16 *meank, float *scores,
                      const int64_t *blk_off, int32_t n_sess, int64_t nb_total,
                      int32_t nb_max, void *ws, size_t ws_bytes,
                      int32_t *dev_status, cudaStream_t stream) {
-  if (!q || !meank || !scores || !blk_off || !ws) return KVC_ERR_INVALID_ARG;
-  if (L < 1 || H < 1 || Hq < 1 || W < 1 || n_sess < 1 || nb_total < 1 || nb_max < 1 ||
-      nb_max > nb_total)
-    return KVC_ERR_INVALID_ARG;
-  if (!head_dim_ok(D) || Hq % H || (int64_t)(Hq / H) * W > KVC_SCORE_MAX_ROWS ||
-      (int64_t)L * H * n_sess > 65535)
-    return KVC_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(meank) || !aligned16(scores) || !aligned16(ws))
-    return KVC_ERR_ALIGN;
-  if (ws_bytes < kvc_score_workspace_size(L, H, Hq, W, n_sess, nb_max, nb_total))
-    return KVC_ERR_WORKSPACE;
-  return from_cuda(kvc::launch_score_meank(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
-                                           nb_total, nb_max, ws, dev_status, stream));
+  return kvc_score_ex(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess, nb_total, nb_max, ws,
+                      ws_bytes, dev_status, KVC_KERNEL_AUTO, stream);
 }
 
 int32_t kvc_score_launches(int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t W,
@@ -138,13 +176,15 @@ size_t kvc_score_qmem_workspace_size(int32_t n_sess, int32_t L, int32_t Hq,
   return kvc::score_qmem_ws_bytes(n_sess, L, Hq, N);
 }
 
-kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
-                          const int32_t *slot_map, int32_t sentinel,
-                          float *rule, int32_t n_sess, int32_t L, int32_t H,
-                          int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
-                          void *ws, size_t ws_bytes, int32_t *dev_status,
-                          cudaStream_t stream) {
+kvc_status kvc_score_qmem_ex(const float *M, const kvc_bf16 *kpool,
+                             const int32_t *slot_map, int32_t sentinel,
+                             float *rule, int32_t n_sess, int32_t L, int32_t H,
+                             int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
+                             void *ws, size_t ws_bytes, int32_t *dev_status,
+                             kvc_kernel kernel, cudaStream_t stream) {
   if (!M || !kpool || !slot_map || !rule || !ws) return KVC_ERR_INVALID_ARG;
+  if (kernel != KVC_KERNEL_AUTO && kernel != KVC_KERNEL_QMEM_TC && kernel != KVC_KERNEL_QMEM_CC)
+    return KVC_ERR_INVALID_ARG;
   if (n_sess < 1 || L < 1 || H < 1 || Hq < 1 || N < 1 || n_slots < 1 || n_slots > INT32_MAX)
     return KVC_ERR_INVALID_ARG;
   if (!head_dim_ok(D) || Hq % H || H > 32 || 32 % H || Hq / H > 8 || n_sess > 65535 ||
@@ -152,8 +192,19 @@ kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
     return KVC_ERR_SHAPE;
   if (!aligned16(M) || !aligned16(kpool) || !aligned16(ws)) return KVC_ERR_ALIGN;
   if (ws_bytes < kvc_score_qmem_workspace_size(n_sess, L, Hq, N)) return KVC_ERR_WORKSPACE;
-  return from_cuda(kvc::launch_score_qmem(M, kpool, slot_map, sentinel, rule, n_sess, L, H, Hq,
-                                          D, N, n_slots, ws, dev_status, stream));
+  return from_cuda_kernel(kvc::launch_score_qmem(M, kpool, slot_map, sentinel, rule, n_sess, L,
+                                                 H, Hq, D, N, n_slots, ws, dev_status,
+                                                 (int)kernel, stream));
+}
+
+kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
+                          const int32_t *slot_map, int32_t sentinel,
+                          float *rule, int32_t n_sess, int32_t L, int32_t H,
+                          int32_t Hq, int32_t D, int32_t N, int64_t n_slots,
+                          void *ws, size_t ws_bytes, int32_t *dev_status,
+                          cudaStream_t stream) {
+  return kvc_score_qmem_ex(M, kpool, slot_map, sentinel, rule, n_sess, L, H, Hq, D, N, n_slots,
+                           ws, ws_bytes, dev_status, KVC_KERNEL_AUTO, stream);
 }
 
 kvc_status kvc_select(const float *scores, const int64_t *seg_off,
@@ -281,13 +332,16 @@ size_t kvc_recover_score_workspace_size(int32_t n_req, int32_t max_blocks, int32
   return kvc::recover_ws_bytes(n_req, max_blocks, block_size, L, H, Hq, D);
 }
 
-kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
-                             int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
-                             const int32_t *seqused_k, const int32_t *count, int32_t n_req,
-                             int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
-                             float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
-                             cudaStream_t stream) {
+kvc_status kvc_recover_score_ex(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
+                                int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
+                                const int32_t *seqused_k, const int32_t *count, int32_t n_req,
+                                int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
+                                float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                kvc_kernel kernel, cudaStream_t stream) {
   if (!q || !lse || !kpool || !block_table || !seqused_k || !count || !state)
+    return KVC_ERR_INVALID_ARG;
+  if (kernel != KVC_KERNEL_AUTO && kernel != KVC_KERNEL_RECOVER_TC &&
+      kernel != KVC_KERNEL_RECOVER_CC)
     return KVC_ERR_INVALID_ARG;
   if (n_req < 1 || L < 1 || H < 1 || Hq < 1 || block_size < 1 || max_blocks < 1 ||
       n_slots < block_size)
@@ -299,9 +353,20 @@ kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16
   if (!aligned16(q) || !aligned16(kpool) || !aligned16(lse) || !aligned16(state) ||
       (ws && !aligned16(ws)))
     return KVC_ERR_ALIGN;
-  return from_cuda(kvc::launch_recover_score(q, lse, kpool, n_slots, block_table, max_blocks,
-                                             seqused_k, count, n_req, L, H, Hq, D, block_size,
-                                             state, ws, ws ? ws_bytes : 0, dev_status, stream));
+  return from_cuda_kernel(kvc::launch_recover_score(
+      q, lse, kpool, n_slots, block_table, max_blocks, seqused_k, count, n_req, L, H, Hq, D,
+      block_size, state, ws, ws ? ws_bytes : 0, dev_status, (int)kernel, stream));
+}
+
+kvc_status kvc_recover_score(const kvc_bf16 *q, const float *lse, const kvc_bf16 *kpool,
+                             int64_t n_slots, const int32_t *block_table, int32_t max_blocks,
+                             const int32_t *seqused_k, const int32_t *count, int32_t n_req,
+                             int32_t L, int32_t H, int32_t Hq, int32_t D, int32_t block_size,
+                             float *state, void *ws, size_t ws_bytes, int32_t *dev_status,
+                             cudaStream_t stream) {
+  return kvc_recover_score_ex(q, lse, kpool, n_slots, block_table, max_blocks, seqused_k, count,
+                              n_req, L, H, Hq, D, block_size, state, ws, ws_bytes, dev_status,
+                              KVC_KERNEL_AUTO, stream);
 }
 
 kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t n_seg,

@@ -51,6 +51,12 @@ inline int device_sm_count() {
   return v;
 }
 
+// kvc_score's host-side argument, shape and alignment checks (everything
+// but the workspace), shared by the entry points that score (kvc_abi.cu).
+kvc_status score_args_status(const void *q, const void *meank, const void *scores,
+                             const int64_t *blk_off, int L, int H, int Hq, int D, int W,
+                             int n_sess, int64_t nb_total, int nb_max);
+
 // ------------------------------------------------------------ launches
 // Each returns cudaGetLastError() of its launch(es).
 
@@ -58,11 +64,13 @@ cudaError_t launch_build_meank(const uint16_t *kraw, uint16_t *meank,
                                int64_t rows, int64_t n_tok, int D,
                                cudaStream_t s);
 
+// `path`: a kvc_kernel value (KVC_KERNEL_AUTO or one KVC_KERNEL_SCORE_*);
+// cudaErrorNotSupported when the named kernel cannot run these sizes.
 cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
                                float *scores, int L, int H, int Hq, int D,
                                int W, const int64_t *blk_off, int n_sess,
                                int64_t nb_total, int nb_max, void *ws,
-                               int32_t *status, cudaStream_t s);
+                               int32_t *status, int path, cudaStream_t s);
 size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
                             int nb_max, int64_t nb_total);
 
@@ -75,7 +83,7 @@ size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max, in
 cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *scores, int L,
                             int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
                             int64_t nb_total, int nb_max, void *ws, int32_t *status,
-                            cudaStream_t s);
+                            int path, cudaStream_t s);
 
 // single-read tcgen05 scorer for 4 query heads per KV head, W = 32, D = 128
 // (score_fused.cu); cudaErrorNotSupported outside that shape.
@@ -88,11 +96,12 @@ cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
                                int D, int T, float decay, float gain,
                                int renorm, cudaStream_t s);
 
+// `path`: KVC_KERNEL_AUTO, KVC_KERNEL_QMEM_TC or KVC_KERNEL_QMEM_CC.
 cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
                               const int32_t *slot_map, int32_t sentinel,
                               float *rule, int n_sess, int L, int H, int Hq,
                               int D, int N, int64_t n_slots, void *ws,
-                              int32_t *status, cudaStream_t s);
+                              int32_t *status, int path, cudaStream_t s);
 size_t score_qmem_ws_bytes(int n_sess, int L, int Hq, int N);
 // tensor-core logits of the rule score (qmem_tc.cu)
 bool qmem_tc_supported(int H, int Hq, int D, int64_t L, int64_t n_slots);
@@ -158,11 +167,12 @@ int conf_trend_max_windows();
 // ActKV paged primitives (recover.cu)
 bool recover_tc_supported(int H, int Hq, int D, int BS);
 size_t recover_ws_bytes(int n_req, int max_blocks, int BS, int L, int H, int Hq, int D);
+// `path`: KVC_KERNEL_AUTO, KVC_KERNEL_RECOVER_TC or KVC_KERNEL_RECOVER_CC.
 cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint16_t *kpool,
                                  int64_t n_slots, const int32_t *block_table, int max_blocks,
                                  const int32_t *seqused, const int32_t *count, int n_req, int L,
                                  int H, int Hq, int D, int BS, float *state, void *ws,
-                                 size_t ws_bytes, int32_t *status, cudaStream_t s);
+                                 size_t ws_bytes, int32_t *status, int path, cudaStream_t s);
 cudaError_t launch_tail_plan(const uint32_t *keepmask, int mask_words, const int32_t *seqused,
                              const int32_t *block_table, int max_blocks, int n_req, int BS,
                              int64_t n_slots, int32_t *src, int32_t *dst, int32_t *n_pairs,

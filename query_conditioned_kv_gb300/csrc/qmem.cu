@@ -24,7 +24,6 @@
 // For 8 KV heads and groups of 2, 4 or 8 query heads the logits come from
 // the tensor-core kernel of qmem_tc.cu instead (same outputs); the CUDA-core
 // kernel below covers every other shape.
-#include <stdlib.h>
 
 #include "kvc_internal.cuh"
 
@@ -334,7 +333,7 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
                               const int32_t *slot_map, int32_t sentinel,
                               float *rule, int n_sess, int L, int H, int Hq,
                               int D, int N, int64_t n_slots, void *ws,
-                              int32_t *status, cudaStream_t s) {
+                              int32_t *status, int path, cudaStream_t s) {
   QArgs a;
   int64_t rows = (int64_t)n_sess * L * Hq;
   a.n_tiles = (N + kTJ - 1) / kTJ;
@@ -363,9 +362,9 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
   a.n_slots = n_slots;
   a.zscale = kLog2e / sqrtf((float)D);
   cudaError_t e;
-  const char *force = getenv("KVC_QMEM_PATH");
-  const bool cc = force && force[0] == 'c' && force[1] == 'c';
-  if (!cc && qmem_tc_supported(H, Hq, D, L, n_slots)) {
+  const bool tc = qmem_tc_supported(H, Hq, D, L, n_slots);
+  if (path == KVC_KERNEL_QMEM_TC && !tc) return cudaErrorNotSupported;
+  if (path != KVC_KERNEL_QMEM_CC && tc) {
     e = launch_qmem_logits_tc(M, kpool, slot_map, sentinel, a.logits, a.part, mb, n_sess, L, H,
                               Hq, D, N, n_slots, a.n_tiles, status, s);
     if (e != cudaSuccess) return e;

@@ -27,7 +27,6 @@
 // is copied to the k-th non-retained slot inside it, so sources and
 // destinations are disjoint and every copy can run at once.
 #include <math.h>
-#include <stdlib.h>
 
 #include <algorithm>
 
@@ -653,11 +652,6 @@ k_tail_compact(uint16_t *kpool, uint16_t *vpool, int64_t n_slots, int L, int row
   }
 }
 
-bool force_cc() {
-  const char *e = getenv("KVC_RECOVER_PATH");
-  return e && e[0] == 'c' && e[1] == 'c';
-}
-
 }  // namespace
 
 bool recover_tc_supported(int H, int Hq, int D, int BS) {
@@ -674,7 +668,7 @@ constexpr int kRecItemsPerCta = 16;
 // the layers are split until there are kRecItemsPerCta items per SM (at most
 // one layer per item).  1 when the requests' pages already give that many.
 int recover_layer_groups(int n_req, int max_blocks, int BS, int L, int H, int Hq, int D) {
-  if (!recover_tc_supported(H, Hq, D, BS) || force_cc()) return 1;
+  if (!recover_tc_supported(H, Hq, D, BS)) return 1;
   const int64_t items = (int64_t)n_req * ((max_blocks + kRecPmax - 1) / kRecPmax);
   const int64_t want = (int64_t)kRecItemsPerCta * device_sm_count();
   if (items >= want) return 1;
@@ -691,7 +685,7 @@ cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint
                                  int64_t n_slots, const int32_t *block_table, int max_blocks,
                                  const int32_t *seqused, const int32_t *count, int n_req, int L,
                                  int H, int Hq, int D, int BS, float *state, void *ws,
-                                 size_t ws_bytes, int32_t *status, cudaStream_t s) {
+                                 size_t ws_bytes, int32_t *status, int path, cudaStream_t s) {
   RecArgs a{};
   a.q = q;
   a.kpool = kpool;
@@ -712,8 +706,9 @@ cudaError_t launch_recover_score(const uint16_t *q, const float *lse, const uint
   a.n_slots = n_slots;
   a.zscale = kLog2eR / sqrtf((float)D);
   const int n_sm = device_sm_count();
-  const bool tc_path = recover_tc_supported(H, Hq, D, BS) && !force_cc() &&
-                       (int64_t)L * n_slots * H < INT32_MAX;
+  const bool tc_ok = recover_tc_supported(H, Hq, D, BS) && (int64_t)L * n_slots * H < INT32_MAX;
+  if (path == KVC_KERNEL_RECOVER_TC && !tc_ok) return cudaErrorNotSupported;
+  const bool tc_path = tc_ok && path != KVC_KERNEL_RECOVER_CC;
   a.n_lg = 1;
   a.partial = nullptr;
   if (!tc_path) {

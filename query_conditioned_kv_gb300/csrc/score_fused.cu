@@ -39,7 +39,6 @@
 // Every wait is bounded (1 s of %globaltimer) and records KVC_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>

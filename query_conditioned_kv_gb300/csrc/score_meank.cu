@@ -22,7 +22,6 @@
 //           w into the block scores.
 // The logit tile is an R×64×D fp32 product from shared memory (q and Mean-K
 // staged transposed so that both operand reads are bank-conflict free).
-#include <stdlib.h>
 
 #include "kvc_internal.cuh"
 
@@ -278,16 +277,12 @@ size_t score_meank_ws_bytes(int L, int H, int Hq, int W, int n_sess,
   return cc > tc ? cc : tc;
 }
 
-// Which scorer runs: the tensor-core one whenever it covers the shape;
-// KVC_SCORE_PATH=cc selects the CUDA-core one (both are tested).
-static bool prefer_cuda_cores() {
-  const char *e = getenv("KVC_SCORE_PATH");
-  return e && e[0] == 'c' && e[1] == 'c';
-}
-
+// Which scorer runs: by default (KVC_KERNEL_AUTO) the tensor-core one
+// whenever it covers the shape, else the CUDA-core one; `path` may name one
+// kernel (both kinds compute the same scores within the stated bound).
 int score_meank_launches(int H, int Hq, int D, int W, int n_sess, int nb_max) {
   int R = (Hq / H) * W;
-  if (!prefer_cuda_cores() && score_tc_supported(R, W, D)) {
+  if (score_tc_supported(R, W, D)) {
     int n = score_tc_launches(R, W, D, n_sess, nb_max);
     if (n > 0) return n;
   }
@@ -298,11 +293,15 @@ cudaError_t launch_score_meank(const uint16_t *q, const uint16_t *meank,
                                float *scores, int L, int H, int Hq, int D,
                                int W, const int64_t *blk_off, int n_sess,
                                int64_t nb_total, int nb_max, void *ws,
-                               int32_t *status, cudaStream_t s) {
-  if (!prefer_cuda_cores() && score_tc_supported((Hq / H) * W, W, D)) {
-    cudaError_t e = launch_score_tc(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
-                                    nb_total, nb_max, ws, status, s);
-    if (e != cudaErrorNotSupported) return e;
+                               int32_t *status, int path, cudaStream_t s) {
+  if (path != KVC_KERNEL_SCORE_CC) {
+    const bool tc = score_tc_supported((Hq / H) * W, W, D);
+    if (!tc && path != KVC_KERNEL_AUTO) return cudaErrorNotSupported;
+    if (tc) {
+      cudaError_t e = launch_score_tc(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
+                                      nb_total, nb_max, ws, status, path, s);
+      if (path != KVC_KERNEL_AUTO || e != cudaErrorNotSupported) return e;
+    }
   }
   ScoreArgs a;
   a.q = q;

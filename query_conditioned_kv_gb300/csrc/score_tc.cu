@@ -36,7 +36,6 @@
 // and MMAs and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include "kvc_internal.cuh"
@@ -1054,20 +1053,11 @@ int persistent_capacity(size_t smem) {
   return per_sm > 0 ? 2 * sms : 0;
 }
 
-// Which tensor-core kernel runs: KVC_SCORE_PATH=fused|ring|persist|split
-// forces one (tests use this); by default the single-read kernel where the
-// shape allows it, else the pipelined cluster kernel, else the persistent
-// one, else split mode.
-enum TcPath { kAuto, kFused, kRing, kPersist, kSplit };
-TcPath forced_path() {
-  const char *e = getenv("KVC_SCORE_PATH");
-  if (!e) return kAuto;
-  if (!strcmp(e, "fused")) return kFused;
-  if (!strcmp(e, "ring")) return kRing;
-  if (!strcmp(e, "persist")) return kPersist;
-  if (!strcmp(e, "split")) return kSplit;
-  return kAuto;
-}
+// Which tensor-core kernel runs: kvc_score (KVC_KERNEL_AUTO) takes the
+// single-read kernel where the shape allows it, else the pipelined cluster
+// kernel, else the persistent one, else split mode; kvc_score_ex names one
+// of them (cudaErrorNotSupported when it cannot run these sizes).
+bool path_allows(int path, int kernel) { return path == KVC_KERNEL_AUTO || path == kernel; }
 
 int ring_cluster(int nb_max) {
   int c = (nb_max + 2047) / 2048;
@@ -1130,9 +1120,8 @@ cudaError_t launch_ring(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
 
 template <int RT, int S, int W>
 cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, int n_units,
-                        const Plan &p, void *ws, cudaStream_t s) {
-  const TcPath forced = forced_path();
-  if (forced == kAuto || forced == kRing || forced == kFused) {
+                        const Plan &p, void *ws, int path, cudaStream_t s) {
+  if (path_allows(path, KVC_KERNEL_SCORE_RING)) {
     const int C = ring_cluster(p.C * p.CH);
     const int nc = ring_clusters<RT, W>(C, a.D);
     if (nc > 0) {
@@ -1140,12 +1129,14 @@ cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
       b.n_chunk = (p.C * p.CH + 127) / 128;  // session length limit in 128-block tiles
       return launch_ring<RT, W>(mk, qm, b, n_units, C, nc, s);
     }
+    if (path == KVC_KERNEL_SCORE_RING) return cudaErrorNotSupported;
   }
   const size_t smem = smem_bytes(RT, a.D, a.n_sess);
-  const int cap = (a.n_sess <= kMaxSessPersist && forced != kSplit)
+  const int cap = (a.n_sess <= kMaxSessPersist && path_allows(path, KVC_KERNEL_SCORE_PERSIST))
                       ? persistent_capacity<RT, S, W>(smem)
                       : 0;
   cudaError_t e;
+  if (path == KVC_KERNEL_SCORE_PERSIST && !(cap > 0 && cap >= p.C)) return cudaErrorNotSupported;
   if (cap > 0 && cap >= p.C) {
     // ws: [counter, pad to 256 B][unit_done[n_units], pad][partials]
     char *w = static_cast<char *>(ws);
@@ -1178,15 +1169,11 @@ cudaError_t launch_plan(const CUtensorMap &mk, const CUtensorMap &qm, TcArgs a, 
 
 template <int RT, int S>
 int launches_rt(const Plan &p, int W, int D, int n_sess) {
-  const TcPath forced = forced_path();
-  if (forced == kAuto || forced == kRing || forced == kFused) {
-    const int C = ring_cluster(p.C * p.CH);
-    const int nc = W == 8    ? ring_clusters<RT, 8>(C, D)
-                   : W == 16 ? ring_clusters<RT, 16>(C, D)
-                             : ring_clusters<RT, 32>(C, D);
-    if (nc > 0) return 1;
-  }
-  if (forced == kSplit) return 2;
+  const int C = ring_cluster(p.C * p.CH);
+  const int nc = W == 8    ? ring_clusters<RT, 8>(C, D)
+                 : W == 16 ? ring_clusters<RT, 16>(C, D)
+                           : ring_clusters<RT, 32>(C, D);
+  if (nc > 0) return 1;
   size_t smem = smem_bytes(RT, D, n_sess);
   int cap = n_sess > kMaxSessPersist ? 0
             : W == 8              ? persistent_capacity<RT, S, 8>(smem)
@@ -1202,10 +1189,7 @@ bool score_tc_supported(int R, int W, int D) { return plan(R, W, D, 1).ok; }
 int score_tc_launches(int R, int W, int D, int n_sess, int nb_max) {
   Plan p = plan(R, W, D, nb_max);
   if (!p.ok) return 0;
-  const TcPath forced = forced_path();
-  if ((forced == kAuto || forced == kFused) && R % W == 0 &&
-      score_fused_supported(R / W, D, W, nb_max))
-    return 1;
+  if (R % W == 0 && score_fused_supported(R / W, D, W, nb_max)) return 1;
   return p.RT == 1 ? launches_rt<1, 2>(p, W, D, n_sess) : launches_rt<2, 1>(p, W, D, n_sess);
 }
 
@@ -1225,19 +1209,15 @@ size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max, in
 cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *scores, int L,
                             int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
                             int64_t nb_total, int nb_max, void *ws, int32_t *status,
-                            cudaStream_t s) {
+                            int path, cudaStream_t s) {
   const int G = Hq / H, R = G * W;
   Plan p = plan(R, W, D, nb_max);
   if (!p.ok) return cudaErrorNotSupported;
-  const TcPath forced = forced_path();
-  if (forced == kAuto || forced == kFused) {
+  if (path_allows(path, KVC_KERNEL_SCORE_FUSED)) {
     cudaError_t e = launch_score_fused(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
                                        nb_total, nb_max, status, s);
-    // forced onto a shape the single-read kernel covers: its failure is the
-    // result (tests rely on this to know that kernel ran)
-    if (e != cudaErrorNotSupported ||
-        (forced == kFused && W > 0 && R % W == 0 && score_fused_supported(R / W, D, W, nb_max)))
-      return e;
+    // named, or a shape the single-read kernel covers: its result stands
+    if (path == KVC_KERNEL_SCORE_FUSED || e != cudaErrorNotSupported) return e;
   }
   CUtensorMap mk_map, q_map;
   uint64_t mk_rows = (uint64_t)L * H * nb_total;
@@ -1267,9 +1247,9 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
   const int n_units = L * H * n_sess;
 #define KVC_TC_W(RTv, Sv)                                                           \
   switch (W) {                                                                      \
-    case 8: return launch_plan<RTv, Sv, 8>(mk_map, q_map, a, n_units, p, ws, s);   \
-    case 16: return launch_plan<RTv, Sv, 16>(mk_map, q_map, a, n_units, p, ws, s); \
-    default: return launch_plan<RTv, Sv, 32>(mk_map, q_map, a, n_units, p, ws, s); \
+    case 8: return launch_plan<RTv, Sv, 8>(mk_map, q_map, a, n_units, p, ws, path, s);   \
+    case 16: return launch_plan<RTv, Sv, 16>(mk_map, q_map, a, n_units, p, ws, path, s); \
+    default: return launch_plan<RTv, Sv, 32>(mk_map, q_map, a, n_units, p, ws, path, s); \
   }
   if (p.RT == 1) {
     KVC_TC_W(1, 2)

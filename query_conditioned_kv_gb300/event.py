@@ -26,8 +26,8 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_recover_score,
-               kvc_recover_score_workspace_size,
+from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_recover_score_ex,
+               kvc_recover_score_workspace_size, kvc_score_ex, kvc_score_qmem_ex,
                kvc_redirect_free,
                kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
                kvc_lrfu_update, kvc_score_qmem, kvc_score_qmem_workspace_size,
@@ -108,6 +108,7 @@ class MeanKEvent:
         self.graph = None
         self.side = torch.cuda.Stream(device=dev)
         self.groups = self._layer_groups(groups_hint(L) if groups is None else groups)
+        self.score_kernel = "auto"  # the scorer run() uses (a kvc_kernel name)
 
     @staticmethod
     def _split(L: int, n: int):
@@ -119,11 +120,14 @@ class MeanKEvent:
         return self._split(self.L, n)
 
     # -- the three steps, on a range of layers [l0, l1) ------------------
-    def score(self, q, meank, stream=None, l0=0, l1=None):
+    def score(self, q, meank, stream=None, l0=0, l1=None, kernel=None):
+        """Scores of layers [l0, l1); `kernel` names one scorer (kvc_score_ex);
+        by default the event's `score_kernel` ("auto": the library's choice)."""
         l1 = self.L if l1 is None else l1
-        kvc_score(q[l0:l1], meank[l0:l1], self.scores[l0:l1], l1 - l0, self.H, self.Hq,
-                  self.D, self.W, self.blk_off, self.n_sess, self.nb_total, self.nb_max,
-                  self.ws, self.dev_status, stream)
+        kernel = self.score_kernel if kernel is None else kernel
+        kvc_score_ex(q[l0:l1], meank[l0:l1], self.scores[l0:l1], l1 - l0, self.H, self.Hq,
+                     self.D, self.W, self.blk_off, self.n_sess, self.nb_total, self.nb_max,
+                     self.ws, kernel, self.dev_status, stream)
 
     def select(self, scores=None, stream=None, l0=0, l1=None):
         l1 = self.L if l1 is None else l1
@@ -321,10 +325,10 @@ class SlotMapEvent:
         self.n_freed = torch.zeros(1, dtype=torch.int32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def score(self, M, kpool, slot_map, stream=None):
-        kvc_score_qmem(M, kpool, slot_map, self.sentinel, self.rule, self.n_sess,
-                       self.L, self.H, self.Hq, self.D, self.N, self.n_slots,
-                       self.ws_score, self.dev_status, stream)
+    def score(self, M, kpool, slot_map, stream=None, kernel="auto"):
+        kvc_score_qmem_ex(M, kpool, slot_map, self.sentinel, self.rule, self.n_sess,
+                          self.L, self.H, self.Hq, self.D, self.N, self.n_slots,
+                          self.ws_score, kernel, self.dev_status, stream)
 
     def select(self, rule=None, stream=None):
         kvc_select(self.rule if rule is None else rule, self.seg_off, self.n_sess,
@@ -379,10 +383,10 @@ class PagedEvent:
         self.tail_mask = torch.empty(n_req, self.words, **i32)
         self.dev_status = torch.zeros(1, **i32)
 
-    def score(self, q, lse, kpool, block_table, seqused, count, stream=None):
-        kvc_recover_score(q, lse, kpool, self.n_slots, block_table, self.max_blocks, seqused,
-                          count, self.n_req, self.L, self.H, self.Hq, self.D, self.BS,
-                          self.state, self.ws, self.dev_status, stream)
+    def score(self, q, lse, kpool, block_table, seqused, count, stream=None, kernel="auto"):
+        kvc_recover_score_ex(q, lse, kpool, self.n_slots, block_table, self.max_blocks,
+                             seqused, count, self.n_req, self.L, self.H, self.Hq, self.D,
+                             self.BS, self.state, self.ws, kernel, self.dev_status, stream)
 
     def lrfu(self, top_p: float = 0.9, lam: float = 0.5, stream=None):
         kvc_lrfu_update(self.state, self.seg_off, self.n_req, self.cap, top_p, lam,

@@ -152,6 +152,42 @@ def test_validation_rejects_before_launch(kvc):
     assert _call(kvc, "kvc_device_status", None, None) == 1
 
 
+def test_kernel_choice_is_validated_before_launch(kvc):
+    """The _ex entry points take only their own kvc_kernel values; the rest of
+    their validation is that of the plain call (no kernel is reached here)."""
+    P = FAKE
+    # a rule-score kernel named for the Mean-K scorer, an unknown value
+    assert _call(kvc, "kvc_score_ex", P, P, P, 1, 2, 4, 64, 16, P, 1, 128, 128, P, 1 << 20,
+                 None, kvc.KERNELS["qmem_tc"], None) == 1
+    assert _call(kvc, "kvc_score_ex", P, P, P, 1, 2, 4, 64, 16, P, 1, 128, 128, P, 1 << 20,
+                 None, 99, None) == 1
+    # a valid kernel, but the plain call's shape rule (Hq % H) still applies
+    assert _call(kvc, "kvc_score_ex", P, P, P, 1, 3, 4, 128, 16, P, 1, 128, 128, P, 1 << 20,
+                 None, kvc.KERNELS["score_ring"], None) == 2
+    assert _call(kvc, "kvc_score_qmem_ex", P, P, P, 0, P, 1, 1, 1, 8, 64, 16, 10, P, 1 << 30,
+                 None, kvc.KERNELS["score_cc"], None) == 1
+    assert _call(kvc, "kvc_recover_score_ex", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128,
+                 16, P, None, 0, None, kvc.KERNELS["qmem_cc"], None) == 1
+    with pytest.raises(ValueError):
+        kvc._kernel("no_such_kernel")
+
+
+def test_static_scratch_limit_matches_the_header(kvc):
+    """The binding reads the fixed scratch array's size from the library; it
+    must be the header's KVC_SCORE_STATIC_SCRATCH_BYTES."""
+    with open(os.path.join(ROOT, "include", "kvc.h")) as f:
+        m = re.search(r"#define\s+KVC_SCORE_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)",
+                      f.read())
+    assert m, "KVC_SCORE_STATIC_SCRATCH_BYTES not found in kvc.h"
+    header = int(m.group(1)) << int(m.group(2))
+    assert kvc.kvc_score_static_scratch_bytes() == header == kvc.SCORE_STATIC_SCRATCH_BYTES
+    # kvc_score's own checks come before the scratch limit: Hq % H is a shape
+    # error even for sizes far beyond the array
+    P = FAKE
+    assert _call(kvc, "kvc_score_static", P, P, P, 64, 3, 4, 128, 32, P, 1, 32768, 32768,
+                 None, None) == 2
+
+
 def test_recover_tensor_core_coverage(kvc):
     """The page tile of ActKV's Table 1 shapes (block 16, 8 KV heads, d 128)
     runs on the tensor cores; other page shapes take the CUDA-core kernel."""

@@ -16,7 +16,6 @@
 """
 from __future__ import annotations
 
-import os
 
 import numpy as np
 import pytest
@@ -64,20 +63,13 @@ def _gpu_recover(kvc, q, lse, kp, bt, seq, cnt, state, n_slots, L, H, Hq, D, BS,
     wsb = kvc.kvc_recover_score_workspace_size(n_req, max_blocks, L, H, Hq, D, BS)
     wst = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV) if ws else None
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    old = os.environ.pop("KVC_RECOVER_PATH", None)
-    if path:
-        os.environ["KVC_RECOVER_PATH"] = path
-    try:
-        kvc.kvc_recover_score(q.to(DEV), torch.from_numpy(lse).to(DEV), kp.to(DEV), n_slots,
-                              torch.from_numpy(bt).to(DEV), max_blocks,
-                              torch.from_numpy(np.asarray(seq, np.int32)).to(DEV),
-                              torch.from_numpy(np.asarray(cnt, np.int32)).to(DEV), n_req, L, H,
-                              Hq, D, BS, st, wst, status)
-        torch.cuda.synchronize()
-    finally:
-        os.environ.pop("KVC_RECOVER_PATH", None)
-        if old is not None:
-            os.environ["KVC_RECOVER_PATH"] = old
+    kvc.kvc_recover_score_ex(q.to(DEV), torch.from_numpy(lse).to(DEV), kp.to(DEV), n_slots,
+                             torch.from_numpy(bt).to(DEV), max_blocks,
+                             torch.from_numpy(np.asarray(seq, np.int32)).to(DEV),
+                             torch.from_numpy(np.asarray(cnt, np.int32)).to(DEV), n_req, L, H,
+                             Hq, D, BS, st, wst, ("recover_" + path) if path else "auto",
+                             status)
+    torch.cuda.synchronize()
     return st.cpu().numpy(), kvc.kvc_device_status(status)
 
 

@@ -137,40 +137,51 @@ def test_score_parity(kvc, orc, name):
     assert_scores_close(got.reshape(-1), c.scores_ref.reshape(-1))
 
 
+# (kernel, config) pairs the named kernel does not cover: the single-read
+# scorer takes 4 query heads per KV head, W = 32 and D = 128 only
+NOT_COVERED = {("fused", "tiny"), ("fused", "gqa6_rows192")}
+
+
 @pytest.mark.parametrize("path", ["cc", "fused", "ring", "persist", "split"])
 @pytest.mark.parametrize("name", ["tiny", "8b_scaled", "ragged_scaled", "gqa6_rows192",
                                   "split_long", "fused_long"])
-def test_score_parity_every_scorer(kvc, orc, name, path, monkeypatch):
+def test_score_parity_every_scorer(kvc, orc, name, path):
     """Every scorer the library can pick — CUDA cores (shapes the tensor-core
     kernels do not cover), the single-read cluster kernel (4 query heads per
     KV head, W = 32, D = 128), the two-pass cluster kernel, the persistent
-    kernel and the two-launch split mode — against the oracle."""
+    kernel and the two-launch split mode — named through kvc_score_ex and
+    compared with the oracle; a kernel that does not cover a shape is
+    refused on the host (KVC_ERR_SHAPE) before any launch."""
     c = case(kvc, orc, name)
-    monkeypatch.setenv("KVC_SCORE_PATH", path)
     out = torch.full_like(c.ev.scores, -1.0)
-    kvc.kvc_score(c.q, c.meank, out, c.cfg.L, c.cfg.H, c.cfg.Hq, c.cfg.D, c.cfg.W,
-                  c.ev.blk_off, c.cfg.n_sess, c.cfg.nb_total, c.ev.nb_max, c.ev.ws,
-                  c.ev.dev_status)
+    args = (c.q, c.meank, out, c.cfg.L, c.cfg.H, c.cfg.Hq, c.cfg.D, c.cfg.W, c.ev.blk_off,
+            c.cfg.n_sess, c.cfg.nb_total, c.ev.nb_max, c.ev.ws, "score_" + path,
+            c.ev.dev_status)
+    if (path, name) in NOT_COVERED:
+        with pytest.raises(kvc.KvcError) as ei:
+            kvc.kvc_score_ex(*args)
+        assert ei.value.code == 2  # KVC_ERR_SHAPE
+        return
+    kvc.kvc_score_ex(*args)
     torch.cuda.synchronize()
     assert kvc.kvc_device_status(c.ev.dev_status) == 0
     assert_scores_close(out.cpu().numpy().reshape(-1), c.scores_ref.reshape(-1))
 
 
 @pytest.mark.parametrize("path", ["fused", "ring"])
-def test_scores_do_not_depend_on_launch_split(kvc, orc, path, monkeypatch):
+def test_scores_do_not_depend_on_launch_split(kvc, orc, path):
     """A unit's scores are the same bits whether its layer is scored alone or
     with the others, and from one run to the next."""
     c = case(kvc, orc, "8b_scaled")
     cfg = c.cfg
-    monkeypatch.setenv("KVC_SCORE_PATH", path)
     full = torch.full_like(c.ev.scores, -1.0)
     again = torch.full_like(c.ev.scores, -1.0)
     one = torch.full_like(c.ev.scores[1:], -1.0)
     args = (cfg.D, cfg.W, c.ev.blk_off, cfg.n_sess, cfg.nb_total, c.ev.nb_max, c.ev.ws,
-            c.ev.dev_status)
-    kvc.kvc_score(c.q, c.meank, full, cfg.L, cfg.H, cfg.Hq, *args)
-    kvc.kvc_score(c.q, c.meank, again, cfg.L, cfg.H, cfg.Hq, *args)
-    kvc.kvc_score(c.q[1:], c.meank[1:], one, 1, cfg.H, cfg.Hq, *args)
+            "score_" + path, c.ev.dev_status)
+    kvc.kvc_score_ex(c.q, c.meank, full, cfg.L, cfg.H, cfg.Hq, *args)
+    kvc.kvc_score_ex(c.q, c.meank, again, cfg.L, cfg.H, cfg.Hq, *args)
+    kvc.kvc_score_ex(c.q[1:], c.meank[1:], one, 1, cfg.H, cfg.Hq, *args)
     torch.cuda.synchronize()
     assert kvc.kvc_device_status(c.ev.dev_status) == 0
     assert torch.equal(full.view(torch.int32), again.view(torch.int32))

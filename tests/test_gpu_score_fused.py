@@ -64,35 +64,32 @@ def _case(orc, name):
     return _CACHE[name]
 
 
-def _score(kvc, cfg, q, mk, boff):
+def _score(kvc, cfg, q, mk, boff, kernel="auto"):
     nb_max = max(cfg.nb)
     ws_bytes = kvc.kvc_score_workspace_size(cfg.L, cfg.H, cfg.Hq, cfg.W, cfg.n_sess, nb_max,
                                            cfg.nb_total)
     ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.full((cfg.L, cfg.H, cfg.nb_total), -1.0, dtype=torch.float32, device=DEV)
-    kvc.kvc_score(q, mk, out, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, boff, cfg.n_sess,
-                  cfg.nb_total, nb_max, ws, st)
+    kvc.kvc_score_ex(q, mk, out, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, boff, cfg.n_sess,
+                     cfg.nb_total, nb_max, ws, kernel, st)
     torch.cuda.synchronize()
     assert kvc.kvc_device_status(st) == 0
     return out
 
 
 @pytest.mark.parametrize("name", list(CASES))
-def test_fused_scores_match_oracle(kvc, orc, name, monkeypatch):
+def test_fused_scores_match_oracle(kvc, orc, name):
     cfg, q, mk, boff, ref = _case(orc, name)
-    monkeypatch.setenv("KVC_SCORE_PATH", "fused")
-    out = _score(kvc, cfg, q, mk, boff)
+    out = _score(kvc, cfg, q, mk, boff, "score_fused")
     assert_scores_close(out.cpu().numpy().reshape(-1), ref.reshape(-1))
 
 
 @pytest.mark.parametrize("name", ["c2_rec", "mixed"])
-def test_fused_is_the_default_and_deterministic(kvc, orc, name, monkeypatch):
-    """Without a forced path the library picks the single-read kernel for this
-    shape; two runs give the same bits."""
+def test_fused_is_the_default_and_deterministic(kvc, orc, name):
+    """Without a named kernel the library picks the single-read kernel for
+    this shape; two runs give the same bits."""
     cfg, q, mk, boff, _ = _case(orc, name)
-    monkeypatch.delenv("KVC_SCORE_PATH", raising=False)
     a = _score(kvc, cfg, q, mk, boff)
-    monkeypatch.setenv("KVC_SCORE_PATH", "fused")
-    b = _score(kvc, cfg, q, mk, boff)
+    b = _score(kvc, cfg, q, mk, boff, "score_fused")
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))

@@ -104,20 +104,12 @@ def test_rule_score_parity(kvc, orc, H, Hq, D):
 
 
 def _rule_gpu(kvc, cfg, M, kp, sm, path=None):
-    import os
     from query_conditioned_kv_gb300.event import SlotMapEvent
     ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots,
                       cfg.budget, cfg.prefix, cfg.sentinel, device=DEV)
-    old = os.environ.pop("KVC_QMEM_PATH", None)
-    if path:
-        os.environ["KVC_QMEM_PATH"] = path
-    try:
-        ev.score(torch.from_numpy(M).to(DEV), kp, torch.from_numpy(sm).to(DEV))
-        torch.cuda.synchronize()
-    finally:
-        os.environ.pop("KVC_QMEM_PATH", None)
-        if old is not None:
-            os.environ["KVC_QMEM_PATH"] = old
+    ev.score(torch.from_numpy(M).to(DEV), kp, torch.from_numpy(sm).to(DEV),
+             kernel="qmem_" + path if path else "auto")
+    torch.cuda.synchronize()
     assert kvc.kvc_device_status(ev.dev_status) == 0
     return ev.rule.cpu().numpy()
 
