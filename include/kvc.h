@@ -56,8 +56,16 @@ extern "C" {
 /* bf16 of -1e4 rounded to nearest even = -9984.0 (bit pattern 0xC61C):
  * the dead-slot key (IntentKV §2 "Layout": K set to -10^4, V set to 0). */
 #define KVC_SENTINEL_K_BITS 0xC61Cu
-/* Longest segment kvc_select accepts (its keys are staged in shared memory). */
-#define KVC_SELECT_MAX_SEG 49152
+/* Longest segment kvc_select stages in shared memory; a launch whose
+ * max_seg_len is larger reads the scores from global memory on every pass
+ * instead (same result, one CTA per segment either way). */
+#define KVC_SELECT_STAGED_SEG 49152
+/* Longest segment kvc_select accepts (KVMem's 10M-token workspace is 312,500
+ * blocks per layer and KV head; token-level sessions run longer). */
+#define KVC_SELECT_MAX_SEG (1 << 30)
+/* Longest segment kvc_lrfu_update accepts (its keys are staged in shared
+ * memory). */
+#define KVC_LRFU_MAX_SEG 49152
 /* Widest query-row set (W * G) kvc_score accepts for one KV head. */
 #define KVC_SCORE_MAX_ROWS 256
 
@@ -95,6 +103,8 @@ typedef enum {
   KVC_KERNEL_SCORE_PERSIST = 3, /* tcgen05, persistent grid, L2 exchange              */
   KVC_KERNEL_SCORE_SPLIT = 4,   /* tcgen05, two launches                              */
   KVC_KERNEL_SCORE_CC = 5,      /* CUDA cores, two launches; any shape                */
+  KVC_KERNEL_SCORE_GROUP = 6,   /* tcgen05, two passes, CTA groups exchanging through
+                                   L2; 129–192 query rows, D = 128                   */
   /* kvc_score_qmem_ex (rule score) */
   KVC_KERNEL_QMEM_TC = 16,      /* tcgen05 logits (8 KV heads, G ∈ {2, 4, 8})         */
   KVC_KERNEL_QMEM_CC = 17,      /* CUDA-core logits; any shape                        */
@@ -296,6 +306,9 @@ kvc_status kvc_score_qmem_ex(const float *M, const kvc_bf16 *kpool,
  *              bit (i%32) of word i/32 is 1 iff item i is kept; bits at or
  *              past n are 0
  * A NaN score is recorded as KVC_ERR_NAN and ranks below every number.
+ * Launches with max_seg_len ≤ KVC_SELECT_STAGED_SEG stage each segment's
+ * keys in shared memory; longer ones read them from global memory on each of
+ * the search's passes (the result is the same).
  * Errors: KVC_ERR_INVALID_ARG, KVC_ERR_BUDGET (budget < 1, n_sink < 0,
  * n_recent < 0, n_sink + n_recent > budget), KVC_ERR_SHAPE (max_seg_len >
  * KVC_SELECT_MAX_SEG), KVC_ERR_ALIGN.
@@ -527,7 +540,7 @@ int32_t kvc_recover_tensor_core(int32_t H, int32_t Hq, int32_t D, int32_t block_
  *   hitmask     device uint32 [n_seg][⌈max_seg_len/32⌉] out, may be NULL
  * Entries with the highest keep scores are then retained with kvc_select.
  * Errors: KVC_ERR_INVALID_ARG (top_p or lambda outside [0, 1]),
- * KVC_ERR_SHAPE (max_seg_len > KVC_SELECT_MAX_SEG).
+ * KVC_ERR_SHAPE (max_seg_len > KVC_LRFU_MAX_SEG).
  * ---------------------------------------------------------------------- */
 kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t n_seg,
                            int32_t max_seg_len, float top_p, float lambda, float *keep_score,

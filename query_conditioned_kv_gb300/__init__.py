@@ -16,7 +16,8 @@ import ctypes
 import os
 
 __all__ = [
-    "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG",
+    "KvcError", "lib", "BLOCK_TOKENS", "SENTINEL_K_BITS", "SELECT_MAX_SEG", "SELECT_STAGED_SEG",
+    "LRFU_MAX_SEG",
     "kvc_status_string", "kvc_version", "kvc_device_status", "kvc_selftest_bounded_wait",
     "kvc_build_meank", "kvc_score_workspace_size", "kvc_score_launches", "kvc_score",
     "kvc_score_ex", "kvc_score_static", "kvc_score_static_scratch_bytes",
@@ -32,7 +33,9 @@ __all__ = [
 
 BLOCK_TOKENS = 32
 SENTINEL_K_BITS = 0xC61C
-SELECT_MAX_SEG = 49152
+SELECT_STAGED_SEG = 49152
+SELECT_MAX_SEG = 1 << 30
+LRFU_MAX_SEG = 49152
 SCORE_MAX_ROWS = 256
 TAIL_MAX_TOKENS = 1 << 20
 
@@ -40,6 +43,7 @@ TAIL_MAX_TOKENS = 1 << 20
 KERNELS = {
     "auto": 0,
     "score_fused": 1, "score_ring": 2, "score_persist": 3, "score_split": 4, "score_cc": 5,
+    "score_group": 6,
     "qmem_tc": 16, "qmem_cc": 17,
     "recover_tc": 32, "recover_cc": 33,
 }

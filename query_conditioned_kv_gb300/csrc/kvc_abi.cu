@@ -23,7 +23,7 @@ kvc_status from_cuda_kernel(cudaError_t e) {
 }
 
 bool score_kernel_ok(kvc_kernel k) {
-  return k == KVC_KERNEL_AUTO || (k >= KVC_KERNEL_SCORE_FUSED && k <= KVC_KERNEL_SCORE_CC);
+  return k == KVC_KERNEL_AUTO || (k >= KVC_KERNEL_SCORE_FUSED && k <= KVC_KERNEL_SCORE_GROUP);
 }
 
 __global__ void k_init_sentinel(uint16_t *kpool, uint16_t *vpool, int L, int H,
@@ -376,7 +376,7 @@ kvc_status kvc_lrfu_update(const float *scores, const int64_t *seg_off, int32_t 
     return KVC_ERR_INVALID_ARG;
   if (!(top_p >= 0.f && top_p <= 1.f) || !(lambda >= 0.f && lambda <= 1.f))
     return KVC_ERR_INVALID_ARG;
-  if (max_seg_len > KVC_SELECT_MAX_SEG) return KVC_ERR_SHAPE;
+  if (max_seg_len > KVC_LRFU_MAX_SEG) return KVC_ERR_SHAPE;
   return from_cuda(kvc::launch_lrfu(scores, seg_off, n_seg, max_seg_len, top_p, lambda,
                                     keep_score, hitmask, dev_status, stream));
 }

@@ -92,6 +92,15 @@ cudaError_t launch_score_fused(const uint16_t *q, const uint16_t *meank, float *
                                int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
                                int64_t nb_total, int nb_max, int32_t *status, cudaStream_t s);
 
+// grouped two-pass tcgen05 scorer for 129–192 query rows per KV head, D = 128
+// (score_group.cu); cudaErrorNotSupported outside that shape.
+bool score_group_supported(int G, int D, int W, int nb_max);
+size_t score_group_ws_bytes();
+cudaError_t launch_score_group(const uint16_t *q, const uint16_t *meank, float *scores, int L,
+                               int H, int Hq, int D, int W, const int64_t *blk_off, int n_sess,
+                               int64_t nb_total, int nb_max, void *ws, int32_t *status,
+                               cudaStream_t s);
+
 cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
                                int D, int T, float decay, float gain,
                                int renorm, cudaStream_t s);

@@ -1190,6 +1190,7 @@ int score_tc_launches(int R, int W, int D, int n_sess, int nb_max) {
   Plan p = plan(R, W, D, nb_max);
   if (!p.ok) return 0;
   if (R % W == 0 && score_fused_supported(R / W, D, W, nb_max)) return 1;
+  if (R % W == 0 && score_group_supported(R / W, D, W, nb_max)) return 1;
   return p.RT == 1 ? launches_rt<1, 2>(p, W, D, n_sess) : launches_rt<2, 1>(p, W, D, n_sess);
 }
 
@@ -1203,7 +1204,9 @@ size_t score_tc_ws_bytes(int L, int H, int Hq, int W, int n_sess, int nb_max, in
   int64_t items = (int64_t)L * H * ((nb_total + p.CH - 1) / p.CH + n_sess);
   size_t persist = 256 + ((size_t)n_units * 4 + 255) / 256 * 256 + (size_t)items * row_bytes;
   size_t split = (size_t)n_units * p.C * row_bytes;
-  return persist > split ? persist : split;
+  size_t ws = persist > split ? persist : split;
+  const size_t group = score_group_ws_bytes();
+  return ws > group ? ws : group;
 }
 
 cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *scores, int L,
@@ -1218,6 +1221,11 @@ cudaError_t launch_score_tc(const uint16_t *q, const uint16_t *meank, float *sco
                                        nb_total, nb_max, status, s);
     // named, or a shape the single-read kernel covers: its result stands
     if (path == KVC_KERNEL_SCORE_FUSED || e != cudaErrorNotSupported) return e;
+  }
+  if (path_allows(path, KVC_KERNEL_SCORE_GROUP)) {
+    cudaError_t e = launch_score_group(q, meank, scores, L, H, Hq, D, W, blk_off, n_sess,
+                                       nb_total, nb_max, ws, status, s);
+    if (path == KVC_KERNEL_SCORE_GROUP || e != cudaErrorNotSupported) return e;
   }
   CUtensorMap mk_map, q_map;
   uint64_t mk_rows = (uint64_t)L * H * nb_total;

@@ -25,6 +25,12 @@
 //      ascending; the keep mask is built in shared memory and written out
 //      word by word.
 // No global scratch; the output is exact and deterministic.
+//
+// Segments longer than shared memory can stage (KVC_SELECT_STAGED_SEG items)
+// take k_select_stream: the same three steps with every pass reading the
+// scores from global memory (the segment stays in L2 between passes), and the
+// ordered sweep run in rounds of 64 items per thread with the scans' totals
+// carried from round to round.
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -81,6 +87,44 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *total,
   return excl;
 }
 
+// Warp 0: from the radix level's histograms (kSelHist copies of 256 bins),
+// the largest digit d whose count from the top reaches `need`; writes the
+// extended prefix and the count still needed among the keys equal to it.
+__device__ __forceinline__ void pick_digit(const uint32_t *hist, int lane, uint32_t prefix,
+                                           uint32_t need, int lo, uint32_t *s_prefix,
+                                           uint32_t *s_need) {
+  // lane l: bins 8l … 8l+7 summed over the histogram copies
+  uint32_t loc[8], lsum = 0;
+#pragma unroll
+  for (int b = 0; b < 8; b++) {
+    uint32_t v = 0;
+    for (int c = 0; c < kSelHist; c++) v += hist[c * 256 + 8 * lane + b];
+    loc[b] = v;
+    lsum += v;
+  }
+  uint32_t sfx = lsum;  // Σ of the bins ≥ 8·lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, sfx, o);
+    if (lane + o < 32) sfx += y;
+  }
+  const uint32_t above = sfx - lsum;  // Σ of the bins ≥ 8·(lane + 1)
+  if (above < need && sfx >= need) {  // exactly one lane
+    uint32_t acc = above;
+    int d = 8 * lane;
+#pragma unroll
+    for (int b = 7; b >= 0; b--)
+      if (acc + loc[b] >= need) {
+        d = 8 * lane + b;
+        break;
+      } else {
+        acc += loc[b];
+      }
+    *s_prefix = prefix | ((uint32_t)d << lo);
+    *s_need = need - acc;
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads)
 k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
          int max_seg_len, int budget, int n_sink, int n_recent,
@@ -128,9 +172,8 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
   for (int w = tid; w < words; w += nt) mask_s[w] = 0u;
 
   // T = the k-th largest non-forced key: the largest T with #(key ≥ T) ≥ k,
-  // found bit by bit from the most significant bit where the candidates
-  // differ (the bits above it are common to all of them), two bits per
-  // step, counting the candidates against three thresholds at once.
+  // found eight bits at a time from the most significant bit where the
+  // candidates differ (the bits above it are common to all of them).
   uint32_t prefix = 0, need = (uint32_t)k;
   const int lane = tid & 31, warp = tid >> 5, n_warps = nt >> 5;
   if (k > 0) {
@@ -175,38 +218,7 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
         if ((key & pmask) == prefix) atomicAdd(&h[(key >> lo) & dmask], 1u);
       }
       __syncthreads();
-      if (warp == 0) {
-        // lane l: bins 8l … 8l+7 summed over the histogram copies
-        uint32_t loc[8], lsum = 0;
-#pragma unroll
-        for (int b = 0; b < 8; b++) {
-          uint32_t v = 0;
-          for (int c = 0; c < kSelHist; c++) v += hist[c * 256 + 8 * lane + b];
-          loc[b] = v;
-          lsum += v;
-        }
-        uint32_t sfx = lsum;  // Σ of the bins ≥ 8·lane
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, sfx, o);
-          if (lane + o < 32) sfx += y;
-        }
-        const uint32_t above = sfx - lsum;  // Σ of the bins ≥ 8·(lane + 1)
-        if (above < need && sfx >= need) {  // exactly one lane
-          uint32_t acc = above;
-          int d = 8 * lane;
-#pragma unroll
-          for (int b = 7; b >= 0; b--)
-            if (acc + loc[b] >= need) {
-              d = 8 * lane + b;
-              break;
-            } else {
-              acc += loc[b];
-            }
-          s_prefix = prefix | ((uint32_t)d << lo);
-          s_need = need - acc;
-        }
-      }
+      if (warp == 0) pick_digit(hist, lane, prefix, need, lo, &s_prefix, &s_need);
       __syncthreads();
       prefix = s_prefix;
       need = s_need;
@@ -274,6 +286,160 @@ k_select(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
   }
 }
 
+// Items per thread in one round of the streaming sweep (the bit masks).
+constexpr int kStreamIPT = 64;
+
+__global__ void __launch_bounds__(kSelThreads)
+k_select_stream(const float *__restrict__ scores, const int64_t *__restrict__ seg_off,
+                int64_t max_seg_len, int budget, int n_sink, int n_recent,
+                int32_t *__restrict__ kept, int32_t *__restrict__ kept_count,
+                uint32_t *__restrict__ keepmask, int64_t words, int32_t *status) {
+  __shared__ uint32_t hist[kSelHist * 256];
+  __shared__ uint32_t s_red[2][32];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ uint32_t s_kmax, s_kmin, s_prefix, s_need;
+  __shared__ int s_nan;
+
+  const int seg = blockIdx.x;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  int32_t *kept_row = kept + (int64_t)seg * budget;
+  uint32_t *mask_row = keepmask ? keepmask + (int64_t)seg * words : nullptr;
+
+  const int64_t off = seg_off[seg], end = seg_off[seg + 1];
+  const bool bad = end < off || end - off > max_seg_len || off < 0;
+  const int n = bad ? 0 : (int)(end - off);
+  if (bad && tid == 0) record_error(status, KVC_ERR_BOUNDS);
+  const float *sc = scores + (bad ? 0 : off);
+
+  if (n <= budget) {  // keep everything (or nothing, on a bad segment)
+    for (int i = tid; i < budget; i += nt) kept_row[i] = i < n ? i : -1;
+    if (mask_row)
+      for (int64_t w = tid; w < words; w += nt) {
+        const int64_t lo = w * 32;
+        mask_row[w] = lo >= n ? 0u : (n - lo >= 32 ? 0xFFFFFFFFu : ((1u << (n - lo)) - 1u));
+      }
+    if (tid == 0) kept_count[seg] = n;
+    return;
+  }
+  const int rec0 = n - n_recent;
+  const int k = budget - n_sink - n_recent;
+  const int lane = tid & 31, warp = tid >> 5, n_warps = nt >> 5;
+  if (tid == 0) s_nan = 0;
+  __syncthreads();
+
+  // pass 1: NaN check over every item, key range of the non-forced ones
+  bool nan = false;
+  uint32_t lmax = 0u, lmin = 0xFFFFFFFFu;
+  for (int i = tid; i < n; i += nt) {
+    const uint32_t key = order_key(sc[i], nan);
+    if (i >= n_sink && i < rec0) {
+      lmax = max(lmax, key);
+      lmin = min(lmin, key);
+    }
+  }
+  if (nan) s_nan = 1;
+  uint32_t prefix = 0, need = (uint32_t)k;
+  if (k > 0) {
+    lmax = __reduce_max_sync(0xFFFFFFFFu, lmax);
+    lmin = __reduce_min_sync(0xFFFFFFFFu, lmin);
+    if (lane == 0) {
+      s_red[0][warp] = lmax;
+      s_red[1][warp] = lmin;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, lane < n_warps ? s_red[0][lane] : 0u);
+      const uint32_t mn =
+          __reduce_min_sync(0xFFFFFFFFu, lane < n_warps ? s_red[1][lane] : 0xFFFFFFFFu);
+      if (lane == 0) {
+        s_kmax = mx;
+        s_kmin = mn;
+      }
+    }
+    __syncthreads();
+    const uint32_t kmax = s_kmax, kmin = s_kmin;
+    int hi = kmax == kmin ? -1 : 31 - __clz(kmax ^ kmin);
+    prefix = hi < 0 ? kmax : hi == 31 ? 0u : (kmax >> (hi + 1)) << (hi + 1);
+    // radix levels, each a pass over the scores
+    while (hi >= 0) {
+      const int lo = hi >= 7 ? hi - 7 : 0;
+      const uint32_t dmask = (2u << (hi - lo)) - 1u;
+      const uint32_t pmask = hi == 31 ? 0u : ~((2u << hi) - 1u);
+      uint32_t *h = hist + (warp % kSelHist) * 256;
+      for (int j = tid; j < kSelHist * 256; j += nt) hist[j] = 0u;
+      __syncthreads();
+      for (int i = n_sink + tid; i < rec0; i += nt) {
+        bool dummy = false;
+        const uint32_t key = order_key(sc[i], dummy);
+        if ((key & pmask) == prefix) atomicAdd(&h[(key >> lo) & dmask], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) pick_digit(hist, lane, prefix, need, lo, &s_prefix, &s_need);
+      __syncthreads();
+      prefix = s_prefix;
+      need = s_need;
+      hi = lo - 1;
+    }
+  }
+  const uint32_t T = prefix;
+
+  // words past the segment's last item are zero (written once, before the
+  // sweep, and never touched by it)
+  const int64_t used_words = ((int64_t)n + 31) / 32;
+  if (mask_row)
+    for (int64_t w = used_words + tid; w < words; w += nt) mask_row[w] = 0u;
+
+  // ordered sweep in rounds of nt·64 items; thread t owns the 64 items from
+  // base + 64t, i.e. mask words 2·(base/64 + t) and 2·(base/64 + t) + 1
+  uint32_t eq_carry = 0, keep_carry = 0;
+  for (int base = 0; base < n; base += nt * kStreamIPT) {
+    const int i0 = base + tid * kStreamIPT;
+    const int cnt = i0 >= n ? 0 : min(kStreamIPT, n - i0);
+    uint64_t eqm = 0, km = 0;
+    for (int e = 0; e < cnt; e++) {
+      const int i = i0 + e;
+      bool keep = i < n_sink || i >= rec0, eq = false;
+      if (!keep && k > 0) {
+        bool dummy = false;
+        const uint32_t key = order_key(sc[i], dummy);
+        keep = key > T;
+        eq = key == T;
+      }
+      km |= (uint64_t)keep << e;
+      eqm |= (uint64_t)eq << e;
+    }
+    uint32_t tot_eq;
+    const uint32_t eq_before = eq_carry + block_excl_scan((uint32_t)__popcll(eqm), &tot_eq,
+                                                         warp_tot);
+    if (eq_before < need) {
+      const uint32_t take = min((uint32_t)__popcll(eqm), need - eq_before);
+      uint64_t m = eqm;
+      for (uint32_t t = 0; t < take; t++) {
+        km |= m & (~m + 1);
+        m &= m - 1;
+      }
+    }
+    uint32_t tot_keep;
+    uint32_t pos = keep_carry + block_excl_scan((uint32_t)__popcll(km), &tot_keep, warp_tot);
+    for (uint64_t m = km; m; m &= m - 1) {
+      if (pos < (uint32_t)budget) kept_row[pos] = i0 + __ffsll((long long)m) - 1;
+      pos++;
+    }
+    if (mask_row && cnt > 0) {
+      const int64_t w0 = i0 / 32;
+      mask_row[w0] = (uint32_t)km;
+      if (w0 + 1 < used_words) mask_row[w0 + 1] = (uint32_t)(km >> 32);
+    }
+    eq_carry += tot_eq;
+    keep_carry += tot_keep;
+  }
+  for (int i = (int)keep_carry + tid; i < budget; i += nt) kept_row[i] = -1;
+  if (tid == 0) {
+    kept_count[seg] = (int32_t)keep_carry;
+    if (s_nan) record_error(status, KVC_ERR_NAN);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const float *scores, const int64_t *seg_off,
@@ -281,6 +447,12 @@ cudaError_t launch_select(const float *scores, const int64_t *seg_off,
                           int n_recent, int32_t *kept, int32_t *kept_count,
                           uint32_t *keepmask, int32_t *status,
                           cudaStream_t s) {
+  if (max_seg_len > KVC_SELECT_STAGED_SEG) {
+    k_select_stream<<<n_seg, kSelThreads, 0, s>>>(scores, seg_off, max_seg_len, budget, n_sink,
+                                                  n_recent, kept, kept_count, keepmask,
+                                                  ((int64_t)max_seg_len + 31) / 32, status);
+    return cudaGetLastError();
+  }
   int words = (max_seg_len + 31) / 32;
   size_t smem = ((size_t)max_seg_len + max_seg_len / 32 + 1 + words + kSelHist * 256) *
                 sizeof(uint32_t);

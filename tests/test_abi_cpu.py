@@ -88,7 +88,8 @@ def test_validation_rejects_before_launch(kvc):
     assert _call(kvc, "kvc_select", P, P, 1, 100, 0, 0, 0, P, P, None, None, None) == 3
     assert _call(kvc, "kvc_select", P, P, 1, 100, 4, 3, 2, P, P, None, None, None) == 3
     assert _call(kvc, "kvc_select", P, P, 1, 100, 4, -1, 0, P, P, None, None, None) == 3
-    assert _call(kvc, "kvc_select", P, P, 1, 49153, 4, 1, 1, P, P, None, None, None) == 2
+    assert _call(kvc, "kvc_select", P, P, 1, (1 << 30) + 1, 4, 1, 1, P, P, None, None,
+                 None) == 2
     # pack: shape, alignment, budget
     assert _call(kvc, "kvc_pack_rerope", P, P, P, P, 1, 1, 128, P, 1, 100, 4, P, P, P,
                  None, None) == 2

@@ -45,6 +45,18 @@ CONFIGS = {
     "gqa6_rows192": W.MeanKConfig(name="g6", L=1, H=2, Hq=12, D=128, W=32,
                                   hist=[32 * 700], budget=64, n_sink=1,
                                   n_recent=8, gamma=W.GAMMA_PLANTED, seed=12),
+    # 6 query heads per KV head (192 rows: the grouped two-pass scorer) over
+    # long and short sessions of several tiles, a partial tile and sessions
+    # shorter than a group's CTA count in tiles
+    "gqa6_long": W.MeanKConfig(name="g6l", L=2, H=2, Hq=12, D=128, W=32,
+                               hist=[32 * 9000, 32 * 300, 32 * 2600, 32 * 1], budget=64,
+                               n_sink=1, n_recent=8, gamma=W.GAMMA_PLANTED, L_pack=1,
+                               seed=15),
+    # the 27B-class unit (6 query heads, 32768 blocks): 128 tiles per unit,
+    # groups of 19 CTAs exchanging through L2 (two groups, one unit each)
+    "gqa6_1m": W.MeanKConfig(name="g6m", L=1, H=2, Hq=12, D=128, W=32, hist=[1048576],
+                             budget=2048, n_sink=1, n_recent=8, gamma=W.GAMMA_PLANTED,
+                             L_pack=1, seed=16),
     # longer than one 8-CTA cluster covers: two-launch split scoring
     "split_long": W.MeanKConfig(name="split", L=1, H=2, Hq=8, D=128, W=32,
                                 hist=[32 * 4500, 32 * 700], budget=96, n_sink=1,
@@ -138,13 +150,15 @@ def test_score_parity(kvc, orc, name):
 
 
 # (kernel, config) pairs the named kernel does not cover: the single-read
-# scorer takes 4 query heads per KV head, W = 32 and D = 128 only
-NOT_COVERED = {("fused", "tiny"), ("fused", "gqa6_rows192")}
+# scorer takes 4 query heads per KV head, W = 32 and D = 128 only; the grouped
+# scorer takes 129–192 query rows per KV head and D = 128
+NOT_COVERED = {("fused", n) for n in ("tiny", "gqa6_rows192", "gqa6_long", "gqa6_1m")} | {
+    ("group", n) for n in ("tiny", "8b_scaled", "ragged_scaled", "split_long", "fused_long")}
 
 
-@pytest.mark.parametrize("path", ["cc", "fused", "ring", "persist", "split"])
+@pytest.mark.parametrize("path", ["cc", "fused", "ring", "persist", "split", "group"])
 @pytest.mark.parametrize("name", ["tiny", "8b_scaled", "ragged_scaled", "gqa6_rows192",
-                                  "split_long", "fused_long"])
+                                  "gqa6_long", "gqa6_1m", "split_long", "fused_long"])
 def test_score_parity_every_scorer(kvc, orc, name, path):
     """Every scorer the library can pick — CUDA cores (shapes the tensor-core
     kernels do not cover), the single-read cluster kernel (4 query heads per
@@ -168,11 +182,12 @@ def test_score_parity_every_scorer(kvc, orc, name, path):
     assert_scores_close(out.cpu().numpy().reshape(-1), c.scores_ref.reshape(-1))
 
 
-@pytest.mark.parametrize("path", ["fused", "ring"])
-def test_scores_do_not_depend_on_launch_split(kvc, orc, path):
+@pytest.mark.parametrize("path,name", [("fused", "8b_scaled"), ("ring", "8b_scaled"),
+                                       ("group", "gqa6_long")])
+def test_scores_do_not_depend_on_launch_split(kvc, orc, path, name):
     """A unit's scores are the same bits whether its layer is scored alone or
     with the others, and from one run to the next."""
-    c = case(kvc, orc, "8b_scaled")
+    c = case(kvc, orc, name)
     cfg = c.cfg
     full = torch.full_like(c.ev.scores, -1.0)
     again = torch.full_like(c.ev.scores, -1.0)

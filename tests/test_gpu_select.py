@@ -94,3 +94,50 @@ def test_select_many_segments_bit_exact(kvc, orc, n_seg):
     assert np.array_equal(cnt, cref)
     assert np.array_equal(kept, kref)
     assert np.array_equal(mask, mref)
+
+
+@pytest.mark.parametrize("budget,n_sink,n_recent", [(2048, 1, 8), (8192, 0, 0), (512, 3, 9)])
+def test_select_long_segments_bit_exact(kvc, orc, budget, n_sink, n_recent):
+    """Segments longer than shared memory can stage (the KVMem 10M-token
+    workspace is 312,500 blocks per layer and KV head; a 1M-token session at
+    token granularity is 1,048,576 items), mixed with short ones in the same
+    launch: the streaming path, with ties, signed zeros and blocks of equal
+    scores, bit-exact against the oracle (indices, counts, keep masks)."""
+    rng = np.random.default_rng(budget + n_sink)
+    lens = [312_500, 1_048_576, kvc.SELECT_STAGED_SEG + 1, 300, budget, 70]
+    parts = []
+    for j, n in enumerate(lens):
+        if j == 0:    # continuous scores with blocks of equal values
+            s = rng.random(n).astype(np.float32)
+            s[1000:1700] = s[5]
+            s[n // 2:n // 2 + 4000] = s[n // 3]
+        elif j == 1:  # a few values only: ties everywhere, signed zeros
+            s = rng.choice(np.array([0.0, -0.0, 1.0, 0.5, 0.25], np.float32), n)
+        else:
+            s = rng.standard_normal(n).astype(np.float32)
+            s[::11] = 0.0
+            s[1::11] = -0.0
+        parts.append(s)
+    scores = np.concatenate(parts)
+    off, kept, cnt, mask = _run(kvc, scores, lens, budget, n_sink, n_recent)
+    kref, cref, mref = orc.select_segments(scores, off, budget, n_sink, n_recent,
+                                           mask_words=mask.shape[1])
+    assert np.array_equal(cnt, cref)
+    assert np.array_equal(kept, kref)
+    assert np.array_equal(mask, mref)
+
+
+def test_select_streaming_path_equals_staged_path(kvc):
+    """The same segments selected through the staged kernel (a launch whose
+    longest segment fits shared memory) and the streaming one (the same
+    segments plus one longer segment in the launch) give the same bits."""
+    rng = np.random.default_rng(5)
+    lens = [4096, 30000, 9000, 49152]
+    scores = rng.random(sum(lens)).astype(np.float32)
+    scores[::13] = 0.75
+    _, k1, c1, m1 = _run(kvc, scores, lens, 256, 1, 4)
+    long_seg = rng.random(200_000).astype(np.float32)
+    _, k2, c2, m2 = _run(kvc, np.concatenate([scores, long_seg]), lens + [200_000], 256, 1, 4)
+    assert np.array_equal(k1, k2[:4]) and np.array_equal(c1, c2[:4])
+    assert np.array_equal(m1, m2[:4, :m1.shape[1]])
+    assert not m2[:4, m1.shape[1]:].any()
