@@ -163,32 +163,6 @@ __device__ __forceinline__ void merge_lse(float &m, float &s, float m2, float s2
   m = mn;
 }
 
-// Packed fp32 pairs (two lanes of one 64-bit register): each lane of
-// fma.rn.f32x2 / add.rn.f32x2 rounds exactly like the scalar instruction.
-__device__ __forceinline__ uint64_t pk2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
 // Pass 1 of this group's columns of one tile for this lane's query row:
 // (max, Σ2^(z·zs − max)) over the `valid` blocks, 32 columns at a time.
 // Column j adds into accumulator j mod 8 (held as four packed pairs).

@@ -34,10 +34,11 @@
 //   * a CTA runs pass 1 of its next unit's first tiles while its group
 //     exchanges, so the tensor pipe keeps working through the exchange:
 //         P1(u0) | P1a(u1) P2(u0) P1b(u1) | P1a(u2) P2(u1) P1b(u2) | … | P2(u_last)
-//   * roles: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2–9 are two
-//     epilogue warpgroups; job j (a row tile or a block half) goes to group
-//     j mod 2 and TMEM buffer j mod 2, so group 0 owns rows 0–127 in pass 1
-//     and group 1 rows 128–R−1.
+//   * roles: warp 0 issues TMA, warp 1 issues tcgen05.mma into TMEM buffer
+//     j mod 2 for job j (a row tile or a block half), warps 2–9 read every
+//     job back, each warp one lane quarter and one half of the job's columns,
+//     so a job's epilogue takes about as long as its MMA and the two buffers
+//     keep the tensor pipe fed.
 // Every wait is bounded (1 s of %globaltimer) and records KVC_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -69,7 +70,8 @@ struct GroupArgs {
   const int64_t *blk_off;
   int32_t *status;
   int *counter;   // [n_groups]: partials published so far (g per unit)
-  float2 *part;   // [n_groups][2][g][256] row partials (max, Σ2^(z−max)), base 2
+  float2 *part;   // [n_groups][2][g][2][256] row partials (max, Σ2^(z−max)), base 2,
+                  // one per column half of a tile
   int L, H, n_sess, R, n2, g, n_groups, max_tiles, ns;
   int64_t nb_total;
   float zscale;   // log2(e)/sqrt(D)
@@ -82,7 +84,8 @@ struct GroupSmem {
   uint64_t *full, *empty, *tfull, *tempty, *qfull, *qempty;
   uint32_t *tmem_holder;
   volatile int *failed;
-  float *lse;  // [256] row LSEs (base 2) of the unit in pass 2
+  float *lse;   // [kGMaxR] row LSEs (base 2) of the unit in pass 2
+  float *comb;  // [2][128] pass-2 partial sums handed from the upper to the lower half
   __device__ GroupSmem(uint8_t *raw, uint32_t q_half, int ns) {
     uint8_t *p = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
@@ -101,10 +104,11 @@ struct GroupSmem {
     tmem_holder = reinterpret_cast<uint32_t *>(qempty + 2);
     failed = reinterpret_cast<volatile int *>(tmem_holder + 1);
     lse = reinterpret_cast<float *>(tmem_holder + 4);
+    comb = lse + kGMaxR;
   }
   static size_t bytes(uint32_t q_half, int ns) {
     return 1024 + 4 * (size_t)q_half + (size_t)ns * kGSlot + (2 * (size_t)ns + 8) * 8 + 16 +
-           256 * 4;
+           kGMaxR * 4 + 256 * 4;
   }
 };
 
@@ -159,82 +163,118 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
   return v;
 }
 
-// Pass 1 of one row tile of one tile for this lane's query row: online
-// (max, Σ2^(z·zs − max)) over the `valid` blocks, 32 columns at a time.
+// Pass 1 of this warp's 128 columns (blocks) of one row tile for this
+// lane's query row: online (max, Σ2^(z·zs − max)) over the `valid` columns,
+// 32 at a time, the next chunk's TMEM load in flight while one is processed.
+// Column j adds into accumulator j mod 8 (held as four packed pairs).
 __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs, float &pm,
                                             float &ps) {
   pm = -INFINITY;
   ps = 0.f;
-#pragma unroll 1
-  for (int c = 0; c < kGTB / 32 && 32 * c < valid; c++) {
-    uint32_t r[32];
-    tmem_issue32(taddr + (uint32_t)(32 * c), r);
-    tmem_wait32(r);
+  const int nch = valid <= 0 ? 0 : (valid >= 128 ? 4 : (valid + 31) / 32);
+  if (nch == 0) return;
+  const uint64_t zs2 = pk2(zs, zs);
+  uint32_t r[2][32];
+  tmem_issue32(taddr, r[0]);
+  tmem_wait32(r[0]);
+#pragma unroll
+  for (int c = 0; c < 4; c++) {
+    if (c >= nch) break;  // warp-uniform
+    if (c + 1 < nch) tmem_issue32(taddr + (uint32_t)(32 * (c + 1)), r[(c + 1) & 1]);
     float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[c & 1][j]);
     const int nv = valid - 32 * c;
     if (nv < 32) {
 #pragma unroll
       for (int j = 0; j < 32; j++)
         if (j >= nv) v[j] = -INFINITY;
     }
-    float m0 = fmaxf(v[0], v[1]), m1 = fmaxf(v[2], v[3]);
+    float m0 = max3(v[0], v[1], v[2]), m1 = max3(v[3], v[4], v[5]);
+    float m2 = max3(v[6], v[7], v[8]), m3 = max3(v[9], v[10], v[11]);
 #pragma unroll
-    for (int j = 4; j < 32; j += 4) {
-      m0 = fmaxf(m0, fmaxf(v[j], v[j + 1]));
-      m1 = fmaxf(m1, fmaxf(v[j + 2], v[j + 3]));
+    for (int j = 12; j < 28; j += 8) {
+      m0 = max3(m0, v[j], v[j + 1]);
+      m1 = max3(m1, v[j + 2], v[j + 3]);
+      m2 = max3(m2, v[j + 4], v[j + 5]);
+      m3 = max3(m3, v[j + 6], v[j + 7]);
     }
-    const float mn = fmaxf(pm, fmaxf(m0, m1) * zs);
-    float acc[8];
-    acc[0] = (pm == -INFINITY) ? 0.f : ps * ex2(pm - mn);
+    m0 = max3(m0, v[28], v[29]);
+    m1 = max3(m1, v[30], v[31]);
+    const float mn = fmaxf(pm, fmaxf(max3(m0, m1, m2), m3) * zs);
+    const uint64_t nmn2 = pk2(-mn, -mn);
+    uint64_t acc[4];
+    acc[0] = pk2((pm == -INFINITY) ? 0.f : ps * ex2(pm - mn), 0.f);
 #pragma unroll
-    for (int k = 1; k < 8; k++) acc[k] = 0.f;
+    for (int k = 1; k < 4; k++) acc[k] = pk2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 32; j++) acc[j & 7] += ex2(fmaf(v[j], zs, -mn));
+    for (int j = 0; j < 32; j += 2) {
+      float x0, x1;
+      upk2(fma2(pk2(v[j], v[j + 1]), zs2, nmn2), x0, x1);
+      acc[(j & 7) >> 1] = add2(acc[(j & 7) >> 1], pk2(ex2(x0), ex2(x1)));
+    }
+    float a8[8];
+#pragma unroll
+    for (int k = 0; k < 4; k++) upk2(acc[k], a8[2 * k], a8[2 * k + 1]);
     pm = mn;
-    ps = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    ps = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+    if (c + 1 < nch) tmem_wait32(r[(c + 1) & 1]);
   }
 }
 
-// Pass 2 of one 128-block half for this lane's block: max over g of
-// z·zs − LSE per window position (LSEs read four at a time from shared
-// memory), then the mean over w of 2^max.
+// Pass 2 of this warp's half of the window positions for this lane's block:
+// for w in [half·W/2, (half+1)·W/2), the max over the G heads of
+// z·zs − LSE (columns g·W + w, each head's W/2 columns one TMEM load, the
+// next head's load in flight), then Σ_w 2^max over this half.
 template <int W>
-__device__ __forceinline__ float group_pass2(uint32_t taddr, int R, float zs, const float *lse) {
-  float mw[W];
+__device__ __forceinline__ float group_pass2(uint32_t taddr, int G, int half, float zs,
+                                             const float *lse) {
+  constexpr int HW = W / 2;
+  float mw[HW];
 #pragma unroll
-  for (int w = 0; w < W; w++) mw[w] = -INFINITY;
+  for (int w = 0; w < HW; w++) mw[w] = -INFINITY;
+  const uint64_t zs2 = pk2(zs, zs);
+  // head g's columns: x = z·zs − LSE, max into mw
+  auto fold = [&](const uint32_t(&rr)[HW], int g) {
+    const float4 *l4 = reinterpret_cast<const float4 *>(lse + g * W + half * HW);
+#pragma unroll
+    for (int j = 0; j < HW; j += 4) {
+      const float4 Lv = l4[j / 4];
+      float x0, x1, x2, x3;
+      upk2(fma2(pk2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])), zs2, pk2(-Lv.x, -Lv.y)),
+           x0, x1);
+      upk2(fma2(pk2(__uint_as_float(rr[j + 2]), __uint_as_float(rr[j + 3])), zs2,
+                pk2(-Lv.z, -Lv.w)),
+           x2, x3);
+      mw[j] = fmaxf(mw[j], x0);
+      mw[j + 1] = fmaxf(mw[j + 1], x1);
+      mw[j + 2] = fmaxf(mw[j + 2], x2);
+      mw[j + 3] = fmaxf(mw[j + 3], x3);
+    }
+  };
+  uint32_t ra[HW], rb[HW];
+  const uint32_t col0 = (uint32_t)(half * HW);
+  tmem_issue<HW>(taddr + col0, ra);
+  tmem_wait<HW>(ra);
 #pragma unroll 1
-  for (int c = 0; 32 * c < R; c++) {
-    uint32_t r[32];
-    tmem_issue32(taddr + (uint32_t)(32 * c), r);
-    tmem_wait32(r);
-    if (32 * c + 32 <= R) {
-      const float4 *l4 = reinterpret_cast<const float4 *>(lse + 32 * c);
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 Lv = l4[j / 4];
-        mw[(j + 0) % W] = fmaxf(mw[(j + 0) % W], fmaf(__uint_as_float(r[j + 0]), zs, -Lv.x));
-        mw[(j + 1) % W] = fmaxf(mw[(j + 1) % W], fmaf(__uint_as_float(r[j + 1]), zs, -Lv.y));
-        mw[(j + 2) % W] = fmaxf(mw[(j + 2) % W], fmaf(__uint_as_float(r[j + 2]), zs, -Lv.z));
-        mw[(j + 3) % W] = fmaxf(mw[(j + 3) % W], fmaf(__uint_as_float(r[j + 3]), zs, -Lv.w));
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; j++)
-        if (32 * c + j < R)
-          mw[j % W] = fmaxf(mw[j % W], fmaf(__uint_as_float(r[j]), zs, -lse[32 * c + j]));
+  for (int g = 0; g < G; g += 2) {  // head g in ra, head g + 1 in rb
+    if (g + 1 < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g + 1) * W), rb);
+    fold(ra, g);
+    if (g + 1 < G) {
+      tmem_wait<HW>(rb);
+      if (g + 2 < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g + 2) * W), ra);
+      fold(rb, g + 1);
+      if (g + 2 < G) tmem_wait<HW>(ra);
     }
   }
   float acc = 0.f;
 #pragma unroll
-  for (int w = 0; w < W; w++) acc += ex2(mw[w]);
+  for (int w = 0; w < HW; w++) acc += ex2(mw[w]);
   return acc;
 }
 
 template <int W>
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __maxnreg__(200)  // 320 threads × 200 registers fit one CTA per SM
 k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
               const __grid_constant__ CUtensorMap tm_mk128,
               const __grid_constant__ CUtensorMap tm_q, GroupArgs a) {
@@ -254,7 +294,7 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
     }
     for (int i = 0; i < 2; i++) {
       mbar_init(smem_u32(sm.tfull + i), 1);
-      mbar_init(smem_u32(sm.tempty + i), 4);  // the 4 warps of the group owning the buffer
+      mbar_init(smem_u32(sm.tempty + i), 8);  // every epilogue warp reads every job
       mbar_init(smem_u32(sm.qfull + i), 1);
       mbar_init(smem_u32(sm.qempty + i), 1);
     }
@@ -424,59 +464,81 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
     __syncwarp();
   } else {
     // ------------------------------------------------------- epilogue
-    const int eg = (warp - 2) >> 2;           // group: job parity, TMEM buffer
-    const int quarter = warp & 3;             // TMEM lane quarter of this warp
+    // All eight warps take every job; warp (half, quarter) reads TMEM lanes
+    // 32·quarter … + 31 and one half of the job's columns: in pass 1 the
+    // blocks [128·half, 128·half + 128) of the tile, in pass 2 the window
+    // positions [half·W/2, (half + 1)·W/2) of every head.
+    const int half = (warp - 2) >> 2;
+    const int quarter = warp & 3;
     const int trow = 32 * quarter + lane;     // this thread's TMEM lane
     const int et = (warp - 2) * 32 + lane;    // 0 … 255
-    const int row = eg * 128 + trow;          // pass 1: this thread's query row
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    const uint32_t tbuf = tmem + lane_base + (uint32_t)eg * kGBufCols;
     const float zs = a.zscale, invW = 1.f / (float)W;
-    const bool row_warp = eg * 128 + 32 * quarter < a.R;  // some lane of the warp is a row
-    uint32_t job = 0;
+    const int G = a.R / W;
+    uint32_t job = 0, p2n = 0;
     bool ok = true;
-    float pm = -INFINITY, ps = 0.f;  // this row's partial of the unit in pass 1
-    auto take = [&]() -> bool {  // wait for this group's next job
-      ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.tfull + eg),
-                                                        ((job >> 1) & 1), sm.failed));
+    // this thread's partials of the unit in pass 1: its row of each row tile
+    // (rows trow and 128 + trow), over this half's columns
+    float pm0 = -INFINITY, ps0 = 0.f, pm1 = -INFINITY, ps1 = 0.f;
+    auto take = [&]() -> uint32_t {  // wait for the next job; its TMEM buffer
+      const uint32_t buf = job & 1;
+      ok = __all_sync(0xFFFFFFFFu, ok && wait_or_abort(smem_u32(sm.tfull + buf),
+                                                        (job >> 1) & 1, sm.failed));
       if (ok) tc_fence_after();
-      return ok;
+      return tmem + lane_base + buf * kGBufCols;
     };
-    auto give = [&]() {  // release the buffer to the MMA warp
+    auto give = [&]() {  // release the job's buffer to the MMA warp
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(sm.tempty + eg));
-      job += 2;
+      if (lane == 0) mbar_arrive(smem_u32(sm.tempty + (job & 1)));
+      job++;
     };
     auto p1_tiles = [&](const GUnit &u, int j0, int j1) {
       for (int j = j0; j < j1; j++) {
-        const int valid = min(kGTB, u.nb - (u.rank_eff + j * a.g) * kGTB);
-        if (take() && row_warp) {
-          float qm, qs;
-          group_pass1(tbuf, valid, zs, qm, qs);
-          if (row < a.R) lse_merge_g(pm, ps, qm, qs);
+        const int valid = min(kGTB, u.nb - (u.rank_eff + j * a.g) * kGTB) - 128 * half;
+        for (int rt = 0; rt < 2; rt++) {
+          const uint32_t tb = take();
+          if (ok && rt * 128 + 32 * quarter < a.R) {  // some lane of the warp is a row
+            float qm, qs;
+            group_pass1(tb + (uint32_t)(128 * half), valid, zs, qm, qs);
+            if (rt == 0)
+              lse_merge_g(pm0, ps0, qm, qs);
+            else if (128 + trow < a.R)
+              lse_merge_g(pm1, ps1, qm, qs);
+          }
+          give();
         }
-        give();
       }
     };
     auto p2_tiles = [&](const GUnit &u) {
       for (int j = 0; j < u.my; j++) {
         const int tile = u.rank_eff + j * a.g;
-        const int blk = tile * kGTB + eg * 128 + trow;  // this lane's block in the unit
-        if (take()) {
-          const float acc = group_pass2<W>(tbuf, a.R, zs, sm.lse);
-          if (blk < u.nb)
-            a.scores[((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0 + blk] = acc * invW;
+        for (int hf = 0; hf < 2; hf++) {
+          const uint32_t tb = take();
+          float part = 0.f;
+          if (ok) part = group_pass2<W>(tb, G, half, zs, sm.lse);
+          give();
+          // the upper half's sum to the lower half's thread of the same lane
+          float *cb = sm.comb + (p2n & 1) * 128;
+          if (half == 1) cb[trow] = part;
+          named_sync(3 + quarter, 64);
+          if (half == 0) {
+            const int blk = tile * kGTB + hf * 128 + trow;  // this lane's block in the unit
+            if (ok && blk < u.nb)
+              a.scores[((int64_t)u.l * a.H + u.h) * a.nb_total + u.b0 + blk] =
+                  (part + cb[trow]) * invW;
+          }
+          p2n++;
         }
-        give();
       }
     };
     // publish this CTA's row partials of the i-th unit and count them
     auto publish = [&](int i) {
-      float2 *dst = a.part + (((int64_t)grp * 2 + (i & 1)) * a.g + rank) * 256;
-      if (row < a.R) dst[row] = make_float2(pm, ps);
-      pm = -INFINITY;
-      ps = 0.f;
+      float2 *dst = a.part + ((((int64_t)grp * 2 + (i & 1)) * a.g + rank) * 2 + half) * 256;
+      dst[trow] = make_float2(pm0, ps0);
+      if (128 + trow < a.R) dst[128 + trow] = make_float2(pm1, ps1);
+      pm0 = pm1 = -INFINITY;
+      ps0 = ps1 = 0.f;
       named_sync(2, 256);
       if (et == 0) {
         __threadfence();
@@ -484,6 +546,7 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
       }
     };
     // wait until the group has published the i-th unit, then form its LSEs
+    // (partials merged in rank order, then column half)
     auto exchange = [&](int i) {
       if (et == 0 && ok && !*sm.failed) {
         const int want = a.g * (i + 1);
@@ -499,9 +562,9 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
       named_sync(2, 256);
       if (*sm.failed) ok = false;
       if (et < a.R) {
-        const float2 *src = a.part + ((int64_t)grp * 2 + (i & 1)) * a.g * 256 + et;
+        const float2 *src = a.part + ((int64_t)grp * 2 + (i & 1)) * a.g * 512 + et;
         float m = -INFINITY, s2 = 0.f;
-        for (int c = 0; c < a.g; c++) {
+        for (int c = 0; c < 2 * a.g; c++) {
           const float2 v = __ldcg(src + (int64_t)c * 256);
           lse_merge_g(m, s2, v.x, v.y);
         }
@@ -647,8 +710,8 @@ bool score_group_supported(int G, int D, int W, int nb_max) {
 
 size_t score_group_ws_bytes() {
   const int n_sm = device_sm_count();
-  // counters (one per group, at most n_sm) + partials [n_sm][2][256] float2
-  return 256 + ((size_t)n_sm * 4 + 255) / 256 * 256 + (size_t)n_sm * 2 * 256 * sizeof(float2);
+  // counters (one per group, at most n_sm) + partials [n_sm][2][2][256] float2
+  return 256 + ((size_t)n_sm * 4 + 255) / 256 * 256 + (size_t)n_sm * 2 * 2 * 256 * sizeof(float2);
 }
 
 cudaError_t launch_score_group(const uint16_t *q, const uint16_t *meank, float *scores, int L,
