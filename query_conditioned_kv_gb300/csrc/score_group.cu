@@ -165,25 +165,23 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 
 // Pass 1 of this warp's 128 columns (blocks) of one row tile for this
 // lane's query row: online (max, Σ2^(z·zs − max)) over the `valid` columns,
-// 32 at a time, the next chunk's TMEM load in flight while one is processed.
-// Column j adds into accumulator j mod 8 (held as four packed pairs).
+// 32 at a time.  Column j adds into accumulator j mod 8 (held as four packed
+// pairs).  (Loading the next chunk ahead would hold a second 32-register
+// buffer and push the warps past the register budget of 320 threads.)
 __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs, float &pm,
                                             float &ps) {
   pm = -INFINITY;
   ps = 0.f;
   const int nch = valid <= 0 ? 0 : (valid >= 128 ? 4 : (valid + 31) / 32);
-  if (nch == 0) return;
   const uint64_t zs2 = pk2(zs, zs);
-  uint32_t r[2][32];
-  tmem_issue32(taddr, r[0]);
-  tmem_wait32(r[0]);
-#pragma unroll
-  for (int c = 0; c < 4; c++) {
-    if (c >= nch) break;  // warp-uniform
-    if (c + 1 < nch) tmem_issue32(taddr + (uint32_t)(32 * (c + 1)), r[(c + 1) & 1]);
+#pragma unroll 1
+  for (int c = 0; c < nch; c++) {
+    uint32_t r[32];
+    tmem_issue32(taddr + (uint32_t)(32 * c), r);
+    tmem_wait32(r);
     float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[c & 1][j]);
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
     const int nv = valid - 32 * c;
     if (nv < 32) {
 #pragma unroll
@@ -218,7 +216,6 @@ __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs,
     for (int k = 0; k < 4; k++) upk2(acc[k], a8[2 * k], a8[2 * k + 1]);
     pm = mn;
     ps = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
-    if (c + 1 < nch) tmem_wait32(r[(c + 1) & 1]);
   }
 }
 
@@ -274,7 +271,7 @@ __device__ __forceinline__ float group_pass2(uint32_t taddr, int G, int half, fl
 }
 
 template <int W>
-__global__ void __maxnreg__(200)  // 320 threads × 200 registers fit one CTA per SM
+__global__ void __launch_bounds__(kGThreads, 1)
 k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
               const __grid_constant__ CUtensorMap tm_mk128,
               const __grid_constant__ CUtensorMap tm_q, GroupArgs a) {
