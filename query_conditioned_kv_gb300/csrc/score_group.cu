@@ -59,7 +59,7 @@ constexpr int kGD = 128;                // head dim
 constexpr int kGTB = 256;               // Mean-K blocks per tile (pass-1 N)
 constexpr uint32_t kGSlot = 32768;      // ring slot: one K-half of a tile, or a half-tile
 constexpr int kGMaxR = 192;             // widest query-row set
-constexpr int kGLook = 2;               // next-unit tiles run ahead of an exchange
+constexpr int kGLook = 3;               // next-unit tiles run ahead of an exchange
 constexpr int kGThreads = 64 + 256;
 constexpr uint32_t kGBufCols = 256;     // TMEM columns per job buffer
 constexpr size_t kGSmemMax = 232448;    // the opt-in per-CTA maximum
@@ -70,8 +70,7 @@ struct GroupArgs {
   const int64_t *blk_off;
   int32_t *status;
   int *counter;   // [n_groups]: partials published so far (g per unit)
-  float2 *part;   // [n_groups][2][g][2][256] row partials (max, Σ2^(z−max)), base 2,
-                  // one per column half of a tile
+  float2 *part;   // [n_groups][2][g][256] row partials (max, Σ2^(z−max)), base 2
   int L, H, n_sess, R, n2, g, n_groups, max_tiles, ns;
   int64_t nb_total;
   float zscale;   // log2(e)/sqrt(D)
@@ -529,11 +528,29 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
         }
       }
     };
-    // publish this CTA's row partials of the i-th unit and count them
+    // publish this CTA's row partials of the i-th unit and count them: the
+    // upper column half hands its partials to the lower half through shared
+    // memory (the LSE and combine buffers, both idle between a unit's pass 2
+    // and the next exchange), which merges them (lower half first) and
+    // writes one partial per row
     auto publish = [&](int i) {
-      float2 *dst = a.part + ((((int64_t)grp * 2 + (i & 1)) * a.g + rank) * 2 + half) * 256;
-      dst[trow] = make_float2(pm0, ps0);
-      if (128 + trow < a.R) dst[128 + trow] = make_float2(pm1, ps1);
+      float2 *tmp = reinterpret_cast<float2 *>(sm.lse);  // [kGMaxR] (lse + comb)
+      if (half == 1) {
+        tmp[trow] = make_float2(pm0, ps0);
+        if (128 + trow < a.R) tmp[128 + trow] = make_float2(pm1, ps1);
+      }
+      named_sync(2, 256);
+      if (half == 0) {
+        float2 *dst = a.part + (((int64_t)grp * 2 + (i & 1)) * a.g + rank) * 256;
+        float2 o = tmp[trow];
+        lse_merge_g(pm0, ps0, o.x, o.y);
+        dst[trow] = make_float2(pm0, ps0);
+        if (128 + trow < a.R) {
+          o = tmp[128 + trow];
+          lse_merge_g(pm1, ps1, o.x, o.y);
+          dst[128 + trow] = make_float2(pm1, ps1);
+        }
+      }
       pm0 = pm1 = -INFINITY;
       ps0 = ps1 = 0.f;
       named_sync(2, 256);
@@ -543,7 +560,7 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
       }
     };
     // wait until the group has published the i-th unit, then form its LSEs
-    // (partials merged in rank order, then column half)
+    // (partials merged in rank order)
     auto exchange = [&](int i) {
       if (et == 0 && ok && !*sm.failed) {
         const int want = a.g * (i + 1);
@@ -559,11 +576,17 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
       named_sync(2, 256);
       if (*sm.failed) ok = false;
       if (et < a.R) {
-        const float2 *src = a.part + ((int64_t)grp * 2 + (i & 1)) * a.g * 512 + et;
+        // g partials, loaded 20 at a time so that their L2 latencies overlap
+        const float2 *src = a.part + ((int64_t)grp * 2 + (i & 1)) * a.g * 256 + et;
         float m = -INFINITY, s2 = 0.f;
-        for (int c = 0; c < 2 * a.g; c++) {
-          const float2 v = __ldcg(src + (int64_t)c * 256);
-          lse_merge_g(m, s2, v.x, v.y);
+        for (int c0 = 0; c0 < a.g; c0 += 20) {
+          float2 v[20];
+#pragma unroll
+          for (int k = 0; k < 20; k++)
+            v[k] = c0 + k < a.g ? __ldcg(src + (int64_t)(c0 + k) * 256)
+                                : make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int k = 0; k < 20; k++) lse_merge_g(m, s2, v[k].x, v[k].y);
         }
         sm.lse[et] = (m == -INFINITY) ? INFINITY : m + log2f(s2);
       }
@@ -707,8 +730,8 @@ bool score_group_supported(int G, int D, int W, int nb_max) {
 
 size_t score_group_ws_bytes() {
   const int n_sm = device_sm_count();
-  // counters (one per group, at most n_sm) + partials [n_sm][2][2][256] float2
-  return 256 + ((size_t)n_sm * 4 + 255) / 256 * 256 + (size_t)n_sm * 2 * 2 * 256 * sizeof(float2);
+  // counters (one per group, at most n_sm) + partials [n_sm][2][256] float2
+  return 256 + ((size_t)n_sm * 4 + 255) / 256 * 256 + (size_t)n_sm * 2 * 256 * sizeof(float2);
 }
 
 cudaError_t launch_score_group(const uint16_t *q, const uint16_t *meank, float *scores, int L,
