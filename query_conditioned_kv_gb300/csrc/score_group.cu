@@ -35,10 +35,10 @@
 //     exchanges, so the tensor pipe keeps working through the exchange:
 //         P1(u0) | P1a(u1) P2(u0) P1b(u1) | P1a(u2) P2(u1) P1b(u2) | … | P2(u_last)
 //   * roles: warp 0 issues TMA, warp 1 issues tcgen05.mma into TMEM buffer
-//     j mod 2 for job j (a row tile or a block half), warps 2–9 read every
-//     job back, each warp one lane quarter and one half of the job's columns,
-//     so a job's epilogue takes about as long as its MMA and the two buffers
-//     keep the tensor pipe fed.
+//     j mod 2 for job j (a row tile or a block half), warps 4–11 (two
+//     warpgroups) read every job back, each warp one lane quarter and one
+//     half of the job's columns; setmaxnreg moves registers from the control
+//     warpgroup to them, so that TMEM loads can run ahead of the arithmetic.
 // Every wait is bounded (1 s of %globaltimer) and records KVC_ERR_TIMEOUT.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -60,7 +60,9 @@ constexpr int kGTB = 256;               // Mean-K blocks per tile (pass-1 N)
 constexpr uint32_t kGSlot = 32768;      // ring slot: one K-half of a tile, or a half-tile
 constexpr int kGMaxR = 192;             // widest query-row set
 constexpr int kGLook = 3;               // next-unit tiles run ahead of an exchange
-constexpr int kGThreads = 64 + 256;
+constexpr int kGThreads = 384;          // warpgroup 0: TMA, MMA (+2 idle warps); 1-2: epilogue
+constexpr int kGCtlRegs = 80;           // registers of warpgroup 0 after setmaxnreg.dec
+constexpr int kGEpiRegs = 208;          // registers of warpgroups 1-2 after setmaxnreg.inc
 constexpr uint32_t kGBufCols = 256;     // TMEM columns per job buffer
 constexpr size_t kGSmemMax = 232448;    // the opt-in per-CTA maximum
 constexpr int kGTarget = 7;             // tiles of a unit a CTA aims to hold
@@ -164,20 +166,16 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 
 // Pass 1 of this warp's 128 columns (blocks) of one row tile for this
 // lane's query row: online (max, Σ2^(z·zs − max)) over the `valid` columns,
-// 32 at a time.  Column j adds into accumulator j mod 8 (held as four packed
-// pairs).  (Loading the next chunk ahead would hold a second 32-register
-// buffer and push the warps past the register budget of 320 threads.)
+// 32 at a time, the next chunk's TMEM load in flight while one is
+// processed.  Column j adds into accumulator j mod 8 (four packed pairs).
 __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs, float &pm,
                                             float &ps) {
   pm = -INFINITY;
   ps = 0.f;
   const int nch = valid <= 0 ? 0 : (valid >= 128 ? 4 : (valid + 31) / 32);
+  if (nch == 0) return;
   const uint64_t zs2 = pk2(zs, zs);
-#pragma unroll 1
-  for (int c = 0; c < nch; c++) {
-    uint32_t r[32];
-    tmem_issue32(taddr + (uint32_t)(32 * c), r);
-    tmem_wait32(r);
+  auto chunk = [&](const uint32_t(&r)[32], int c) {
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
@@ -215,52 +213,67 @@ __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs,
     for (int k = 0; k < 4; k++) upk2(acc[k], a8[2 * k], a8[2 * k + 1]);
     pm = mn;
     ps = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+  };
+  uint32_t ra[32], rb[32];
+  tmem_issue32(taddr, ra);
+  tmem_wait32(ra);
+#pragma unroll 1
+  for (int c = 0; c < nch; c += 2) {  // chunk c in ra, chunk c + 1 in rb
+    if (c + 1 < nch) tmem_issue32(taddr + (uint32_t)(32 * (c + 1)), rb);
+    chunk(ra, c);
+    if (c + 1 < nch) {
+      tmem_wait32(rb);
+      if (c + 2 < nch) tmem_issue32(taddr + (uint32_t)(32 * (c + 2)), ra);
+      chunk(rb, c + 1);
+      if (c + 2 < nch) tmem_wait32(ra);
+    }
   }
 }
 
 // Pass 2 of this warp's half of the window positions for this lane's block:
 // for w in [half·W/2, (half+1)·W/2), the max over the G heads of
-// z·zs − LSE (columns g·W + w, each head's W/2 columns one TMEM load, the
-// next head's load in flight), then Σ_w 2^max over this half.
+// z·zs − LSE (columns g·W + w), then Σ_w 2^max over this half.  The heads'
+// W/2-column loads are issued in two batches (half of the heads each), so a
+// job waits for two TMEM latencies instead of one per head.
 template <int W>
 __device__ __forceinline__ float group_pass2(uint32_t taddr, int G, int half, float zs,
                                              const float *lse) {
   constexpr int HW = W / 2;
+  constexpr int GB = kGMaxR / W / 2;  // heads per batch
   float mw[HW];
 #pragma unroll
   for (int w = 0; w < HW; w++) mw[w] = -INFINITY;
   const uint64_t zs2 = pk2(zs, zs);
-  // head g's columns: x = z·zs − LSE, max into mw
-  auto fold = [&](const uint32_t(&rr)[HW], int g) {
-    const float4 *l4 = reinterpret_cast<const float4 *>(lse + g * W + half * HW);
-#pragma unroll
-    for (int j = 0; j < HW; j += 4) {
-      const float4 Lv = l4[j / 4];
-      float x0, x1, x2, x3;
-      upk2(fma2(pk2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])), zs2, pk2(-Lv.x, -Lv.y)),
-           x0, x1);
-      upk2(fma2(pk2(__uint_as_float(rr[j + 2]), __uint_as_float(rr[j + 3])), zs2,
-                pk2(-Lv.z, -Lv.w)),
-           x2, x3);
-      mw[j] = fmaxf(mw[j], x0);
-      mw[j + 1] = fmaxf(mw[j + 1], x1);
-      mw[j + 2] = fmaxf(mw[j + 2], x2);
-      mw[j + 3] = fmaxf(mw[j + 3], x3);
-    }
-  };
-  uint32_t ra[HW], rb[HW];
   const uint32_t col0 = (uint32_t)(half * HW);
-  tmem_issue<HW>(taddr + col0, ra);
-  tmem_wait<HW>(ra);
 #pragma unroll 1
-  for (int g = 0; g < G; g += 2) {  // head g in ra, head g + 1 in rb
-    if (g + 1 < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g + 1) * W), rb);
-    fold(ra, g);
-    if (g + 1 < G) {
-      tmem_wait<HW>(rb);
-      if (g + 2 < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g + 2) * W), ra);
-      fold(rb, g + 1);
-      if (g + 2 < G) tmem_wait<HW>(ra);
+  for (int g0 = 0; g0 < G; g0 += GB) {
+    uint32_t r[GB][HW];
+#pragma unroll
+    for (int k = 0; k < GB; k++)
+      if (g0 + k < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g0 + k) * W), r[k]);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int k = 0; k < GB; k++) {
+      if (g0 + k >= G) break;
+#pragma unroll
+      for (int j = 0; j < HW; j += 4)
+        asm volatile("" : "+r"(r[k][j]), "+r"(r[k][j + 1]), "+r"(r[k][j + 2]), "+r"(r[k][j + 3]));
+      const float4 *l4 = reinterpret_cast<const float4 *>(lse + (g0 + k) * W + half * HW);
+#pragma unroll
+      for (int j = 0; j < HW; j += 4) {
+        const float4 Lv = l4[j / 4];
+        float x0, x1, x2, x3;
+        upk2(fma2(pk2(__uint_as_float(r[k][j]), __uint_as_float(r[k][j + 1])), zs2,
+                  pk2(-Lv.x, -Lv.y)),
+             x0, x1);
+        upk2(fma2(pk2(__uint_as_float(r[k][j + 2]), __uint_as_float(r[k][j + 3])), zs2,
+                  pk2(-Lv.z, -Lv.w)),
+             x2, x3);
+        mw[j] = fmaxf(mw[j], x0);
+        mw[j + 1] = fmaxf(mw[j + 1], x1);
+        mw[j + 2] = fmaxf(mw[j + 2], x2);
+        mw[j + 3] = fmaxf(mw[j + 3], x3);
+      }
     }
   }
   float acc = 0.f;
@@ -301,10 +314,16 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_holder;
+  // Registers move from the control warpgroup (TMA, MMA, two idle warps) to
+  // the two epilogue warpgroups: 128·kGCtlRegs + 256·kGEpiRegs stays within
+  // the 384·168 the block is launched with.  Each branch starts with its
+  // setmaxnreg, so the budget covers all the code of that role.
 
   // The step order every role walks, for this CTA's units u_0 … u_{n−1}:
   //   P1(u0) | P1a(u1) P2(u0) P1b(u1) | … | P2(u_{n−1})
   // with P1a = the first `look` tiles of a unit and P1b = the rest.
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGCtlRegs));
   if (warp == 0) {
     // ------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -458,16 +477,18 @@ k_score_group(const __grid_constant__ CUtensorMap tm_mk256,
       if (!ok) *sm.failed = 1;
     }
     __syncwarp();
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGEpiRegs));
     // ------------------------------------------------------- epilogue
     // All eight warps take every job; warp (half, quarter) reads TMEM lanes
     // 32·quarter … + 31 and one half of the job's columns: in pass 1 the
     // blocks [128·half, 128·half + 128) of the tile, in pass 2 the window
     // positions [half·W/2, (half + 1)·W/2) of every head.
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int trow = 32 * quarter + lane;     // this thread's TMEM lane
-    const int et = (warp - 2) * 32 + lane;    // 0 … 255
+    const int et = (warp - 4) * 32 + lane;    // 0 … 255
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     const float zs = a.zscale, invW = 1.f / (float)W;
     const int G = a.R / W;
@@ -670,7 +691,14 @@ int group_resident_ctas(size_t smem, int R) {
   if (have >= 0) return have;
   auto kern = k_score_group<W>;
   int n = 0, per_sm = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+  cudaFuncAttributes fa{};
+  // the register split (setmaxnreg) needs the block launched with at least
+  // (128·kGCtlRegs + 256·kGEpiRegs) / 384 registers a thread
+  const bool regs_ok =
+      cudaFuncGetAttributes(&fa, kern) == cudaSuccess &&
+      (int64_t)fa.numRegs * kGThreads >= 128 * (int64_t)kGCtlRegs + 256 * (int64_t)kGEpiRegs;
+  if (regs_ok &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
           cudaSuccess &&
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGThreads, smem) ==
           cudaSuccess &&
