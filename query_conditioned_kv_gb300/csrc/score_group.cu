@@ -166,36 +166,35 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 
 // Pass 1 of this warp's 128 columns (blocks) of one row tile for this
 // lane's query row: online (max, Σ2^(z·zs − max)) over the `valid` columns,
-// 32 at a time, the next chunk's TMEM load in flight while one is
-// processed.  Column j adds into accumulator j mod 8 (four packed pairs).
+// 64 at a time (two TMEM loads per job).  Column j adds into accumulator
+// j mod 8 (four packed pairs).
 __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs, float &pm,
                                             float &ps) {
   pm = -INFINITY;
   ps = 0.f;
-  const int nch = valid <= 0 ? 0 : (valid >= 128 ? 4 : (valid + 31) / 32);
-  if (nch == 0) return;
+  const int nch = valid <= 0 ? 0 : (valid >= 128 ? 2 : (valid + 63) / 64);
   const uint64_t zs2 = pk2(zs, zs);
-  auto chunk = [&](const uint32_t(&r)[32], int c) {
-    float v[32];
+#pragma unroll 1
+  for (int c = 0; c < nch; c++) {
+    float v[64];
+    tmem_ld64(taddr + (uint32_t)(64 * c), v);
+    const int nv = valid - 64 * c;
+    if (nv < 64) {
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
-    const int nv = valid - 32 * c;
-    if (nv < 32) {
-#pragma unroll
-      for (int j = 0; j < 32; j++)
+      for (int j = 0; j < 64; j++)
         if (j >= nv) v[j] = -INFINITY;
     }
     float m0 = max3(v[0], v[1], v[2]), m1 = max3(v[3], v[4], v[5]);
     float m2 = max3(v[6], v[7], v[8]), m3 = max3(v[9], v[10], v[11]);
 #pragma unroll
-    for (int j = 12; j < 28; j += 8) {
+    for (int j = 12; j < 60; j += 8) {
       m0 = max3(m0, v[j], v[j + 1]);
       m1 = max3(m1, v[j + 2], v[j + 3]);
       m2 = max3(m2, v[j + 4], v[j + 5]);
       m3 = max3(m3, v[j + 6], v[j + 7]);
     }
-    m0 = max3(m0, v[28], v[29]);
-    m1 = max3(m1, v[30], v[31]);
+    m0 = max3(m0, v[60], v[61]);
+    m1 = max3(m1, v[62], v[63]);
     const float mn = fmaxf(pm, fmaxf(max3(m0, m1, m2), m3) * zs);
     const uint64_t nmn2 = pk2(-mn, -mn);
     uint64_t acc[4];
@@ -203,7 +202,7 @@ __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs,
 #pragma unroll
     for (int k = 1; k < 4; k++) acc[k] = pk2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
+    for (int j = 0; j < 64; j += 2) {
       float x0, x1;
       upk2(fma2(pk2(v[j], v[j + 1]), zs2, nmn2), x0, x1);
       acc[(j & 7) >> 1] = add2(acc[(j & 7) >> 1], pk2(ex2(x0), ex2(x1)));
@@ -213,67 +212,52 @@ __device__ __forceinline__ void group_pass1(uint32_t taddr, int valid, float zs,
     for (int k = 0; k < 4; k++) upk2(acc[k], a8[2 * k], a8[2 * k + 1]);
     pm = mn;
     ps = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
-  };
-  uint32_t ra[32], rb[32];
-  tmem_issue32(taddr, ra);
-  tmem_wait32(ra);
-#pragma unroll 1
-  for (int c = 0; c < nch; c += 2) {  // chunk c in ra, chunk c + 1 in rb
-    if (c + 1 < nch) tmem_issue32(taddr + (uint32_t)(32 * (c + 1)), rb);
-    chunk(ra, c);
-    if (c + 1 < nch) {
-      tmem_wait32(rb);
-      if (c + 2 < nch) tmem_issue32(taddr + (uint32_t)(32 * (c + 2)), ra);
-      chunk(rb, c + 1);
-      if (c + 2 < nch) tmem_wait32(ra);
-    }
   }
 }
 
 // Pass 2 of this warp's half of the window positions for this lane's block:
 // for w in [half·W/2, (half+1)·W/2), the max over the G heads of
-// z·zs − LSE (columns g·W + w), then Σ_w 2^max over this half.  The heads'
-// W/2-column loads are issued in two batches (half of the heads each), so a
-// job waits for two TMEM latencies instead of one per head.
+// z·zs − LSE (columns g·W + w, each head's W/2 columns one TMEM load, the
+// next head's load in flight), then Σ_w 2^max over this half.
 template <int W>
 __device__ __forceinline__ float group_pass2(uint32_t taddr, int G, int half, float zs,
                                              const float *lse) {
   constexpr int HW = W / 2;
-  constexpr int GB = kGMaxR / W / 2;  // heads per batch
   float mw[HW];
 #pragma unroll
   for (int w = 0; w < HW; w++) mw[w] = -INFINITY;
   const uint64_t zs2 = pk2(zs, zs);
+  // head g's columns: x = z·zs − LSE, max into mw
+  auto fold = [&](const uint32_t(&rr)[HW], int g) {
+    const float4 *l4 = reinterpret_cast<const float4 *>(lse + g * W + half * HW);
+#pragma unroll
+    for (int j = 0; j < HW; j += 4) {
+      const float4 Lv = l4[j / 4];
+      float x0, x1, x2, x3;
+      upk2(fma2(pk2(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1])), zs2, pk2(-Lv.x, -Lv.y)),
+           x0, x1);
+      upk2(fma2(pk2(__uint_as_float(rr[j + 2]), __uint_as_float(rr[j + 3])), zs2,
+                pk2(-Lv.z, -Lv.w)),
+           x2, x3);
+      mw[j] = fmaxf(mw[j], x0);
+      mw[j + 1] = fmaxf(mw[j + 1], x1);
+      mw[j + 2] = fmaxf(mw[j + 2], x2);
+      mw[j + 3] = fmaxf(mw[j + 3], x3);
+    }
+  };
+  uint32_t ra[HW], rb[HW];
   const uint32_t col0 = (uint32_t)(half * HW);
+  tmem_issue<HW>(taddr + col0, ra);
+  tmem_wait<HW>(ra);
 #pragma unroll 1
-  for (int g0 = 0; g0 < G; g0 += GB) {
-    uint32_t r[GB][HW];
-#pragma unroll
-    for (int k = 0; k < GB; k++)
-      if (g0 + k < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g0 + k) * W), r[k]);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int k = 0; k < GB; k++) {
-      if (g0 + k >= G) break;
-#pragma unroll
-      for (int j = 0; j < HW; j += 4)
-        asm volatile("" : "+r"(r[k][j]), "+r"(r[k][j + 1]), "+r"(r[k][j + 2]), "+r"(r[k][j + 3]));
-      const float4 *l4 = reinterpret_cast<const float4 *>(lse + (g0 + k) * W + half * HW);
-#pragma unroll
-      for (int j = 0; j < HW; j += 4) {
-        const float4 Lv = l4[j / 4];
-        float x0, x1, x2, x3;
-        upk2(fma2(pk2(__uint_as_float(r[k][j]), __uint_as_float(r[k][j + 1])), zs2,
-                  pk2(-Lv.x, -Lv.y)),
-             x0, x1);
-        upk2(fma2(pk2(__uint_as_float(r[k][j + 2]), __uint_as_float(r[k][j + 3])), zs2,
-                  pk2(-Lv.z, -Lv.w)),
-             x2, x3);
-        mw[j] = fmaxf(mw[j], x0);
-        mw[j + 1] = fmaxf(mw[j + 1], x1);
-        mw[j + 2] = fmaxf(mw[j + 2], x2);
-        mw[j + 3] = fmaxf(mw[j + 3], x3);
-      }
+  for (int g = 0; g < G; g += 2) {  // head g in ra, head g + 1 in rb
+    if (g + 1 < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g + 1) * W), rb);
+    fold(ra, g);
+    if (g + 1 < G) {
+      tmem_wait<HW>(rb);
+      if (g + 2 < G) tmem_issue<HW>(taddr + col0 + (uint32_t)((g + 2) * W), ra);
+      fold(rb, g + 1);
+      if (g + 2 < G) tmem_wait<HW>(ra);
     }
   }
   float acc = 0.f;
