@@ -342,14 +342,17 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
       uint32_t s = 0, qi = 0;
       bool ok = true;
       int prev_unit = -1;
-      auto load_tile = [&](int row0, int i) -> bool {
+      // tiles multiplied twice stay in L2 until their second read (evict
+      // last); second reads and the kept tiles are the last use (evict first)
+      const uint64_t keep = l2_evict_last(), drop = l2_evict_first();
+      auto load_tile = [&](int row0, int i, uint64_t pol) -> bool {
         const int slot = s % kFNS;
         if (!wait_or_abort(smem_u32(sm.empty + slot), ((s / kFNS) & 1) ^ 1, sm.failed))
           return false;
         mbar_expect_tx(smem_u32(sm.full + slot), kFTile);
         for (int kb = 0; kb < 2; kb++)
-          tma_load_2d(smem_u32(sm.ring + slot * kFTile + kb * (kFTile / 2)), &tm_mk, kb * 64,
-                      row0 + (rank + i * C) * kFTB, smem_u32(sm.full + slot));
+          tma_load_2d_hint(smem_u32(sm.ring + slot * kFTile + kb * (kFTile / 2)), &tm_mk, kb * 64,
+                           row0 + (rank + i * C) * kFTB, smem_u32(sm.full + slot), pol);
         s++;
         return true;
       };
@@ -371,12 +374,14 @@ k_score_fused(const __grid_constant__ CUtensorMap tm_mk, const __grid_constant__
             qi++;
           }
         }
-        for (int i = 0; i < u.n_rec && ok; i++) ok = load_tile(u.mk_row0, i);      // A(u)
+        for (int i = 0; i < u.n_rec && ok; i++) ok = load_tile(u.mk_row0, i, keep);  // A(u)
         if (prev_unit >= 0) {
           const FUnit prev = funit(a, prev_unit, C, rank);
-          for (int i = 0; i < prev.n_rec && ok; i++) ok = load_tile(prev.mk_row0, i);  // R(prev)
+          for (int i = 0; i < prev.n_rec && ok; i++)
+            ok = load_tile(prev.mk_row0, i, drop);                                    // R(prev)
         }
-        for (int i = u.n_rec; i < u.my_tiles && ok; i++) ok = load_tile(u.mk_row0, i);  // B(u)
+        for (int i = u.n_rec; i < u.my_tiles && ok; i++)
+          ok = load_tile(u.mk_row0, i, drop);                                         // B(u)
         if (last) break;
         prev_unit = unit;
       }
