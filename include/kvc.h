@@ -106,8 +106,12 @@ typedef enum {
   KVC_KERNEL_SCORE_GROUP = 6,   /* tcgen05, two passes, CTA groups exchanging through
                                    L2; 129–192 query rows, D = 128                   */
   /* kvc_score_qmem_ex (rule score) */
-  KVC_KERNEL_QMEM_TC = 16,      /* tcgen05 logits (8 KV heads, G ∈ {2, 4, 8})         */
+  KVC_KERNEL_QMEM_TC = 16,      /* tcgen05 logits (8 KV heads, G ∈ {2, 4}), rule
+                                   phase in the same kernel from L2                  */
   KVC_KERNEL_QMEM_CC = 17,      /* CUDA-core logits; any shape                        */
+  KVC_KERNEL_QMEM_TC_SPILL = 18, /* tcgen05 logits (8 KV heads, G ∈ {2, 4, 8})
+                                    spilled to the workspace, rule phase in a
+                                    second kernel                                 */
   /* kvc_recover_score_ex (LSE-recovery score) */
   KVC_KERNEL_RECOVER_TC = 32,   /* tcgen05 page tiles (H 8, block 16, G ∈ {2, 4, 8})  */
   KVC_KERNEL_RECOVER_CC = 33    /* CUDA cores; any shape                              */
@@ -279,7 +283,8 @@ kvc_status kvc_score_qmem(const float *M, const kvc_bf16 *kpool,
                           void *ws, size_t ws_bytes, int32_t *dev_status,
                           cudaStream_t stream);
 /* kvc_score_qmem with the logits kernel named by `kernel` (KVC_KERNEL_AUTO,
- * KVC_KERNEL_QMEM_TC or KVC_KERNEL_QMEM_CC). */
+ * KVC_KERNEL_QMEM_TC, KVC_KERNEL_QMEM_TC_SPILL or KVC_KERNEL_QMEM_CC).  AUTO
+ * takes QMEM_TC where it applies, then QMEM_TC_SPILL, then QMEM_CC. */
 kvc_status kvc_score_qmem_ex(const float *M, const kvc_bf16 *kpool,
                              const int32_t *slot_map, int32_t sentinel,
                              float *rule, int32_t n_sess, int32_t L, int32_t H,

@@ -206,14 +206,20 @@ def _qmem_case(args, dev):
                             cfg.decay, cfg.gain, 1)
     ev = SlotMapEvent(cfg.n_sess, cfg.N, cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.n_slots, cfg.budget,
                       cfg.prefix, cfg.sentinel, device=dev)
+    times = []
     for _ in range(args.iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
         ev.score(M, kp, sm, kernel=args.kernel)
+        b.record()
+        times.append((a, b))
     torch.cuda.synchronize()
     st = kvc.kvc_device_status(ev.dev_status)
     if st != 0:
         raise SystemExit(f"device status {st}: {kvc.kvc_status_string(st)}")
+    ms = sorted(a.elapsed_time(b) for a, b in times)
     print(f"profile case qmem: {args.iters} launches, {cfg.n_sess} sessions x {cfg.N} "
-          f"positions, {cfg.L} layers ok")
+          f"positions, {cfg.L} layers ok; score median {ms[len(ms) // 2]:.3f} ms")
 
 
 

@@ -44,7 +44,7 @@ KERNELS = {
     "auto": 0,
     "score_fused": 1, "score_ring": 2, "score_persist": 3, "score_split": 4, "score_cc": 5,
     "score_group": 6,
-    "qmem_tc": 16, "qmem_cc": 17,
+    "qmem_tc": 16, "qmem_cc": 17, "qmem_tc_spill": 18,
     "recover_tc": 32, "recover_cc": 33,
 }
 

@@ -183,7 +183,8 @@ kvc_status kvc_score_qmem_ex(const float *M, const kvc_bf16 *kpool,
                              void *ws, size_t ws_bytes, int32_t *dev_status,
                              kvc_kernel kernel, cudaStream_t stream) {
   if (!M || !kpool || !slot_map || !rule || !ws) return KVC_ERR_INVALID_ARG;
-  if (kernel != KVC_KERNEL_AUTO && kernel != KVC_KERNEL_QMEM_TC && kernel != KVC_KERNEL_QMEM_CC)
+  if (kernel != KVC_KERNEL_AUTO && kernel != KVC_KERNEL_QMEM_TC && kernel != KVC_KERNEL_QMEM_CC &&
+      kernel != KVC_KERNEL_QMEM_TC_SPILL)
     return KVC_ERR_INVALID_ARG;
   if (n_sess < 1 || L < 1 || H < 1 || Hq < 1 || N < 1 || n_slots < 1 || n_slots > INT32_MAX)
     return KVC_ERR_INVALID_ARG;

@@ -105,7 +105,8 @@ cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
                                int D, int T, float decay, float gain,
                                int renorm, cudaStream_t s);
 
-// `path`: KVC_KERNEL_AUTO, KVC_KERNEL_QMEM_TC or KVC_KERNEL_QMEM_CC.
+// `path`: KVC_KERNEL_AUTO, KVC_KERNEL_QMEM_TC, KVC_KERNEL_QMEM_TC_SPILL or
+// KVC_KERNEL_QMEM_CC.
 cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
                               const int32_t *slot_map, int32_t sentinel,
                               float *rule, int n_sess, int L, int H, int Hq,
@@ -115,11 +116,16 @@ size_t score_qmem_ws_bytes(int n_sess, int L, int Hq, int N);
 // tensor-core logits of the rule score (qmem_tc.cu)
 bool qmem_tc_supported(int H, int Hq, int D, int64_t L, int64_t n_slots);
 size_t qmem_tc_mb_bytes(int n_sess, int L, int Hq);
+// fused: the rule phase runs inside the logits kernel from L2 (writes
+// rule_l, [n_sess][L][N]); otherwise the logits and tile partials are
+// spilled for k_qmem_lse / k_qmem_rule.  cudaErrorNotSupported for a fused
+// launch with groups of 8 query heads or one that cannot make every CTA
+// resident.
 cudaError_t launch_qmem_logits_tc(const float *M, const uint16_t *kpool, const int32_t *slot_map,
-                                  int32_t sentinel, float *logits, float2 *part, uint16_t *mb,
-                                  int n_sess, int L, int H, int Hq, int D, int N,
-                                  int64_t n_slots, int n_tiles, int32_t *status,
-                                  cudaStream_t s);
+                                  int32_t sentinel, float *logits, float2 *part, float *lse,
+                                  int *counter, float *rule_l, uint16_t *mb, int n_sess, int L,
+                                  int H, int Hq, int D, int N, int64_t n_slots, int n_tiles,
+                                  bool fused, int32_t *status, cudaStream_t s);
 
 cudaError_t launch_select(const float *scores, const int64_t *seg_off,
                           int n_seg, int max_seg_len, int budget, int n_sink,

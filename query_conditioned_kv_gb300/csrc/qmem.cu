@@ -22,8 +22,10 @@
 //                  2^(z − LSE) over (l, hq) per position.
 // Dead positions (slot = sentinel) carry z = −inf and rule = −1.
 // For 8 KV heads and groups of 2, 4 or 8 query heads the logits come from
-// the tensor-core kernel of qmem_tc.cu instead (same outputs); the CUDA-core
-// kernel below covers every other shape.
+// the tensor-core kernel of qmem_tc.cu instead; by default that kernel also
+// forms each layer's share of the rule score while the logits are still in
+// L2 (k_qmem_rule_sum then adds the layers), so the logits never go to DRAM.
+// The CUDA-core kernel below covers every other shape.
 
 #include "kvc_internal.cuh"
 
@@ -289,6 +291,34 @@ k_qmem_rule(QArgs a) {
   a.rule[(int64_t)r * a.N + j] = out;
 }
 
+// rule[r][j] = Σ_l rule_l[r][l][j] (each layer's Σ_hq 2^(z − LSE), formed
+// by the fused tensor-core kernel), −1 for a dead position.
+__global__ void __launch_bounds__(256)
+k_qmem_rule_sum(const float *__restrict__ rule_l, const int32_t *__restrict__ slot_map,
+                float *__restrict__ rule, int L, int N, int32_t sentinel, int64_t n_slots) {
+  const int r = blockIdx.y;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= N) return;
+  const int32_t u = slot_map[(int64_t)r * N + j];
+  const bool live = u != sentinel && u >= 0 && u < n_slots;
+  float out = -1.f;
+  if (live) {
+    const float *src = rule_l + (int64_t)r * L * N + j;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int l = 0;
+    for (; l + 4 <= L; l += 4) {
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; k++) v[k] = __ldcs(src + (int64_t)(l + k) * N);
+#pragma unroll
+      for (int k = 0; k < 4; k++) acc[k] += v[k];
+    }
+    for (; l < L; l++) acc[0] += __ldcs(src + (int64_t)l * N);
+    out = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  }
+  rule[(int64_t)r * N + j] = out;
+}
+
 // LSE per (session, layer, query head) from the tile partials, then the
 // rule sum over (layer, query head) per position.
 cudaError_t launch_qmem_reduce(const QArgs &a, cudaStream_t s) {
@@ -318,15 +348,20 @@ cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
   return cudaGetLastError();
 }
 
+// Scratch: logits [n_sess][L][Hq][N] fp32, tile partials, LSEs, the
+// two-term bf16 copy of M that the tensor-core logits read, and for the
+// fused finish one counter per (session, layer) and rule_l [n_sess][L][N].
 size_t score_qmem_ws_bytes(int n_sess, int L, int Hq, int N) {
   int64_t rows = (int64_t)n_sess * L * Hq;
   int n_tiles = (N + kTJ - 1) / kTJ;
   size_t logits = (size_t)rows * N * sizeof(float);
   size_t part = (size_t)rows * n_tiles * sizeof(float2);
   size_t lse = (size_t)rows * sizeof(float);
+  size_t counters = (size_t)n_sess * L * sizeof(int);
+  size_t rule_l = (size_t)n_sess * L * N * sizeof(float);
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
-  // + the two-term bf16 copy of M that the tensor-core logits read
-  return al(logits) + al(part) + al(lse) + al(qmem_tc_mb_bytes(n_sess, L, Hq));
+  return al(logits) + al(part) + al(lse) + al(qmem_tc_mb_bytes(n_sess, L, Hq)) + al(counters) +
+         al(rule_l);
 }
 
 cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
@@ -346,6 +381,10 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
   a.lse = reinterpret_cast<float *>(w);
   w += al((size_t)rows * sizeof(float));
   uint16_t *mb = reinterpret_cast<uint16_t *>(w);
+  w += al(qmem_tc_mb_bytes(n_sess, L, Hq));
+  int *counter = reinterpret_cast<int *>(w);
+  w += al((size_t)n_sess * L * sizeof(int));
+  float *rule_l = reinterpret_cast<float *>(w);
   a.M = M;
   a.kpool = kpool;
   a.slot_map = slot_map;
@@ -363,10 +402,23 @@ cudaError_t launch_score_qmem(const float *M, const uint16_t *kpool,
   a.zscale = kLog2e / sqrtf((float)D);
   cudaError_t e;
   const bool tc = qmem_tc_supported(H, Hq, D, L, n_slots);
-  if (path == KVC_KERNEL_QMEM_TC && !tc) return cudaErrorNotSupported;
-  if (path != KVC_KERNEL_QMEM_CC && tc) {
-    e = launch_qmem_logits_tc(M, kpool, slot_map, sentinel, a.logits, a.part, mb, n_sess, L, H,
-                              Hq, D, N, n_slots, a.n_tiles, status, s);
+  if ((path == KVC_KERNEL_QMEM_TC || path == KVC_KERNEL_QMEM_TC_SPILL) && !tc)
+    return cudaErrorNotSupported;
+  if (tc && (path == KVC_KERNEL_AUTO || path == KVC_KERNEL_QMEM_TC)) {
+    e = launch_qmem_logits_tc(M, kpool, slot_map, sentinel, a.logits, a.part, a.lse, counter,
+                              rule_l, mb, n_sess, L, H, Hq, D, N, n_slots, a.n_tiles, true,
+                              status, s);
+    if (e == cudaSuccess) {
+      k_qmem_rule_sum<<<dim3((N + 255) / 256, n_sess), 256, 0, s>>>(rule_l, slot_map, rule, L, N,
+                                                                     sentinel, n_slots);
+      return cudaGetLastError();
+    }
+    if (e != cudaErrorNotSupported || path == KVC_KERNEL_QMEM_TC) return e;
+  }
+  if (tc && path != KVC_KERNEL_QMEM_CC) {
+    e = launch_qmem_logits_tc(M, kpool, slot_map, sentinel, a.logits, a.part, a.lse, counter,
+                              rule_l, mb, n_sess, L, H, Hq, D, N, n_slots, a.n_tiles, false,
+                              status, s);
     if (e != cudaSuccess) return e;
     return launch_qmem_reduce(a, s);
   }

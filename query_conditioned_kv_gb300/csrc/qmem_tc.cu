@@ -17,9 +17,25 @@
 // gather through the slot map).  Both fill the same 128-byte-swizzled
 // layout.  Dead positions (slot = sentinel) get z = −inf.
 //
-// Output is what the CUDA-core logits kernel writes: the fp32 logits (base
-// 2) and, per 256-position tile, (max, Σ2^(z−max)) per query head, which
-// k_qmem_lse and k_qmem_rule then reduce.
+// Two ways to finish the rule score from the logits:
+//  * spilled: the kernel writes what the CUDA-core logits kernel writes, the
+//    fp32 logits (base 2) and, per 256-position tile, (max, Σ2^(z−max)) per
+//    query head; k_qmem_lse and k_qmem_rule reduce them afterwards, so the
+//    logits go to DRAM and come back (one fp32 per position and query head).
+//  * fused (FUSED = true, groups of 2 or 4): items run tile fastest, so
+//    all tiles of one (session, layer) row are done within about one wave
+//    of the grid.  Three more roles join the kernel.  A publisher warp
+//    counts each item the epilogue finished into its row's counter; the
+//    publisher holding the row's last tile then merges the tile partials
+//    into the row's LSEs and publishes them.  A share team of four warps takes this CTA's items in
+//    order: once an item's row is published it forms Σ_hq 2^(z − LSE) per
+//    position from the logits still in L2, writes that layer's share of the
+//    rule score, and drops the logit lines from L2 without a write-back.
+//    k_qmem_rule_sum adds the layers; the logits never reach DRAM.
+//    Publishers wait only for epilogues, which wait for no other CTA, and
+//    nothing waits for a share team, so every wait ends once every CTA is
+//    resident (the launch is cooperative).
+
 #include <algorithm>
 
 #include "kvc_internal.cuh"
@@ -34,13 +50,17 @@ constexpr int kTJ = 256;         // positions per item (one LSE-partial tile)
 constexpr int kPos = 16;         // positions per MMA tile
 constexpr int kH = 8;            // KV heads: kPos · kH = 128 rows
 constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2–5 epilogue
+constexpr int kThreadsFused = 352;  // + warp 6, the publisher, and warps 7–10, the share team
 constexpr int kMB = 2;           // memory-row buffers
 constexpr int kNacc = 4;         // TMEM accumulators
 
 struct QtcArgs {
   const int32_t *slot_map;  // [n_sess][N]
   float *logits;            // [n_sess][L][Hq][N], base-2 logits
-  float2 *part;             // [n_sess][L][Hq][n_tiles]
+  float2 *part;             // spilled: [n_sess][L][Hq][n_tiles]; fused: [n_sess][L][n_tiles][Hq]
+  int *counter;             // fused: [n_sess][L] items done (+1 once the LSEs are out)
+  float *lse;               // fused: [n_sess][L][Hq], base 2
+  float *rule_l;            // fused: [n_sess][L][N], Σ_hq 2^(z − LSE)
   int32_t *status;
   int n_sess, L, Hq, G, D, N, n_tiles, sentinel;
   int64_t n_slots;
@@ -52,8 +72,10 @@ struct QtcSmem {
   uint8_t *ring, *mb;
   uint64_t *full, *empty, *mfull, *mempty, *tfull, *tempty;
   float2 *red;  // [4 warps][8 heads][G]
+  float *lse_w;  // fused: [4 share warps][Hq] LSEs of the row being shared
   uint32_t *tmem_holder;
   volatile int *failed;
+  int *items_done;  // fused: items whose logits and partials the epilogue wrote
   __device__ QtcSmem(uint8_t *raw, int NS, int KB, int Hq) {
     uint8_t *p = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
@@ -69,12 +91,15 @@ struct QtcSmem {
     tfull = mempty + kMB;
     tempty = tfull + kNacc;
     red = reinterpret_cast<float2 *>(tempty + kNacc);
-    tmem_holder = reinterpret_cast<uint32_t *>(red + 4 * Hq);
+    lse_w = reinterpret_cast<float *>(red + 4 * Hq);
+    tmem_holder = reinterpret_cast<uint32_t *>(lse_w + 4 * Hq);
     failed = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    items_done = const_cast<int *>(failed + 1);
   }
   static size_t bytes(int NS, int KB, int Hq) {
     return 1024 + (size_t)NS * KB * 16384 + (size_t)kMB * KB * 2 * Hq * 128 +
-           (size_t)(2 * NS + 2 * kMB + 2 * kNacc) * 8 + (size_t)4 * Hq * 8 + 16;
+           (size_t)(2 * NS + 2 * kMB + 2 * kNacc) * 8 + (size_t)4 * Hq * 8 +
+           (size_t)4 * Hq * 4 + 16;
   }
 };
 
@@ -110,8 +135,8 @@ __device__ __forceinline__ void group_cols(const float (&v)[8 * G], int h, float
   }
 }
 
-template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int G, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kThreadsFused : kThreads, 1)
 k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
                  const __grid_constant__ CUtensorMap tm_k8,
                  const __grid_constant__ CUtensorMap tm_m, QtcArgs a, int NS,
@@ -139,6 +164,7 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
       mbar_init(smem_u32(sm.tfull + i), 1);
       mbar_init(smem_u32(sm.tempty + i), 4);
     }
+    *sm.items_done = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) alloc_tmem_cols(sm.tmem_holder, tmem_cols);
@@ -147,13 +173,23 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
   tc_fence_after();
   const uint32_t tmem = *sm.tmem_holder;
 
-  // item → (session fastest, tile, layer): the sessions that share a prefix
-  // read its rows at about the same time, from L2 after the first.
+  // spilled: item → (session fastest, tile, layer), so the sessions that
+  // share a prefix read its rows at about the same time, from L2 after the
+  // first.  fused: item → (tile fastest, session, layer), so a row's tiles
+  // are done together; the next session's prefix tiles follow one row (less
+  // than a wave) later.
   auto decode = [&](int64_t item, int &r, int &tile, int &l) {
-    r = (int)(item % a.n_sess);
-    const int64_t rest = item / a.n_sess;
-    tile = (int)(rest % a.n_tiles);
-    l = (int)(rest / a.n_tiles);
+    if constexpr (FUSED) {
+      tile = (int)(item % a.n_tiles);
+      const int64_t rest = item / a.n_tiles;
+      r = (int)(rest % a.n_sess);
+      l = (int)(rest / a.n_sess);
+    } else {
+      r = (int)(item % a.n_sess);
+      const int64_t rest = item / a.n_sess;
+      tile = (int)(rest % a.n_tiles);
+      l = (int)(rest / a.n_tiles);
+    }
   };
 
   if (warp == 0) {
@@ -290,15 +326,21 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
       if (!ok) *sm.failed = 1;
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // --------------------------------------------------- epilogue
+    // The four warps pass the same named barriers in the same order whatever
+    // happens: a failed wait skips work, never a barrier, and the warps agree
+    // on failure (named_sync_and) before leaving the item loop together.
     const int quarter = warp & 3;
     const int row = 32 * quarter + lane;
     const int sp = row / kH, h = row % kH;  // position in the tile, KV head
     const int et = (warp - 2) * 32 + lane;  // 0 … 127
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    uint64_t keep = 0;
+    if constexpr (FUSED) keep = l2_evict_last();
     uint32_t t = 0;
     bool ok = true;
+    int n_done = 0;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
       int r, tile, l;
       decode(item, r, tile, l);
@@ -316,9 +358,9 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
         const int32_t u = j < a.N ? __ldg(smap + j) : a.sentinel;
         const bool live = u != a.sentinel && u >= 0 && u < a.n_slots;
         const int buf = t % kNacc;
-        ok = __all_sync(0xFFFFFFFFu,
-                        ok && mbar_wait_bounded(smem_u32(sm.tfull + buf), (t / kNacc) & 1,
-                                                sm.failed));
+        const bool got =
+            ok && mbar_wait_bounded(smem_u32(sm.tfull + buf), (t / kNacc) & 1, sm.failed);
+        ok = __all_sync(0xFFFFFFFFu, got);
         float zh[G], zl[G];
         if (ok) {
           tc_fence_after();
@@ -338,11 +380,16 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(sm.tempty + buf));
         t++;
-        if (!ok) break;
+        if (!ok) continue;
 #pragma unroll
         for (int g = 0; g < G; g++) {
           const float z = (zh[g] + zl[g]) * a.zscale;
-          if (j < a.N) lrow[(int64_t)g * a.N + j] = live ? z : -INFINITY;
+          if (j < a.N) {
+            float *dst = lrow + (int64_t)g * a.N + j;
+            const float zv = live ? z : -INFINITY;
+            if constexpr (FUSED) st_hint_f32(dst, zv, keep);
+            else *dst = zv;
+          }
           if (live) {
             if (z > m[g]) {
               sum[g] = sum[g] * ex2(m[g] - z) + 1.f;
@@ -353,7 +400,6 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
           }
         }
       }
-      if (!ok) break;
       // (max, sum) per query head over the item's 256 positions
 #pragma unroll
       for (int g = 0; g < G; g++) {
@@ -367,20 +413,167 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
       if (lane < kH)
 #pragma unroll
         for (int g = 0; g < G; g++) sm.red[(quarter * kH + h) * G + g] = make_float2(m[g], sum[g]);
-      named_sync(1, 128);
-      if (et < HQ) {
+      ok = named_sync_and(1, 128, ok);
+      if (ok && et < HQ) {
         float mm = -INFINITY, ss = 0.f;
         for (int q4 = 0; q4 < 4; q4++) {
           const float2 v = sm.red[q4 * HQ + et];
           merge(mm, ss, v.x, v.y);
         }
-        a.part[(((int64_t)r * a.L + l) * HQ + et) * a.n_tiles + tile] = make_float2(mm, ss);
+        const int64_t rl = (int64_t)r * a.L + l;
+        a.part[FUSED ? (rl * a.n_tiles + tile) * HQ + et : (rl * HQ + et) * a.n_tiles + tile] =
+            make_float2(mm, ss);
       }
       named_sync(1, 128);
+      if (!ok) break;
+      if constexpr (FUSED) {
+        // hand the item to the publisher: every epilogue write of it comes
+        // before this release (the barrier above orders the other threads')
+        n_done++;
+        if (et == 0) st_release_cta(sm.items_done, n_done);
+      }
     }
     if (!ok) {
       *sm.failed = 1;
       if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+    }
+  } else if (warp == 6) {
+    // --------------------------------------------- publisher (fused only)
+    // Counts each item the epilogue finished into its (session, layer) row;
+    // the CTA holding the row's last tile waits for the row's count, merges
+    // the row's tile partials into its LSEs and publishes them (the counter
+    // then reads n_tiles + 1).  Waits only for epilogues, which wait for no
+    // other CTA.
+    if constexpr (FUSED) {
+      bool ok = true;
+      int k = 0;
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, k++) {
+        if (lane == 0) {
+          const uint64_t t0 = global_ns();
+          while (ld_acquire_cta(sm.items_done) < k + 1) {
+            if (*sm.failed || global_ns() - t0 > 1000000000ull) {
+              ok = false;
+              break;
+            }
+            __nanosleep(256);
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        int r, tile, l;
+        decode(item, r, tile, l);
+        const int64_t rl = (int64_t)r * a.L + l;
+        // release the epilogue's writes of the item (acquired above at CTA
+        // scope) to the row
+        if (lane == 0) atom_add_acq_rel_gpu(a.counter + rl, 1);
+        if (tile == a.n_tiles - 1) {
+          // The row's merger: the CTA holding its last tile, which is this
+          // CTA's last item of the row, so the wait below never waits on
+          // this publisher.  (The last finisher, the natural choice, is
+          // mostly one slow CTA, which then falls further behind.)
+          if (lane == 0) {
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_gpu(a.counter + rl) < a.n_tiles) {
+              if (*sm.failed || global_ns() - t0 > 1000000000ull) {
+                ok = false;
+                break;
+              }
+              __nanosleep(128);
+            }
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          __syncwarp();  // lane 0's acquire orders the other lanes' loads too
+          if (!ok) break;
+          // the row's tile partials, [tile][Hq]: lanes take consecutive query
+          // heads (one 256-byte read per instruction for 32 heads), 32 tiles
+          // in flight, merged in tile order
+          for (int hq = lane; hq < HQ; hq += 32) {
+            const float2 *src = a.part + rl * a.n_tiles * HQ + hq;
+            float mm = -INFINITY, ss = 0.f;
+            for (int t0 = 0; t0 < a.n_tiles; t0 += 32) {
+              float2 v[32];
+#pragma unroll
+              for (int kk = 0; kk < 32; kk++)
+                v[kk] = t0 + kk < a.n_tiles ? __ldcg(src + (int64_t)(t0 + kk) * HQ)
+                                            : make_float2(-INFINITY, 0.f);
+#pragma unroll
+              for (int kk = 0; kk < 32; kk++) merge(mm, ss, v[kk].x, v[kk].y);
+            }
+            a.lse[rl * HQ + hq] = mm == -INFINITY ? -INFINITY : mm + log2f(ss);
+          }
+          __syncwarp();
+          if (lane == 0) atom_add_acq_rel_gpu(a.counter + rl, 1);
+        }
+      }
+      if (!ok) {
+        *sm.failed = 1;
+        if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ---------------------------------------------- share team (fused only)
+    // Each warp takes 64 of an item's 256 positions, for this CTA's items in
+    // order: once the item's row has published its LSEs, it forms
+    // Σ_hq 2^(z − LSE) per position from the logits still in L2, writes that
+    // layer's share, and drops its whole 128-byte logit lines from L2.  No
+    // other role waits for it.
+    if constexpr (FUSED) {
+      const int w = warp - 7;
+      float *lw = sm.lse_w + w * HQ;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        int r, tile, l;
+        decode(item, r, tile, l);
+        const int64_t rl = (int64_t)r * a.L + l;
+        if (lane == 0) {
+          const uint64_t t0 = global_ns();
+          while (ld_acquire_gpu(a.counter + rl) < a.n_tiles + 1) {
+            if (*sm.failed || global_ns() - t0 > 1000000000ull) {
+              ok = false;
+              break;
+            }
+            __nanosleep(256);
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        __syncwarp();  // lane 0's acquire orders the other lanes' loads too
+        if (!ok) break;
+        for (int hq = lane; hq < HQ; hq += 32) lw[hq] = __ldcg(a.lse + rl * HQ + hq);
+        __syncwarp();
+        const int j0 = tile * kTJ;
+        const int valid = min(kTJ, a.N - j0);
+        const float *zb = a.logits + rl * HQ * a.N + j0;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; hf++) {
+          const int pp = 64 * w + 32 * hf + lane;
+          float acc = 0.f;
+#pragma unroll 1
+          for (int h0 = 0; h0 < HQ; h0 += 16) {
+            float z[16];
+#pragma unroll
+            for (int kk = 0; kk < 16; kk++)
+              z[kk] = pp < valid ? __ldcg(zb + (int64_t)(h0 + kk) * a.N + pp) : -INFINITY;
+#pragma unroll
+            for (int kk = 0; kk < 16; kk++) {
+              const float L2v = lw[h0 + kk];
+              if (L2v != -INFINITY) acc += ex2(z[kk] - L2v);
+            }
+          }
+          if (pp < valid) a.rule_l[rl * a.N + j0 + pp] = acc;
+        }
+        // every value this warp read has been used: drop its lines
+        __syncwarp();
+        for (int idx = lane; idx < 2 * HQ; idx += 32) {
+          const int c0 = 64 * w + 32 * (idx / HQ), hq = idx % HQ;
+          if (c0 + 32 > valid) continue;
+          const float *line = zb + (int64_t)hq * a.N + c0;
+          if ((reinterpret_cast<uintptr_t>(line) & 127u) == 0u) l2_discard_line(line);
+        }
+      }
+      if (!ok) {
+        *sm.failed = 1;
+        if (lane == 0) record_error(a.status, KVC_ERR_TIMEOUT);
+      }
     }
   }
 
@@ -441,19 +634,19 @@ size_t qmem_tc_mb_bytes(int n_sess, int L, int Hq) {
 }
 
 cudaError_t launch_qmem_logits_tc(const float *M, const uint16_t *kpool, const int32_t *slot_map,
-                                  int32_t sentinel, float *logits, float2 *part, uint16_t *mb,
-                                  int n_sess, int L, int H, int Hq, int D, int N,
-                                  int64_t n_slots, int n_tiles, int32_t *status,
-                                  cudaStream_t s) {
+                                  int32_t sentinel, float *logits, float2 *part, float *lse,
+                                  int *counter, float *rule_l, uint16_t *mb, int n_sess, int L,
+                                  int H, int Hq, int D, int N, int64_t n_slots, int n_tiles,
+                                  bool fused, int32_t *status, cudaStream_t s) {
   const int64_t rows_rl = (int64_t)n_sess * L;
   const int64_t n = rows_rl * Hq * D;
-  k_qmem_split<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(M, mb, rows_rl, Hq, D);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   QtcArgs a{};
   a.slot_map = slot_map;
   a.logits = logits;
   a.part = part;
+  a.counter = counter;
+  a.lse = lse;
+  a.rule_l = rule_l;
   a.status = status;
   a.n_sess = n_sess;
   a.L = L;
@@ -478,20 +671,48 @@ cudaError_t launch_qmem_logits_tc(const float *M, const uint16_t *kpool, const i
   uint32_t cols = 32;
   while (cols < (uint32_t)(kNacc * 2 * Hq)) cols <<= 1;
   const int64_t n_items = (int64_t)n_sess * n_tiles * L;
-  const unsigned grid = (unsigned)std::min<int64_t>(n_items, device_sm_count());
-#define KVC_QTC_CASE(GV)                                                                     \
-  if (a.G == GV) {                                                                           \
-    e = cudaFuncSetAttribute(k_qmem_logits_tc<GV>,                                           \
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);        \
-    if (e != cudaSuccess) return e;                                                          \
-    k_qmem_logits_tc<GV><<<grid, kThreads, smem, s>>>(tm_k128, tm_k8, tm_m, a, NS, cols);    \
-    return cudaGetLastError();                                                               \
+  int64_t grid = std::min<int64_t>(n_items, device_sm_count());
+  cudaError_t e = cudaSuccess;
+  // kernel of group size GV and the chosen finish
+  auto launch = [&](auto kern) -> cudaError_t {
+    cudaError_t e2 =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e2 != cudaSuccess) return e2;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(fused ? kThreadsFused : kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    if (fused) {
+      // a CTA's share team waits for rows that other CTAs finish: all of
+      // them must be resident
+      int per_sm = 0;
+      e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreadsFused, smem);
+      if (e2 != cudaSuccess) return e2;
+      if (per_sm < 1) return cudaErrorNotSupported;
+      grid = std::min<int64_t>(grid, (int64_t)per_sm * device_sm_count());
+      e2 = cudaMemsetAsync(counter, 0, (size_t)rows_rl * sizeof(int), s);
+      if (e2 != cudaSuccess) return e2;
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+    }
+    cfg.gridDim = dim3((unsigned)grid);
+    k_qmem_split<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(M, mb, rows_rl, Hq, D);
+    e2 = cudaGetLastError();
+    if (e2 != cudaSuccess) return e2;
+    return cudaLaunchKernelEx(&cfg, kern, tm_k128, tm_k8, tm_m, a, NS, cols);
+  };
+  switch (a.G) {
+    case 2: e = fused ? launch(k_qmem_logits_tc<2, true>) : launch(k_qmem_logits_tc<2, false>); break;
+    case 4: e = fused ? launch(k_qmem_logits_tc<4, true>) : launch(k_qmem_logits_tc<4, false>); break;
+    // G = 8: the epilogue's registers leave no room for the fused finish's
+    // extra warps (352 threads at 254 registers exceed the register file)
+    case 8: e = fused ? cudaErrorNotSupported : launch(k_qmem_logits_tc<8, false>); break;
+    default: return cudaErrorInvalidValue;
   }
-  KVC_QTC_CASE(2)
-  KVC_QTC_CASE(4)
-  KVC_QTC_CASE(8)
-#undef KVC_QTC_CASE
-  return cudaErrorInvalidValue;
+  return e;
 }
 
 }  // namespace kvc

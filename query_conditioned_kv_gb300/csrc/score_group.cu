@@ -158,12 +158,6 @@ __device__ __forceinline__ void lse_merge_g(float &m, float &s, float m2, float 
   m = mn;
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Pass 1 of this warp's 128 columns (blocks) of one row tile for this
 // lane's query row: online (max, Σ2^(z·zs − max)) over the `valid` columns,
 // 64 at a time (two TMEM loads per job).  Column j adds into accumulator

@@ -167,6 +167,12 @@ def test_kernel_choice_is_validated_before_launch(kvc):
                  None, kvc.KERNELS["score_ring"], None) == 2
     assert _call(kvc, "kvc_score_qmem_ex", P, P, P, 0, P, 1, 1, 1, 8, 64, 16, 10, P, 1 << 30,
                  None, kvc.KERNELS["score_cc"], None) == 1
+    # every rule-score kernel is accepted (the shape rule then answers)
+    for name in ("qmem_tc", "qmem_tc_spill", "qmem_cc"):
+        assert _call(kvc, "kvc_score_qmem_ex", P, P, P, 0, P, 1, 1, 2, 9, 64, 16, 10, P,
+                     1 << 30, None, kvc.KERNELS[name], None) == 2
+    assert _call(kvc, "kvc_score_qmem_ex", P, P, P, 0, P, 1, 1, 2, 9, 64, 16, 10, P, 1 << 30,
+                 None, 19, None) == 1
     assert _call(kvc, "kvc_recover_score_ex", P, P, P, 1 << 12, P, 8, P, P, 1, 1, 8, 32, 128,
                  16, P, None, 0, None, kvc.KERNELS["qmem_cc"], None) == 1
     with pytest.raises(ValueError):

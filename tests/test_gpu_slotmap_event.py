@@ -137,13 +137,83 @@ def test_rule_score_gathered_rows(kvc, orc, Hq):
     M = memory_chain(orc, cfg)
     got = _rule_gpu(kvc, cfg, M, kp, sm)
     cc = _rule_gpu(kvc, cfg, M, kp, sm, "cc")
+    spill = _rule_gpu(kvc, cfg, M, kp, sm, "tc_spill")
     kpb = W.bf16_bits(kp)
     for r in range(cfg.n_sess):
         ref = orc.rule_session(M[r], kpb, sm[r], cfg.H, cfg.sentinel)
         dead = sm[r] == cfg.sentinel
         assert np.all(got[r][dead] == -1.0) and np.all(cc[r][dead] == -1.0)
+        assert np.all(spill[r][dead] == -1.0)
         assert_scores_close(got[r][~dead], ref[~dead], "rule (tensor cores)")
         assert_scores_close(cc[r][~dead], ref[~dead], "rule (CUDA cores)")
+        assert_scores_close(spill[r][~dead], ref[~dead], "rule (tensor cores, spilled)")
+
+
+@pytest.mark.parametrize("n_sess,L,N,Hq", [(4, 3, 8192, 32), (1, 2, 51200, 32),
+                                           (2, 2, 4000, 16), (3, 2, 1008, 16),
+                                           (2, 2, 4000, 64)])
+def test_rule_score_every_finish(kvc, orc, n_sess, L, N, Hq):
+    """The three ways to the rule score against the oracle: the tensor-core
+    kernel that forms each layer's share from the logits still in L2 (rows of
+    one (session, layer) counted and their LSEs published inside the kernel),
+    the tensor-core kernel that spills the logits for a second kernel, and the
+    CUDA-core kernel.  Cases: rows spread over several waves of the grid; a
+    row of 200 tiles, more than one wave on a 152-SM part; N not a multiple
+    of 32 (4000, 1008: partial L2 lines are kept, not dropped); 5% of the
+    private positions already dead.  The in-kernel finish repeats bit for
+    bit.  Groups of 8 query heads have no in-kernel finish: naming it is
+    refused before any launch, and the library's own choice is the spilled
+    one."""
+    cfg = small_cfg(H=8, D=128, Hq=Hq, n_sess=n_sess, L=L, N=N,
+                    prefix=256 if N > 2000 else 128)
+    rng = np.random.default_rng(N + Hq)
+    sm = with_prior_redirects(cfg, cfg.slot_maps(), rng)
+    kp = kpool_of(cfg, DEV)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    M = memory_chain(orc, cfg)
+    auto = _rule_gpu(kvc, cfg, M, kp, sm)
+    spill = _rule_gpu(kvc, cfg, M, kp, sm, "tc_spill")
+    cc = _rule_gpu(kvc, cfg, M, kp, sm, "cc")
+    runs = [("spilled", spill), ("CUDA cores", cc)]
+    if Hq // 8 <= 4:
+        fused = _rule_gpu(kvc, cfg, M, kp, sm, "tc")
+        fused2 = _rule_gpu(kvc, cfg, M, kp, sm, "tc")
+        assert np.array_equal(fused.view(np.uint32), fused2.view(np.uint32))
+        assert np.array_equal(auto.view(np.uint32), fused.view(np.uint32))
+        runs.append(("fused", fused))
+    else:
+        with pytest.raises(kvc.KvcError) as ei:
+            _rule_gpu(kvc, cfg, M, kp, sm, "tc")
+        assert ei.value.code == 2
+        assert np.array_equal(auto.view(np.uint32), spill.view(np.uint32))
+    kpb = W.bf16_bits(kp)
+    for r in range(cfg.n_sess):
+        ref = orc.rule_session(M[r], kpb, sm[r], cfg.H, cfg.sentinel)
+        dead = sm[r] == cfg.sentinel
+        for name, got in runs:
+            assert np.all(got[r][dead] == -1.0), name
+            assert_scores_close(got[r][~dead], ref[~dead], f"rule ({name})")
+
+
+def test_rule_score_long_session(kvc, orc):
+    """One session longer than two waves of 256-position tiles, one layer:
+    a row whose items span three turns of every CTA.  The in-kernel finish
+    (the library's choice) against the oracle."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    N = (2 * n_sm + 1) * 256 + 16
+    cfg = small_cfg(H=8, D=128, Hq=32, n_sess=1, L=1, N=N, prefix=256)
+    rng = np.random.default_rng(7)
+    sm = with_prior_redirects(cfg, cfg.slot_maps(), rng)
+    kp = kpool_of(cfg, DEV)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    M = memory_chain(orc, cfg)
+    auto = _rule_gpu(kvc, cfg, M, kp, sm)
+    fused = _rule_gpu(kvc, cfg, M, kp, sm, "tc")
+    assert np.array_equal(auto.view(np.uint32), fused.view(np.uint32))
+    ref = orc.rule_session(M[0], W.bf16_bits(kp), sm[0], cfg.H, cfg.sentinel)
+    dead = sm[0] == cfg.sentinel
+    assert np.all(fused[0][dead] == -1.0)
+    assert_scores_close(fused[0][~dead], ref[~dead], "rule (long session)")
 
 
 def _redirect_case(orc, cfg, rng):
