@@ -27,6 +27,10 @@
 // L2 (k_qmem_rule_sum then adds the layers), so the logits never go to DRAM.
 // The CUDA-core kernel below covers every other shape.
 
+#include <string.h>
+
+#include <type_traits>
+
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -38,33 +42,54 @@ constexpr int kLogitThreads = 256;
 
 // ----------------------------------------------------------- update
 
+// One warp per (session, layer, query head) row; lane takes PER = D/32
+// consecutive elements (one 8- or 4-byte word per token), eight tokens of
+// loads in flight.  The token sum runs in token order per element.
+template <int PER>
 __global__ void __launch_bounds__(256)
 k_qmem_update(float *__restrict__ M, const uint16_t *__restrict__ q,
-              int64_t rows, int D, int T, float decay, float gain,
-              int renorm) {
-  int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  int lane = threadIdx.x & 31;
+              int64_t rows, int T, float decay, float gain, int renorm) {
+  using Word = typename std::conditional<PER == 4, uint2, uint32_t>::type;
+  constexpr int D = 32 * PER;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const int per = D / 32;  // 2 or 4 elements per lane
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint16_t *src = q + row * (int64_t)T * D + lane * per;
-  for (int t = 0; t < T; t++)
-    for (int e = 0; e < per; e++)
-      acc[e] += __uint_as_float((uint32_t)src[(int64_t)t * D + e] << 16);
-  float *m = M + row * D + lane * per;
-  float v[4], n2 = 0.f;
-  for (int e = 0; e < per; e++) {
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; e++) acc[e] = 0.f;
+  const Word *src = reinterpret_cast<const Word *>(q + row * (int64_t)T * D) + lane;
+  auto add = [&](const Word &w) {
+    uint32_t u[PER / 2];
+    memcpy(u, &w, sizeof(w));
+#pragma unroll
+    for (int e = 0; e < PER; e++) acc[e] += (e & 1) ? bf16_hi(u[e >> 1]) : bf16_lo(u[e >> 1]);
+  };
+  int t = 0;
+  for (; t + 8 <= T; t += 8) {
+    Word w[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) w[k] = __ldcs(src + (int64_t)(t + k) * (D / PER));
+#pragma unroll
+    for (int k = 0; k < 8; k++) add(w[k]);
+  }
+  for (; t < T; t++) add(__ldcs(src + (int64_t)t * (D / PER)));
+  float *m = M + row * D + lane * PER;
+  float v[PER], n2 = 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; e++) {
     v[e] = fmaf(decay, m[e], gain * (acc[e] / (float)T));
     n2 = fmaf(v[e], v[e], n2);
   }
   if (renorm) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xFFFFFFFFu, n2, o);
-    float n = sqrtf(n2);
+    const float n = sqrtf(n2);
     if (n > 0.f)
-      for (int e = 0; e < per; e++) v[e] = v[e] / n;
+#pragma unroll
+      for (int e = 0; e < PER; e++) v[e] = v[e] / n;
   }
-  for (int e = 0; e < per; e++) m[e] = v[e];
+#pragma unroll
+  for (int e = 0; e < PER; e++) m[e] = v[e];
 }
 
 // ------------------------------------------------------------ score
@@ -342,9 +367,14 @@ cudaError_t launch_qmem_reduce(const QArgs &a, cudaStream_t s) {
 cudaError_t launch_qmem_update(float *M, const uint16_t *q, int64_t rows,
                                int D, int T, float decay, float gain,
                                int renorm, cudaStream_t s) {
-  int64_t threads = rows * 32;
-  k_qmem_update<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-      M, q, rows, D, T, decay, gain, renorm);
+  const int64_t threads = rows * 32;
+  const unsigned grid = (unsigned)((threads + 255) / 256);
+  if (D == 128)
+    k_qmem_update<4><<<grid, 256, 0, s>>>(M, q, rows, T, decay, gain, renorm);
+  else if (D == 64)
+    k_qmem_update<2><<<grid, 256, 0, s>>>(M, q, rows, T, decay, gain, renorm);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
