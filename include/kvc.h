@@ -82,7 +82,9 @@ typedef enum {
   KVC_ERR_BOUNDS = 7,      /* device: an index or offset was out of range    */
   KVC_ERR_NAN = 8,         /* device: a NaN score reached kvc_select         */
   KVC_ERR_TIMEOUT = 9,     /* device: a bounded wait gave up                 */
-  KVC_ERR_CAPACITY = 10    /* device: the freed-slot list overflowed         */
+  KVC_ERR_CAPACITY = 10,   /* device: the freed-slot list overflowed; host:
+                              more blocks needed at once than repository slots */
+  KVC_ERR_IO = 11          /* host: the repository's backing file failed     */
 } kvc_status;
 
 /* Kernel choice for the entry points that have more than one kernel for the
@@ -404,6 +406,128 @@ kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
                            int64_t n_tok, int32_t budget, const float *rope_tab,
                            kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview, int32_t *n_hits,
                            int32_t *dev_status, cudaStream_t stream);
+
+/* kvc_pack_tiered with only some of the history in host memory (the
+ * repository view below holds the rest in its backing file).  The unit
+ * (l, h, g) — layer, KV head and block g of the history (tokens 32g …
+ * 32g + 31, counted over all sessions) — sits in host slot
+ * s = host_slot[(l·H + h)·(n_tok/32) + g]; its raw K rows are at
+ *   kslots_host + s·slot_elems + t·D   (t < 32),
+ * its V rows likewise from vslots_host.  Only misses read host memory; a
+ * missed unit whose slot is outside [0, n_slots) is recorded as
+ * KVC_ERR_BOUNDS and packed as zeros.
+ *   kslots_host, vslots_host  host bf16, page-locked and mapped (as for
+ *                 kvc_pack_tiered), slot_elems ≥ 32·D apart
+ *   host_slot     device int32 [L][H][n_tok / 32]
+ * Other arguments, outputs and errors as kvc_pack_tiered, plus
+ * KVC_ERR_INVALID_ARG for a NULL host_slot, n_slots < 1 or slot_elems too
+ * small, and KVC_ERR_ALIGN when slot_elems·2 is not a multiple of 16. */
+kvc_status kvc_pack_tiered_slots(const kvc_bf16 *kslots_host, const kvc_bf16 *vslots_host,
+                                 int64_t slot_elems, int32_t n_slots, const int32_t *host_slot,
+                                 const int32_t *kept_prev, const int32_t *kept_count_prev,
+                                 const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
+                                 const int32_t *kept, const int32_t *kept_count, int32_t L,
+                                 int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
+                                 int64_t n_tok, int32_t budget, const float *rope_tab,
+                                 kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview,
+                                 int32_t *n_hits, int32_t *dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Repository view (KVMem, "Tiered movement": a repository view tracks where
+ * each block lives; the execution view holds only the selected blocks;
+ * blocks recalled often prefer host RAM over NVMe; misses move in bulk).
+ * Host code only: no GPU work, no CUDA call.  Not thread-safe: one thread
+ * at a time per repository.
+ *
+ * The unit of placement is what one (layer, KV head) selects: 32 tokens of
+ * raw K and V of one layer and head, one record [2][32][D] bf16 (K rows,
+ * then V rows).  Unit u = (l·H + h)·n_blocks + g.  Every unit put is
+ * written to the backing file (the NVMe tier) at offset u·record_bytes.
+ * Host RAM holds at most n_slots units, in the caller's arena
+ * [n_slots][2][32][D] (page-locked and mapped when kvc_pack_tiered_slots
+ * reads it: pass kslots_host = arena, vslots_host = arena + 32·D,
+ * slot_elems = 2·32·D).  The GPU tier is the previous execution view, which
+ * kvc_pack_tiered_slots reuses by itself.
+ *
+ * Placement: a unit counts one use per step in which its (layer, head) keeps
+ * its block for some session.  When a step needs units that are not in host
+ * RAM, they take free slots first, then the slots of the units with the
+ * fewest uses (ties: the least recently used, then the lowest index) among
+ * those the step does not need; units are immutable once put, so an
+ * eviction writes nothing.  Units read from the file are grouped into runs of
+ * consecutive units (consecutive blocks of one layer and head), one vectored
+ * read per run, the runs spread over io_threads threads.
+ * ---------------------------------------------------------------------- */
+typedef struct kvc_repo kvc_repo;
+
+typedef struct {
+  int64_t steps;          /* kvc_repo_step calls                              */
+  int64_t needed;         /* units needed from host RAM, summed over steps     */
+  int64_t host_hits;      /* of those, already in host RAM                     */
+  int64_t fetched;        /* read from the backing file                        */
+  int64_t read_calls;     /* vectored reads issued for them                    */
+  int64_t bytes_read;
+  int64_t evictions;      /* host slots taken from another block               */
+  int64_t bytes_written;  /* by kvc_repo_put                                   */
+} kvc_repo_stats;
+
+/* flags of kvc_repo_create: read and write the backing file around the
+ * operating system's page cache (O_DIRECT), so that reads come from the
+ * device; the arena must then be 4096-byte aligned (page-locked allocations
+ * are), and file systems without direct I/O refuse the file (KVC_ERR_IO). */
+#define KVC_REPO_DIRECT_IO 1
+
+/* Creates (or truncates) the backing file at `path`, sized for L·H·n_blocks
+ * records.  arena: host memory for n_slots records, owned by the caller and
+ * kept alive until kvc_repo_destroy.  io_threads in [1, 64].  Errors:
+ * KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D ∉ {64, 128}), KVC_ERR_ALIGN (direct
+ * I/O with an arena not 4096-byte aligned), KVC_ERR_IO. */
+kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_t H, int32_t D,
+                           int32_t n_slots, kvc_bf16 *arena, int32_t io_threads, int32_t flags,
+                           kvc_repo **out);
+
+/* Puts blocks b0 … b0 + nb − 1 of every layer and head, taken from host
+ * bf16 [L][H][n_tok][D] arrays (block g = tokens 32g … 32g + 31): each unit
+ * is written to the backing file and, while free slots remain, kept in host
+ * RAM (layer-major, then head, then block).  Putting a unit again overwrites
+ * it.  Errors: KVC_ERR_INVALID_ARG (range outside the history or the
+ * repository), KVC_ERR_IO. */
+kvc_status kvc_repo_put(kvc_repo *repo, int64_t b0, int64_t nb, const kvc_bf16 *kraw,
+                        const kvc_bf16 *vraw, int64_t n_tok);
+
+/* The units one step uses and the ones it misses, from its kept lists and
+ * the previous step's (host int32 copies of kvc_select's outputs for the L
+ * packed layers, [L][H][n_sess][budget] and [L][H][n_sess]; kept_prev NULL
+ * on the first step): kept index kb of (l, h, r) is unit
+ * (l·H + h)·n_blocks + tok_off[r]/32 + kb.  used: every kept unit; need: the
+ * kept units whose (l, h, r) did not keep them last step (the reads
+ * kvc_pack_tiered_slots makes from host memory).  Both come out sorted and
+ * unique; each array holds L·H·n_blocks entries.  Errors:
+ * KVC_ERR_INVALID_ARG, KVC_ERR_BOUNDS (a kept index outside its session). */
+kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
+                         const int32_t *kept_prev, const int32_t *kept_count_prev, int32_t L,
+                         int32_t H, int32_t n_sess, int32_t budget, const int64_t *tok_off,
+                         int64_t n_blocks, int64_t *used, int64_t *n_used, int64_t *need,
+                         int64_t *n_need);
+
+/* One step: counts a use of every unit in `used`, brings every unit of
+ * `need` into host RAM (reading the missing ones from the backing file) and
+ * writes host_slot[u] (host int32 [L·H·n_blocks]) = the slot of unit u, or
+ * −1.  Every unit of `need` must have been put.  Errors: KVC_ERR_INVALID_ARG
+ * (an index out of range or never put), KVC_ERR_CAPACITY (more units in
+ * `need` than slots), KVC_ERR_IO; after an error the step's slot table is
+ * not written. */
+kvc_status kvc_repo_step(kvc_repo *repo, const int64_t *used, int64_t n_used,
+                         const int64_t *need, int64_t n_need, int32_t *host_slot);
+
+/* Where unit u lives: 0 not put, 1 host RAM (and the file), 2 the file only;
+ * −1 for a bad handle or index. */
+int32_t kvc_repo_where(const kvc_repo *repo, int64_t u);
+
+kvc_status kvc_repo_get_stats(const kvc_repo *repo, kvc_repo_stats *out);
+
+/* Closes the backing file (which stays on disk) and frees the repository. */
+void kvc_repo_destroy(kvc_repo *repo);
 
 /* ------------------------------------------------------------------------
  * Dead slot (IntentKV §2 "Layout", §4 check 3): writes K = bf16(−1e4) =

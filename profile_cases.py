@@ -17,6 +17,7 @@ event once to produce realistic inputs for the stage, then launches the stage
   python profile_cases.py paged  --sessions 4 --iters 3
   python profile_cases.py tiered --layers 8 --iters 2
   python profile_cases.py confidence --iters 3
+  python profile_cases.py repo   --layers 8 --slots 1024 --iters 3 --path /tmp/kvc_repo.bin
 
 event_timing times a whole Mean-K event (score → select → pack, one CUDA
 graph) on a full workload — tiny, 8b, 27b or ragged — with L2 flushed
@@ -28,7 +29,12 @@ compression operation at the Table 1 shapes (6K → 4K tokens per request,
 36 layers) on `--sessions` requests: score → LRFU → select → plan →
 compaction, `--iters` times.  The tiered case runs `--iters` pairs of agent
 steps of the host-resident 8B-class event reduced to `--layers` layers; the
-confidence case runs the confidence monitor on its bench workload.
+confidence case runs the confidence monitor on its bench workload.  The repo
+case runs `--iters` pairs of steps of the same event with the raw history of
+the packed layers in a repository (a backing file at `--path`, direct I/O
+where the file system allows it, `--slots` blocks in host RAM) and prints
+one JSON line per step: time, units (layer, head, block) used and missed,
+units read from the file and their rate.
 """
 from __future__ import annotations
 
@@ -40,11 +46,13 @@ import sys
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem",
-                                     "event_timing", "paged", "tiered", "confidence"])
+                                     "event_timing", "paged", "tiered", "confidence", "repo"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sessions", type=int, default=8)
     ap.add_argument("--config", choices=["tiny", "8b", "27b", "ragged"], default="8b")
+    ap.add_argument("--slots", type=int, default=1024)
+    ap.add_argument("--path", default="/tmp/kvc_repo.bin")
     ap.add_argument("--kernel", default="auto",
                     help="scorer to run (a kvc_kernel name: score_fused, score_ring, "
                          "qmem_cc, recover_cc, ...); default: the library's choice")
@@ -73,6 +81,9 @@ def main(argv=None) -> None:
         return
     if args.case == "confidence":
         _confidence_case(args, dev)
+        return
+    if args.case == "repo":
+        _repo_case(args, dev)
         return
     base = {"8b": W.config_8b, "27b": W.config_27b, "tiny": W.config_tiny,
             "ragged": W.config_ragged}[args.config]()
@@ -272,6 +283,63 @@ def _tiered_case(args, dev):
     print(f"tiered: {2 * args.iters} steps on {cfg.L} layers, status {st}")
     if st != 0:
         raise SystemExit(1)
+
+
+def _repo_case(args, dev):
+    import json
+    import time
+
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import RepoTieredEvent
+
+    cfg = W.scaled(W.config_8b(), L=args.layers)
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = cfg.meank_direct(dev)
+    kvc.kvc_build_meank(kraw, meank, cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    meank_h, kraw_h, vraw_h = (t.cpu().pin_memory() for t in (meank, kraw, vraw))
+    del kraw, vraw, meank
+    n_blocks = cfg.n_tok // 32
+    direct = True
+    try:
+        repo = kvc.KvcRepo(args.path, n_blocks, cfg.lp, cfg.H, cfg.D, args.slots,
+                           io_threads=8, direct=True)
+    except kvc.KvcError:
+        direct = False
+        repo = kvc.KvcRepo(args.path, n_blocks, cfg.lp, cfg.H, cfg.D, args.slots, io_threads=8)
+    t0 = time.time()
+    repo.put(0, n_blocks, kraw_h, vraw_h, cfg.n_tok)
+    put_s = time.time() - t0
+    del kraw_h, vraw_h
+    qs = [cfg.q(dev, step=0), cfg.q(dev, step=1)]
+    ev = RepoTieredEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+                         cfg.n_recent, theta=cfg.theta, device=dev, stage_layers=4, repo=repo)
+    rec = repo.slot_elems * 2
+    print(json.dumps({"repo": {"blocks": n_blocks, "record_bytes": rec, "slots": args.slots,
+                               "units": repo.n_units, "file_bytes": repo.n_units * rec,
+                               "direct_io": direct,
+                               "put_s": round(put_s, 2)}}))
+    for i in range(2 * args.iters):
+        before = repo.stats()
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        ev.step(qs[i % 2], meank_h)
+        torch.cuda.synchronize(dev)
+        ms = (time.perf_counter() - t) * 1e3
+        after = repo.stats()
+        fetched = after["fetched"] - before["fetched"]
+        read = after["bytes_read"] - before["bytes_read"]
+        print(json.dumps({"step": i, "ms": round(ms, 2), "used": ev.last_plan[0],
+                          "missed": ev.last_plan[1], "read_from_file": fetched,
+                          "read_calls": after["read_calls"] - before["read_calls"],
+                          "file_GBps": round(read / (ms * 1e-3) / 1e9, 2) if read else 0.0}))
+    st = kvc.kvc_device_status(ev.dev_status)
+    repo.close()
+    os.remove(args.path)
+    if st != 0:
+        raise SystemExit(f"device status {st}")
 
 
 def _confidence_case(args, dev):

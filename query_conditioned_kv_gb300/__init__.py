@@ -29,6 +29,7 @@ __all__ = [
     "kvc_recover_tensor_core", "kvc_tail_plan", "kvc_tail_compact",
     "kvc_lrfu_update", "kvc_token_confidence", "kvc_conf_trend_budget",
     "TAIL_MAX_TOKENS",
+    "kvc_pack_tiered_slots", "kvc_repo_plan", "KvcRepo",
 ]
 
 BLOCK_TOKENS = 32
@@ -94,6 +95,18 @@ _SIGS = {
                                    _I64, _I32, _P, _P, _P, _P, _P]),
     "kvc_pack_tiered": (_c.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P,
                                    _I32, _I64, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "kvc_pack_tiered_slots": (_c.c_int, [_P, _P, _I64, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                         _I32, _I32, _I32, _P, _I32, _I64, _I32, _P, _P, _P,
+                                         _P, _P, _P, _P]),
+    "kvc_repo_create": (_c.c_int, [_c.c_char_p, _I64, _I32, _I32, _I32, _I32, _P, _I32, _I32,
+                                   _c.POINTER(_c.c_void_p)]),
+    "kvc_repo_put": (_c.c_int, [_P, _I64, _I64, _P, _P, _I64]),
+    "kvc_repo_plan": (_c.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _I64, _P, _P,
+                                 _P, _P]),
+    "kvc_repo_step": (_c.c_int, [_P, _P, _I64, _P, _I64, _P]),
+    "kvc_repo_where": (_I32, [_P, _I64]),
+    "kvc_repo_get_stats": (_c.c_int, [_P, _P]),
+    "kvc_repo_destroy": (None, [_P]),
     "kvc_init_sentinel": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _I32,
                                      _P]),
     "kvc_redirect_free_workspace_size": (_SZ, [_I32, _I32, _I64]),
@@ -302,6 +315,128 @@ def kvc_pack_tiered(kraw_host, vraw_host, kept_prev, kept_count_prev, kcache_pre
                             n_tok, budget, _ptr(rope_tab), _ptr(kcache), _ptr(kview),
                             _ptr(vview), _ptr(n_hits), _ptr(dev_status), _stream(stream)),
         "kvc_pack_tiered")
+
+
+def kvc_pack_tiered_slots(kslots_host, vslots_host, slot_elems, n_slots, host_slot, kept_prev,
+                          kept_count_prev, kcache_prev, vview_prev, kept, kept_count, L, H, D,
+                          tok_off, n_sess, n_tok, budget, rope_tab, kcache, kview, vview,
+                          n_hits=None, dev_status=None, stream=None):
+    _ok(lib.kvc_pack_tiered_slots(_host_ptr(kslots_host), _host_ptr(vslots_host), slot_elems,
+                                  n_slots, _ptr(host_slot), _ptr(kept_prev),
+                                  _ptr(kept_count_prev), _ptr(kcache_prev), _ptr(vview_prev),
+                                  _ptr(kept), _ptr(kept_count), L, H, D, _ptr(tok_off), n_sess,
+                                  n_tok, budget, _ptr(rope_tab), _ptr(kcache), _ptr(kview),
+                                  _ptr(vview), _ptr(n_hits), _ptr(dev_status), _stream(stream)),
+        "kvc_pack_tiered_slots")
+
+
+def _np_ptr(a, dtype):
+    """Address of a C-contiguous host array of the given dtype (None → NULL)."""
+    import numpy as np
+    if a is None:
+        return None
+    if hasattr(a, "is_cuda"):  # a CPU torch tensor
+        if a.is_cuda or not a.is_contiguous():
+            raise ValueError("expected a contiguous host tensor")
+        return a.data_ptr()
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags.c_contiguous:
+        raise ValueError(f"expected a C-contiguous numpy array of {np.dtype(dtype).name}")
+    return a.ctypes.data
+
+
+def kvc_repo_plan(kept, kept_count, kept_prev, kept_count_prev, L, H, n_sess, budget, tok_off,
+                  n_blocks):
+    """(used, need): sorted int64 unit indices (l·H + h)·n_blocks + g of one
+    step (host arrays in)."""
+    import numpy as np
+    used = np.empty(L * H * n_blocks, np.int64)
+    need = np.empty(L * H * n_blocks, np.int64)
+    nu, nn = _c.c_int64(0), _c.c_int64(0)
+    _ok(lib.kvc_repo_plan(_np_ptr(kept, np.int32), _np_ptr(kept_count, np.int32),
+                          _np_ptr(kept_prev, np.int32), _np_ptr(kept_count_prev, np.int32),
+                          L, H, n_sess, budget, _np_ptr(tok_off, np.int64), n_blocks,
+                          used.ctypes.data, _c.addressof(nu), need.ctypes.data,
+                          _c.addressof(nn)), "kvc_repo_plan")
+    return used[:nu.value].copy(), need[:nn.value].copy()
+
+
+class _RepoStats(_c.Structure):
+    _fields_ = [(n, _c.c_int64) for n in ("steps", "needed", "host_hits", "fetched",
+                                          "read_calls", "bytes_read", "evictions",
+                                          "bytes_written")]
+
+
+class KvcRepo:
+    """The repository view (kvc_repo_*): units (layer, KV head, 32-token
+    block) of raw K/V in a backing file, up to n_slots of them in a host arena
+    [n_slots][2][32][D] (pinned when a GPU is present, so
+    kvc_pack_tiered_slots can read it)."""
+
+    def __init__(self, path, n_blocks, L, H, D, n_slots, io_threads=4, direct=False):
+        import numpy as np
+        import torch
+        self.n_blocks, self.L, self.H, self.D, self.n_slots = n_blocks, L, H, D, n_slots
+        self.n_units = L * H * n_blocks
+        self.half = 32 * D
+        self.slot_elems = 2 * self.half
+        if torch.cuda.is_available():
+            # 4096-byte aligned (direct I/O needs it; the pinned allocator
+            # does not promise it)
+            raw = torch.empty(n_slots * self.slot_elems + 2048, dtype=torch.bfloat16,
+                              pin_memory=True)
+            off = (-raw.data_ptr() % 4096) // 2
+            self._raw = raw
+            self.arena = raw[off:off + n_slots * self.slot_elems]
+            base = self.arena.data_ptr()
+        else:  # host-only use: a 4096-byte-aligned numpy buffer
+            raw = np.empty(n_slots * self.slot_elems + 2048, np.uint16)
+            off = (-raw.ctypes.data % 4096) // 2
+            self._raw = raw
+            self.arena = raw[off:off + n_slots * self.slot_elems]
+            base = self.arena.ctypes.data
+        self._h = _c.c_void_p()
+        _ok(lib.kvc_repo_create(str(path).encode(), n_blocks, L, H, D, n_slots, base,
+                                io_threads, 1 if direct else 0, _c.byref(self._h)),
+            "kvc_repo_create")
+        self.host_slot = np.full(self.n_units, -1, np.int32)
+
+    def put(self, b0, nb, kraw, vraw, n_tok):
+        """Blocks b0 … b0+nb−1 from host [L][H][n_tok][D] bf16 arrays."""
+        import numpy as np
+        _ok(lib.kvc_repo_put(self._h, b0, nb, _np_ptr(kraw, np.uint16),
+                             _np_ptr(vraw, np.uint16), n_tok), "kvc_repo_put")
+
+    def step(self, used, need):
+        """Brings `need` into host slots; returns the slot of every unit (−1: file only)."""
+        import numpy as np
+        used = np.ascontiguousarray(used, np.int64)
+        need = np.ascontiguousarray(need, np.int64)
+        _ok(lib.kvc_repo_step(self._h, used.ctypes.data, len(used), need.ctypes.data,
+                              len(need), self.host_slot.ctypes.data), "kvc_repo_step")
+        return self.host_slot
+
+    def where(self, g) -> int:
+        return int(lib.kvc_repo_where(self._h, g))
+
+    def stats(self) -> dict:
+        st = _RepoStats()
+        _ok(lib.kvc_repo_get_stats(self._h, _c.addressof(st)), "kvc_repo_get_stats")
+        return {n: int(getattr(st, n)) for n, _ in _RepoStats._fields_}
+
+    def slots(self):
+        """(kslots, vslots): the arena's K and V bases for kvc_pack_tiered_slots."""
+        return self.arena, self.arena[self.half:]
+
+    def close(self):
+        if self._h:
+            lib.kvc_repo_destroy(self._h)
+            self._h = _c.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def kvc_init_sentinel(kpool, vpool, L, H, D, n_slots, sentinel, stream=None):

@@ -88,7 +88,10 @@ const char *kvc_status_string(kvc_status s) {
     case KVC_ERR_BOUNDS: return "device: index or offset out of range";
     case KVC_ERR_NAN: return "device: NaN score";
     case KVC_ERR_TIMEOUT: return "device: bounded wait timed out";
-    case KVC_ERR_CAPACITY: return "device: freed-slot list overflowed its capacity";
+    case KVC_ERR_CAPACITY:
+      return "capacity exceeded (device: the freed-slot list; host: more blocks needed at once "
+             "than repository slots)";
+    case KVC_ERR_IO: return "host: reading or writing the repository's backing file failed";
   }
   return "unknown status";
 }
@@ -254,14 +257,18 @@ kvc_status kvc_pack_rerope(const kvc_bf16 *kraw, const kvc_bf16 *vraw,
                                            dev_status, stream));
 }
 
-kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
-                           const int32_t *kept_prev, const int32_t *kept_count_prev,
-                           const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
-                           const int32_t *kept, const int32_t *kept_count, int32_t L,
-                           int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
-                           int64_t n_tok, int32_t budget, const float *rope_tab,
-                           kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview, int32_t *n_hits,
-                           int32_t *dev_status, cudaStream_t stream) {
+namespace {
+
+// Shared checks and launch of kvc_pack_tiered / kvc_pack_tiered_slots.
+kvc_status pack_tiered_common(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
+                              const int32_t *host_slot, int64_t slot_elems, int32_t n_slots,
+                              const int32_t *kept_prev, const int32_t *kept_count_prev,
+                              const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
+                              const int32_t *kept, const int32_t *kept_count, int32_t L,
+                              int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
+                              int64_t n_tok, int32_t budget, const float *rope_tab,
+                              kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview,
+                              int32_t *n_hits, int32_t *dev_status, cudaStream_t stream) {
   if (!kraw_host || !vraw_host || !kept || !kept_count || !tok_off || !rope_tab || !kcache ||
       !kview || !vview)
     return KVC_ERR_INVALID_ARG;
@@ -270,9 +277,12 @@ kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
   if (budget < 1 || budget > 65535) return KVC_ERR_BUDGET;
   if (!head_dim_ok(D) || n_tok % KVC_BLOCK_TOKENS || (int64_t)L * n_sess > 65535)
     return KVC_ERR_SHAPE;
+  if (host_slot && (n_slots < 1 || slot_elems < (int64_t)KVC_BLOCK_TOKENS * D))
+    return KVC_ERR_INVALID_ARG;
   if (!aligned16(kraw_host) || !aligned16(vraw_host) || !aligned16(rope_tab) ||
       !aligned16(kcache) || !aligned16(kview) || !aligned16(vview) ||
-      (kcache_prev && !aligned16(kcache_prev)) || (vview_prev && !aligned16(vview_prev)))
+      (kcache_prev && !aligned16(kcache_prev)) || (vview_prev && !aligned16(vview_prev)) ||
+      (host_slot && (slot_elems * 2) % 16))
     return KVC_ERR_ALIGN;
   // the host history must be page-locked and mapped: use its device-side address
   void *kdev = nullptr, *vdev = nullptr;
@@ -281,12 +291,43 @@ kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
     cudaGetLastError();  // clear the query's error
     return KVC_ERR_INVALID_ARG;
   }
-  kraw_host = static_cast<const kvc_bf16 *>(kdev);
-  vraw_host = static_cast<const kvc_bf16 *>(vdev);
-  return from_cuda(kvc::launch_pack_tiered(kraw_host, vraw_host, kept_prev, kept_count_prev,
-                                           kcache_prev, vview_prev, kept, kept_count, L, H, D,
-                                           tok_off, n_sess, n_tok, budget, rope_tab, kcache,
-                                           kview, vview, n_hits, dev_status, stream));
+  return from_cuda(kvc::launch_pack_tiered(
+      static_cast<const kvc_bf16 *>(kdev), static_cast<const kvc_bf16 *>(vdev), host_slot,
+      slot_elems, n_slots, kept_prev, kept_count_prev, kcache_prev, vview_prev, kept,
+      kept_count, L, H, D, tok_off, n_sess, n_tok, budget, rope_tab, kcache, kview, vview,
+      n_hits, dev_status, stream));
+}
+
+}  // namespace
+
+kvc_status kvc_pack_tiered(const kvc_bf16 *kraw_host, const kvc_bf16 *vraw_host,
+                           const int32_t *kept_prev, const int32_t *kept_count_prev,
+                           const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
+                           const int32_t *kept, const int32_t *kept_count, int32_t L,
+                           int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
+                           int64_t n_tok, int32_t budget, const float *rope_tab,
+                           kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview, int32_t *n_hits,
+                           int32_t *dev_status, cudaStream_t stream) {
+  return pack_tiered_common(kraw_host, vraw_host, nullptr, 0, 0, kept_prev, kept_count_prev,
+                            kcache_prev, vview_prev, kept, kept_count, L, H, D, tok_off, n_sess,
+                            n_tok, budget, rope_tab, kcache, kview, vview, n_hits, dev_status,
+                            stream);
+}
+
+kvc_status kvc_pack_tiered_slots(const kvc_bf16 *kslots_host, const kvc_bf16 *vslots_host,
+                                 int64_t slot_elems, int32_t n_slots, const int32_t *host_slot,
+                                 const int32_t *kept_prev, const int32_t *kept_count_prev,
+                                 const kvc_bf16 *kcache_prev, const kvc_bf16 *vview_prev,
+                                 const int32_t *kept, const int32_t *kept_count, int32_t L,
+                                 int32_t H, int32_t D, const int64_t *tok_off, int32_t n_sess,
+                                 int64_t n_tok, int32_t budget, const float *rope_tab,
+                                 kvc_bf16 *kcache, kvc_bf16 *kview, kvc_bf16 *vview,
+                                 int32_t *n_hits, int32_t *dev_status, cudaStream_t stream) {
+  if (!host_slot) return KVC_ERR_INVALID_ARG;
+  return pack_tiered_common(kslots_host, vslots_host, host_slot, slot_elems, n_slots, kept_prev,
+                            kept_count_prev, kcache_prev, vview_prev, kept, kept_count, L, H, D,
+                            tok_off, n_sess, n_tok, budget, rope_tab, kcache, kview, vview,
+                            n_hits, dev_status, stream);
 }
 
 kvc_status kvc_init_sentinel(kvc_bf16 *kpool, kvc_bf16 *vpool, int32_t L,

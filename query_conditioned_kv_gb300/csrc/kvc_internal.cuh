@@ -144,7 +144,10 @@ cudaError_t launch_pack_rerope(const uint16_t *kraw, const uint16_t *vraw,
                                uint16_t *vview, int32_t *status,
                                cudaStream_t s);
 
+// host_slot: NULL (the history is [L][H][n_tok][D] in host memory) or the
+// slot of each block in host slot arenas (slot_elems apart, n_slots slots).
 cudaError_t launch_pack_tiered(const uint16_t *kraw_host, const uint16_t *vraw_host,
+                               const int32_t *host_slot, int64_t slot_elems, int32_t n_slots,
                                const int32_t *kept_prev, const int32_t *kept_count_prev,
                                const uint16_t *kcache_prev, const uint16_t *vview_prev,
                                const int32_t *kept, const int32_t *kept_count, int L, int H,

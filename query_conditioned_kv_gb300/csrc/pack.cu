@@ -138,7 +138,11 @@ k_pack_rerope(PackArgs a) {
 // ------------------------------------------------------------ tiered
 
 struct TieredArgs {
-  const uint16_t *kraw_host, *vraw_host;     // [L][H][n_tok][D], host memory
+  const uint16_t *kraw_host, *vraw_host;     // [L][H][n_tok][D], host memory; with
+                                             // host_slot: slot arenas, see below
+  const int32_t *host_slot;  // NULL, or [L][H][n_tok / 32]: host slot of each unit
+  int64_t slot_elems;        // elements from one slot to the next
+  int32_t n_slots;
   const int32_t *kept_prev, *kept_count_prev;
   const uint16_t *kcache_prev, *vview_prev;  // [L][H][n_sess][32·budget][D]
   const int32_t *kept, *kept_count;
@@ -168,6 +172,11 @@ __device__ __forceinline__ int find_prev(const int32_t *list, int n, int kb) {
 // previous raw-K cache, its V from the previous V view, both in HBM) or, for
 // a miss, straight from host memory over the CPU–GPU link.  The block's raw
 // K also goes to this step's raw-K cache, so the next step can reuse it.
+// With a slot table, host memory holds only some units (layer, head,
+// block): unit (l, h, g) (g counted over the whole history) sits in slot
+// host_slot[(l·H + h)·(n_tok/32) + g], its K rows at
+// kraw_host + slot·slot_elems + t·D (V likewise); a unit without a slot is
+// recorded as KVC_ERR_BOUNDS and packed as zeros.
 template <int D>
 __global__ void __launch_bounds__(2 * D)
 k_pack_tiered(TieredArgs a) {
@@ -233,6 +242,22 @@ k_pack_tiered(TieredArgs a) {
       const int64_t src = (row0 + (int64_t)ip * kBlock + tok) * D;
       ksrc = a.kcache_prev + src;
       vsrc = a.vview_prev + src;
+    } else if (a.host_slot) {
+      const int32_t sl =
+          __ldg(a.host_slot + ((int64_t)l * a.H + h) * (a.n_tok / kBlock) + t0 / kBlock + kb);
+      if (sl < 0 || sl >= a.n_slots) {
+        if (threadIdx.x == 0) record_error(a.status, KVC_ERR_BOUNDS);
+        st_stream(a.kview + dst + 8 * c, zero);
+        st_stream(a.kview + dst + HALF + 8 * c, zero);
+        st_stream(a.vview + dst + 8 * c, zero);
+        st_stream(a.vview + dst + HALF + 8 * c, zero);
+        st_stream(a.kcache + dst + 8 * c, zero);
+        st_stream(a.kcache + dst + HALF + 8 * c, zero);
+        continue;
+      }
+      const int64_t src = (int64_t)sl * a.slot_elems + (int64_t)tok * D;
+      ksrc = a.kraw_host + src;
+      vsrc = a.vraw_host + src;
     } else {
       const int64_t src = (((int64_t)l * a.H + h) * a.n_tok + t0 + (int64_t)kb * kBlock + tok) * D;
       ksrc = a.kraw_host + src;
@@ -257,6 +282,7 @@ k_pack_tiered(TieredArgs a) {
 }  // namespace
 
 cudaError_t launch_pack_tiered(const uint16_t *kraw_host, const uint16_t *vraw_host,
+                               const int32_t *host_slot, int64_t slot_elems, int32_t n_slots,
                                const int32_t *kept_prev, const int32_t *kept_count_prev,
                                const uint16_t *kcache_prev, const uint16_t *vview_prev,
                                const int32_t *kept, const int32_t *kept_count, int L, int H,
@@ -264,10 +290,30 @@ cudaError_t launch_pack_tiered(const uint16_t *kraw_host, const uint16_t *vraw_h
                                int budget, const float *rope_tab, uint16_t *kcache,
                                uint16_t *kview, uint16_t *vview, int32_t *n_hits,
                                int32_t *status, cudaStream_t s) {
-  TieredArgs a{kraw_host, vraw_host, kept_prev, kept_count_prev, kcache_prev, vview_prev,
-               kept,      kept_count, tok_off,  rope_tab,        kcache,      kview,
-               vview,     n_hits,     status,   L,               H,           n_sess,
-               budget,    n_tok};
+  TieredArgs a{};
+  a.kraw_host = kraw_host;
+  a.vraw_host = vraw_host;
+  a.host_slot = host_slot;
+  a.slot_elems = slot_elems;
+  a.n_slots = n_slots;
+  a.kept_prev = kept_prev;
+  a.kept_count_prev = kept_count_prev;
+  a.kcache_prev = kcache_prev;
+  a.vview_prev = vview_prev;
+  a.kept = kept;
+  a.kept_count = kept_count;
+  a.tok_off = tok_off;
+  a.rope_tab = rope_tab;
+  a.kcache = kcache;
+  a.kview = kview;
+  a.vview = vview;
+  a.n_hits = n_hits;
+  a.status = status;
+  a.L = L;
+  a.H = H;
+  a.n_sess = n_sess;
+  a.budget = budget;
+  a.n_tok = n_tok;
   dim3 grid(budget, L * n_sess);
   if (D == 128)
     k_pack_tiered<128><<<grid, 256, 0, s>>>(a);

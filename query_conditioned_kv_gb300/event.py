@@ -26,7 +26,8 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_recover_score_ex,
+from . import (BLOCK_TOKENS, kvc_pack_rerope, kvc_pack_tiered, kvc_pack_tiered_slots,
+               kvc_repo_plan, kvc_recover_score_ex,
                kvc_recover_score_workspace_size, kvc_score_ex, kvc_score_qmem_ex,
                kvc_redirect_free,
                kvc_redirect_free_workspace_size, kvc_rope_table, kvc_score,
@@ -285,6 +286,65 @@ class TieredMeanKEvent(MeanKEvent):
         self.score_tiered(q, meank_host)
         self.select()
         self.pack_tiered(kraw_host, vraw_host)
+        self.cur, self.steps = 1 - cur, self.steps + 1
+
+
+class RepoTieredEvent(TieredMeanKEvent):
+    """KVMem's tiered view with its repository view ("Tiered movement": the
+    repository view tracks where each block lives, blocks recalled often
+    prefer host RAM over NVMe).  The raw history lives in a KvcRepo: every
+    block in its backing file, the most-used ones in host slots.  A step
+    scores and selects as TieredMeanKEvent, copies the packed layers' kept
+    lists to the host, plans the blocks the step uses and the ones it misses
+    (kvc_repo_plan), brings the misses into host slots (kvc_repo_step: one
+    vectored read per run of consecutive blocks) and packs with
+    kvc_pack_tiered_slots, which reuses the previous view on the GPU and reads
+    only the misses from the slots.  The repository holds the L_pack packed
+    layers: repo.L == L_pack, repo.n_blocks == n_tok / 32."""
+
+    def __init__(self, *args, repo, **kw):
+        super().__init__(*args, **kw)
+        if repo.L != self.L_pack or repo.H != self.H or repo.D != self.D or \
+                repo.n_blocks * BLOCK_TOKENS != self.n_tok:
+            raise ValueError("the repository must hold the packed layers of this history")
+        self.repo = repo
+        self.host_slot = torch.empty(repo.n_units, dtype=torch.int32, device=self.device)
+        self.tok_off_host = self.tok_off.cpu().numpy()
+        self.prev_host = None
+        self.last_plan = (0, 0)  # (blocks used, blocks missed) of the last step
+
+    def pack_repo(self):
+        cur, prev = self.cur, 1 - self.cur
+        first = self.steps == 0
+        Lp = self.L_pack
+        kept = self.kept_sets[cur][:Lp].cpu().numpy().reshape(-1)
+        cnt = self.count_sets[cur][:Lp].cpu().numpy().reshape(-1)
+        kp, cp = (None, None) if first else self.prev_host
+        used, need = kvc_repo_plan(kept, cnt, kp, cp, Lp, self.H, self.n_sess, self.budget,
+                                   self.tok_off_host, self.repo.n_blocks)
+        slots = self.repo.step(used, need)
+        self.host_slot.copy_(torch.from_numpy(slots))
+        ks, vs = self.repo.slots()
+        kvc_pack_tiered_slots(ks, vs, self.repo.slot_elems, self.repo.n_slots, self.host_slot,
+                              None if first else self.kept_sets[prev][:Lp],
+                              None if first else self.count_sets[prev][:Lp],
+                              None if first else self.kcaches[prev],
+                              None if first else self.vviews[prev],
+                              self.kept_sets[cur][:Lp], self.count_sets[cur][:Lp], Lp, self.H,
+                              self.D, self.tok_off, self.n_sess, self.n_tok, self.budget,
+                              self.rope_tab, self.kcaches[cur], self.kview, self.vviews[cur],
+                              self.n_hits, self.dev_status)
+        self.prev_host = (kept, cnt)
+        self.last_plan = (len(used), len(need))
+
+    def step(self, q, meank_host):
+        """One agent step; afterwards kview / vview hold this step's view."""
+        cur = self.cur
+        self.kept, self.kept_count = self.kept_sets[cur], self.count_sets[cur]
+        self.vview = self.vviews[cur]
+        self.score_tiered(q, meank_host)
+        self.select()
+        self.pack_repo()
         self.cur, self.steps = 1 - cur, self.steps + 1
 
 

@@ -148,3 +148,84 @@ def test_tiered_full_size_8b(kvc, orc):
             assert np.array_equal(_bits(tie.vviews[cur][l, h, 0]), vv_ref)
             check_rerope_k(_bits(tie.kview[l, h, 0]), kv_ref, raw)
             assert np.array_equal(_bits(tie.kcaches[cur][l, h, 0]), raw)
+
+
+def test_repository_view_matches_tiered(kvc, tmp_path):
+    """KVMem's repository view: the packed layers' raw history in a backing
+    file, one unit per (layer, head, block), with 64 fewer host slots than
+    units (the last layer and head's recent blocks, kept by every step, start
+    out on file only), so units move between the file and host RAM.  Three steps' views, raw-K caches and hit
+    counts bit for bit equal to TieredMeanKEvent's (whole history pinned in
+    host memory); the repository's counters agree with its plans."""
+    from query_conditioned_kv_gb300.event import RepoTieredEvent, TieredMeanKEvent
+    cfg = W.scaled(W.config_8b(), L=4, L_pack=2, hist=[16384, 9216, 32768], budget=48)
+    kraw, vraw = cfg.kv_raw(DEV)
+    meank = cfg.meank_direct(DEV)
+    kvc.kvc_build_meank(kraw, meank, cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    meank_h = meank.cpu().pin_memory()
+    kraw_h, vraw_h = kraw.cpu().pin_memory(), vraw.cpu().pin_memory()
+    n_blocks = cfg.n_tok // 32
+    args = (cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+            cfg.n_recent)
+    kw = dict(L_pack=cfg.lp, theta=cfg.theta, pos0=cfg.pos0, device=DEV)
+    tie = TieredMeanKEvent(*args, stage_layers=2, **kw)
+    n_units = cfg.lp * cfg.H * n_blocks
+    repo = kvc.KvcRepo(tmp_path / "hist.bin", n_blocks, cfg.lp, cfg.H, cfg.D,
+                       n_slots=n_units - 64, io_threads=4)
+    repo.put(0, n_blocks, kraw_h, vraw_h, cfg.n_tok)
+    assert repo.where(n_units - 1) == 2
+    rep = RepoTieredEvent(*args, stage_layers=2, repo=repo, **kw)
+    missed = 0
+    for step in range(3):
+        q = cfg.q(DEV, step=step)
+        cur = tie.cur
+        tie.n_hits.zero_()
+        rep.n_hits.zero_()
+        tie.step(q, meank_h, kraw_h, vraw_h)
+        rep.step(q, meank_h)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_status(tie.dev_status) == 0
+        assert kvc.kvc_device_status(rep.dev_status) == 0
+        assert torch.equal(rep.kept_sets[cur], tie.kept_sets[cur])
+        assert torch.equal(rep.kview, tie.kview)
+        assert torch.equal(rep.vviews[cur], tie.vviews[cur])
+        assert torch.equal(rep.kcaches[cur], tie.kcaches[cur])
+        assert int(rep.n_hits.item()) == int(tie.n_hits.item())
+        n_used, n_need = rep.last_plan
+        assert 0 < n_need <= n_used
+        missed += n_need
+        assert repo.where(n_units - 1) == 1  # a recent block: kept, so in host RAM
+    st = repo.stats()
+    assert st["steps"] == 3 and st["needed"] == missed
+    assert st["fetched"] > 0 and st["evictions"] > 0
+    assert st["bytes_read"] == st["fetched"] * repo.slot_elems * 2
+    repo.close()
+
+
+def test_slots_pack_refuses_a_missing_slot(kvc, tmp_path):
+    """A missed block without a host slot is recorded as KVC_ERR_BOUNDS on
+    the device and packed as zeros, not read from a wrong address."""
+    cfg = W.scaled(W.config_8b(), L=1, L_pack=1, hist=[4096], budget=16)
+    from query_conditioned_kv_gb300.event import MeanKEvent
+    kraw, vraw = cfg.kv_raw(DEV)
+    meank = cfg.meank_direct(DEV)
+    kvc.kvc_build_meank(kraw, meank, cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    args = (cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget, cfg.n_sink,
+            cfg.n_recent)
+    ev = MeanKEvent(*args, L_pack=cfg.lp, theta=cfg.theta, pos0=cfg.pos0, device=DEV)
+    ev.score(cfg.q(DEV), meank)
+    ev.select()
+    n_blocks = cfg.n_tok // 32
+    repo = kvc.KvcRepo(tmp_path / "m.bin", n_blocks, cfg.lp, cfg.H, cfg.D, n_slots=4)
+    slots = torch.full((repo.n_units,), -1, dtype=torch.int32, device=DEV)
+    kcache = torch.empty_like(ev.kview)
+    ev.kview.fill_(1)
+    ks, vs = repo.slots()
+    kvc.kvc_pack_tiered_slots(ks, vs, repo.slot_elems, repo.n_slots, slots, None, None, None,
+                              None, ev.kept, ev.kept_count, cfg.lp, cfg.H, cfg.D, ev.tok_off,
+                              ev.n_sess, ev.n_tok, ev.budget, ev.rope_tab, kcache, ev.kview,
+                              ev.vview, None, ev.dev_status)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_status(ev.dev_status) == 7
+    assert int(ev.kview.abs().max().item()) == 0
+    repo.close()
