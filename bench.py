@@ -18,7 +18,8 @@ and so is ActKV's paged compression operation (LSE-recovery score → select →
 tail plan → in-place compaction) at 1, 4, 16 and 64 requests of 6K → 4K
 tokens (`actkv_event`; `--no-paged` skips it), and KVMem's tiered view with the
 index and raw history in host memory, cold and warm steps (`tiered_event`;
-`--no-tiered` skips it), and ActKV's confidence monitor (`confidence_monitor`;
+`--no-tiered` skips it), and its repository view with the raw history in a
+backing file (`repo_event`; `--no-repo` skips it), and ActKV's confidence monitor (`confidence_monitor`;
 `--no-confidence` skips it).  The 27B-class 1M-token event (64 layers scored, 16
 packed) and the 128-session ragged event are measured the same way as the
 headline, each with its own roofline and a scaled oracle baseline on a seeded
@@ -848,6 +849,84 @@ def tiered_e2e(args, cfg, dev, h_q0, h_mk, h_k, h_v):
 
 # -------------------------------------------------- confidence monitor
 
+REPO_WORKLOAD = ("repo_8b_8layers: the 8b_128k history reduced to 8 layers (scored and "
+                 "packed), its raw K/V in a repository: 262,144 units (layer, KV head, "
+                 "32-token block) of 16 KB in a backing file, 65,536 of them in host slots; "
+                 "two alternating query windows")
+
+
+def repo_event(args, dev, reps: int = 2):
+    """KVMem's repository view: the tiered event with the packed layers' raw
+    history in a backing file (direct I/O where the file system allows it)
+    and only some units in host RAM.  Each step: tiled scoring of the host
+    index, select, the kept lists to the host, the plan, the misses brought
+    into host slots from the file, the tiered pack from the slots.  Wall time
+    per step with a device synchronize on both sides; step 0 is cold."""
+    import os
+    import tempfile
+    import time
+
+    import torch
+    import query_conditioned_kv_gb300 as kvc
+    import workloads as W
+    from query_conditioned_kv_gb300.event import RepoTieredEvent
+
+    cfg = W.scaled(W.config_8b(), L=8)
+    kraw, vraw = cfg.kv_raw(dev)
+    meank = cfg.meank_direct(dev)
+    kvc.kvc_build_meank(kraw, meank, cfg.lp, cfg.H, cfg.D, cfg.n_tok)
+    meank_h, kraw_h, vraw_h = (t.cpu().pin_memory() for t in (meank, kraw, vraw))
+    del kraw, vraw, meank
+    torch.cuda.empty_cache()
+    n_blocks, slots = cfg.n_tok // 32, 65536
+    fd, path = tempfile.mkstemp(prefix="kvc_repo_", suffix=".bin")
+    os.close(fd)
+    try:
+        direct = True
+        try:
+            repo = kvc.KvcRepo(path, n_blocks, cfg.lp, cfg.H, cfg.D, slots, io_threads=8,
+                               direct=True)
+        except kvc.KvcError:
+            direct = False
+            repo = kvc.KvcRepo(path, n_blocks, cfg.lp, cfg.H, cfg.D, slots, io_threads=8)
+        t0 = time.time()
+        repo.put(0, n_blocks, kraw_h, vraw_h, cfg.n_tok)
+        put_s = time.time() - t0
+        del kraw_h, vraw_h
+        qs = [cfg.q(dev, step=0), cfg.q(dev, step=1)]
+        ev = RepoTieredEvent(cfg.L, cfg.H, cfg.Hq, cfg.D, cfg.W, cfg.hist, cfg.budget,
+                             cfg.n_sink, cfg.n_recent, theta=cfg.theta, device=dev,
+                             stage_layers=4, repo=repo)
+        steps = []
+        for i in range(2 * reps):
+            before = repo.stats()
+            torch.cuda.synchronize(dev)
+            t = time.perf_counter()
+            ev.step(qs[i % 2], meank_h)
+            torch.cuda.synchronize(dev)
+            ms = (time.perf_counter() - t) * 1e3
+            after = repo.stats()
+            read = after["bytes_read"] - before["bytes_read"]
+            steps.append({"ms": round(ms, 3), "units_used": ev.last_plan[0],
+                          "units_missed": ev.last_plan[1],
+                          "units_from_file": after["fetched"] - before["fetched"],
+                          "file_reads": after["read_calls"] - before["read_calls"],
+                          "file_gbs": round(read / (ms * 1e-3) / 1e9, 2) if read else 0.0})
+        if kvc.kvc_device_status(ev.dev_status) != 0:
+            raise RuntimeError("device status error in the repository event")
+        rec = repo.slot_elems * 2
+        out = {"workload": REPO_WORKLOAD, "file_bytes": repo.n_units * rec,
+               "record_bytes": rec, "host_slots": slots, "direct_io": direct,
+               "put_s": round(put_s, 2), "tokens_per_step": cfg.n_tok, "steps": steps,
+               "warm_ms": min(x["ms"] for x in steps[2:]) if len(steps) > 2 else None,
+               "note": "wall time per step (host planning and file reads are part of it); "
+                       "step 0 starts with layers 0-1 in host RAM and the rest on file"}
+        repo.close()
+        return out
+    finally:
+        os.remove(path)
+
+
 def confidence_monitor(args, dev, peak, reps: int = 10):
     """ActKV's confidence monitor: token confidence of one decode step (64
     rows of 151936 fp32 logits, top-20) and the trace trend + budget update
@@ -1034,6 +1113,8 @@ def main():
                     help="skip the 128-session ragged event measurement")
     ap.add_argument("--no-slotmap", action="store_true",
                     help="skip the QueryMemory (slot-map) event measurement")
+    ap.add_argument("--no-repo", action="store_true",
+                    help="skip the repository-view measurement (repo_event)")
     ap.add_argument("--no-tiered", action="store_true",
                     help="skip the host-resident (tiered) event measurement")
     ap.add_argument("--no-confidence", action="store_true",
@@ -1075,6 +1156,10 @@ def main():
         import torch
         torch.cuda.empty_cache()
         line["tiered_event"] = tiered_event(args, torch.device("cuda", local_rank), peaks()[0])
+    if not args.no_repo:
+        import torch
+        torch.cuda.empty_cache()
+        line["repo_event"] = repo_event(args, torch.device("cuda", local_rank))
     if not args.no_paged:
         import torch
         torch.cuda.empty_cache()
