@@ -495,8 +495,9 @@ kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_
 kvc_status kvc_repo_put(kvc_repo *repo, int64_t b0, int64_t nb, const kvc_bf16 *kraw,
                         const kvc_bf16 *vraw, int64_t n_tok);
 
-/* The units one step uses and the ones it misses, from its kept lists and
- * the previous step's (host int32 copies of kvc_select's outputs for the L
+/* The units one step uses and the ones it misses (work in proportion to the
+ * kept entries, not to the history), from its kept lists and the previous
+ * step's (host int32 copies of kvc_select's outputs for the L
  * packed layers, [L][H][n_sess][budget] and [L][H][n_sess]; kept_prev NULL
  * on the first step): kept index kb of (l, h, r) is unit
  * (l·H + h)·n_blocks + tok_off[r]/32 + kb.  used: every kept unit; need: the
@@ -511,14 +512,26 @@ kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
                          int64_t *n_need);
 
 /* One step: counts a use of every unit in `used`, brings every unit of
- * `need` into host RAM (reading the missing ones from the backing file) and
- * writes host_slot[u] (host int32 [L·H·n_blocks]) = the slot of unit u, or
- * −1.  Every unit of `need` must have been put.  Errors: KVC_ERR_INVALID_ARG
- * (an index out of range or never put), KVC_ERR_CAPACITY (more units in
- * `need` than slots), KVC_ERR_IO; after an error the step's slot table is
- * not written. */
+ * `need` into host RAM (reading the missing ones from the backing file) and,
+ * if host_slot is not NULL, writes host_slot[u] (host int32 [L·H·n_blocks])
+ * = the slot of unit u, or −1.  The slots that changed are also kept for
+ * kvc_repo_changes, so that a caller holding the table elsewhere (on the
+ * GPU) can update only those entries.  Every unit of `need` must have been
+ * put.  Errors: KVC_ERR_INVALID_ARG (an index out of range or never put),
+ * KVC_ERR_CAPACITY (more units in `need` than slots; nothing changes),
+ * KVC_ERR_IO (the step's evictions stand and its fetched units have no slot,
+ * both listed by kvc_repo_changes; host_slot is not written). */
 kvc_status kvc_repo_step(kvc_repo *repo, const int64_t *used, int64_t n_used,
                          const int64_t *need, int64_t n_need, int32_t *host_slot);
+
+/* The whole slot table now: host_slot[u] (host int32 [L·H·n_blocks]) = the
+ * slot of unit u, or −1 (for a first copy of the table elsewhere). */
+kvc_status kvc_repo_slots(const kvc_repo *repo, int32_t *host_slot);
+
+/* The last kvc_repo_step's slot changes: units[i] now has slot slots[i]
+ * (−1: evicted).  Writes at most cap entries and returns how many there are
+ * (−1 for a bad handle or arguments). */
+int64_t kvc_repo_changes(const kvc_repo *repo, int64_t *units, int32_t *slots, int64_t cap);
 
 /* Where unit u lives: 0 not put, 1 host RAM (and the file), 2 the file only;
  * −1 for a bad handle or index. */

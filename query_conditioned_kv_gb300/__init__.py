@@ -105,6 +105,8 @@ _SIGS = {
                                  _P, _P]),
     "kvc_repo_step": (_c.c_int, [_P, _P, _I64, _P, _I64, _P]),
     "kvc_repo_where": (_I32, [_P, _I64]),
+    "kvc_repo_slots": (_c.c_int, [_P, _P]),
+    "kvc_repo_changes": (_I64, [_P, _P, _P, _I64]),
     "kvc_repo_get_stats": (_c.c_int, [_P, _P]),
     "kvc_repo_destroy": (None, [_P]),
     "kvc_init_sentinel": (_c.c_int, [_P, _P, _I32, _I32, _I32, _I64, _I32,
@@ -406,14 +408,31 @@ class KvcRepo:
         _ok(lib.kvc_repo_put(self._h, b0, nb, _np_ptr(kraw, np.uint16),
                              _np_ptr(vraw, np.uint16), n_tok), "kvc_repo_put")
 
-    def step(self, used, need):
-        """Brings `need` into host slots; returns the slot of every unit (−1: file only)."""
+    def step(self, used, need, table=True):
+        """Brings `need` into host slots.  With `table`, returns the slot of
+        every unit (−1: file only); otherwise None (see changes())."""
         import numpy as np
         used = np.ascontiguousarray(used, np.int64)
         need = np.ascontiguousarray(need, np.int64)
         _ok(lib.kvc_repo_step(self._h, used.ctypes.data, len(used), need.ctypes.data,
-                              len(need), self.host_slot.ctypes.data), "kvc_repo_step")
+                              len(need), self.host_slot.ctypes.data if table else None),
+            "kvc_repo_step")
+        return self.host_slot if table else None
+
+    def slot_table(self):
+        """The slot of every unit now (without taking a step)."""
+        _ok(lib.kvc_repo_slots(self._h, self.host_slot.ctypes.data), "kvc_repo_slots")
         return self.host_slot
+
+    def changes(self):
+        """(units, slots) whose slot the last step changed (−1: evicted)."""
+        import numpy as np
+        n = int(lib.kvc_repo_changes(self._h, None, None, 0))
+        units = np.empty(n, np.int64)
+        slots = np.empty(n, np.int32)
+        if n:
+            lib.kvc_repo_changes(self._h, units.ctypes.data, slots.ctypes.data, n)
+        return units, slots
 
     def where(self, g) -> int:
         return int(lib.kvc_repo_where(self._h, g))

@@ -39,6 +39,8 @@ struct kvc_repo {
   std::vector<int64_t> last;       // unit → last step that kept it
   std::vector<uint8_t> pinned;     // scratch: needed by the current step
   std::vector<int32_t> free_slots;
+  std::vector<int64_t> chg_unit;   // the last step's slot changes: unit …
+  std::vector<int32_t> chg_slot;   // … and its new slot (−1: evicted)
   uint16_t *staging = nullptr;     // one record, 4096-byte aligned
   kvc_repo_stats st{};
 };
@@ -199,8 +201,9 @@ kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
   if (!kept || !kept_count || !tok_off || !used || !n_used || !need || !n_need || L < 1 ||
       H < 1 || n_sess < 1 || budget < 1 || n_blocks < 1 || (kept_prev && !kept_count_prev))
     return KVC_ERR_INVALID_ARG;
-  const int64_t n_units = (int64_t)L * H * n_blocks;
-  std::vector<uint8_t> mu((size_t)n_units, 0), mn((size_t)n_units, 0);
+  // collected per kept entry, then sorted and made unique: the work grows
+  // with the kept lists, not with the history
+  std::vector<int64_t> vu, vn;
   for (int64_t seg = 0; seg < (int64_t)L * H * n_sess; seg++) {
     const int r = (int)(seg % n_sess);
     const int64_t ubase = (seg / n_sess) * n_blocks;  // unit of (l, h, block 0)
@@ -216,23 +219,24 @@ kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
     for (int i = 0; i < cnt; i++) {
       const int kb = list[i];
       if (kb < 0 || kb >= nb) return KVC_ERR_BOUNDS;
-      mu[(size_t)(ubase + g0 + kb)] = 1;
-      if (!prev || find_in(prev, cp, kb) < 0) mn[(size_t)(ubase + g0 + kb)] = 1;
+      vu.push_back(ubase + g0 + kb);
+      if (!prev || find_in(prev, cp, kb) < 0) vn.push_back(ubase + g0 + kb);
     }
   }
-  int64_t nu = 0, nn = 0;
-  for (int64_t u = 0; u < n_units; u++) {
-    if (mu[(size_t)u]) used[nu++] = u;
-    if (mn[(size_t)u]) need[nn++] = u;
+  for (auto *v : {&vu, &vn}) {
+    std::sort(v->begin(), v->end());
+    v->erase(std::unique(v->begin(), v->end()), v->end());
   }
-  *n_used = nu;
-  *n_need = nn;
+  std::copy(vu.begin(), vu.end(), used);
+  std::copy(vn.begin(), vn.end(), need);
+  *n_used = (int64_t)vu.size();
+  *n_need = (int64_t)vn.size();
   return KVC_OK;
 }
 
 kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const int64_t *need,
                          int64_t n_need, int32_t *host_slot) {
-  if (!r || !host_slot || n_used < 0 || n_need < 0 || (n_used && !used) || (n_need && !need))
+  if (!r || n_used < 0 || n_need < 0 || (n_used && !used) || (n_need && !need))
     return KVC_ERR_INVALID_ARG;
   for (int64_t i = 0; i < n_used; i++)
     if (used[i] < 0 || used[i] >= r->n_units) return KVC_ERR_INVALID_ARG;
@@ -254,6 +258,8 @@ kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const
     unpin();
     return KVC_ERR_CAPACITY;
   }
+  r->chg_unit.clear();
+  r->chg_slot.clear();
   r->st.steps++;
   const int64_t step = r->st.steps;
   for (int64_t i = 0; i < n_used; i++) {
@@ -291,8 +297,11 @@ kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const
     std::nth_element(cand.begin(), cand.begin() + (ptrdiff_t)(k - 1), cand.end(), colder);
     for (size_t i = 0; i < k; i++) {
       const int32_t s = cand[i];
-      r->slot_of[(size_t)r->block_in[(size_t)s]] = -1;
+      const int64_t old = r->block_in[(size_t)s];
+      r->slot_of[(size_t)old] = -1;
       r->block_in[(size_t)s] = -1;
+      r->chg_unit.push_back(old);
+      r->chg_slot.push_back(-1);
       r->st.evictions++;
       dest.push_back(s);
     }
@@ -300,6 +309,8 @@ kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const
   for (size_t i = 0; i < fetch.size(); i++) {
     r->slot_of[(size_t)fetch[i]] = dest[i];
     r->block_in[(size_t)dest[i]] = fetch[i];
+    r->chg_unit.push_back(fetch[i]);
+    r->chg_slot.push_back(dest[i]);
   }
 
   // runs of consecutive units (consecutive blocks of one layer and head):
@@ -340,13 +351,33 @@ kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const
       r->block_in[(size_t)s] = -1;
       r->free_slots.push_back(s);
     }
+    // the evictions stand: report them, and the fetched units as slotless
+    for (size_t i = 0; i < r->chg_slot.size(); i++)
+      if (r->chg_slot[i] >= 0) r->chg_slot[i] = -1;
     return KVC_ERR_IO;
   }
   r->st.fetched += (int64_t)fetch.size();
   r->st.read_calls += (int64_t)runs.size();
   r->st.bytes_read += (int64_t)fetch.size() * r->rec_bytes;
+  if (host_slot)
+    for (int64_t u = 0; u < r->n_units; u++) host_slot[u] = r->slot_of[(size_t)u];
+  return KVC_OK;
+}
+
+kvc_status kvc_repo_slots(const kvc_repo *r, int32_t *host_slot) {
+  if (!r || !host_slot) return KVC_ERR_INVALID_ARG;
   for (int64_t u = 0; u < r->n_units; u++) host_slot[u] = r->slot_of[(size_t)u];
   return KVC_OK;
+}
+
+int64_t kvc_repo_changes(const kvc_repo *r, int64_t *units, int32_t *slots, int64_t cap) {
+  if (!r || cap < 0 || (cap > 0 && (!units || !slots))) return -1;
+  const int64_t n = (int64_t)r->chg_unit.size();
+  for (int64_t i = 0; i < std::min(n, cap); i++) {
+    units[i] = r->chg_unit[(size_t)i];
+    slots[i] = r->chg_slot[(size_t)i];
+  }
+  return n;
 }
 
 int32_t kvc_repo_where(const kvc_repo *r, int64_t u) {

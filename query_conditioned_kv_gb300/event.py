@@ -297,7 +297,8 @@ class RepoTieredEvent(TieredMeanKEvent):
     scores and selects as TieredMeanKEvent, copies the packed layers' kept
     lists to the host, plans the blocks the step uses and the ones it misses
     (kvc_repo_plan), brings the misses into host slots (kvc_repo_step: one
-    vectored read per run of consecutive blocks) and packs with
+    vectored read per run of consecutive blocks), applies the slots that
+    changed to the slot table it keeps on the GPU, and packs with
     kvc_pack_tiered_slots, which reuses the previous view on the GPU and reads
     only the misses from the slots.  The repository holds the L_pack packed
     layers: repo.L == L_pack, repo.n_blocks == n_tok / 32."""
@@ -308,7 +309,8 @@ class RepoTieredEvent(TieredMeanKEvent):
                 repo.n_blocks * BLOCK_TOKENS != self.n_tok:
             raise ValueError("the repository must hold the packed layers of this history")
         self.repo = repo
-        self.host_slot = torch.empty(repo.n_units, dtype=torch.int32, device=self.device)
+        # the slot table stays on the GPU; each step applies only its changes
+        self.host_slot = torch.from_numpy(repo.slot_table().copy()).to(self.device)
         self.tok_off_host = self.tok_off.cpu().numpy()
         self.prev_host = None
         self.last_plan = (0, 0)  # (blocks used, blocks missed) of the last step
@@ -322,8 +324,11 @@ class RepoTieredEvent(TieredMeanKEvent):
         kp, cp = (None, None) if first else self.prev_host
         used, need = kvc_repo_plan(kept, cnt, kp, cp, Lp, self.H, self.n_sess, self.budget,
                                    self.tok_off_host, self.repo.n_blocks)
-        slots = self.repo.step(used, need)
-        self.host_slot.copy_(torch.from_numpy(slots))
+        self.repo.step(used, need, table=False)
+        units, slots = self.repo.changes()
+        if len(units):
+            self.host_slot[torch.from_numpy(units).to(self.device)] = \
+                torch.from_numpy(slots).to(self.device)
         ks, vs = self.repo.slots()
         kvc_pack_tiered_slots(ks, vs, self.repo.slot_elems, self.repo.n_slots, self.host_slot,
                               None if first else self.kept_sets[prev][:Lp],

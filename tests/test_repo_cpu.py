@@ -123,6 +123,7 @@ def test_repo_records_and_placement_follow_the_policy(tmp_path):
     assert [repo.where(u) for u in range(n_units)] == [1] * n_slots + [2] * (n_units - n_slots)
     rng = np.random.default_rng(2)
     hot = [3, 17, 30, 100, 200]  # kept in most steps: they should end up holding slots
+    table = repo.slot_table().copy()  # a copy kept up to date from the changes alone
     for step in range(40):
         used = set(rng.choice(n_units, size=6, replace=False).tolist())
         if step % 4:
@@ -132,6 +133,9 @@ def test_repo_records_and_placement_follow_the_policy(tmp_path):
         used = sorted(used)
         repo.step(used, need)
         model.step(used, need)
+        units, slots = repo.changes()
+        table[units] = slots
+        assert np.array_equal(table, repo.host_slot), f"step {step}: changes"
         res = {u for u in range(n_units) if repo.where(u) == 1}
         assert res == model.resident(), f"step {step}"
         assert all(repo.host_slot[g] >= 0 for g in need)
