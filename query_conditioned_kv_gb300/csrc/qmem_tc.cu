@@ -22,9 +22,11 @@
 //    fp32 logits (base 2) and, per 256-position tile, (max, Σ2^(z−max)) per
 //    query head; k_qmem_lse and k_qmem_rule reduce them afterwards, so the
 //    logits go to DRAM and come back (one fp32 per position and query head).
-//  * fused (FUSED = true, groups of 2 or 4): items run tile fastest, so
-//    all tiles of one (session, layer) row are done within about one wave
-//    of the grid.  Three more roles join the kernel.  A publisher warp
+//  * fused (FUSED = true, groups of 2 or 4): items walk blocks of eight
+//    sessions tile by tile (the block's sessions fastest), so the sessions
+//    that share a prefix read each prefix tile back to back (from L2 after
+//    the first) and all tiles of one (session, layer) row are done within
+//    a few waves of the grid.  Three more roles join the kernel.  A publisher warp
 //    counts each item the epilogue finished into its row's counter; the
 //    publisher holding the row's last tile then merges the tile partials
 //    into the row's LSEs and publishes them.  A share team of four warps takes this CTA's items in
@@ -51,6 +53,7 @@ constexpr int kPos = 16;         // positions per MMA tile
 constexpr int kH = 8;            // KV heads: kPos · kH = 128 rows
 constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2–5 epilogue
 constexpr int kThreadsFused = 352;  // + warp 6, the publisher, and warps 7–10, the share team
+constexpr int kSessBlock = 8;    // fused: sessions that walk their tiles together
 constexpr int kMB = 2;           // memory-row buffers
 constexpr int kNacc = 4;         // TMEM accumulators
 
@@ -180,10 +183,24 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
   // than a wave) later.
   auto decode = [&](int64_t item, int &r, int &tile, int &l) {
     if constexpr (FUSED) {
-      tile = (int)(item % a.n_tiles);
-      const int64_t rest = item / a.n_tiles;
-      r = (int)(rest % a.n_sess);
-      l = (int)(rest / a.n_sess);
+      // blocks of kSessBlock sessions (the last one may be smaller), walked
+      // tile by tile with the block's sessions fastest
+      const int64_t per_layer = (int64_t)a.n_sess * a.n_tiles;
+      l = (int)(item / per_layer);
+      const int64_t rem = item % per_layer;
+      const int full = a.n_sess / kSessBlock;
+      const int64_t in_full = (int64_t)full * kSessBlock * a.n_tiles;
+      if (rem < in_full) {
+        const int sb = (int)(rem / ((int64_t)kSessBlock * a.n_tiles));
+        const int q = (int)(rem % ((int64_t)kSessBlock * a.n_tiles));
+        tile = q / kSessBlock;
+        r = sb * kSessBlock + q % kSessBlock;
+      } else {
+        const int rb = a.n_sess - full * kSessBlock;
+        const int q = (int)(rem - in_full);
+        tile = q / rb;
+        r = full * kSessBlock + q % rb;
+      }
     } else {
       r = (int)(item % a.n_sess);
       const int64_t rest = item / a.n_sess;
