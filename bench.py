@@ -496,6 +496,52 @@ SLOTMAP_WORKLOAD = ("slotmap_64x32k: 64 sessions x 32768 positions (4096-positio
                     "4 memory turns of 32 queries, 8192 kept positions per session")
 
 
+def _oracle_slotmap(cfg, kp, sm_np, dev, n_sample: int = 4, seed: int = 11):
+    """The oracle on 4 of the 64 sessions of the slot-map event: rule score
+    over every layer and query head, then select, one thread per session.
+    Inputs from the seeded generators only: the sessions' memories rebuilt
+    with the oracle from the generator's query turns, their K rows gathered
+    by position from the generated pool.  Redirect + free (integer work,
+    negligible next to the score) is not timed."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+    import torch
+    import oracle
+    import workloads as W
+
+    rng = np.random.default_rng(seed)
+    sample = [0] + [int(x) for x in rng.choice(np.arange(1, cfg.n_sess), size=n_sample - 1,
+                                               replace=False)]
+    M_ref = np.zeros((len(sample), cfg.L, cfg.Hq, cfg.D), np.float32)
+    for t in range(cfg.turns):
+        qt = cfg.q_turn(t, dev)
+        M_ref = oracle.qmem_update(M_ref, W.bf16_bits(qt[sample]), cfg.decay, cfg.gain)
+        del qt
+    rows = []
+    for r in sample:
+        slots = torch.from_numpy(sm_np[r].astype(np.int64)).to(dev)
+        rows.append(W.bf16_bits(kp[:, slots]))  # [L][N][H][D], position → row
+        del slots
+    ident = np.arange(cfg.N, dtype=np.int32)
+
+    def one(i):
+        ref = oracle.rule_session(M_ref[i], rows[i], ident, cfg.H, -1)
+        oracle.select(ref, cfg.budget, 0, 0)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=len(sample)) as ex:
+        list(ex.map(one, range(len(sample))))
+    secs = time.perf_counter() - t0
+    frac = len(sample) / cfg.n_sess
+    return {"value": cfg.n_sess * cfg.N * frac / secs, "unit": UNIT, "cores": len(sample),
+            "kind": "oracle", "scaled": True,
+            "sample": f"{len(sample)} of {cfg.n_sess} sessions (sessions {sample}): rule score "
+                      f"over {cfg.L} layers x {cfg.Hq} query heads + select, fp64 C oracle, one "
+                      f"thread per session; {secs:.1f} s wall; tokens scaled by {frac:.4f}; "
+                      "redirect + free not timed"}
+
+
 def slot_map_event(args, dev, peak, reps: int = 3):
     """The QueryMemory-mode event (rule score over the paged K pool → token
     select → redirect + free) on the full 64 x 32768 workload, each stage
@@ -593,7 +639,13 @@ def slot_map_event(args, dev, peak, reps: int = 3):
         "freed_slots": n_freed, "reps": reps,
         "l2": "inputs (135.6 GB of K) far exceed the 129 MB L2; no flush",
     }
-    del kp, ev, M
+    if not args.no_cpu_baseline:
+        del ev, M
+        torch.cuda.empty_cache()
+        out["cpu_baseline"] = _oracle_slotmap(cfg, kp, sm_np, dev)
+        del kp
+    else:
+        del kp, ev, M
     torch.cuda.empty_cache()
     return out
 

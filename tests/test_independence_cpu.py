@@ -46,9 +46,16 @@ def test_benchmark_loads_the_oracle_only_in_its_cpu_legs():
         src = f.read()
     top = [ln for ln in src.splitlines() if re.match(r"(import|from)\s+oracle\b", ln)]
     assert not top  # no module-level import: only inside the CPU-baseline functions
+    # and those functions run only in the CPU-baseline legs (never in a timed region)
+    for fn in ("_oracle_event", "_oracle_slotmap"):
+        callers = [m.start() for m in re.finditer(rf"(?<!def ){fn}\(", src)]
+        for pos in callers:
+            caller = re.findall(r"^def (\w+)", src[:pos], re.M)
+            assert not caller or caller[-1] in (fn, "cpu_baseline", "run_reference",
+                                                 "config_event", "slot_map_event"), caller[-1:]
     for m in re.finditer(r"^\s+(?:import|from)\s+oracle\b", src, re.M):
         fn = re.findall(r"^def (\w+)", src[:m.start()], re.M)[-1]
-        assert fn in ("_oracle_event",), fn
+        assert fn in ("_oracle_event", "_oracle_slotmap"), fn
 
 
 def test_binding_without_its_library_fails_loudly(tmp_path):
