@@ -195,6 +195,36 @@ def test_rule_score_every_finish(kvc, orc, n_sess, L, N, Hq):
             assert_scores_close(got[r][~dead], ref[~dead], f"rule ({name})")
 
 
+@pytest.mark.parametrize("n_sess,L,N,dead_sess", [(2, 1, 48, None), (1, 1, 256, None),
+                                                  (3, 2, 256, 1), (2, 3, 1008, 0)])
+def test_rule_score_fused_edges(kvc, orc, n_sess, L, N, dead_sess):
+    """Edges of the in-kernel finish: a session shorter than one 256-position
+    tile, exactly one tile (one item, one CTA doing every role), and a
+    session whose every position is already dead (its rows have no live
+    position, so their LSE is −inf and every rule is −1).  Against the
+    oracle, and the spilled finish bit for bit on the dead session."""
+    cfg = small_cfg(H=8, D=128, Hq=32, n_sess=n_sess, L=L, N=N, prefix=16, budget=8)
+    rng = np.random.default_rng(N + L)
+    sm = with_prior_redirects(cfg, cfg.slot_maps(), rng)
+    if dead_sess is not None:
+        sm[dead_sess, :] = cfg.sentinel
+    kp = kpool_of(cfg, DEV)
+    kvc.kvc_init_sentinel(kp, None, cfg.L, cfg.H, cfg.D, cfg.n_slots, cfg.sentinel)
+    M = memory_chain(orc, cfg)
+    fused = _rule_gpu(kvc, cfg, M, kp, sm, "tc")
+    spill = _rule_gpu(kvc, cfg, M, kp, sm, "tc_spill")
+    kpb = W.bf16_bits(kp)
+    for r in range(cfg.n_sess):
+        ref = orc.rule_session(M[r], kpb, sm[r], cfg.H, cfg.sentinel)
+        dead = sm[r] == cfg.sentinel
+        assert np.all(fused[r][dead] == -1.0) and np.all(ref[dead] == -1.0)
+        if (~dead).any():
+            assert_scores_close(fused[r][~dead], ref[~dead], f"rule session {r}")
+    if dead_sess is not None:
+        assert np.all(fused[dead_sess] == -1.0)
+        assert np.array_equal(fused[dead_sess], spill[dead_sess])
+
+
 def test_rule_score_long_session(kvc, orc):
     """One session longer than two waves of 256-position tiles, one layer:
     a row whose items span three turns of every CTA.  The in-kernel finish
