@@ -259,3 +259,31 @@ def test_repo_plan_matches_brute_force(first):
     with pytest.raises(kvc.KvcError) as e:
         kvc.kvc_repo_plan(bad, cnt2, None, None, Lp, Hp, n_sess, budget, tok_off, n_blocks)
     assert e.value.code == 7
+
+
+def test_repo_io_error_leaves_a_consistent_table(tmp_path):
+    """A failed file read (the backing file cut short after the put): the
+    step reports KVC_ERR_IO, its evictions stand, its fetched units end up
+    without a slot, changes() lists both, and the repository keeps working
+    for units still in host RAM."""
+    import os
+    n_blocks, n_slots = 16, 8
+    k, v, n_tok = _history(n_blocks, 9)
+    path = tmp_path / "io.bin"
+    repo = kvc.KvcRepo(path, n_blocks, L, H, D, n_slots)
+    repo.put(0, n_blocks, k, v, n_tok)  # units 0..7 hold the slots
+    before = repo.slot_table().copy()
+    os.truncate(path, 0)
+    with pytest.raises(kvc.KvcError) as e:
+        repo.step([20, 21], [20, 21])  # both on file only: reads hit end of file
+    assert e.value.code == 11
+    units, slots = repo.changes()
+    table = before.copy()
+    table[units] = slots
+    assert np.array_equal(table, repo.slot_table())
+    assert repo.where(20) == 2 and repo.where(21) == 2  # still on file, no slot
+    # the two evicted units and the two that failed to arrive, all slotless
+    assert (slots == -1).all() and sorted(units.tolist()) == [0, 1, 20, 21]
+    assert int((repo.slot_table() >= 0).sum()) == n_slots - 2
+    repo.step([3], [3] if repo.where(3) == 1 else [])  # a resident unit still works
+    repo.close()
