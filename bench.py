@@ -813,6 +813,20 @@ def tiered_event(args, dev, peak, reps: int = 3):
             if rep >= args.warmup:
                 rows[k].append([marks[i].elapsed_time(marks[i + 1]) for i in range(3)])
                 hits[k] = int(ev.n_hits.item())
+    # the same steps pipelined (each tile's select and pack under the next
+    # tiles' copies), as TieredMeanKEvent.step runs them by default
+    piped = {"cold": [], "warm": []}
+    for rep in range(args.warmup + reps):
+        ev.steps = 0
+        for k, q in (("cold", qs[0]), ("warm", qs[1])):
+            a, b = ev_pair()
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            ev.step(q, meank_h, kraw_h, vraw_h)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= args.warmup:
+                piped[k].append(a.elapsed_time(b))
     if kvc.kvc_device_status(ev.dev_status) != 0:
         raise RuntimeError("device status error in the tiered event")
     n_units = cfg.lp * cfg.H * cfg.n_sess
@@ -836,6 +850,10 @@ def tiered_event(args, dev, peak, reps: int = 3):
             "score_h2d_gbs": meank_bytes / (sc * 1e-3) / 1e9,
             "score_frac_of_h2d_copy": meank_bytes / (sc * 1e-3) / 1e9 / link_gbs,
             "pack_host_read_gbs": miss * 2 * blk_bytes / (pk * 1e-3) / 1e9,
+            "ms_per_step_pipelined": round(statistics.median(piped[k]), 4),
+            "note": "stages_ms from the stages run one after another; the pipelined "
+                    "step (each index tile's select and pack under the next tiles' "
+                    "copies) is what TieredMeanKEvent.step and e2e run",
         }
     del ev, meank_h, kraw_h, vraw_h
     torch.cuda.empty_cache()

@@ -243,8 +243,11 @@ class TieredMeanKEvent(MeanKEvent):
         self.n_hits = torch.zeros(1, dtype=torch.int32, device=dev)
         self.cur, self.steps = 0, 0
 
-    def score_tiered(self, q, meank_host):
-        """Scores of every layer from the host-resident index [L][H][nb][D]."""
+    def score_tiered(self, q, meank_host, after_tile=None):
+        """Scores of every layer from the host-resident index [L][H][nb][D].
+        `after_tile(l0, l1)`, if given, is called after each tile's score is
+        queued (on the current stream, while the copy stream brings in the
+        next tiles)."""
         main = torch.cuda.current_stream(self.device)
         cs = self.copy_stream
         cs.wait_stream(main)
@@ -264,28 +267,48 @@ class TieredMeanKEvent(MeanKEvent):
                       self.ws, self.dev_status, main)
             free[b] = torch.cuda.Event()
             free[b].record(main)
+            if after_tile is not None:
+                after_tile(l0, l1)
 
-    def pack_tiered(self, kraw_host, vraw_host):
+    def pack_tiered(self, kraw_host, vraw_host, l0=0, l1=None):
+        """The tiered pack of packed layers [l0, l1) (all of them by default)."""
+        l1 = self.L_pack if l1 is None else min(l1, self.L_pack)
+        if l1 <= l0:
+            return
         cur, prev = self.cur, 1 - self.cur
         first = self.steps == 0
-        kvc_pack_tiered(kraw_host, vraw_host,
-                        None if first else self.kept_sets[prev][:self.L_pack],
-                        None if first else self.count_sets[prev][:self.L_pack],
-                        None if first else self.kcaches[prev],
-                        None if first else self.vviews[prev],
-                        self.kept_sets[cur][:self.L_pack], self.count_sets[cur][:self.L_pack],
-                        self.L_pack, self.H, self.D, self.tok_off, self.n_sess, self.n_tok,
-                        self.budget, self.rope_tab, self.kcaches[cur], self.kview,
-                        self.vviews[cur], self.n_hits, self.dev_status)
+        sl = slice(l0, l1)
+        kvc_pack_tiered(kraw_host[sl], vraw_host[sl],
+                        None if first else self.kept_sets[prev][sl],
+                        None if first else self.count_sets[prev][sl],
+                        None if first else self.kcaches[prev][sl],
+                        None if first else self.vviews[prev][sl],
+                        self.kept_sets[cur][sl], self.count_sets[cur][sl],
+                        l1 - l0, self.H, self.D, self.tok_off, self.n_sess, self.n_tok,
+                        self.budget, self.rope_tab, self.kcaches[cur][sl], self.kview[sl],
+                        self.vviews[cur][sl], self.n_hits, self.dev_status)
 
-    def step(self, q, meank_host, kraw_host, vraw_host):
-        """One agent step; afterwards kview / vview hold this step's view."""
+    def step(self, q, meank_host, kraw_host, vraw_host, pipelined=True):
+        """One agent step; afterwards kview / vview hold this step's view.
+        Pipelined (the default): each index tile's select and pack are queued
+        right after its score, so they run while the copy stream brings in
+        the next tiles (layers are independent: the same outputs bit for bit
+        as score, select, pack one after another)."""
         cur = self.cur
         self.kept, self.kept_count = self.kept_sets[cur], self.count_sets[cur]
         self.vview = self.vviews[cur]
-        self.score_tiered(q, meank_host)
-        self.select()
-        self.pack_tiered(kraw_host, vraw_host)
+        if pipelined:
+            main = torch.cuda.current_stream(self.device)
+
+            def tile(l0, l1):
+                self.select(stream=main, l0=l0, l1=l1)
+                self.pack_tiered(kraw_host, vraw_host, l0, l1)
+
+            self.score_tiered(q, meank_host, after_tile=tile)
+        else:
+            self.score_tiered(q, meank_host)
+            self.select()
+            self.pack_tiered(kraw_host, vraw_host)
         self.cur, self.steps = 1 - cur, self.steps + 1
 
 
