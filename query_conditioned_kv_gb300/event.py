@@ -242,6 +242,10 @@ class TieredMeanKEvent(MeanKEvent):
         self.vviews = [self.vview, torch.empty_like(self.vview)]
         self.n_hits = torch.zeros(1, dtype=torch.int32, device=dev)
         self.cur, self.steps = 0, 0
+        # per staging buffer: an event after the last score that read it
+        # (kept across calls, so the next step's first copies need wait only
+        # for that, not for the previous step's select and pack)
+        self.stage_free = [None, None]
 
     def score_tiered(self, q, meank_host, after_tile=None):
         """Scores of every layer from the host-resident index [L][H][nb][D].
@@ -250,8 +254,7 @@ class TieredMeanKEvent(MeanKEvent):
         next tiles)."""
         main = torch.cuda.current_stream(self.device)
         cs = self.copy_stream
-        cs.wait_stream(main)
-        free = [None, None]
+        free = self.stage_free
         for gi, (l0, l1) in enumerate(self._split(self.L, -(-self.L // self.stage_layers))):
             b = gi % 2
             n = l1 - l0
