@@ -126,6 +126,37 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NC]) {
   else tmem_ld64(taddr, v);
 }
 
+// Two TMEM loads of NC columns (a tile's hi and lo products) in flight at
+// once, with one wait.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_two(uint32_t ta, uint32_t tb, float (&va)[NC],
+                                            float (&vb)[NC]) {
+  if constexpr (NC == 16 || NC == 32) {
+    uint32_t ra[NC], rb[NC];
+    if constexpr (NC == 32) {
+      tmem_issue32(ta, ra);
+      tmem_issue32(tb, rb);
+    } else {
+      tmem_issue<16>(ta, ra);
+      tmem_issue<16>(tb, rb);
+    }
+    tmem_wait<NC>(ra);
+    // rb's loads completed at the same wait; the empty statement keeps its
+    // uses below it
+#pragma unroll
+    for (int i = 0; i < NC; i += 4)
+      asm volatile("" : "+r"(rb[i]), "+r"(rb[i + 1]), "+r"(rb[i + 2]), "+r"(rb[i + 3])::"memory");
+#pragma unroll
+    for (int i = 0; i < NC; i++) {
+      va[i] = __uint_as_float(ra[i]);
+      vb[i] = __uint_as_float(rb[i]);
+    }
+  } else {
+    tmem_ld_cols<NC>(ta, va);
+    tmem_ld_cols<NC>(tb, vb);
+  }
+}
+
 // The G columns of head h's group among NC = 8·G consecutive ones.
 template <int G>
 __device__ __forceinline__ void group_cols(const float (&v)[8 * G], int h, float (&z)[G]) {
@@ -370,10 +401,18 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
         m[g] = -INFINITY;
         sum[g] = 0.f;
       }
+      // liveness of this thread's position in each of the item's 16 tiles,
+      // loaded together so that one load latency is paid per item, not per tile
+      uint32_t live_mask = 0u;
+#pragma unroll
       for (int b = 0; b < kTJ / kPos; b++) {
         const int j = j0 + b * kPos + sp;
         const int32_t u = j < a.N ? __ldg(smap + j) : a.sentinel;
-        const bool live = u != a.sentinel && u >= 0 && u < a.n_slots;
+        live_mask |= (uint32_t)(u != a.sentinel && u >= 0 && u < a.n_slots) << b;
+      }
+      for (int b = 0; b < kTJ / kPos; b++) {
+        const int j = j0 + b * kPos + sp;
+        const bool live = (live_mask >> b) & 1u;
         const int buf = t % kNacc;
         const bool got =
             ok && mbar_wait_bounded(smem_u32(sm.tfull + buf), (t / kNacc) & 1, sm.failed);
@@ -382,16 +421,10 @@ k_qmem_logits_tc(const __grid_constant__ CUtensorMap tm_k128,
         if (ok) {
           tc_fence_after();
           const uint32_t taddr = tmem + lane_base + (uint32_t)(buf * NC2);
-          {
-            float v[HQ];
-            tmem_ld_cols<HQ>(taddr, v);
-            group_cols<G>(v, h, zh);
-          }
-          {
-            float v[HQ];
-            tmem_ld_cols<HQ>(taddr + HQ, v);
-            group_cols<G>(v, h, zl);
-          }
+          float vh[HQ], vl[HQ];
+          tmem_ld_two<HQ>(taddr, taddr + HQ, vh, vl);
+          group_cols<G>(vh, h, zh);
+          group_cols<G>(vl, h, zl);
         }
         tc_fence_before();
         __syncwarp();
