@@ -18,6 +18,7 @@ event once to produce realistic inputs for the stage, then launches the stage
   python profile_cases.py tiered --layers 8 --iters 2
   python profile_cases.py confidence --iters 3
   python profile_cases.py repo   --layers 8 --slots 1024 --iters 3 --path /tmp/kvc_repo.bin
+  python profile_cases.py select_long --seg-len 312500 --segments 288 --budget 2048 --iters 10
 
 event_timing times a whole Mean-K event (score → select → pack, one CUDA
 graph) on a full workload — tiny, 8b, 27b or ragged — with L2 flushed
@@ -34,7 +35,11 @@ case runs `--iters` pairs of steps of the same event with the raw history of
 the packed layers in a repository (a backing file at `--path`, direct I/O
 where the file system allows it, `--slots` blocks in host RAM) and prints
 one JSON line per step: time, units (layer, head, block) used and missed,
-units read from the file and their rate.
+units read from the file and their rate.  The select_long case times
+kvc_select on `--segments` segments of `--seg-len` items each (longer than
+shared memory stages: the streaming kernel), seeded uniform scores with a run
+of equal values per segment, and prints one JSON line: the median time per
+launch and per segment.
 """
 from __future__ import annotations
 
@@ -46,13 +51,17 @@ import sys
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["score", "select", "pack", "event", "meank", "qmem",
-                                     "event_timing", "paged", "tiered", "confidence", "repo"])
+                                     "event_timing", "paged", "tiered", "confidence", "repo",
+                                     "select_long"])
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--sessions", type=int, default=8)
     ap.add_argument("--config", choices=["tiny", "8b", "27b", "ragged"], default="8b")
     ap.add_argument("--slots", type=int, default=1024)
     ap.add_argument("--path", default="/tmp/kvc_repo.bin")
+    ap.add_argument("--seg-len", type=int, default=312_500)
+    ap.add_argument("--segments", type=int, default=288)
+    ap.add_argument("--budget", type=int, default=2048)
     ap.add_argument("--kernel", default="auto",
                     help="scorer to run (a kvc_kernel name: score_fused, score_ring, "
                          "qmem_cc, recover_cc, ...); default: the library's choice")
@@ -84,6 +93,9 @@ def main(argv=None) -> None:
         return
     if args.case == "repo":
         _repo_case(args, dev)
+        return
+    if args.case == "select_long":
+        _select_long_case(args, dev)
         return
     base = {"8b": W.config_8b, "27b": W.config_27b, "tiny": W.config_tiny,
             "ragged": W.config_ragged}[args.config]()
@@ -340,6 +352,52 @@ def _repo_case(args, dev):
     os.remove(args.path)
     if st != 0:
         raise SystemExit(f"device status {st}")
+
+
+def _select_long_case(args, dev):
+    import json
+
+    import torch
+
+    import query_conditioned_kv_gb300 as kvc
+
+    n, S, budget = args.seg_len, args.segments, args.budget
+    if n <= kvc.SELECT_STAGED_SEG:
+        raise SystemExit(f"--seg-len must exceed {kvc.SELECT_STAGED_SEG} (the staged kernel's limit)")
+    g = torch.Generator(device=dev)
+    g.manual_seed(n + S)
+    scores = torch.rand(S, n, generator=g, device=dev)
+    scores[:, 1000:1700] = scores[:, 5:6]  # a run of equal scores in every segment
+    scores = scores.reshape(-1).contiguous()
+    off = torch.arange(S + 1, dtype=torch.int64, device=dev) * n
+    words = (n + 31) // 32
+    kept = torch.empty(S, budget, dtype=torch.int32, device=dev)
+    cnt = torch.empty(S, dtype=torch.int32, device=dev)
+    mask = torch.empty(S, words, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ms = []
+    for k in range(args.iters + 2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kvc.kvc_select(scores, off, S, n, budget, 1, 8, kept, cnt, mask, st)
+        b.record(stream)
+        b.synchronize()
+        if k >= 2:
+            ms.append(a.elapsed_time(b))
+    code = kvc.kvc_device_status(st)
+    if code != 0:
+        raise SystemExit(f"device status {code}: {kvc.kvc_status_string(code)}")
+    if not bool((cnt == budget).all()):
+        raise SystemExit("a segment did not keep exactly the budget")
+    med = sorted(ms)[len(ms) // 2]
+    print(json.dumps({"case": "select_long", "segments": S, "seg_len": n, "budget": budget,
+                      "n_sink": 1, "n_recent": 8, "launches": len(ms),
+                      "ms_per_launch_median": round(med, 4),
+                      "us_per_segment": round(1e3 * med / S, 3),
+                      "scores_gb": round(S * n * 4 / 1e9, 3),
+                      "l2": "scores exceed the 129 MB L2" if S * n * 4 > (129 << 20)
+                      else "scores fit in L2 (launches back to back)"}))
 
 
 def _confidence_case(args, dev):
