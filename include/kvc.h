@@ -84,7 +84,9 @@ typedef enum {
   KVC_ERR_TIMEOUT = 9,     /* device: a bounded wait gave up                 */
   KVC_ERR_CAPACITY = 10,   /* device: the freed-slot list overflowed; host:
                               more blocks needed at once than repository slots */
-  KVC_ERR_IO = 11          /* host: the repository's backing file failed     */
+  KVC_ERR_IO = 11,         /* host: the repository's backing file failed     */
+  KVC_ERR_NOMEM = 12       /* host: the repository's tables or scratch could
+                              not be allocated (nothing changed)             */
 } kvc_status;
 
 /* Kernel choice for the entry points that have more than one kernel for the
@@ -481,7 +483,7 @@ typedef struct {
  * records.  arena: host memory for n_slots records, owned by the caller and
  * kept alive until kvc_repo_destroy.  io_threads in [1, 64].  Errors:
  * KVC_ERR_INVALID_ARG, KVC_ERR_SHAPE (D ∉ {64, 128}), KVC_ERR_ALIGN (direct
- * I/O with an arena not 4096-byte aligned), KVC_ERR_IO. */
+ * I/O with an arena not 4096-byte aligned), KVC_ERR_IO, KVC_ERR_NOMEM. */
 kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_t H, int32_t D,
                            int32_t n_slots, kvc_bf16 *arena, int32_t io_threads, int32_t flags,
                            kvc_repo **out);
@@ -504,7 +506,8 @@ kvc_status kvc_repo_put(kvc_repo *repo, int64_t b0, int64_t nb, const kvc_bf16 *
  * kept units whose (l, h, r) did not keep them last step (the reads
  * kvc_pack_tiered_slots makes from host memory).  Both come out sorted and
  * unique; each array holds L·H·n_blocks entries.  Errors:
- * KVC_ERR_INVALID_ARG, KVC_ERR_BOUNDS (a kept index outside its session). */
+ * KVC_ERR_INVALID_ARG, KVC_ERR_BOUNDS (a kept index outside its session),
+ * KVC_ERR_NOMEM. */
 kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
                          const int32_t *kept_prev, const int32_t *kept_count_prev, int32_t L,
                          int32_t H, int32_t n_sess, int32_t budget, const int64_t *tok_off,
@@ -520,7 +523,8 @@ kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
  * put.  Errors: KVC_ERR_INVALID_ARG (an index out of range or never put),
  * KVC_ERR_CAPACITY (more units in `need` than slots; nothing changes),
  * KVC_ERR_IO (the step's evictions stand and its fetched units have no slot,
- * both listed by kvc_repo_changes; host_slot is not written). */
+ * both listed by kvc_repo_changes; host_slot is not written), KVC_ERR_NOMEM
+ * (scratch for the step could not be allocated; nothing changes). */
 kvc_status kvc_repo_step(kvc_repo *repo, const int64_t *used, int64_t n_used,
                          const int64_t *need, int64_t n_need, int32_t *host_slot);
 

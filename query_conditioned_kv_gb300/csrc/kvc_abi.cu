@@ -92,6 +92,7 @@ const char *kvc_status_string(kvc_status s) {
       return "capacity exceeded (device: the freed-slot list; host: more blocks needed at once "
              "than repository slots)";
     case KVC_ERR_IO: return "host: reading or writing the repository's backing file failed";
+    case KVC_ERR_NOMEM: return "host: out of memory for the repository's tables";
   }
   return "unknown status";
 }

@@ -16,6 +16,7 @@
 #include <algorithm>
 #include <atomic>
 #include <new>
+#include <stdexcept>
 #include <thread>
 #include <vector>
 
@@ -63,8 +64,8 @@ bool pwrite_all(int fd, const void *buf, int64_t n, int64_t off) {
 }
 
 // One vectored read of consecutive records into their slots, repeated on a
-// short read until every byte is in.
-bool preadv_all(int fd, std::vector<iovec> iov, int64_t off) {
+// short read until every byte is in (iov is advanced in place).
+bool preadv_all(int fd, std::vector<iovec> &iov, int64_t off) {
   size_t first = 0;
   while (first < iov.size()) {
     const int cnt = (int)std::min<size_t>(iov.size() - first, IOV_MAX);
@@ -113,6 +114,188 @@ int find_in(const int32_t *list, int n, int kb) {
   return -1;
 }
 
+kvc_status repo_plan(const int32_t *kept, const int32_t *kept_count, const int32_t *kept_prev,
+                     const int32_t *kept_count_prev, int32_t L, int32_t H, int32_t n_sess,
+                     int32_t budget, const int64_t *tok_off, int64_t n_blocks, int64_t *used,
+                     int64_t *n_used, int64_t *need, int64_t *n_need) {
+  // collected per kept entry, then sorted and made unique: the work grows
+  // with the kept lists, not with the history
+  std::vector<int64_t> vu, vn;
+  for (int64_t seg = 0; seg < (int64_t)L * H * n_sess; seg++) {
+    const int r = (int)(seg % n_sess);
+    const int64_t ubase = (seg / n_sess) * n_blocks;  // unit of (l, h, block 0)
+    const int64_t t0 = tok_off[r], t1 = tok_off[r + 1];
+    if (t0 < 0 || t1 < t0 || t0 % kTok || (t1 - t0) % kTok || t1 / kTok > n_blocks)
+      return KVC_ERR_INVALID_ARG;
+    const int64_t nb = (t1 - t0) / kTok, g0 = t0 / kTok;
+    const int cnt = kept_count[seg];
+    if (cnt < 0 || cnt > budget) return KVC_ERR_BOUNDS;
+    const int32_t *list = kept + seg * budget;
+    const int32_t *prev = kept_prev ? kept_prev + seg * budget : nullptr;
+    const int cp = prev ? std::min(std::max(kept_count_prev[seg], 0), budget) : 0;
+    for (int i = 0; i < cnt; i++) {
+      const int kb = list[i];
+      if (kb < 0 || kb >= nb) return KVC_ERR_BOUNDS;
+      vu.push_back(ubase + g0 + kb);
+      if (!prev || find_in(prev, cp, kb) < 0) vn.push_back(ubase + g0 + kb);
+    }
+  }
+  for (auto *v : {&vu, &vn}) {
+    std::sort(v->begin(), v->end());
+    v->erase(std::unique(v->begin(), v->end()), v->end());
+  }
+  std::copy(vu.begin(), vu.end(), used);
+  std::copy(vn.begin(), vn.end(), need);
+  *n_used = (int64_t)vu.size();
+  *n_need = (int64_t)vn.size();
+  return KVC_OK;
+}
+
+// kvc_repo_step's body.  Everything it allocates is allocated before the
+// repository changes, so an allocation failure (an exception, turned into
+// KVC_ERR_NOMEM by the caller) leaves the repository as it was.
+kvc_status repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const int64_t *need,
+                     int64_t n_need, int32_t *host_slot) {
+  // the step's needed units, once each
+  std::vector<int64_t> want;
+  std::vector<int64_t> fetch;
+  want.reserve((size_t)n_need);
+  fetch.reserve((size_t)n_need);
+  for (int64_t i = 0; i < n_need; i++)
+    if (!r->pinned[(size_t)need[i]]) {
+      r->pinned[(size_t)need[i]] = 1;
+      want.push_back(need[i]);
+    }
+  struct Unpin {  // the pins are scratch of this call, whatever happens
+    kvc_repo *r;
+    const std::vector<int64_t> &want;
+    ~Unpin() {
+      for (int64_t g : want) r->pinned[(size_t)g] = 0;
+    }
+  } unpin{r, want};
+  if ((int64_t)want.size() > r->n_slots) return KVC_ERR_CAPACITY;
+  for (int64_t g : want)
+    if (r->slot_of[(size_t)g] < 0) fetch.push_back(g);
+  std::sort(fetch.begin(), fetch.end());
+  // slots for the fetched units: free ones first, then k taken from others
+  const size_t n_free = std::min(fetch.size(), r->free_slots.size());
+  const size_t k = fetch.size() - n_free;  // want fits the slots, so k candidates exist
+  // runs of consecutive units (consecutive blocks of one layer and head):
+  // one vectored read each (at most 1 GiB)
+  struct Run {
+    int64_t off;
+    size_t first, n;
+    std::vector<iovec> iov;
+  };
+  std::vector<Run> runs;
+  const size_t max_run = (size_t)std::max<int64_t>(1, (1LL << 30) / r->rec_bytes);
+  for (size_t i = 0; i < fetch.size(); i++) {
+    if (i == 0 || fetch[i] != fetch[i - 1] + 1 || runs.back().n >= max_run)
+      runs.push_back(Run{fetch[i] * r->rec_bytes, i, 0, {}});
+    runs.back().n++;
+  }
+  for (Run &run : runs) run.iov.reserve(run.n);
+  std::vector<int32_t> dest, cand;
+  dest.reserve(fetch.size());
+  if (k > 0) cand.reserve((size_t)r->n_slots);
+  std::vector<int64_t> chg_unit;
+  std::vector<int32_t> chg_slot;
+  chg_unit.reserve(fetch.size() + k);
+  chg_slot.reserve(fetch.size() + k);
+
+  // ---- from here on nothing allocates: the repository changes
+  r->st.steps++;
+  const int64_t step = r->st.steps;
+  for (int64_t i = 0; i < n_used; i++) {
+    r->uses[(size_t)used[i]]++;
+    r->last[(size_t)used[i]] = step;
+  }
+  r->st.needed += (int64_t)want.size();
+  r->st.host_hits += (int64_t)(want.size() - fetch.size());
+  for (size_t i = 0; i < n_free; i++) dest.push_back(r->free_slots[r->free_slots.size() - 1 - i]);
+  r->free_slots.resize(r->free_slots.size() - n_free);
+  if (k > 0) {
+    // the slots of the least-used units the step does not need (ties: the
+    // least recently used, then the lowest index), with this step's uses counted
+    for (int32_t s = 0; s < r->n_slots; s++) {
+      const int64_t b = r->block_in[(size_t)s];
+      if (b >= 0 && !r->pinned[(size_t)b]) cand.push_back(s);
+    }
+    auto colder = [&](int32_t x, int32_t y) {
+      const int64_t bx = r->block_in[(size_t)x], by = r->block_in[(size_t)y];
+      if (r->uses[(size_t)bx] != r->uses[(size_t)by])
+        return r->uses[(size_t)bx] < r->uses[(size_t)by];
+      if (r->last[(size_t)bx] != r->last[(size_t)by]) return r->last[(size_t)bx] < r->last[(size_t)by];
+      return bx < by;
+    };
+    std::nth_element(cand.begin(), cand.begin() + (ptrdiff_t)(k - 1), cand.end(), colder);
+    for (size_t i = 0; i < k; i++) {
+      const int32_t s = cand[i];
+      const int64_t old = r->block_in[(size_t)s];
+      r->slot_of[(size_t)old] = -1;
+      r->block_in[(size_t)s] = -1;
+      chg_unit.push_back(old);
+      chg_slot.push_back(-1);
+      r->st.evictions++;
+      dest.push_back(s);
+    }
+  }
+  for (size_t i = 0; i < fetch.size(); i++) {
+    r->slot_of[(size_t)fetch[i]] = dest[i];
+    r->block_in[(size_t)dest[i]] = fetch[i];
+    chg_unit.push_back(fetch[i]);
+    chg_slot.push_back(dest[i]);
+  }
+  for (Run &run : runs)
+    for (size_t i = run.first; i < run.first + run.n; i++)
+      run.iov.push_back(iovec{r->arena + (int64_t)dest[i] * r->rec_elems, (size_t)r->rec_bytes});
+  r->chg_unit.swap(chg_unit);
+  r->chg_slot.swap(chg_slot);
+
+  std::atomic<bool> io_ok{true};
+  auto worker = [&](int t, int nt) {
+    for (size_t j = (size_t)t; j < runs.size(); j += (size_t)nt)
+      if (!preadv_all(r->fd, runs[j].iov, runs[j].off)) io_ok = false;
+  };
+  const int nt = (int)std::min<size_t>((size_t)r->io_threads, runs.size());
+  if (nt <= 1) {
+    worker(0, 1);
+  } else {
+    std::thread pool[64];
+    int started = 0;
+    for (int t = 1; t < nt; t++) {
+      try {
+        pool[started] = std::thread(worker, t, nt);
+        started++;
+      } catch (...) {
+        worker(t, nt);  // no thread to be had: this thread reads that share too
+      }
+    }
+    worker(0, nt);
+    for (int t = 0; t < started; t++) pool[t].join();
+  }
+  if (!io_ok) {
+    // the fetched units' slots hold nothing valid: give them back (the free
+    // list's capacity is n_slots, so this does not allocate)
+    for (int64_t g : fetch) {
+      const int32_t s = r->slot_of[(size_t)g];
+      r->slot_of[(size_t)g] = -1;
+      r->block_in[(size_t)s] = -1;
+      r->free_slots.push_back(s);
+    }
+    // the evictions stand: report them, and the fetched units as slotless
+    for (size_t i = 0; i < r->chg_slot.size(); i++)
+      if (r->chg_slot[i] >= 0) r->chg_slot[i] = -1;
+    return KVC_ERR_IO;
+  }
+  r->st.fetched += (int64_t)fetch.size();
+  r->st.read_calls += (int64_t)runs.size();
+  r->st.bytes_read += (int64_t)fetch.size() * r->rec_bytes;
+  if (host_slot)
+    for (int64_t u = 0; u < r->n_units; u++) host_slot[u] = r->slot_of[(size_t)u];
+  return KVC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -128,7 +311,7 @@ kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_
   const bool direct = (flags & KVC_REPO_DIRECT_IO) != 0;
   if (direct && (reinterpret_cast<uintptr_t>(arena) & 4095u)) return KVC_ERR_ALIGN;
   kvc_repo *r = new (std::nothrow) kvc_repo;
-  if (!r) return KVC_ERR_INVALID_ARG;
+  if (!r) return KVC_ERR_NOMEM;
   r->direct = direct;
   r->n_blocks = n_blocks;
   r->n_units = (int64_t)L * H * n_blocks;
@@ -157,13 +340,22 @@ kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_
     delete r;
     return KVC_ERR_IO;
   }
-  r->slot_of.assign((size_t)r->n_units, -1);
-  r->stored.assign((size_t)r->n_units, 0);
-  r->uses.assign((size_t)r->n_units, 0);
-  r->last.assign((size_t)r->n_units, 0);
-  r->pinned.assign((size_t)r->n_units, 0);
-  r->block_in.assign((size_t)n_slots, -1);
-  r->free_slots.resize((size_t)n_slots);
+  try {
+    r->slot_of.assign((size_t)r->n_units, -1);
+    r->stored.assign((size_t)r->n_units, 0);
+    r->uses.assign((size_t)r->n_units, 0);
+    r->last.assign((size_t)r->n_units, 0);
+    r->pinned.assign((size_t)r->n_units, 0);
+    r->block_in.assign((size_t)n_slots, -1);
+    // the free list's capacity stays n_slots for the repository's life, so
+    // giving slots back never allocates
+    r->free_slots.resize((size_t)n_slots);
+  } catch (const std::exception &) {  // std::bad_alloc, std::length_error
+    close(r->fd);
+    free(r->staging);
+    delete r;
+    return KVC_ERR_NOMEM;
+  }
   for (int32_t i = 0; i < n_slots; i++) r->free_slots[(size_t)i] = n_slots - 1 - i;
   *out = r;
   return KVC_OK;
@@ -201,38 +393,14 @@ kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
   if (!kept || !kept_count || !tok_off || !used || !n_used || !need || !n_need || L < 1 ||
       H < 1 || n_sess < 1 || budget < 1 || n_blocks < 1 || (kept_prev && !kept_count_prev))
     return KVC_ERR_INVALID_ARG;
-  // collected per kept entry, then sorted and made unique: the work grows
-  // with the kept lists, not with the history
-  std::vector<int64_t> vu, vn;
-  for (int64_t seg = 0; seg < (int64_t)L * H * n_sess; seg++) {
-    const int r = (int)(seg % n_sess);
-    const int64_t ubase = (seg / n_sess) * n_blocks;  // unit of (l, h, block 0)
-    const int64_t t0 = tok_off[r], t1 = tok_off[r + 1];
-    if (t0 < 0 || t1 < t0 || t0 % kTok || (t1 - t0) % kTok || t1 / kTok > n_blocks)
-      return KVC_ERR_INVALID_ARG;
-    const int64_t nb = (t1 - t0) / kTok, g0 = t0 / kTok;
-    const int cnt = kept_count[seg];
-    if (cnt < 0 || cnt > budget) return KVC_ERR_BOUNDS;
-    const int32_t *list = kept + seg * budget;
-    const int32_t *prev = kept_prev ? kept_prev + seg * budget : nullptr;
-    const int cp = prev ? std::min(std::max(kept_count_prev[seg], 0), budget) : 0;
-    for (int i = 0; i < cnt; i++) {
-      const int kb = list[i];
-      if (kb < 0 || kb >= nb) return KVC_ERR_BOUNDS;
-      vu.push_back(ubase + g0 + kb);
-      if (!prev || find_in(prev, cp, kb) < 0) vn.push_back(ubase + g0 + kb);
-    }
+  try {
+    return repo_plan(kept, kept_count, kept_prev, kept_count_prev, L, H, n_sess, budget, tok_off,
+                     n_blocks, used, n_used, need, n_need);
+  } catch (const std::exception &) {  // std::bad_alloc, std::length_error
+    return KVC_ERR_NOMEM;
   }
-  for (auto *v : {&vu, &vn}) {
-    std::sort(v->begin(), v->end());
-    v->erase(std::unique(v->begin(), v->end()), v->end());
-  }
-  std::copy(vu.begin(), vu.end(), used);
-  std::copy(vn.begin(), vn.end(), need);
-  *n_used = (int64_t)vu.size();
-  *n_need = (int64_t)vn.size();
-  return KVC_OK;
 }
+
 
 kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const int64_t *need,
                          int64_t n_need, int32_t *host_slot) {
@@ -243,125 +411,11 @@ kvc_status kvc_repo_step(kvc_repo *r, const int64_t *used, int64_t n_used, const
   for (int64_t i = 0; i < n_need; i++)
     if (need[i] < 0 || need[i] >= r->n_units || !r->stored[(size_t)need[i]])
       return KVC_ERR_INVALID_ARG;
-  // the step's needed units, once each
-  std::vector<int64_t> want;
-  want.reserve((size_t)n_need);
-  for (int64_t i = 0; i < n_need; i++)
-    if (!r->pinned[(size_t)need[i]]) {
-      r->pinned[(size_t)need[i]] = 1;
-      want.push_back(need[i]);
-    }
-  auto unpin = [&]() {
-    for (int64_t g : want) r->pinned[(size_t)g] = 0;
-  };
-  if ((int64_t)want.size() > r->n_slots) {
-    unpin();
-    return KVC_ERR_CAPACITY;
+  try {
+    return repo_step(r, used, n_used, need, n_need, host_slot);
+  } catch (const std::exception &) {  // std::bad_alloc, std::length_error
+    return KVC_ERR_NOMEM;
   }
-  r->chg_unit.clear();
-  r->chg_slot.clear();
-  r->st.steps++;
-  const int64_t step = r->st.steps;
-  for (int64_t i = 0; i < n_used; i++) {
-    r->uses[(size_t)used[i]]++;
-    r->last[(size_t)used[i]] = step;
-  }
-  std::vector<int64_t> fetch;
-  for (int64_t g : want)
-    if (r->slot_of[(size_t)g] < 0) fetch.push_back(g);
-  std::sort(fetch.begin(), fetch.end());
-  r->st.needed += (int64_t)want.size();
-  r->st.host_hits += (int64_t)(want.size() - fetch.size());
-
-  // slots for the fetched units: free ones, then those of the least-used
-  // units the step does not need
-  std::vector<int32_t> dest;
-  while (dest.size() < fetch.size() && !r->free_slots.empty()) {
-    dest.push_back(r->free_slots.back());
-    r->free_slots.pop_back();
-  }
-  if (dest.size() < fetch.size()) {
-    std::vector<int32_t> cand;
-    for (int32_t s = 0; s < r->n_slots; s++) {
-      const int64_t b = r->block_in[(size_t)s];
-      if (b >= 0 && !r->pinned[(size_t)b]) cand.push_back(s);
-    }
-    const size_t k = fetch.size() - dest.size();  // cand holds ≥ k: want fits the slots
-    auto colder = [&](int32_t x, int32_t y) {
-      const int64_t bx = r->block_in[(size_t)x], by = r->block_in[(size_t)y];
-      if (r->uses[(size_t)bx] != r->uses[(size_t)by])
-        return r->uses[(size_t)bx] < r->uses[(size_t)by];
-      if (r->last[(size_t)bx] != r->last[(size_t)by]) return r->last[(size_t)bx] < r->last[(size_t)by];
-      return bx < by;
-    };
-    std::nth_element(cand.begin(), cand.begin() + (ptrdiff_t)(k - 1), cand.end(), colder);
-    for (size_t i = 0; i < k; i++) {
-      const int32_t s = cand[i];
-      const int64_t old = r->block_in[(size_t)s];
-      r->slot_of[(size_t)old] = -1;
-      r->block_in[(size_t)s] = -1;
-      r->chg_unit.push_back(old);
-      r->chg_slot.push_back(-1);
-      r->st.evictions++;
-      dest.push_back(s);
-    }
-  }
-  for (size_t i = 0; i < fetch.size(); i++) {
-    r->slot_of[(size_t)fetch[i]] = dest[i];
-    r->block_in[(size_t)dest[i]] = fetch[i];
-    r->chg_unit.push_back(fetch[i]);
-    r->chg_slot.push_back(dest[i]);
-  }
-
-  // runs of consecutive units (consecutive blocks of one layer and head):
-  // one vectored read each (at most 1 GiB)
-  struct Run {
-    int64_t off;
-    std::vector<iovec> iov;
-  };
-  std::vector<Run> runs;
-  const size_t max_run = (size_t)std::max<int64_t>(1, (1LL << 30) / r->rec_bytes);
-  for (size_t i = 0; i < fetch.size(); i++) {
-    if (i == 0 || fetch[i] != fetch[i - 1] + 1 || runs.back().iov.size() >= max_run)
-      runs.push_back(Run{fetch[i] * r->rec_bytes, {}});
-    runs.back().iov.push_back(
-        iovec{r->arena + (int64_t)r->slot_of[(size_t)fetch[i]] * r->rec_elems,
-              (size_t)r->rec_bytes});
-  }
-  std::atomic<bool> io_ok{true};
-  auto worker = [&](int t, int nt) {
-    for (size_t j = (size_t)t; j < runs.size(); j += (size_t)nt)
-      if (!preadv_all(r->fd, runs[j].iov, runs[j].off)) io_ok = false;
-  };
-  const int nt = (int)std::min<size_t>((size_t)r->io_threads, runs.size());
-  if (nt <= 1) {
-    worker(0, 1);
-  } else {
-    std::vector<std::thread> pool;
-    for (int t = 1; t < nt; t++) pool.emplace_back(worker, t, nt);
-    worker(0, nt);
-    for (auto &th : pool) th.join();
-  }
-  unpin();
-  if (!io_ok) {
-    // the fetched units' slots hold nothing valid: give them back
-    for (int64_t g : fetch) {
-      const int32_t s = r->slot_of[(size_t)g];
-      r->slot_of[(size_t)g] = -1;
-      r->block_in[(size_t)s] = -1;
-      r->free_slots.push_back(s);
-    }
-    // the evictions stand: report them, and the fetched units as slotless
-    for (size_t i = 0; i < r->chg_slot.size(); i++)
-      if (r->chg_slot[i] >= 0) r->chg_slot[i] = -1;
-    return KVC_ERR_IO;
-  }
-  r->st.fetched += (int64_t)fetch.size();
-  r->st.read_calls += (int64_t)runs.size();
-  r->st.bytes_read += (int64_t)fetch.size() * r->rec_bytes;
-  if (host_slot)
-    for (int64_t u = 0; u < r->n_units; u++) host_slot[u] = r->slot_of[(size_t)u];
-  return KVC_OK;
 }
 
 kvc_status kvc_repo_slots(const kvc_repo *r, int32_t *host_slot) {

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(kvc):
 
 
 def test_status_strings(kvc):
-    for code in range(0, 11):
+    for code in range(0, 13):
         s = kvc.kvc_status_string(code)
         assert s and s != "unknown status"
     assert kvc.kvc_status_string(99) == "unknown status"
