@@ -93,11 +93,27 @@ def ncu_traffic(kernel: str):
                 continue
             k, v = line.strip().split("=", 1)
             rows[k.strip()] = v.strip()
-    src = rows.get(f"{kernel}.source")
-    if not src:
-        return None
-    with open(os.path.join(ROOT, src), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    parts = sorted(k for k in rows if k.startswith(f"{kernel}.part"))
+    if parts:
+        # the kernel's own source: "path :: start marker :: end marker" per
+        # part (an empty marker: the start or end of the file), concatenated
+        text = ""
+        for k in parts:
+            path_, start, end = (x.strip() for x in rows[k].split("::"))
+            with open(os.path.join(ROOT, path_), encoding="utf-8") as f:
+                body = f.read()
+            i = body.find(start) if start else 0
+            j = body.find(end, i) if end else len(body)
+            if i < 0 or j < 0:  # a marker is gone: the source has changed
+                return None
+            text += body[i:j]
+        sha = hashlib.sha256(text.encode("utf-8")).hexdigest()[:16]
+    else:
+        src = rows.get(f"{kernel}.source")
+        if not src:
+            return None
+        with open(os.path.join(ROOT, src), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
     if sha != rows.get(f"{kernel}.sha"):
         return None
     scale = float(rows.get(f"{kernel}.scale", "1"))
