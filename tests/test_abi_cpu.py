@@ -137,6 +137,15 @@ def test_validation_rejects_before_launch(kvc):
                  4, P, P, P, P, None, None, None) == 1
     assert _call(kvc, "kvc_pack_tiered", U, P, None, None, None, None, P, P, 1, 1, 128, P, 1,
                  128, 4, P, P, P, P, None, None, None) == 4
+    # tiered pack from repository slots: no slot table, slots smaller than a
+    # block, no slots, a slot stride that breaks 16-byte alignment
+    def slots(slot_elems, n_slots, table):
+        return _call(kvc, "kvc_pack_tiered_slots", P, P, slot_elems, n_slots, table, None, None,
+                     None, None, P, P, 1, 1, 128, P, 1, 128, 4, P, P, P, P, None, None, None)
+    assert slots(2 * 32 * 128, 4, None) == 1
+    assert slots(32 * 128 - 8, 4, P) == 1
+    assert slots(2 * 32 * 128, 0, P) == 1
+    assert slots(2 * 32 * 128 + 4, 4, P) == 4
     # LRFU: p or lambda outside [0, 1]; a segment longer than the staging allows
     assert _call(kvc, "kvc_lrfu_update", P, P, 1, 64, ctypes.c_float(1.5), ctypes.c_float(0.5),
                  P, None, None, None) == 1
