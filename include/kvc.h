@@ -491,9 +491,12 @@ kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_
 /* Puts blocks b0 … b0 + nb − 1 of every layer and head, taken from host
  * bf16 [L][H][n_tok][D] arrays (block g = tokens 32g … 32g + 31): each unit
  * is written to the backing file and, while free slots remain, kept in host
- * RAM (layer-major, then head, then block).  Putting a unit again overwrites
- * it.  Errors: KVC_ERR_INVALID_ARG (range outside the history or the
- * repository), KVC_ERR_IO. */
+ * RAM (slots taken layer-major, then head, then block).  The (layer, head)
+ * rows are spread over io_threads threads, each writing up to 64 consecutive
+ * records per vectored write.  Putting a unit again overwrites it.  Errors:
+ * KVC_ERR_INVALID_ARG (range outside the history or the repository),
+ * KVC_ERR_IO (units whose write failed are not marked as put),
+ * KVC_ERR_NOMEM. */
 kvc_status kvc_repo_put(kvc_repo *repo, int64_t b0, int64_t nb, const kvc_bf16 *kraw,
                         const kvc_bf16 *vraw, int64_t n_tok);
 

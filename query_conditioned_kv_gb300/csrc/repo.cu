@@ -42,7 +42,6 @@ struct kvc_repo {
   std::vector<int32_t> free_slots;
   std::vector<int64_t> chg_unit;   // the last step's slot changes: unit …
   std::vector<int32_t> chg_slot;   // … and its new slot (−1: evicted)
-  uint16_t *staging = nullptr;     // one record, 4096-byte aligned
   kvc_repo_stats st{};
 };
 
@@ -50,15 +49,27 @@ namespace {
 
 constexpr int kTok = KVC_BLOCK_TOKENS;
 
-bool pwrite_all(int fd, const void *buf, int64_t n, int64_t off) {
-  const char *p = static_cast<const char *>(buf);
-  while (n > 0) {
-    const ssize_t w = pwrite(fd, p, (size_t)std::min<int64_t>(n, 1 << 30), (off_t)off);
+// One vectored write of consecutive records, repeated on a short write until
+// every byte is out (iov is advanced in place).
+bool pwritev_all(int fd, std::vector<iovec> &iov, int64_t off) {
+  size_t first = 0;
+  while (first < iov.size()) {
+    const int cnt = (int)std::min<size_t>(iov.size() - first, IOV_MAX);
+    const ssize_t w = pwritev(fd, iov.data() + first, cnt, (off_t)off);
     if (w < 0 && errno == EINTR) continue;
     if (w <= 0) return false;
-    p += w;
-    n -= w;
     off += w;
+    size_t done = (size_t)w;
+    while (done > 0 && first < iov.size()) {
+      if (done >= iov[first].iov_len) {
+        done -= iov[first].iov_len;
+        first++;
+      } else {
+        iov[first].iov_base = static_cast<char *>(iov[first].iov_base) + done;
+        iov[first].iov_len -= done;
+        done = 0;
+      }
+    }
   }
   return true;
 }
@@ -112,6 +123,80 @@ int find_in(const int32_t *list, int n, int kb) {
     else hi = mid - 1;
   }
   return -1;
+}
+
+// kvc_repo_put's body.  Slots go to the put units in order (layer, head,
+// block) while free ones remain; then the io_threads threads take the
+// (layer, head) rows in turn and write each row's records as vectored writes
+// of up to kPutChunk consecutive records, gathering every record into its
+// slot or, for a unit without one, into the thread's own staging records.
+constexpr int64_t kPutChunk = 64;
+
+kvc_status repo_put(kvc_repo *r, int64_t b0, int64_t nb, const kvc_bf16 *kraw,
+                    const kvc_bf16 *vraw, int64_t n_tok) {
+  const int64_t rows = (int64_t)r->L * r->H;
+  const int nt = (int)std::max<int64_t>(1, std::min<int64_t>(r->io_threads, rows));
+  const int64_t chunk = std::min(kPutChunk, nb);
+  // allocations first: staging records and the iovec lists of every thread
+  uint16_t *staging = nullptr;
+  if (posix_memalign(reinterpret_cast<void **>(&staging), 4096,
+                     (size_t)(nt * chunk * r->rec_bytes)) != 0)
+    return KVC_ERR_NOMEM;
+  struct Free {
+    void *p;
+    ~Free() { free(p); }
+  } free_staging{staging};
+  std::vector<std::vector<iovec>> iovs((size_t)nt);
+  for (auto &v : iovs) v.reserve((size_t)chunk);
+  // ---- from here on nothing allocates
+  for (int64_t lh = 0; lh < rows; lh++)
+    for (int64_t g = b0; g < b0 + nb; g++) {
+      const int64_t u = lh * r->n_blocks + g;
+      if (r->slot_of[(size_t)u] < 0 && !r->free_slots.empty()) {
+        const int32_t slot = r->free_slots.back();
+        r->free_slots.pop_back();
+        r->slot_of[(size_t)u] = slot;
+        r->block_in[(size_t)slot] = u;
+      }
+    }
+  std::atomic<bool> io_ok{true};
+  auto worker = [&](int t) {
+    std::vector<iovec> &iov = iovs[(size_t)t];
+    uint16_t *mine = staging + (int64_t)t * chunk * r->rec_elems;
+    for (int64_t lh = t; lh < rows && io_ok; lh += nt)
+      for (int64_t g0 = b0; g0 < b0 + nb && io_ok; g0 += chunk) {
+        const int64_t n = std::min(chunk, b0 + nb - g0);
+        iov.clear();
+        for (int64_t i = 0; i < n; i++) {
+          const int64_t u = lh * r->n_blocks + g0 + i;
+          const int32_t slot = r->slot_of[(size_t)u];
+          uint16_t *dst = slot >= 0 ? r->arena + (int64_t)slot * r->rec_elems
+                                    : mine + i * r->rec_elems;
+          gather_record(r, u, kraw, vraw, n_tok, dst);
+          iov.push_back(iovec{dst, (size_t)r->rec_bytes});
+        }
+        if (!pwritev_all(r->fd, iov, (lh * r->n_blocks + g0) * r->rec_bytes)) {
+          io_ok = false;
+          break;
+        }
+        for (int64_t i = 0; i < n; i++) r->stored[(size_t)(lh * r->n_blocks + g0 + i)] = 1;
+      }
+  };
+  std::thread pool[64];
+  int started = 0;
+  for (int t = 1; t < nt; t++) {
+    try {
+      pool[started] = std::thread(worker, t);
+      started++;
+    } catch (...) {
+      worker(t);  // no thread to be had: this thread writes that share too
+    }
+  }
+  worker(0);
+  for (int t = 0; t < started; t++) pool[t].join();
+  if (!io_ok) return KVC_ERR_IO;
+  r->st.bytes_written += rows * nb * r->rec_bytes;
+  return KVC_OK;
 }
 
 kvc_status repo_plan(const int32_t *kept, const int32_t *kept_count, const int32_t *kept_prev,
@@ -333,10 +418,8 @@ kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_
   }
 #endif
   r->fd = open(path, oflags, 0600);
-  if (r->fd < 0 || ftruncate(r->fd, (off_t)(r->n_units * r->rec_bytes)) != 0 ||
-      posix_memalign(reinterpret_cast<void **>(&r->staging), 4096, (size_t)r->rec_bytes) != 0) {
+  if (r->fd < 0 || ftruncate(r->fd, (off_t)(r->n_units * r->rec_bytes)) != 0) {
     if (r->fd >= 0) close(r->fd);
-    r->staging = nullptr;
     delete r;
     return KVC_ERR_IO;
   }
@@ -352,7 +435,6 @@ kvc_status kvc_repo_create(const char *path, int64_t n_blocks, int32_t L, int32_
     r->free_slots.resize((size_t)n_slots);
   } catch (const std::exception &) {  // std::bad_alloc, std::length_error
     close(r->fd);
-    free(r->staging);
     delete r;
     return KVC_ERR_NOMEM;
   }
@@ -366,23 +448,11 @@ kvc_status kvc_repo_put(kvc_repo *r, int64_t b0, int64_t nb, const kvc_bf16 *kra
   if (!r || !kraw || !vraw || b0 < 0 || nb < 1 || n_tok < 1 || b0 + nb > r->n_blocks ||
       (b0 + nb) * kTok > n_tok)
     return KVC_ERR_INVALID_ARG;
-  for (int64_t lh = 0; lh < (int64_t)r->L * r->H; lh++)
-    for (int64_t g = b0; g < b0 + nb; g++) {
-      const int64_t u = lh * r->n_blocks + g;
-      int32_t slot = r->slot_of[(size_t)u];
-      if (slot < 0 && !r->free_slots.empty()) {
-        slot = r->free_slots.back();
-        r->free_slots.pop_back();
-        r->slot_of[(size_t)u] = slot;
-        r->block_in[(size_t)slot] = u;
-      }
-      uint16_t *dst = slot >= 0 ? r->arena + (int64_t)slot * r->rec_elems : r->staging;
-      gather_record(r, u, kraw, vraw, n_tok, dst);
-      if (!pwrite_all(r->fd, dst, r->rec_bytes, u * r->rec_bytes)) return KVC_ERR_IO;
-      r->stored[(size_t)u] = 1;
-      r->st.bytes_written += r->rec_bytes;
-    }
-  return KVC_OK;
+  try {
+    return repo_put(r, b0, nb, kraw, vraw, n_tok);
+  } catch (const std::exception &) {  // std::bad_alloc, std::length_error
+    return KVC_ERR_NOMEM;
+  }
 }
 
 kvc_status kvc_repo_plan(const int32_t *kept, const int32_t *kept_count,
@@ -449,7 +519,6 @@ kvc_status kvc_repo_get_stats(const kvc_repo *r, kvc_repo_stats *out) {
 void kvc_repo_destroy(kvc_repo *r) {
   if (!r) return;
   if (r->fd >= 0) close(r->fd);
-  free(r->staging);
   delete r;
 }
 

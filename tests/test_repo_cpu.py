@@ -171,6 +171,27 @@ def test_repo_reads_runs_in_one_call_each(tmp_path):
     repo.close()
 
 
+@pytest.mark.parametrize("io_threads", [1, 4, 7])
+def test_repo_put_writes_every_record(tmp_path, io_threads):
+    """Rows longer than one vectored write (150 blocks: writes of 64, 64, 22
+    records), more rows than some thread counts divide evenly, most units
+    without a host slot (written from staging records): every unit read back
+    from the file, a slot's worth at a time, equals its gather."""
+    n_blocks, n_slots = 150, 16
+    k, v, n_tok = _history(n_blocks, 11)
+    repo = kvc.KvcRepo(tmp_path / "w.bin", n_blocks, L, H, D, n_slots, io_threads=io_threads)
+    repo.put(0, 100, k, v, n_tok)
+    repo.put(100, n_blocks - 100, k, v, n_tok)
+    n_units = L * H * n_blocks
+    assert repo.stats()["bytes_written"] == n_units * 2 * TOK * D * 2
+    assert all(repo.where(u) in (1, 2) for u in range(n_units))
+    for u0 in range(0, n_units, n_slots):
+        need = list(range(u0, min(u0 + n_slots, n_units)))
+        repo.step(need, need)
+        _check_slots(repo, k, v, n_blocks)
+    repo.close()
+
+
 def test_repo_errors(tmp_path):
     n_blocks = 12
     k, v, n_tok = _history(n_blocks, 4)
