@@ -332,18 +332,26 @@ def kvc_pack_tiered_slots(kslots_host, vslots_host, slot_elems, n_slots, host_sl
         "kvc_pack_tiered_slots")
 
 
-def _np_ptr(a, dtype):
-    """Address of a C-contiguous host array of the given dtype (None → NULL)."""
+def _np_ptr(a, dtype, count=None):
+    """Address of a C-contiguous host array of the given dtype (None → NULL);
+    with `count`, the array must hold at least that many elements (the C side
+    reads that many)."""
     import numpy as np
     if a is None:
         return None
-    if hasattr(a, "is_cuda"):  # a CPU torch tensor
+    if hasattr(a, "is_cuda"):  # a CPU torch tensor: elements of the same size
         if a.is_cuda or not a.is_contiguous():
             raise ValueError("expected a contiguous host tensor")
-        return a.data_ptr()
-    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags.c_contiguous:
-        raise ValueError(f"expected a C-contiguous numpy array of {np.dtype(dtype).name}")
-    return a.ctypes.data
+        if a.element_size() != np.dtype(dtype).itemsize:
+            raise ValueError(f"expected {np.dtype(dtype).itemsize}-byte elements")
+        n, ptr = a.numel(), a.data_ptr()
+    else:
+        if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags.c_contiguous:
+            raise ValueError(f"expected a C-contiguous numpy array of {np.dtype(dtype).name}")
+        n, ptr = a.size, a.ctypes.data
+    if count is not None and n < count:
+        raise ValueError(f"expected at least {count} elements, got {n}")
+    return ptr
 
 
 def kvc_repo_plan(kept, kept_count, kept_prev, kept_count_prev, L, H, n_sess, budget, tok_off,
@@ -354,9 +362,12 @@ def kvc_repo_plan(kept, kept_count, kept_prev, kept_count_prev, L, H, n_sess, bu
     used = np.empty(L * H * n_blocks, np.int64)
     need = np.empty(L * H * n_blocks, np.int64)
     nu, nn = _c.c_int64(0), _c.c_int64(0)
-    _ok(lib.kvc_repo_plan(_np_ptr(kept, np.int32), _np_ptr(kept_count, np.int32),
-                          _np_ptr(kept_prev, np.int32), _np_ptr(kept_count_prev, np.int32),
-                          L, H, n_sess, budget, _np_ptr(tok_off, np.int64), n_blocks,
+    segs = L * H * n_sess
+    _ok(lib.kvc_repo_plan(_np_ptr(kept, np.int32, segs * budget),
+                          _np_ptr(kept_count, np.int32, segs),
+                          _np_ptr(kept_prev, np.int32, segs * budget),
+                          _np_ptr(kept_count_prev, np.int32, segs),
+                          L, H, n_sess, budget, _np_ptr(tok_off, np.int64, n_sess + 1), n_blocks,
                           used.ctypes.data, _c.addressof(nu), need.ctypes.data,
                           _c.addressof(nn)), "kvc_repo_plan")
     return used[:nu.value].copy(), need[:nn.value].copy()
@@ -405,8 +416,9 @@ class KvcRepo:
     def put(self, b0, nb, kraw, vraw, n_tok):
         """Blocks b0 … b0+nb−1 from host [L][H][n_tok][D] bf16 arrays."""
         import numpy as np
-        _ok(lib.kvc_repo_put(self._h, b0, nb, _np_ptr(kraw, np.uint16),
-                             _np_ptr(vraw, np.uint16), n_tok), "kvc_repo_put")
+        n = self.L * self.H * n_tok * self.D
+        _ok(lib.kvc_repo_put(self._h, b0, nb, _np_ptr(kraw, np.uint16, n),
+                             _np_ptr(vraw, np.uint16, n), n_tok), "kvc_repo_put")
 
     def step(self, used, need, table=True):
         """Brings `need` into host slots.  With `table`, returns the slot of

@@ -206,6 +206,13 @@ def test_repo_errors(tmp_path):
     with pytest.raises(kvc.KvcError) as e:  # outside the history
         repo.put(10, 3, k, v, n_tok)
     assert e.value.code == 1
+    with pytest.raises(ValueError):  # a history array shorter than n_tok says
+        repo.put(0, 1, k[:, :, :TOK], v, n_tok)
+    with pytest.raises(ValueError):  # 4-byte elements where bf16 is expected
+        repo.put(0, 1, k.astype(np.float32), v, n_tok)
+    with pytest.raises(ValueError):  # kept lists shorter than L·H·n_sess·budget
+        kvc.kvc_repo_plan(np.zeros(5, np.int32), np.zeros(L * H, np.int32), None, None, L, H,
+                          1, 4, np.array([0, n_tok], np.int64), n_blocks)
     n_units = L * H * n_blocks
     assert repo.where(-1) == -1 and repo.where(n_units) == -1 and repo.where(9) == 0
     repo.step([0, 5], [5])  # the repository still works after refused calls
