@@ -1227,33 +1227,34 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, local_rank)
+    import torch
+    dev = torch.device("cuda", local_rank)
+
+    def extra(key, fn):
+        """One extra workload's measurement under `key`.  If it fails, the key
+        holds the error and the line (the headline measured above) still
+        prints."""
+        torch.cuda.empty_cache()
+        try:
+            line[key] = fn()
+        except Exception as e:
+            line[key] = {"error": f"{type(e).__name__}: {e}"}
+            print(f"bench: {key} failed: {type(e).__name__}: {e}", file=sys.stderr, flush=True)
+
     for name, flag in (("27b_1m", args.no_27b), ("ragged_128", args.no_ragged)):
         if not flag:
-            import torch
-            torch.cuda.empty_cache()
-            line["event_" + name] = config_event(args, torch.device("cuda", local_rank), name=name,
-                                                 peak=peaks()[0])
+            extra("event_" + name,
+                  lambda name=name: config_event(args, dev, name=name, peak=peaks()[0]))
     if not args.no_slotmap:
-        import torch
-        torch.cuda.empty_cache()
-        line["slotmap_event"] = slot_map_event(args, torch.device("cuda", local_rank),
-                                               peaks()[0])
+        extra("slotmap_event", lambda: slot_map_event(args, dev, peaks()[0]))
     if not args.no_tiered:
-        import torch
-        torch.cuda.empty_cache()
-        line["tiered_event"] = tiered_event(args, torch.device("cuda", local_rank), peaks()[0])
+        extra("tiered_event", lambda: tiered_event(args, dev, peaks()[0]))
     if not args.no_repo:
-        import torch
-        torch.cuda.empty_cache()
-        line["repo_event"] = repo_event(args, torch.device("cuda", local_rank))
+        extra("repo_event", lambda: repo_event(args, dev))
     if not args.no_paged:
-        import torch
-        torch.cuda.empty_cache()
-        line["actkv_event"] = paged_event(args, torch.device("cuda", local_rank), peaks()[0])
+        extra("actkv_event", lambda: paged_event(args, dev, peaks()[0]))
     if not args.no_confidence:
-        import torch
-        line["confidence_monitor"] = confidence_monitor(args, torch.device("cuda", local_rank),
-                                                        peaks()[0])
+        extra("confidence_monitor", lambda: confidence_monitor(args, dev, peaks()[0]))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

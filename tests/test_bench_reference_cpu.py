@@ -38,3 +38,43 @@ def test_reference_arm_other_ranks_exit_without_work():
     p = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_extra_workload_failure_keeps_the_line(monkeypatch, capsys):
+    """An extra workload that fails (here: the slot-map event, as if the disk
+    or the device ran out) is reported under its own key, and the line with
+    the headline and the other workloads still prints."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test",
+                                                  os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    ran = []
+
+    def ok(name):
+        def run(*args, **kw):
+            ran.append(name)
+            return {"ok": name}
+        return run
+
+    def fails(*args, **kw):
+        ran.append("slotmap")
+        raise OSError("No space left on device")
+
+    monkeypatch.setattr(bench, "run_ours", lambda *a: {"metric": "m", "value": 1.0})
+    monkeypatch.setattr(bench, "peaks", lambda: (6702.8, 1910.5))
+    monkeypatch.setattr(bench, "config_event", lambda args, dev, name, peak: ok(name)())
+    monkeypatch.setattr(bench, "slot_map_event", fails)
+    for fn, name in (("tiered_event", "tiered"), ("repo_event", "repo"),
+                     ("paged_event", "paged"), ("confidence_monitor", "confidence")):
+        monkeypatch.setattr(bench, fn, ok(name))
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main()
+    out = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(out) == 1
+    d = json.loads(out[0])
+    assert ran == ["27b_1m", "ragged_128", "slotmap", "tiered", "repo", "paged", "confidence"]
+    assert d["value"] == 1.0 and d["slotmap_event"] == {"error": "OSError: No space left on device"}
+    assert d["event_27b_1m"] == {"ok": "27b_1m"} and d["confidence_monitor"] == {"ok": "confidence"}
